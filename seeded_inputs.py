@@ -1,0 +1,104 @@
+"""Seeded synthetic operands and the workload list shared by the tests, the
+benchmark and the oracle checks.
+
+This module draws random numbers and nothing else: it holds none of the
+GEMM's arithmetic, so both the CUDA path's callers and the CPU oracle can take
+their inputs from it without sharing any part of the method.
+
+Recipe (one CPU ``torch.Generator`` per shape, seeded with the workload's
+seed; A is drawn first, then B; values are drawn in fp32 and cast to the
+input dtype by torch with round-to-nearest-even):
+  * ``uniform``: iid U[-1, 1) as ``rand * 2 - 1``;
+  * ``normal``:  iid N(0, 1/K) as ``randn * K**-0.5`` (the standard deviation
+    is read as 1/sqrt(K)).
+The shapes are the Llama-3-70B projection sizes used as GEMM workloads in
+"A Blackwell GEMM by Hand in CuTe DSL" (section 1, gemm_math.py shape table);
+only their sizes are used, no model weights.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+F16, BF16, F32 = 0, 1, 2
+TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32}
+DTYPE_NAME = {F16: "f16", BF16: "bf16", F32: "f32"}
+
+
+@dataclass(frozen=True)
+class Shape:
+    M: int
+    N: int
+    K: int
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    shapes: tuple
+    dtype_in: int
+    dtype_out: int
+    dist: str
+    seed: int
+
+
+WORKLOADS = {
+    "small_256": Workload("small_256", (Shape(256, 256, 256),), F16, F32, "uniform", 0),
+    "square_4096": Workload("square_4096", (Shape(4096, 4096, 4096),), F16, F16, "uniform", 1),
+    "prefill": Workload("prefill", (Shape(8192, 8192, 8192), Shape(8192, 28672, 8192)),
+                        BF16, BF16, "normal", 2),
+    "decode_m256": Workload("decode_m256", (Shape(256, 28672, 8192), Shape(256, 8192, 28672),
+                                            Shape(256, 10240, 8192), Shape(256, 8192, 8192)),
+                            F16, F16, "uniform", 3),
+    "sweep_bf16_f32": Workload("sweep_bf16_f32", (
+        Shape(1024, 1024, 1024), Shape(2048, 2048, 2048), Shape(8192, 8192, 8192),
+        Shape(16384, 16384, 16384), Shape(4095, 4097, 4096), Shape(1000, 3000, 2000)),
+        BF16, F32, "uniform", 4),
+}
+
+
+def make_operands(M: int, N: int, K: int, dtype_in: int, dist: str = "uniform",
+                  seed: int = 0):
+    """Return (A, B): CPU tensors of shape (M, K) and (N, K) in the input dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    td = TORCH_DTYPE[dtype_in]
+    if dist == "uniform":
+        A = (torch.rand(M, K, generator=g) * 2 - 1).to(td)
+        B = (torch.rand(N, K, generator=g) * 2 - 1).to(td)
+    elif dist == "normal":
+        s = float(K) ** -0.5 if K > 0 else 1.0
+        A = (torch.randn(M, K, generator=g) * s).to(td)
+        B = (torch.randn(N, K, generator=g) * s).to(td)
+    else:
+        raise ValueError(f"unknown distribution {dist!r}")
+    return A, B
+
+
+def make_small_int_operands(M: int, N: int, K: int, dtype_in: int, seed: int = 0, lo: int = -3,
+                            hi: int = 3):
+    """iid integers in [lo, hi], stored in the input dtype (exact in fp16/bf16)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    td = TORCH_DTYPE[dtype_in]
+    A = torch.randint(lo, hi + 1, (M, K), generator=g).to(td)
+    B = torch.randint(lo, hi + 1, (N, K), generator=g).to(td)
+    return A, B
+
+
+def sample_indices(n: int, count: int, seed: int, must=()):
+    """Sorted unique indices in [0, n): `count` seeded draws plus the listed
+    ones that fall inside the range (tile edges, the last row/column)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    pick = torch.randint(0, max(n, 1), (count,), generator=g).tolist() if n > 0 else []
+    idx = {i for i in pick} | {i if i >= 0 else n + i for i in must}
+    return sorted(i for i in idx if 0 <= i < n)
+
+
+def rademacher(n: int, seed: int):
+    """A seeded +-1 vector (float64), for Freivalds-style checks."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return (torch.randint(0, 2, (n,), generator=g).to(torch.float64) * 2 - 1)

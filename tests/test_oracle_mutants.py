@@ -1,0 +1,103 @@
+"""The oracle's pins must catch plausible mistakes in the oracle itself.
+
+Each case plants one mistake in a copy of oracle.c (a dropped term, a wrong
+sign, a wrong index, a transposed operand, a wrong tie rule, truncation, a
+mis-scaled subnormal), compiles the copy on the CPU into a temporary library,
+and asserts that at least one pin check rejects it.  The committed oracle is
+never modified.
+"""
+import os
+import subprocess
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+from tests import exact
+
+F16, BF16, F32 = 0, 1, 2
+TD = {F16: torch.float16, BF16: torch.bfloat16}
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "drop_last_term": ("for (int64_t k = 0; k < K; ++k) s +=",
+                       "for (int64_t k = 0; k < K - 1; ++k) s +="),
+    "wrong_sign": ("s += lut[a_row[k]] * lut[b_row[k]];", "s -= lut[a_row[k]] * lut[b_row[k]];"),
+    "reversed_index": ("s += lut[a_row[k]] * lut[b_row[k]];",
+                       "s += lut[a_row[k]] * lut[b_row[K - 1 - k]];"),
+    # B walked with unit stride across j, as if it were stored transposed
+    "transposed_B": ("dot_row(a_row, jb->B + j * jb->K, jb->K, jb->lut)",
+                     "dot_row(a_row, jb->B + j, jb->K, jb->lut)"),
+    "A_for_B": ("dot_row(a_row, jb->B + j * jb->K, jb->K, jb->lut)",
+                "dot_row(a_row, jb->A + j * jb->K, jb->K, jb->lut)"),
+    "ties_away": ("(rem == 0.5 && fmod(n, 2.0) != 0.0)", "(rem == 0.5)"),
+    "truncate": ("if (rem > 0.5 ||", "if (rem > 2.0 ||"),
+    "subnormal_scale": ("v = ldexp((double)frac, f->emin - f->frac_bits);",
+                        "v = ldexp((double)frac, f->emin - f->frac_bits - 1);"),
+    "no_overflow": ("if (ee > f->emax) return inf_bits;", "if (ee > f->emax + 1) return inf_bits;"),
+    "bf16_as_f16_in": ("g_lut[ORACLE_BF16][b] = decode_bits(b, &FMT_BF16);",
+                       "g_lut[ORACLE_BF16][b] = decode_bits(b, &FMT_F16);"),
+}
+
+
+def _build_mutant(tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new))
+    lib = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    str(path), "-o", str(lib), "-lm"], check=True)
+    return oracle.load_library(str(lib))
+
+
+def _pins_pass(lib) -> bool:
+    """A compact run of the pin families; False as soon as one rejects."""
+    # all-ones -> K, both input formats
+    for dt in (F16, BF16):
+        for K in (1, 130, 2000):
+            A = torch.ones(2, K, dtype=TD[dt])
+            got = oracle.decode(oracle.gemm(A, A, dt, F32, lib=lib), F32, lib=lib)
+            if not np.all(got == K):
+                return False
+    # identity B -> A (includes subnormal fp16 inputs)
+    A = torch.tensor([[2.0**-24, 3 * 2.0**-24, 0.5, -1.5, 2.0**-20, -7.0]], dtype=torch.float16)
+    I = torch.eye(6, dtype=torch.float16)
+    if not np.array_equal(oracle.gemm(A, I, F16, F16, lib=lib),
+                          A.view(torch.int16).numpy().view(np.uint16)):
+        return False
+    # small integers, non-square, bf16 inputs
+    A, B = si.make_small_int_operands(5, 3, 37, BF16, seed=1)
+    ints = A.to(torch.int64).numpy() @ B.to(torch.int64).numpy().T
+    got = oracle.decode(oracle.gemm(A, B, BF16, F32, lib=lib), F32, lib=lib)
+    if not np.array_equal(got, ints.astype(np.float64)):
+        return False
+    # exact-rational brute force, fp16 output (ties, rounding)
+    A, B = si.make_operands(4, 3, 24, F16, "uniform", seed=2)
+    ex = exact.exact_gemm(A, B)
+    got = oracle.decode(oracle.gemm(A, B, F16, F16, lib=lib), F16, lib=lib)
+    for i in range(4):
+        for j in range(3):
+            if Fraction(float(got[i, j])) != exact.round_exact(ex[i][j], F16):
+                return False
+    # rounding routine against numpy on ties and overflow
+    x = np.array([1.0 + 2.0**-11, 1.0 + 3 * 2.0**-11, 65520.0, 70000.0, 2.0**-25 * 3])
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).view(np.uint16)
+    if not np.array_equal(oracle.round_to(x, F16, lib=lib), want):
+        return False
+    return True
+
+
+def test_committed_oracle_passes(tmp_path):
+    assert _pins_pass(oracle.load_library(oracle.build()))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    lib = _build_mutant(tmp_path, name)
+    assert not _pins_pass(lib), f"planted mistake {name!r} slipped past the pins"
