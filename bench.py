@@ -1,0 +1,336 @@
+"""Benchmark of the GB300 GEMM  C = A . B^T  (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload square_4096|...]
+
+A step is one GEMM over the workload's synthetic seeded operands (inputs
+resident in HBM).  Between timed steps a 512 MiB buffer is overwritten to
+flush the 129 MB L2, outside the timed events; each step is timed with CUDA
+events on the stream the kernel is launched on.  `value` is TFLOP/s (2MNK per
+step) over all ranks; `e2e` is the same metric through gemm_run_host with
+pinned host buffers (host->device copies of A and B and the device->host copy
+of C inside the timed region).  `cpu_baseline` times the CPU oracle on a
+bounded sample of the same product (whole rows of C) on the host cores, and
+those rows double as a full-size parity check of the GPU result.
+
+Multi-GPU: the GEMM does not exchange data between GPUs; N ranks run N
+independent replicas ("weak" scaling, value = all ranks' FLOPs / max time).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+from dense_gemm_blackwell_02_gb300 import roofline as rl  # noqa: E402
+
+METRIC = "GEMM TFLOP/s (4096³ fp16) & % of tensor peak; decode-shape HBM GB/s"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+KERNEL_SOURCES = "dense_gemm_blackwell_02_gb300/csrc/*"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, KERNEL_SOURCES))):
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "util": float(parts[4]),
+                             "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
+                             "sw_power": parts[9]})
+            except ValueError:
+                continue
+        loaded = [r for r in rows if r["util"] >= 50] or rows
+        if not loaded:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in loaded):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in loaded), "reasons": reasons,
+                "samples": len(loaded)}
+
+
+def workload_shape(name: str):
+    wl = si.WORKLOADS[name]
+    return wl, wl.shapes[0]
+
+
+def cpu_rows_sample(A, B, din, dout, M, target_s=10.0):
+    """Oracle rows timed on the host cores: calibrate on a few rows, then time
+    enough rows for ~target_s seconds.  Returns (rows, bits, seconds, threads)."""
+    import oracle
+    N, K = B.shape[0], B.shape[1]
+    probe = si.sample_indices(M, 32, seed=99)
+    t0 = time.perf_counter()
+    oracle.gemm_select(A, B, probe, None, din, dout)
+    t = max(time.perf_counter() - t0, 1e-3)
+    nrows = int(min(M, max(32, len(probe) * target_s / t)))
+    rows = si.sample_indices(M, nrows, seed=7, must=(0, 127, 128, 255, 256, -1))
+    t0 = time.perf_counter()
+    bits = oracle.gemm_select(A, B, rows, None, din, dout)
+    dt = time.perf_counter() - t0
+    return rows, bits, dt, os.cpu_count()
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores on bounded samples."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    wl, s = workload_shape(args.workload)
+    A, B = si.make_operands(s.M, s.N, s.K, wl.dtype_in, wl.dist, wl.seed)
+    rows_per_step = max(1, int(os.environ.get("GEMM_REF_ROWS", "64")))
+    times = []
+    for step in range(args.warmup + args.steps):
+        rows = si.sample_indices(s.M, rows_per_step, seed=1000 + step)
+        t0 = time.perf_counter()
+        oracle.gemm_select(A, B, rows, None, wl.dtype_in, wl.dtype_out)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append((len(rows), dt))
+    flops = sum(2.0 * r * s.N * s.K for r, _ in times)
+    secs = sum(t for _, t in times)
+    value = flops / secs / 1e12
+    sample = (f"{rows_per_step} seeded rows of C per step ({2.0 * rows_per_step * s.N * s.K / 1e9:.2f}"
+              f" GFLOP), binary64 accumulation, all host threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / max(len(times), 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "M": s.M, "N": s.N, "K": s.K,
+                       "dtype_in": si.DTYPE_NAME[wl.dtype_in], "dtype_out": si.DTYPE_NAME[wl.dtype_out],
+                       "dist": wl.dist, "seed": wl.seed},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    from dense_gemm_blackwell_02_gb300.binding import Gemm
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", rank=rank, world_size=ws)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    wl, s = workload_shape(args.workload)
+    M, N, K = s.M, s.N, s.K
+    din, dout = wl.dtype_in, wl.dtype_out
+    A_cpu, B_cpu = si.make_operands(M, N, K, din, wl.dist, wl.seed)
+    A, B = A_cpu.to(dev), B_cpu.to(dev)
+    C = torch.empty(M, N, dtype=si.TORCH_DTYPE[dout], device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    g = Gemm()
+    if args.config:
+        g.set_config(**json.loads(args.config))
+
+    def step():
+        g.run(A, B, C, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    code, word = g.device_status(stream)
+    if code != 0:
+        raise RuntimeError(f"device status after warm-up: {code} ({word:#x})")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    # keep the GPU busy for a moment so the sampler sees the clocks under load
+    t_end = time.perf_counter() + 0.6
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(per_ms)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    code, word = g.device_status(stream)
+    if code != 0:
+        raise RuntimeError(f"device status after timing: {code} ({word:#x})")
+    cfg = g.last_config()
+    flops = rl.gemm_flops(M, N, K)
+    ms_per_step = total_ms / args.steps
+    value = ws * flops * args.steps / (total_ms * 1e-3) / 1e12
+    kernel_tflops = flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with pinned host buffers
+    A_h = A_cpu.pin_memory()
+    B_h = B_cpu.pin_memory()
+    C_h = torch.empty(M, N, dtype=si.TORCH_DTYPE[dout]).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    g.run_host(A_h, B_h, C_h, din, dout, stream=stream)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        g.run_host(A_h, B_h, C_h, din, dout, stream=stream)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    out_b = 4 if dout == si.F32 else 2
+    e2e = {"value": flops / e2e_s / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": 2 * (M * K + N * K), "d2h_bytes_per_step": out_b * M * N}
+
+    line = None
+    if rank == 0:
+        # ---- CPU oracle on whole rows: the cpu_baseline, and a full-size parity check
+        import numpy as np
+        from tests import parity as par
+        rows, want, cpu_s, threads = cpu_rows_sample(A_cpu, B_cpu, din, dout, M,
+                                                      target_s=args.cpu_seconds)
+        got = par.bits_of(C[rows])
+        metrics = par.check(got, want, dout, what="bench rows")
+        e2e_rows = par.bits_of(C_h[rows])
+        assert np.array_equal(e2e_rows, got), "gemm_run_host disagrees with gemm_run"
+        cpu_value = 2.0 * len(rows) * N * K / cpu_s / 1e12
+
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        traffic = None
+        tf_path = os.path.join(ROOT, "profiles", "traffic.json")
+        if os.path.exists(tf_path):
+            rec = json.load(open(tf_path)).get(args.workload)
+            if rec and rec.get("source_hash") == kernel_source_hash():
+                traffic = rec.get("bytes_per_launch")
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": si.DTYPE_NAME[din], "data": "synthetic",
+            "config": {"workload": args.workload, "M": M, "N": N, "K": K,
+                       "dtype_in": si.DTYPE_NAME[din], "dtype_out": si.DTYPE_NAME[dout],
+                       "dist": wl.dist, "seed": wl.seed, "l2": "flushed (512 MiB write between steps)",
+                       "kernel": cfg, "parallelism": "replicas" if ws > 1 else "single-gpu"},
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak,
+                         "unit": "TFLOP/s", "frac": kernel_tflops / peak, "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16_tflops (burst; fp16 has the same dense rate)",
+                         "algorithmic_flops_per_launch": flops},
+            "cpu_baseline": {"value": cpu_value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{len(rows)} whole rows of C ({2.0 * len(rows) * N * K / 1e9:.1f}"
+                                       f" GFLOP) in {cpu_s:.1f} s"},
+            "parity": {"rows_checked": len(rows), **metrics},
+        }
+        print(json.dumps(line))
+    g.close()
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="square_4096", choices=sorted(si.WORKLOADS))
+    ap.add_argument("--config", default=None, help="JSON gemm_config_t override (sweeps)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

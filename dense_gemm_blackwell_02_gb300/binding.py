@@ -1,0 +1,188 @@
+"""ctypes binding of libgemm.so (include/gemm.h): argument marshalling only.
+
+Every step of the GEMM runs inside the library's CUDA kernels; this module
+passes pointers, sizes, dtype codes and the caller's CUDA stream.  If the
+library is missing it raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+F16, BF16, F32 = 0, 1, 2
+STATUS_NAMES = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
+                3: "GEMM_ERR_CUDA", 4: "GEMM_ERR_OOM", 5: "GEMM_ERR_TIMEOUT"}
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgemm.so")
+
+# Every function include/gemm.h declares (checked against the header by the tests).
+EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "gemm_set_config",
+           "gemm_last_config", "gemm_device_status", "gemm_set_wait_limit",
+           "gemm_set_test_stall", "gemm_sm_count", "gemm_status_string")
+
+
+class GemmConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("variant", "block_n", "splits", "stages",
+                                                "group_m", "max_ctas", "reserved0", "reserved1")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_ if not n.startswith("reserved")}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{STATUS_NAMES.get(code, code)}{': ' + what if what else ''}")
+
+
+_lib = None
+
+
+def lib():
+    """Load libgemm.so (built in-tree) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run "
+                           "`python -m dense_gemm_blackwell_02_gb300.build` first")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, u32, u64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32,
+                              ctypes.c_uint64)
+    L.gemm_create.argtypes = [ctypes.POINTER(vp)]
+    L.gemm_destroy.argtypes = [vp]
+    L.gemm_run.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp]
+    L.gemm_run_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp]
+    L.gemm_set_config.argtypes = [vp, ctypes.POINTER(GemmConfig)]
+    L.gemm_last_config.argtypes = [vp, ctypes.POINTER(GemmConfig)]
+    L.gemm_device_status.argtypes = [vp, vp, ctypes.POINTER(u32)]
+    L.gemm_set_wait_limit.argtypes = [vp, u64]
+    L.gemm_set_test_stall.argtypes = [vp, i32]
+    L.gemm_sm_count.argtypes = [vp]
+    L.gemm_sm_count.restype = i32
+    L.gemm_status_string.argtypes = [i32]
+    L.gemm_status_string.restype = ctypes.c_char_p
+    for name in EXPORTS:
+        if name not in ("gemm_sm_count", "gemm_status_string"):
+            getattr(L, name).restype = i32
+    _lib = L
+    return L
+
+
+def _check(code: int, what: str = ""):
+    if code != 0:
+        raise GemmError(code, what)
+
+
+def torch_dtype_code(dt) -> int:
+    import torch
+    return {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32}[dt]
+
+
+def _stream_ptr(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class Gemm:
+    """One library handle (workspace, status word, tensor-map cache)."""
+
+    def __init__(self):
+        h = ctypes.c_void_p()
+        _check(lib().gemm_create(ctypes.byref(h)), "gemm_create")
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if self._h:
+            lib().gemm_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def sm_count(self) -> int:
+        return lib().gemm_sm_count(self._h)
+
+    # ------------------------------------------------------------ raw pointers --
+    def run_ptr(self, a_ptr, b_ptr, c_ptr, M, N, K, dtype_in, dtype_out, stream_ptr=0) -> int:
+        """gemm_run on raw device pointers; returns the status code."""
+        return lib().gemm_run(self._h, a_ptr, b_ptr, c_ptr, M, N, K, dtype_in, dtype_out,
+                              stream_ptr)
+
+    # ----------------------------------------------------------- torch tensors --
+    def run(self, A, B, C, stream=None):
+        """C = A @ B.T for CUDA tensors A (M,K), B (N,K), C (M,N), all contiguous."""
+        if not (A.is_cuda and B.is_cuda and C.is_cuda):
+            raise ValueError("A, B and C must be CUDA tensors")
+        if not (A.is_contiguous() and B.is_contiguous() and C.is_contiguous()):
+            raise ValueError("A, B and C must be contiguous (row-major, K-major operands)")
+        if A.dim() != 2 or B.dim() != 2 or C.dim() != 2:
+            raise ValueError("A, B and C must be 2-D")
+        M, K = A.shape
+        N, K2 = B.shape
+        if K != K2 or tuple(C.shape) != (M, N):
+            raise ValueError(f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, "
+                             f"C {tuple(C.shape)}")
+        if A.dtype != B.dtype:
+            raise ValueError("A and B must share a dtype")
+        code = self.run_ptr(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                            torch_dtype_code(A.dtype), torch_dtype_code(C.dtype),
+                            _stream_ptr(stream, A.device))
+        _check(code, f"gemm_run M={M} N={N} K={K}")
+        return C
+
+    def run_host(self, A, B, C, dtype_in, dtype_out, stream=None):
+        """gemm_run_host on CPU tensors (pinned for asynchronous copies)."""
+        M, K = A.shape
+        N = B.shape[0]
+        sp = 0 if stream is None else _stream_ptr(stream, None)
+        code = lib().gemm_run_host(self._h, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                                   dtype_in, dtype_out, sp)
+        _check(code, "gemm_run_host")
+        return C
+
+    # ----------------------------------------------------------------- control --
+    def set_config(self, variant=0, block_n=0, splits=0, stages=0, group_m=0, max_ctas=0):
+        cfg = GemmConfig(variant, block_n, splits, stages, group_m, max_ctas, 0, 0)
+        _check(lib().gemm_set_config(self._h, ctypes.byref(cfg)), "gemm_set_config")
+
+    def reset_config(self):
+        _check(lib().gemm_set_config(self._h, None), "gemm_set_config")
+
+    def last_config(self) -> dict:
+        cfg = GemmConfig()
+        _check(lib().gemm_last_config(self._h, ctypes.byref(cfg)), "gemm_last_config")
+        return cfg.as_dict()
+
+    def device_status(self, stream=None):
+        """(status code, raw device word) after synchronising the stream."""
+        import torch
+        detail = ctypes.c_uint32(0)
+        sp = _stream_ptr(stream, torch.cuda.current_device())
+        code = lib().gemm_device_status(self._h, sp, ctypes.byref(detail))
+        return code, detail.value
+
+    def set_wait_limit(self, ns: int):
+        _check(lib().gemm_set_wait_limit(self._h, int(ns)), "gemm_set_wait_limit")
+
+    def set_test_stall(self, enable: bool):
+        _check(lib().gemm_set_test_stall(self._h, 1 if enable else 0), "gemm_set_test_stall")
+
+
+def status_string(code: int) -> str:
+    return lib().gemm_status_string(code).decode()

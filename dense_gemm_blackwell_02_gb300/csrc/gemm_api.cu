@@ -1,0 +1,386 @@
+// C ABI of libgemm.so (declared in include/gemm.h): argument validation, the
+// shape -> kernel-configuration heuristic, TMA tensor-map encoding with a small
+// cache, workspace management, launch, and the device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "gemm.h"
+#include "launch.h"
+#include "umma.cuh"
+
+using namespace gb300;
+
+namespace {
+
+constexpr int kTmapCacheSize = 16;
+
+struct TmapKey {
+  const void* ptr;
+  int64_t rows, cols;
+  int32_t dtype, box_rows;
+  bool operator==(const TmapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && cols == o.cols && dtype == o.dtype &&
+           box_rows == o.box_rows;
+  }
+};
+
+struct TmapEntry {
+  TmapKey key;
+  CUtensorMap map;
+  bool valid;
+};
+
+}  // namespace
+
+struct gemm_ctx {
+  int device = 0;
+  int sms = 0;
+  uint32_t* d_status = nullptr;
+  float* d_ws = nullptr;
+  size_t ws_bytes = 0;
+  uint32_t* d_ctr = nullptr;
+  size_t ctr_count = 0;
+  void* d_stage[3] = {nullptr, nullptr, nullptr};  // gemm_run_host: A, B, C
+  size_t stage_bytes[3] = {0, 0, 0};
+  gemm_config_t forced = {};
+  gemm_config_t last = {};
+  uint64_t wait_limit_ns = 2000000000ull;
+  int32_t test_stall = 0;
+  TmapEntry cache[kTmapCacheSize] = {};
+  int cache_next = 0;
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D tensor map over a row-major rows x cols matrix of 16-bit elements, 128-byte
+// swizzle, box {64, box_rows}; out-of-range elements read as zero (M, N and K tails).
+bool make_operand_map(gemm_ctx* h, const void* ptr, int64_t rows, int64_t cols, int dtype,
+                      int box_rows, CUtensorMap* out) {
+  const TmapKey key{ptr, rows, cols, dtype, box_rows};
+  for (auto& e : h->cache)
+    if (e.valid && e.key == key) {
+      *out = e.map;
+      return true;
+    }
+  auto fn = encode_fn();
+  if (!fn) return false;
+  CUtensorMap m;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  TmapEntry& slot = h->cache[h->cache_next];
+  h->cache_next = (h->cache_next + 1) % kTmapCacheSize;
+  slot.key = key;
+  slot.map = m;
+  slot.valid = true;
+  *out = m;
+  return true;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+size_t out_size(gemm_dtype_t d) { return d == GEMM_F32 ? 4 : 2; }
+
+bool valid_dtype(int d) { return d == GEMM_F16 || d == GEMM_BF16 || d == GEMM_F32; }
+
+struct Choice {
+  int variant, bn, stages, splits, kb_per_split, group_m, grid;
+  int64_t tiles, units, k_blocks, num_m, num_n;
+};
+
+gemm_status_t choose(const gemm_ctx* h, int64_t M, int64_t N, int64_t K, Choice* c) {
+  const gemm_config_t& f = h->forced;
+  c->variant = f.variant ? f.variant : 1;
+  if (c->variant != 1) return GEMM_ERR_INVALID_ARG;
+  c->bn = f.block_n ? f.block_n : (N <= 128 ? 128 : 256);
+  c->stages = f.stages ? f.stages : (c->bn == 256 ? 4 : 6);
+  if (!one_cta_supported(c->bn, c->stages)) return GEMM_ERR_INVALID_ARG;
+  c->k_blocks = ceil_div(K, kBlockK);
+  c->num_m = ceil_div(M, kBlockM);
+  c->num_n = ceil_div(N, c->bn);
+  c->tiles = c->num_m * c->num_n;
+  int64_t s;
+  if (f.splits) {
+    s = f.splits;
+  } else if (c->tiles * 2 <= h->sms && c->k_blocks >= 8) {
+    // Fewer tiles than half the SMs: slice K so every SM has work ("A Blackwell
+    // GEMM by Hand in CuTe DSL", section 9: decode shapes are decided by waves).
+    s = h->sms / c->tiles;
+    if (s > c->k_blocks / 4) s = c->k_blocks / 4;
+    if (s > 32) s = 32;
+    if (s < 1) s = 1;
+  } else {
+    s = 1;
+  }
+  if (s > c->k_blocks) s = c->k_blocks;
+  const int64_t per = ceil_div(c->k_blocks, s);
+  s = ceil_div(c->k_blocks, per);  // no empty slice
+  c->splits = (int)s;
+  c->kb_per_split = (int)per;
+  c->units = c->tiles * s;
+  c->group_m = f.group_m ? f.group_m : 16;
+  int64_t cap = f.max_ctas ? f.max_ctas : h->sms;
+  if (cap > h->sms) cap = h->sms;
+  c->grid = (int)(c->units < cap ? c->units : cap);
+  if (c->units > INT32_MAX || c->tiles * 4 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  return GEMM_OK;
+}
+
+gemm_status_t ensure_workspace(gemm_ctx* h, size_t ws_bytes, size_t ctr_count) {
+  if (ws_bytes > h->ws_bytes) {
+    if (h->d_ws) cudaFree(h->d_ws);
+    h->d_ws = nullptr;
+    h->ws_bytes = 0;
+    if (cudaMalloc(&h->d_ws, ws_bytes) != cudaSuccess) return GEMM_ERR_OOM;
+    h->ws_bytes = ws_bytes;
+  }
+  if (ctr_count > h->ctr_count) {
+    if (h->d_ctr) cudaFree(h->d_ctr);
+    h->d_ctr = nullptr;
+    h->ctr_count = 0;
+    if (cudaMalloc(&h->d_ctr, ctr_count * sizeof(uint32_t)) != cudaSuccess) return GEMM_ERR_OOM;
+    if (cudaMemset(h->d_ctr, 0, ctr_count * sizeof(uint32_t)) != cudaSuccess) return GEMM_ERR_CUDA;
+    h->ctr_count = ctr_count;
+  }
+  return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gemm_status_string(gemm_status_t s) {
+  switch (s) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_UNSUPPORTED: return "unsupported (dtype, alignment, K % 8, or device)";
+    case GEMM_ERR_CUDA: return "CUDA error";
+    case GEMM_ERR_OOM: return "out of memory";
+    case GEMM_ERR_TIMEOUT: return "kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+gemm_status_t gemm_create(gemm_handle_t* out) {
+  if (!out) return GEMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED;
+  gemm_ctx* h = new (std::nothrow) gemm_ctx();
+  if (!h) return GEMM_ERR_OOM;
+  h->device = dev;
+  h->sms = sms;
+  if (cudaMalloc(&h->d_status, sizeof(uint32_t)) != cudaSuccess) {
+    delete h;
+    return GEMM_ERR_OOM;
+  }
+  if (cudaMemset(h->d_status, 0, sizeof(uint32_t)) != cudaSuccess) {
+    cudaFree(h->d_status);
+    delete h;
+    return GEMM_ERR_CUDA;
+  }
+  *out = h;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_destroy(gemm_handle_t h) {
+  if (!h) return GEMM_OK;
+  cudaDeviceSynchronize();
+  cudaFree(h->d_status);
+  if (h->d_ws) cudaFree(h->d_ws);
+  if (h->d_ctr) cudaFree(h->d_ctr);
+  for (auto* p : h->d_stage)
+    if (p) cudaFree(p);
+  delete h;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  if (!cfg) {
+    h->forced = gemm_config_t{};
+    return GEMM_OK;
+  }
+  const gemm_config_t& c = *cfg;
+  if (c.variant < 0 || c.variant > 1) return GEMM_ERR_INVALID_ARG;
+  if (c.block_n != 0 && c.block_n != 128 && c.block_n != 256) return GEMM_ERR_INVALID_ARG;
+  if (c.splits < 0 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0) return GEMM_ERR_INVALID_ARG;
+  if (c.stages) {
+    const int bn = c.block_n ? c.block_n : 256;
+    if (!one_cta_supported(bn, c.stages)) return GEMM_ERR_INVALID_ARG;
+  }
+  h->forced = c;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_last_config(gemm_handle_t h, gemm_config_t* out) {
+  if (!h || !out) return GEMM_ERR_INVALID_ARG;
+  *out = h->last;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_set_wait_limit(gemm_handle_t h, uint64_t ns) {
+  if (!h || ns == 0) return GEMM_ERR_INVALID_ARG;
+  h->wait_limit_ns = ns;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_set_test_stall(gemm_handle_t h, int32_t enable) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  h->test_stall = enable ? 1 : 0;
+  return GEMM_OK;
+}
+
+int32_t gemm_sm_count(gemm_handle_t h) { return h ? h->sms : 0; }
+
+gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M,
+                       int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                       gemm_stream_t stream_) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype_in) || !valid_dtype(dtype_out)) return GEMM_ERR_INVALID_ARG;
+  if (dtype_in == GEMM_F32) return GEMM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const size_t osz = out_size(dtype_out);
+  if (reinterpret_cast<uintptr_t>(C) % osz) return GEMM_ERR_UNSUPPORTED;
+  if (K == 0) {  // the empty sum: C = 0 (all-zero bits in every output format)
+    if (cudaMemsetAsync(C, 0, (size_t)M * (size_t)N * osz, stream) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    return GEMM_OK;
+  }
+  if (K % 8) return GEMM_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(B) % 16)
+    return GEMM_ERR_UNSUPPORTED;
+
+  Choice ch;
+  gemm_status_t st = choose(h, M, N, K, &ch);
+  if (st != GEMM_OK) return st;
+
+  LaunchSpec s;
+  std::memset(&s, 0, sizeof(s));
+  s.bn = ch.bn;
+  s.stages = ch.stages;
+  s.out = dtype_out == GEMM_F16 ? kOutF16 : dtype_out == GEMM_BF16 ? kOutBF16 : kOutF32;
+  s.grid = ch.grid;
+  s.stream = stream;
+  if (!make_operand_map(h, A, M, K, dtype_in, kBlockM, &s.tmA) ||
+      !make_operand_map(h, B, N, K, dtype_in, ch.bn, &s.tmB))
+    return GEMM_ERR_CUDA;
+
+  GemmParams& p = s.p;
+  p.C = C;
+  p.M = (int32_t)M;
+  p.N = (int32_t)N;
+  p.K = (int32_t)K;
+  p.num_m_tiles = (int32_t)ch.num_m;
+  p.num_n_tiles = (int32_t)ch.num_n;
+  p.tiles = (int32_t)ch.tiles;
+  p.k_blocks = (int32_t)ch.k_blocks;
+  p.splits = ch.splits;
+  p.kb_per_split = ch.kb_per_split;
+  p.units = (int32_t)ch.units;
+  p.group_m = ch.group_m;
+  p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0) ? 1 : 0;
+  p.idesc = idesc_f16_kmajor(kBlockM, ch.bn, dtype_in == GEMM_BF16);
+  p.status = h->d_status;
+  p.wait_limit_ns = h->wait_limit_ns;
+  p.test_stall = h->test_stall;
+  if (ch.splits > 1) {
+    const size_t ws = (size_t)ch.tiles * ch.splits * kBlockM * ch.bn * sizeof(float);
+    st = ensure_workspace(h, ws, (size_t)ch.tiles * 4);
+    if (st != GEMM_OK) return st;
+    p.workspace = h->d_ws;
+    p.counters = h->d_ctr;
+  }
+  if (launch_one_cta(s) != cudaSuccess) return GEMM_ERR_CUDA;
+  h->last = gemm_config_t{ch.variant, ch.bn, ch.splits, ch.stages, ch.group_m, ch.grid, 0, 0};
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_device_status(gemm_handle_t h, gemm_stream_t stream_, uint32_t* detail) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, h->d_status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (detail) *detail = word;
+  if (word == 0) return GEMM_OK;
+  // An aborted split-K run may leave arrival counters behind: clear them too.
+  cudaMemset(h->d_status, 0, sizeof(uint32_t));
+  if (h->d_ctr) cudaMemset(h->d_ctr, 0, h->ctr_count * sizeof(uint32_t));
+  if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+  return GEMM_ERR_TIMEOUT;
+}
+
+gemm_status_t gemm_run_host(gemm_handle_t h, const void* A_host, const void* B_host, void* C_host,
+                            int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in,
+                            gemm_dtype_t dtype_out, gemm_stream_t stream_) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype_in) || !valid_dtype(dtype_out)) return GEMM_ERR_INVALID_ARG;
+  if (dtype_in == GEMM_F32) return GEMM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (!C_host || (K > 0 && (!A_host || !B_host))) return GEMM_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const size_t bytes[3] = {(size_t)M * K * 2, (size_t)N * K * 2, (size_t)M * N * out_size(dtype_out)};
+  for (int i = 0; i < 3; ++i) {
+    if (bytes[i] > h->stage_bytes[i]) {
+      if (h->d_stage[i]) cudaFree(h->d_stage[i]);
+      h->d_stage[i] = nullptr;
+      h->stage_bytes[i] = 0;
+      if (cudaMalloc(&h->d_stage[i], bytes[i]) != cudaSuccess) return GEMM_ERR_OOM;
+      h->stage_bytes[i] = bytes[i];
+    }
+  }
+  if (K > 0) {
+    if (cudaMemcpyAsync(h->d_stage[0], A_host, bytes[0], cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(h->d_stage[1], B_host, bytes[1], cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess)
+      return GEMM_ERR_CUDA;
+  }
+  gemm_status_t st = gemm_run(h, h->d_stage[0], h->d_stage[1], h->d_stage[2], M, N, K, dtype_in,
+                              dtype_out, stream_);
+  if (st != GEMM_OK) return st;
+  if (cudaMemcpyAsync(C_host, h->d_stage[2], bytes[2], cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return GEMM_ERR_CUDA;
+  return gemm_device_status(h, stream_, nullptr);
+}
+
+}  // extern "C"

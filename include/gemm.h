@@ -1,0 +1,145 @@
+/*
+ * gemm.h -- C ABI of libgemm.so, a GB300 (sm_103a) dense tensor-core GEMM.
+ *
+ *     C = A . B^T        A: M x K,  B: N x K,  C: M x N
+ *
+ * The operation is the one defined in "A Blackwell GEMM by Hand in CuTe DSL",
+ * section 1 (C_{MxN} = A_{MxK} B_{NxK}^T, both operands K-major), with fp16 or
+ * bf16 inputs, fp32 accumulation, and C written as fp16, bf16 or fp32
+ * (round-to-nearest-even from the fp32 accumulator).  The kernels are built
+ * from TMA, mbarriers, tcgen05.mma into Tensor Memory and warp specialisation
+ * (same page, sections 2-3 and 8; "Optimizing GEMMs using tcgen05 - Part 1").
+ *
+ * Layout.  All matrices are dense and row-major with no padding:
+ *   A[i][k] at A + (i*K + k) elements, B[j][k] at B + (j*K + k),
+ *   C[i][j] at C + (i*N + j).
+ * "K-major" means K is the contiguous dimension of A and B.
+ *
+ * Ownership.  The caller owns A, B and C (device memory unless stated), and
+ * keeps them alive until the work queued on `stream` has finished.  A handle
+ * owns its split-K workspace, its device status word, its tensor-map cache and
+ * the staging buffers of gemm_run_host.  One handle serves one host thread and
+ * one stream at a time: calls that overlap on the GPU through one handle race
+ * on its workspace.
+ *
+ * Errors.  Every call returns a gemm_status_t.  Argument problems are reported
+ * synchronously and nothing is launched.  gemm_run is asynchronous: a kernel
+ * whose internal wait ran out of time (a hang that was cut short) is reported
+ * later by gemm_device_status, which synchronises the stream.
+ */
+#ifndef GB300_GEMM_H
+#define GB300_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t (a CUstream); 0 / NULL is the legacy default stream. */
+typedef struct CUstream_st* gemm_stream_t;
+
+typedef struct gemm_ctx* gemm_handle_t;
+
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_F32 = 2 } gemm_dtype_t;
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad handle, bad config */
+  GEMM_ERR_UNSUPPORTED = 2, /* dtype combination, K % 8 != 0, pointer not 16-byte aligned,
+                               no sm_103 device */
+  GEMM_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
+  GEMM_ERR_OOM = 4,         /* device or host allocation failed */
+  GEMM_ERR_TIMEOUT = 5      /* a kernel wait exceeded its limit (see gemm_device_status) */
+} gemm_status_t;
+
+/*
+ * Kernel selection.  Zero in any field means "choose automatically".
+ *   variant   1 = one CTA per 128-row tile (cta_group::1)
+ *             2 = a CTA pair per 256-row tile (cta_group::2, cluster of 2)
+ *   block_n   128 or 256 columns of C per tile
+ *   splits    K slices per tile (1 = no split; >1 = split-K with a deterministic
+ *             in-kernel reduction in slice order)
+ *   stages    depth of the shared-memory operand ring
+ *   group_m   grouped rasterisation: M tiles per group
+ *   max_ctas  cap on the persistent grid (0 = one CTA per SM)
+ */
+typedef struct {
+  int32_t variant;
+  int32_t block_n;
+  int32_t splits;
+  int32_t stages;
+  int32_t group_m;
+  int32_t max_ctas;
+  int32_t reserved0;
+  int32_t reserved1;
+} gemm_config_t;
+
+/* Create a handle on the current CUDA device.  Fails with GEMM_ERR_UNSUPPORTED
+ * if that device is not compute capability 10.3.  *out is NULL on failure. */
+gemm_status_t gemm_create(gemm_handle_t* out);
+
+/* Release a handle and everything it owns.  Synchronises the device first.
+ * NULL is accepted and ignored. */
+gemm_status_t gemm_destroy(gemm_handle_t h);
+
+/*
+ * Queue C = A . B^T on `stream`.
+ *   A, B, C     device pointers, 16-byte aligned, layouts as above.
+ *   M, N, K     sizes >= 0.  M == 0 or N == 0 is a no-op; K == 0 writes C = 0.
+ *               K must be a multiple of 8 (TMA rows must be 16-byte multiples).
+ *   dtype_in    GEMM_F16 or GEMM_BF16 (A and B share it).
+ *   dtype_out   GEMM_F16, GEMM_BF16 or GEMM_F32.
+ * Neither allocates on the steady path nor synchronises: the split-K workspace
+ * grows on the first call that needs more of it (an allocation, outside any
+ * stream capture you may be doing, so warm a shape up first).
+ */
+gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M,
+                       int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                       gemm_stream_t stream);
+
+/*
+ * The same product with HOST buffers: copies A and B to device staging buffers
+ * owned by the handle, runs the GEMM and copies C back, all on `stream`, then
+ * synchronises `stream` and reports kernel timeouts like gemm_device_status.
+ * Page-locked host memory makes the copies asynchronous DMA; pageable memory
+ * works but is slower.
+ */
+gemm_status_t gemm_run_host(gemm_handle_t h, const void* A_host, const void* B_host, void* C_host,
+                            int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in,
+                            gemm_dtype_t dtype_out, gemm_stream_t stream);
+
+/* Force a kernel configuration for later runs (NULL restores automatic choice).
+ * Invalid combinations are rejected here with GEMM_ERR_INVALID_ARG; a forced
+ * choice that cannot serve a given shape makes gemm_run fail the same way. */
+gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg);
+
+/* The configuration the last successful gemm_run on this handle launched. */
+gemm_status_t gemm_last_config(gemm_handle_t h, gemm_config_t* out);
+
+/* Synchronise `stream`, read and clear the handle's device status word.
+ * Returns GEMM_ERR_TIMEOUT if a kernel gave up waiting since the last call
+ * (the output of that run is undefined), else GEMM_OK.  *detail, if non-NULL,
+ * receives the raw word (code << 24 | wait site << 16 | block index). */
+gemm_status_t gemm_device_status(gemm_handle_t h, gemm_stream_t stream, uint32_t* detail);
+
+/* Upper bound, in nanoseconds, on any single wait inside the kernels (default
+ * 2 s).  Must be > 0. */
+gemm_status_t gemm_set_wait_limit(gemm_handle_t h, uint64_t ns);
+
+/* Test hook: when enabled, the MMA-issuing thread of every CTA first waits on
+ * a barrier that nothing ever arrives on, so the wait limit runs out and the
+ * run ends with GEMM_ERR_TIMEOUT instead of a result.  Off by default. */
+gemm_status_t gemm_set_test_stall(gemm_handle_t h, int32_t enable);
+
+/* Number of SMs of the handle's device. */
+int32_t gemm_sm_count(gemm_handle_t h);
+
+/* Static description of a status code; never NULL. */
+const char* gemm_status_string(gemm_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_GEMM_H */

@@ -1,0 +1,119 @@
+"""Comparison rules between the CUDA path and the CPU oracle (tests only).
+
+Tolerances (the GEMM's stated bar):
+  * fp16 / bf16 C: every element within 1 unit in the last place of the
+    oracle's correctly rounded value: |ord(gpu) - ord(oracle)| <= 1, where ord
+    maps a bit pattern to a monotone integer (+0 and -0 both map to 0).
+  * fp32 C: relative Frobenius error <= 1e-5 and max abs error <= 1e-2.
+  * integer-valued inputs (every partial sum exact in fp32): bit-exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import seeded_inputs as si
+
+F16, BF16, F32 = 0, 1, 2
+FRO_TOL = 1e-5
+ABS_TOL = 1e-2
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    """Bit patterns of a (CPU or CUDA) fp16/bf16/fp32 tensor as uint16/uint32."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.float32:
+        return t.view(torch.int32).numpy().view(np.uint32)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def ordinal(bits: np.ndarray) -> np.ndarray:
+    b = bits.astype(np.int64)
+    sign = np.int64(1) << (8 * bits.dtype.itemsize - 1)
+    mag = b & (sign - 1)
+    return np.where(b & sign, -mag, mag)
+
+
+def ulp_distance(got_bits: np.ndarray, want_bits: np.ndarray) -> np.ndarray:
+    return np.abs(ordinal(got_bits) - ordinal(want_bits))
+
+
+def check(got_bits: np.ndarray, want_bits: np.ndarray, dtype_out: int, exact: bool = False,
+          what: str = ""):
+    """Assert the stated tolerance; returns a dict of error metrics."""
+    assert got_bits.shape == want_bits.shape, (got_bits.shape, want_bits.shape)
+    if exact:
+        bad = np.argwhere(got_bits != want_bits)
+        assert bad.size == 0, f"{what}: {len(bad)} elements differ bitwise, first at {bad[:5]}"
+        return {"max_ulp": 0}
+    if dtype_out == F32:
+        g = got_bits.view(np.float32).astype(np.float64)
+        w = want_bits.view(np.float32).astype(np.float64)
+        assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+        err = g - w
+        fro = float(np.linalg.norm(err) / max(np.linalg.norm(w), 1e-300))
+        mx = float(np.max(np.abs(err))) if err.size else 0.0
+        assert fro <= FRO_TOL and mx <= ABS_TOL, f"{what}: rel fro {fro:.3g}, max abs {mx:.3g}"
+        return {"rel_fro": fro, "max_abs": mx}
+    d = ulp_distance(got_bits, want_bits)
+    mx = int(d.max()) if d.size else 0
+    if mx > 1:
+        idx = np.unravel_index(int(np.argmax(d)), d.shape)
+        raise AssertionError(f"{what}: {int((d > 1).sum())} elements beyond 1 ulp; worst {mx} ulp "
+                             f"at {idx}")
+    return {"max_ulp": mx, "frac_off_by_one": float((d == 1).mean()) if d.size else 0.0}
+
+
+def oracle_full(A, B, dtype_in, dtype_out):
+    return oracle.gemm(A, B, dtype_in, dtype_out)
+
+
+def run_gpu(g, A, B, dtype_out, device="cuda"):
+    """Copy the CPU operands to the device, run the library, return C's bits."""
+    Ad, Bd = A.to(device), B.to(device)
+    C = torch.empty(A.shape[0], B.shape[0], dtype=si.TORCH_DTYPE[dtype_out], device=device)
+    g.run(Ad, Bd, C)
+    torch.cuda.synchronize()
+    return C
+
+
+def freivalds(A, B, C_gpu, dtype_out, seeds=(0, 1, 2)):
+    """Freivalds' check in float64 on the host: for x in {+-1}^N,
+    |C x - A (B^T x)|_i <= sum_j (ulp_out(C_ij)/2 + gamma sum_k |A_ik B_jk|),
+    gamma = K 2^-24 (worst-case fp32 accumulation).  Processes rows in chunks."""
+    M, K = A.shape
+    N = B.shape[0]
+    gamma = K * 2.0 ** -24
+    colsum_absB = torch.zeros(K, dtype=torch.float64)
+    for j0 in range(0, N, 4096):
+        colsum_absB += B[j0:j0 + 4096].to(torch.float64).abs().sum(0)
+    xs = [si.rademacher(N, s) for s in seeds]
+    btx = [torch.zeros(K, dtype=torch.float64) for _ in xs]
+    for j0 in range(0, N, 4096):
+        Bc = B[j0:j0 + 4096].to(torch.float64)
+        for t, x in enumerate(xs):
+            btx[t] += x[j0:j0 + 4096] @ Bc
+    worst = 0.0
+    Cc = C_gpu
+    for i0 in range(0, M, 1024):
+        Ac = A[i0:i0 + 1024].to(torch.float64)
+        Cr = Cc[i0:i0 + 1024].cpu().to(torch.float64)
+        assert torch.isfinite(Cr).all(), "non-finite output"
+        mag = Cr.abs()
+        if dtype_out == F32:
+            half_ulp = torch.ldexp(torch.ones_like(mag), torch.floor(torch.log2(mag.clamp_min(2.0 ** -126))).to(torch.int32) - 24)
+        else:
+            frac = 10 if dtype_out == F16 else 7
+            emin = -14 if dtype_out == F16 else -126
+            e = torch.floor(torch.log2(mag.clamp_min(2.0 ** emin))).to(torch.int32)
+            half_ulp = torch.ldexp(torch.ones_like(mag), e - frac - 1)
+        bound = half_ulp.sum(1) + gamma * (Ac.abs() @ colsum_absB)
+        for t, x in enumerate(xs):
+            y = Cr @ x
+            z = Ac @ btx[t]
+            r = (y - z).abs() / bound
+            worst = max(worst, float(r.max()))
+            bad = torch.nonzero(r > 1.0)
+            assert bad.numel() == 0, f"Freivalds failed at rows {(bad[:5].flatten() + i0).tolist()}"
+    return worst

@@ -1,0 +1,187 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, element by
+element, at sizes the oracle finishes in seconds: several tiles, ragged tails,
+ring wrap-around, split-K, persistent scheduling, every dtype pair."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+F16, BF16, F32 = 0, 1, 2
+TD = si.TORCH_DTYPE
+
+
+@pytest.fixture(scope="module")
+def g():
+    from dense_gemm_blackwell_02_gb300.binding import Gemm
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    h = Gemm()
+    yield h
+    h.close()
+
+
+def _case(g, M, N, K, dtype_in, dtype_out, dist="uniform", seed=0, exact=False, ints=False):
+    if ints:
+        A, B = si.make_small_int_operands(M, N, K, dtype_in, seed=seed)
+    else:
+        A, B = si.make_operands(M, N, K, dtype_in, dist, seed)
+    C = parity.run_gpu(g, A, B, dtype_out)
+    want = oracle.gemm(A, B, dtype_in, dtype_out)
+    st = g.device_status()
+    assert st[0] == 0, f"device status {st}"
+    return parity.check(parity.bits_of(C), want, dtype_out, exact=exact,
+                        what=f"M={M} N={N} K={K} in={dtype_in} out={dtype_out} {g.last_config()}")
+
+
+def test_small_256_config(g):
+    # 256^3, fp16 in, fp32 out, U[-1,1] from seed 0 (the small workload)
+    wl = si.WORKLOADS["small_256"]
+    s = wl.shapes[0]
+    _case(g, s.M, s.N, s.K, wl.dtype_in, wl.dtype_out, wl.dist, wl.seed)
+
+
+@pytest.mark.parametrize("dtype_in", [F16, BF16])
+@pytest.mark.parametrize("dtype_out", [F16, BF16, F32])
+def test_dtype_pairs(g, dtype_in, dtype_out):
+    g.reset_config()
+    _case(g, 384, 640, 512, dtype_in, dtype_out, "uniform", seed=21)
+
+
+@pytest.mark.parametrize("dtype_in", [F16, BF16])
+@pytest.mark.parametrize("dtype_out", [F16, BF16, F32])
+def test_small_integers_bit_exact(g, dtype_in, dtype_out):
+    g.reset_config()
+    _case(g, 300, 520, 1000, dtype_in, dtype_out, seed=22, exact=True, ints=True)
+
+
+# K around the ring depth S = 4 (BN 256) and 6 (BN 128): K = 64 S - 64 never recycles a
+# stage, 64 S exactly fills the ring once, 64 S + 64 recycles; plus K tails < 64.
+@pytest.mark.parametrize("K", [8, 56, 64, 72, 192, 256, 320, 384, 448, 1000, 2048])
+def test_k_edges(g, K):
+    g.reset_config()
+    _case(g, 256, 512, K, F16, F32, seed=23)
+
+
+@pytest.mark.parametrize("M,N", [(1, 1), (1, 256), (127, 255), (129, 257), (200, 300),
+                                 (1000, 3000), (130, 4097), (513, 8)])
+def test_ragged_shapes(g, M, N):
+    g.reset_config()
+    _case(g, M, N, 128, BF16, F32, seed=24)
+    _case(g, M, N, 136, F16, F16, seed=25)
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_forced_tiles_and_splits(g, bn, splits):
+    g.set_config(variant=1, block_n=bn, splits=splits)
+    try:
+        _case(g, 300, 700, 1024, F16, F32, seed=26)
+        _case(g, 256, 512, 960, BF16, BF16, seed=27)
+        cfg = g.last_config()
+        kb = 960 // 64                       # k-blocks of the last case
+        per = -(-kb // splits)
+        assert cfg["block_n"] == bn and cfg["splits"] == -(-kb // per)
+    finally:
+        g.reset_config()
+
+
+@pytest.mark.parametrize("max_ctas", [1, 2, 5, 37])
+def test_persistent_loops_many_units_per_cta(g, max_ctas):
+    # few CTAs: each walks many tiles, so both accumulator slots and the operand
+    # ring go through many phases
+    g.set_config(max_ctas=max_ctas, group_m=3)
+    try:
+        _case(g, 640, 1280, 704, F16, F16, seed=28)
+    finally:
+        g.reset_config()
+
+
+def test_split_k_small_ints_exact_and_deterministic(g):
+    g.set_config(splits=5)
+    try:
+        A, B = si.make_small_int_operands(256, 768, 2048, BF16, seed=29)
+        C1 = parity.run_gpu(g, A, B, F32)
+        C2 = parity.run_gpu(g, A, B, F32)
+        want = oracle.gemm(A, B, BF16, F32)
+        parity.check(parity.bits_of(C1), want, F32, exact=True, what="split-K ints")
+        assert torch.equal(C1.view(torch.int32), C2.view(torch.int32))
+        # non-integer inputs: run to run identical bits (fixed slice order)
+        A, B = si.make_operands(256, 768, 2048, F16, "uniform", 30)
+        C3 = parity.run_gpu(g, A, B, F32)
+        C4 = parity.run_gpu(g, A, B, F32)
+        assert torch.equal(C3.view(torch.int32), C4.view(torch.int32))
+    finally:
+        g.reset_config()
+
+
+def test_all_ones_and_identity(g):
+    for dt in (F16, BF16):
+        K = 4096
+        A = torch.ones(130, K, dtype=TD[dt])
+        B = torch.ones(260, K, dtype=TD[dt])
+        C = parity.run_gpu(g, A, B, F32)
+        assert torch.all(C == K)
+        C = parity.run_gpu(g, A, B, dt)
+        assert torch.all(C.float() == K)
+        A, _ = si.make_operands(200, 1, 512, dt, "uniform", 31)
+        I = torch.eye(512, dtype=TD[dt])
+        C = parity.run_gpu(g, A, I, dt)
+        assert torch.equal(C.cpu().view(torch.int16), A.view(torch.int16))
+
+
+def test_rank1_exact(g):
+    M, N, K = 192, 320, 512
+    gen = torch.Generator().manual_seed(32)
+    u = 2.0 ** torch.randint(-3, 4, (M,), generator=gen).double()
+    v = 2.0 ** torch.randint(-3, 4, (N,), generator=gen).double()
+    a = torch.randint(-3, 4, (K,), generator=gen).double()
+    b = torch.randint(-3, 4, (K,), generator=gen).double()
+    A = (u[:, None] * a[None]).to(torch.bfloat16)
+    B = (v[:, None] * b[None]).to(torch.bfloat16)
+    C = parity.run_gpu(g, A, B, F32).cpu().double()
+    assert torch.equal(C, u[:, None] * v[None] * float((a * b).sum()))
+
+
+def test_k_zero_and_empty(g):
+    C = torch.full((5, 7), 3.0, device="cuda")
+    A = torch.empty(5, 0, dtype=torch.float16, device="cuda")
+    B = torch.empty(7, 0, dtype=torch.float16, device="cuda")
+    g.run(A, B, C)
+    torch.cuda.synchronize()
+    assert torch.all(C == 0)
+    A = torch.empty(0, 64, dtype=torch.float16, device="cuda")
+    B = torch.ones(7, 64, dtype=torch.float16, device="cuda")
+    C = torch.empty(0, 7, device="cuda")
+    g.run(A, B, C)
+
+
+def test_rejections(g):
+    from dense_gemm_blackwell_02_gb300.binding import GemmError
+    A = torch.ones(64, 60, dtype=torch.float16, device="cuda")
+    B = torch.ones(64, 60, dtype=torch.float16, device="cuda")
+    C = torch.empty(64, 64, device="cuda")
+    with pytest.raises(GemmError) as e:        # K % 8 != 0
+        g.run(A, B, C)
+    assert e.value.code == 2
+    base = torch.ones(64 * 64 + 8, dtype=torch.float16, device="cuda")
+    A = base[4:4 + 64 * 64].view(64, 64)       # 8-byte aligned only
+    B = torch.ones(64, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(GemmError) as e:
+        g.run(A, B, C)
+    assert e.value.code == 2
+    assert g.run_ptr(0, B.data_ptr(), C.data_ptr(), 64, 64, 64, 0, 2, 0) == 1
+    assert g.run_ptr(B.data_ptr(), B.data_ptr(), C.data_ptr(), -1, 64, 64, 0, 2, 0) == 1
+    assert g.run_ptr(B.data_ptr(), B.data_ptr(), C.data_ptr(), 64, 64, 64, 2, 2, 0) == 2
+    assert g.run_ptr(B.data_ptr(), B.data_ptr(), C.data_ptr(), 64, 64, 64, 0, 7, 0) == 1
+
+
+def test_run_host_matches_device(g):
+    A, B = si.make_operands(300, 500, 256, F16, "uniform", 33)
+    Cd = parity.run_gpu(g, A, B, F16)
+    Ch = torch.empty(300, 500, dtype=torch.float16).pin_memory()
+    g.run_host(A.pin_memory(), B.pin_memory(), Ch, F16, F16)
+    assert torch.equal(Ch.view(torch.int16), Cd.cpu().view(torch.int16))
