@@ -12,6 +12,7 @@ from __future__ import annotations
 import argparse
 import glob
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -21,8 +22,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-BUILD_DIR = os.path.join(PKG, "_build")
+BUILD_DIR = os.path.join(PKG, "_build", platform.machine())
 LIB = os.path.join(PKG, "libgemm.so")
+STAMP = LIB + ".arch"  # host architecture the library was built on
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -60,7 +62,8 @@ def _stale(target, deps) -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     srcs = _sources()
     headers = _headers()
-    if not force and not _stale(LIB, srcs + headers + [__file__]):
+    same_arch = os.path.exists(STAMP) and open(STAMP).read().strip() == platform.machine()
+    if not force and same_arch and not _stale(LIB, srcs + headers + [__file__]):
         return LIB
     os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
@@ -85,6 +88,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(platform.machine())
     return LIB
 
 

@@ -28,6 +28,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 
 import numpy as np
@@ -41,7 +42,9 @@ _lib = None
 
 def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so next to it (gcc, no GPU needed)."""
-    if (not force and os.path.exists(_LIB_PATH)
+    stamp = _LIB_PATH + ".arch"
+    same_arch = os.path.exists(stamp) and open(stamp).read().strip() == platform.machine()
+    if (not force and same_arch and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
@@ -49,6 +52,8 @@ def build(force: bool = False) -> str:
            _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
+    with open(stamp, "w") as f:
+        f.write(platform.machine())
     return _LIB_PATH
 
 
