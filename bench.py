@@ -142,9 +142,9 @@ def cpu_rows_sample(A, B, din, dout, M, target_s=10.0):
     nrows = int(min(M, max(32, len(probe) * target_s / t)))
     rows = si.sample_indices(M, nrows, seed=7, must=(0, 127, 128, 255, 256, -1))
     t0 = time.perf_counter()
-    bits = oracle.gemm_select(A, B, rows, None, din, dout)
+    bits, c64 = oracle.gemm_select(A, B, rows, None, din, dout, want_f64=True)
     dt = time.perf_counter() - t0
-    return rows, bits, dt, os.cpu_count()
+    return rows, bits, c64, dt, os.cpu_count()
 
 
 def run_reference(args):
@@ -273,10 +273,11 @@ def run_ours(args):
         # ---- CPU oracle on whole rows: the cpu_baseline, and a full-size parity check
         import numpy as np
         from tests import parity as par
-        rows, want, cpu_s, threads = cpu_rows_sample(A_cpu, B_cpu, din, dout, M,
-                                                      target_s=args.cpu_seconds)
+        rows, want, c64, cpu_s, threads = cpu_rows_sample(A_cpu, B_cpu, din, dout, M,
+                                                           target_s=args.cpu_seconds)
         got = par.bits_of(C[rows])
-        metrics = par.check(got, want, dout, what="bench rows")
+        metrics = par.check(got, want, dout, what="bench rows", c64=c64,
+                            sigma=par.sigma_of(A_cpu, B_cpu, rows), K=K)
         e2e_rows = par.bits_of(C_h[rows])
         assert np.array_equal(e2e_rows, got), "gemm_run_host disagrees with gemm_run"
         cpu_value = 2.0 * len(rows) * N * K / cpu_s / 1e12

@@ -2,9 +2,17 @@
 
 Tolerances (the GEMM's stated bar):
   * fp16 / bf16 C: every element within 1 unit in the last place of the
-    oracle's correctly rounded value: |ord(gpu) - ord(oracle)| <= 1, where ord
+    oracle's correctly rounded value, |ord(gpu) - ord(oracle)| <= 1, where ord
     maps a bit pattern to a monotone integer (+0 and -0 both map to 0).
-  * fp32 C: relative Frobenius error <= 1e-5 and max abs error <= 1e-2.
+    Reading for elements whose exact value nearly cancels: there an output ulp
+    is smaller than any fp32 accumulator's rounding error, so such an element
+    instead passes when |gpu - exact| <= ulp_out(exact)/2 + tau, with
+    tau = 8 * 2^-24 * sqrt(K) * sigma,  sigma = sqrt(sum_k (a_ik b_jk)^2)
+    (a random walk of K fp32 roundings of partial sums of size ~sigma, with a
+    factor 8 of headroom).  For typical elements tau is far below half an
+    output ulp, so the 1-ulp rule is what binds.
+  * fp32 C: relative Frobenius error <= 1e-5 and max abs error <= 1e-2, and
+    every element within ulp/2 + tau of the exact sum.
   * integer-valued inputs (every partial sum exact in fp32): bit-exact.
 """
 from __future__ import annotations
@@ -39,30 +47,88 @@ def ulp_distance(got_bits: np.ndarray, want_bits: np.ndarray) -> np.ndarray:
     return np.abs(ordinal(got_bits) - ordinal(want_bits))
 
 
+def _decode(bits: np.ndarray, dtype_out: int) -> np.ndarray:
+    if dtype_out == F32:
+        return bits.view(np.float32).astype(np.float64)
+    t = torch.from_numpy(bits.view(np.int16).copy())
+    return t.view(torch.float16 if dtype_out == F16 else torch.bfloat16).double().numpy()
+
+
+def ulp_of(x: np.ndarray, dtype_out: int) -> np.ndarray:
+    """Spacing of the output format at |x| (subnormal spacing below the normal range)."""
+    frac, emin = {F16: (10, -14), BF16: (7, -126), F32: (23, -126)}[dtype_out]
+    mag = np.maximum(np.abs(x), 2.0 ** emin)
+    return np.exp2(np.floor(np.log2(mag)) - frac)
+
+
+def sigma_of(A, B, rows=None) -> np.ndarray:
+    """sqrt(sum_k (a_ik b_jk)^2) for the selected rows (float64 on the host)."""
+    a = A if rows is None else A[rows]
+    a2 = a.to(torch.float64).square()
+    out = torch.empty(a.shape[0], B.shape[0], dtype=torch.float64)
+    for j0 in range(0, B.shape[0], 8192):
+        out[:, j0:j0 + 8192] = a2 @ B[j0:j0 + 8192].to(torch.float64).square().T
+    return out.sqrt().numpy()
+
+
+def tau_of(sigma: np.ndarray, K: int) -> np.ndarray:
+    return 8.0 * 2.0 ** -24 * np.sqrt(max(K, 1)) * sigma
+
+
 def check(got_bits: np.ndarray, want_bits: np.ndarray, dtype_out: int, exact: bool = False,
-          what: str = ""):
-    """Assert the stated tolerance; returns a dict of error metrics."""
+          what: str = "", c64: np.ndarray = None, sigma: np.ndarray = None, K: int = None):
+    """Assert the stated tolerance; returns a dict of error metrics.
+
+    want_bits: the oracle's rounded output; c64: its unrounded binary64 sums;
+    sigma/K: the accumulation scale for the cancellation reading above."""
     assert got_bits.shape == want_bits.shape, (got_bits.shape, want_bits.shape)
     if exact:
         bad = np.argwhere(got_bits != want_bits)
         assert bad.size == 0, f"{what}: {len(bad)} elements differ bitwise, first at {bad[:5]}"
         return {"max_ulp": 0}
+    g = _decode(got_bits, dtype_out)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    out = {}
     if dtype_out == F32:
-        g = got_bits.view(np.float32).astype(np.float64)
-        w = want_bits.view(np.float32).astype(np.float64)
-        assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+        w = _decode(want_bits, dtype_out)
         err = g - w
         fro = float(np.linalg.norm(err) / max(np.linalg.norm(w), 1e-300))
         mx = float(np.max(np.abs(err))) if err.size else 0.0
         assert fro <= FRO_TOL and mx <= ABS_TOL, f"{what}: rel fro {fro:.3g}, max abs {mx:.3g}"
-        return {"rel_fro": fro, "max_abs": mx}
-    d = ulp_distance(got_bits, want_bits)
-    mx = int(d.max()) if d.size else 0
-    if mx > 1:
-        idx = np.unravel_index(int(np.argmax(d)), d.shape)
-        raise AssertionError(f"{what}: {int((d > 1).sum())} elements beyond 1 ulp; worst {mx} ulp "
-                             f"at {idx}")
-    return {"max_ulp": mx, "frac_off_by_one": float((d == 1).mean()) if d.size else 0.0}
+        out.update({"rel_fro": fro, "max_abs": mx})
+        d = None
+    else:
+        d = ulp_distance(got_bits, want_bits)
+        out.update({"max_ulp": int(d.max()) if d.size else 0,
+                    "frac_beyond_1ulp": float((d > 1).mean()) if d.size else 0.0})
+    if c64 is not None and sigma is not None:
+        bound = ulp_of(c64, dtype_out) / 2 + tau_of(sigma, K)
+        err = np.abs(g - c64)
+        ok = err <= bound
+        if d is not None:
+            ok |= d <= 1
+        if not ok.all():
+            idx = np.argwhere(~ok)[:5]
+            detail = [(tuple(int(v) for v in ij), float(c64[tuple(ij)]), float(g[tuple(ij)]),
+                       float(bound[tuple(ij)])) for ij in idx]
+            raise AssertionError(f"{what}: {int((~ok).sum())} elements outside tolerance; "
+                                 f"(index, exact, gpu, bound): {detail}")
+        out["max_err_over_tau"] = float((err / tau_of(sigma, K)).max()) if err.size else 0.0
+    elif d is not None and out["max_ulp"] > 1:
+        raise AssertionError(f"{what}: elements beyond 1 ulp and no cancellation data given")
+    return out
+
+
+def oracle_check(got_bits, A, B, dtype_in, dtype_out, rows=None, cols=None, what="",
+                 exact=False):
+    """Oracle on the same inputs (optionally selected rows/cols), then check()."""
+    want, c64 = oracle.gemm_select(A, B, rows, cols, dtype_in, dtype_out, want_f64=True)
+    if exact:
+        return check(got_bits, want, dtype_out, exact=True, what=what)
+    sig = sigma_of(A, B, rows)
+    if cols is not None:
+        sig = sig[:, cols]
+    return check(got_bits, want, dtype_out, what=what, c64=c64, sigma=sig, K=A.shape[1])
 
 
 def oracle_full(A, B, dtype_in, dtype_out):
