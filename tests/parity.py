@@ -113,7 +113,11 @@ def check(got_bits: np.ndarray, want_bits: np.ndarray, dtype_out: int, exact: bo
                        float(bound[tuple(ij)])) for ij in idx]
             raise AssertionError(f"{what}: {int((~ok).sum())} elements outside tolerance; "
                                  f"(index, exact, gpu, bound): {detail}")
-        out["max_err_over_tau"] = float((err / tau_of(sigma, K)).max()) if err.size else 0.0
+        # how close the worst element came to its bound (<= 1 passes)
+        rel = err / bound
+        if d is not None:
+            rel = np.where(d <= 1, 0.0, rel)
+        out["max_err_over_bound"] = float(rel.max()) if rel.size else 0.0
     elif d is not None and out["max_ulp"] > 1:
         raise AssertionError(f"{what}: elements beyond 1 ulp and no cancellation data given")
     return out
