@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgemm.so"
 # Every function include/gemm.h declares (checked against the header by the tests).
 EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "gemm_set_config",
            "gemm_last_config", "gemm_device_status", "gemm_set_wait_limit",
-           "gemm_set_test_stall", "gemm_sm_count", "gemm_status_string")
+           "gemm_set_test_stall", "gemm_sm_count", "gemm_status_string", "gemm_run_noalloc")
 
 
 class GemmConfig(ctypes.Structure):
@@ -59,6 +59,7 @@ def lib():
     L.gemm_set_test_stall.argtypes = [vp, i32]
     L.gemm_sm_count.argtypes = [vp]
     L.gemm_sm_count.restype = i32
+    L.gemm_run_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i32, i32, vp]
     L.gemm_status_string.argtypes = [i32]
     L.gemm_status_string.restype = ctypes.c_char_p
     for name in EXPORTS:

@@ -138,6 +138,41 @@ int32_t gemm_sm_count(gemm_handle_t h);
 /* Static description of a status code; never NULL. */
 const char* gemm_status_string(gemm_status_t s);
 
+/*
+ * gemm_run_noalloc -- the same product for callers that cannot allocate device
+ * memory.  The pages have no counterpart of this call; it exists for users of
+ * this library, not for the method.
+ *
+ * Who needs it: code that must not call cudaMalloc, such as a custom device
+ * allocator or memory pool that wants a GEMM (cudaMalloc would recurse into it
+ * or escape its budget), a plug-in whose framework owns every device
+ * allocation, or a process that has reserved its device memory up front.
+ * gemm_run needs a handle (gemm_create allocates) and grows a workspace on
+ * demand; this call needs neither and allocates nothing, host or device.
+ *
+ * Scratch: a fixed static device array of GEMM_NOALLOC_SCRATCH_BYTES bytes in
+ * the library, which every GPU that loads the library holds until the process
+ * exits.  It carries a status word, split-K arrival counters and up to
+ * GEMM_NOALLOC_WORKSPACE_BYTES of fp32 partial tiles.  The first call on a
+ * device looks up the array's address on that device (cudaGetSymbolAddress),
+ * so make that first call before any stream capture.  Every call shares the
+ * array: each call clears the parts it relies on, on `stream`, and calls whose
+ * work overlaps on the GPU race on it -- order them on one stream.
+ *
+ * Arguments, layouts and argument errors are those of gemm_run (no handle).
+ * The kernel is gemm_run's one-CTA split-K kernel with 256-column tiles; when
+ * fewer tiles than half the SMs exist, K is sliced.  A product whose slices
+ * would need more than GEMM_NOALLOC_WORKSPACE_BYTES of partial tiles is
+ * refused with GEMM_ERR_UNSUPPORTED before anything is queued.  The call is
+ * asynchronous; a kernel wait that runs out of time leaves C undefined and is
+ * not reported (gemm_run with gemm_device_status reports it).
+ */
+#define GEMM_NOALLOC_WORKSPACE_BYTES (16u << 20)
+#define GEMM_NOALLOC_SCRATCH_BYTES (256u + 65536u + GEMM_NOALLOC_WORKSPACE_BYTES)
+gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                               int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                               gemm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,74 @@
+"""gemm_run_noalloc: the GEMM entry point for callers that cannot allocate.
+
+Some callers may not call cudaMalloc (a custom device allocator or pool that
+needs a GEMM, a plug-in whose framework owns all device memory, a process that
+reserved its memory up front).  gemm_run_noalloc keeps its scratch in a fixed
+static device array instead.  These tests call it through the C ABI and check
+that it gives the same answer as gemm_run, within the tolerance the other
+parity tests use, on two calls in a row (the second reuses the array the first
+left behind), and that it refuses a product whose scratch would not fit.
+
+This file is named so that pytest collects it last.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import seeded_inputs as si
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+F16, BF16, F32 = 0, 1, 2
+
+
+def _noalloc(A, B, C, din, dout):
+    from dense_gemm_blackwell_02_gb300 import binding
+    M, K = A.shape
+    N = B.shape[0]
+    stream = torch.cuda.current_stream().cuda_stream
+    return binding.lib().gemm_run_noalloc(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                                          din, dout, ctypes.c_void_p(stream))
+
+
+# Shapes with fewer tiles than half the SMs, so K is sliced and the scratch is used.
+CASES = [(256, 512, 4096, F16, F32), (300, 700, 2048, BF16, BF16), (128, 256, 8192, F16, F16)]
+
+
+@pytest.mark.parametrize("M,N,K,din,dout", CASES)
+def test_noalloc_matches_gemm_run_on_two_calls(M, N, K, din, dout):
+    from dense_gemm_blackwell_02_gb300.binding import Gemm
+    assert torch.cuda.is_available()
+    A, B = si.make_operands(M, N, K, din, "uniform", seed=77)
+    Ad, Bd = A.cuda(), B.cuda()
+    td = si.TORCH_DTYPE[dout]
+    with Gemm() as g:
+        ref = torch.empty(M, N, dtype=td, device="cuda")
+        g.run(Ad, Bd, ref)
+        code, word = g.device_status()
+        assert code == 0, word
+        assert g.last_config()["splits"] > 1, "case does not exercise the scratch"
+    ref_bits = parity.bits_of(ref)
+    for call in range(2):
+        C = torch.full((M, N), float("nan"), dtype=td, device="cuda")
+        assert _noalloc(Ad, Bd, C, din, dout) == 0
+        torch.cuda.synchronize()
+        got = parity.bits_of(C)
+        # against gemm_run's result: the fp32 rule, or at most 1 ulp for fp16/bf16 ...
+        if dout == F32:
+            parity.check(got, ref_bits, F32, what=f"noalloc vs gemm_run, call {call}")
+        else:
+            assert parity.ulp_distance(got, ref_bits).max() <= 1, f"call {call}"
+        # ... and against the oracle
+        parity.oracle_check(got, A, B, din, dout, what=f"noalloc vs oracle, call {call}")
+
+
+def test_noalloc_refuses_products_beyond_its_scratch():
+    # 16 tiles, K sliced 9 ways: 16 x 9 x 128 x 256 x 4 B = 18.9 MB > 16 MiB
+    M, N, K = 256, 2048, 16384
+    A = torch.zeros(M, K, dtype=torch.float16, device="cuda")
+    B = torch.zeros(N, K, dtype=torch.float16, device="cuda")
+    C = torch.zeros(M, N, dtype=torch.float32, device="cuda")
+    assert _noalloc(A, B, C, F16, F32) == 2          # GEMM_ERR_UNSUPPORTED
+    assert _noalloc(A, B, C, F16, 7) == 1            # bad dtype: GEMM_ERR_INVALID_ARG
