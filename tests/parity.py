@@ -129,9 +129,8 @@ def oracle_check(got_bits, A, B, dtype_in, dtype_out, rows=None, cols=None, what
     want, c64 = oracle.gemm_select(A, B, rows, cols, dtype_in, dtype_out, want_f64=True)
     if exact:
         return check(got_bits, want, dtype_out, exact=True, what=what)
-    sig = sigma_of(A, B, rows)
-    if cols is not None:
-        sig = sig[:, cols]
+    Bs = B if cols is None else B[list(cols)]
+    sig = sigma_of(A, Bs, rows)
     return check(got_bits, want, dtype_out, what=what, c64=c64, sigma=sig, K=A.shape[1])
 
 
