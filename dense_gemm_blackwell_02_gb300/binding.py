@@ -22,7 +22,8 @@ EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "gemm_set
 
 class GemmConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("variant", "block_n", "splits", "stages",
-                                                "group_m", "max_ctas", "reserved0", "reserved1")]
+                                                "group_m", "max_ctas", "chain_kblocks",
+                                                "reserved")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_ if not n.startswith("reserved")}
@@ -158,8 +159,9 @@ class Gemm:
         return C
 
     # ----------------------------------------------------------------- control --
-    def set_config(self, variant=0, block_n=0, splits=0, stages=0, group_m=0, max_ctas=0):
-        cfg = GemmConfig(variant, block_n, splits, stages, group_m, max_ctas, 0, 0)
+    def set_config(self, variant=0, block_n=0, splits=0, stages=0, group_m=0, max_ctas=0,
+                   chain_kblocks=0):
+        cfg = GemmConfig(variant, block_n, splits, stages, group_m, max_ctas, chain_kblocks, 0)
         _check(lib().gemm_set_config(self._h, ctypes.byref(cfg)), "gemm_set_config")
 
     def reset_config(self):

@@ -54,6 +54,7 @@ struct gemm_ctx {
   int32_t test_stall = 0;
   TmapEntry cache[kTmapCacheSize] = {};
   int cache_next = 0;
+  int resident[2][2][3] = {};  // [cta_group-1][bn==256][out]: co-resident units (0: unknown)
 };
 
 namespace {
@@ -71,10 +72,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D tensor map over a row-major rows x cols matrix of 16-bit elements, 128-byte
-// swizzle, box {64, box_rows}; out-of-range elements read as zero (M, N and K tails).
-bool make_operand_map(gemm_ctx* h, const void* ptr, int64_t rows, int64_t cols, int dtype,
-                      int box_rows, CUtensorMap* out) {
+// 2-D tensor map over a row-major rows x cols matrix, 128-byte swizzle, box of 128
+// bytes of columns x box_rows rows.  Loads read out-of-range elements as zero (M, N and
+// K tails); stores skip them.
+bool make_map(gemm_ctx* h, const void* ptr, int64_t rows, int64_t cols, int dtype,
+              int box_rows, CUtensorMap* out) {
   const TmapKey key{ptr, rows, cols, dtype, box_rows};
   for (auto& e : h->cache)
     if (e.valid && e.key == key) {
@@ -84,12 +86,14 @@ bool make_operand_map(gemm_ctx* h, const void* ptr, int64_t rows, int64_t cols, 
   auto fn = encode_fn();
   if (!fn) return false;
   CUtensorMap m;
+  const cuuint64_t esz = dtype == GEMM_F32 ? 4 : 2;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)box_rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * esz};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt =
-      dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt = dtype == GEMM_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dtype == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUresult r = fn(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -110,28 +114,44 @@ size_t out_size(gemm_dtype_t d) { return d == GEMM_F32 ? 4 : 2; }
 bool valid_dtype(int d) { return d == GEMM_F16 || d == GEMM_BF16 || d == GEMM_F32; }
 
 struct Choice {
-  int variant, bn, stages, splits, kb_per_split, group_m, grid;
+  int variant, bn, stages, splits, kb_per_split, group_m, grid, chain_kb;
   int64_t tiles, units, k_blocks, num_m, num_n;
 };
 
-gemm_status_t choose(const gemm_ctx* h, int64_t M, int64_t N, int64_t K, Choice* c) {
+int out_kind(gemm_dtype_t d) { return d == GEMM_F16 ? kOutF16 : d == GEMM_BF16 ? kOutBF16 : kOutF32; }
+
+// Units of this configuration that can run at once: CTAs (variant 1) or CTA pairs
+// (variant 2), from the occupancy query, at most one CTA per SM.
+int resident_units(gemm_ctx* h, int cg, int bn, int stages, int out) {
+  int& slot = h->resident[cg - 1][bn == 256 ? 1 : 0][out];
+  if (slot == 0) {
+    int n = max_resident_units(cg, bn, stages, out);
+    const int cap = h->sms / cg;
+    slot = (n <= 0 || n > cap) ? cap : n;
+  }
+  return slot;
+}
+
+gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choice* c) {
   const gemm_config_t& f = h->forced;
-  c->variant = f.variant ? f.variant : 1;
-  if (c->variant != 1) return GEMM_ERR_INVALID_ARG;
+  // A CTA pair (256-row tiles, each CTA loading half of B) whenever M fills one.
+  c->variant = f.variant ? f.variant : (M > kBlockM ? 2 : 1);
+  const int cg = c->variant;
   c->bn = f.block_n ? f.block_n : (N <= 128 ? 128 : 256);
-  c->stages = f.stages ? f.stages : (c->bn == 256 ? 4 : 6);
-  if (!one_cta_supported(c->bn, c->stages)) return GEMM_ERR_INVALID_ARG;
+  c->stages = f.stages ? f.stages : default_stages(cg, c->bn);
+  if (!kernel_supported(cg, c->bn, c->stages)) return GEMM_ERR_INVALID_ARG;
   c->k_blocks = ceil_div(K, kBlockK);
-  c->num_m = ceil_div(M, kBlockM);
+  c->num_m = ceil_div(M, (int64_t)kBlockM * cg);
   c->num_n = ceil_div(N, c->bn);
   c->tiles = c->num_m * c->num_n;
+  const int slots = resident_units(h, cg, c->bn, c->stages, out);
   int64_t s;
   if (f.splits) {
     s = f.splits;
-  } else if (c->tiles * 2 <= h->sms && c->k_blocks >= 8) {
-    // Fewer tiles than half the SMs: slice K so every SM has work ("A Blackwell
-    // GEMM by Hand in CuTe DSL", section 9: decode shapes are decided by waves).
-    s = h->sms / c->tiles;
+  } else if (c->tiles * 2 <= slots && c->k_blocks >= 8) {
+    // Fewer tiles than half the resident units: slice K so every SM has work ("A
+    // Blackwell GEMM by Hand in CuTe DSL", section 9: decode shapes are decided by waves).
+    s = slots / c->tiles;
     if (s > c->k_blocks / 4) s = c->k_blocks / 4;
     if (s > 32) s = 32;
     if (s < 1) s = 1;
@@ -145,10 +165,12 @@ gemm_status_t choose(const gemm_ctx* h, int64_t M, int64_t N, int64_t K, Choice*
   c->kb_per_split = (int)per;
   c->units = c->tiles * s;
   c->group_m = f.group_m ? f.group_m : 16;
-  int64_t cap = f.max_ctas ? f.max_ctas : h->sms;
-  if (cap > h->sms) cap = h->sms;
-  c->grid = (int)(c->units < cap ? c->units : cap);
-  if (c->units > INT32_MAX || c->tiles * 4 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  c->chain_kb = f.chain_kblocks ? f.chain_kblocks : kChainKBlocks;
+  int64_t cap = slots;
+  if (f.max_ctas) cap = f.max_ctas / cg > 0 ? f.max_ctas / cg : 1;
+  if (cap > slots) cap = slots;
+  c->grid = (int)((c->units < cap ? c->units : cap) * cg);
+  if (c->units > INT32_MAX || c->tiles * cg * 8 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   return GEMM_OK;
 }
 
@@ -233,12 +255,15 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
     return GEMM_OK;
   }
   const gemm_config_t& c = *cfg;
-  if (c.variant < 0 || c.variant > 1) return GEMM_ERR_INVALID_ARG;
+  if (c.variant < 0 || c.variant > 2) return GEMM_ERR_INVALID_ARG;
   if (c.block_n != 0 && c.block_n != 128 && c.block_n != 256) return GEMM_ERR_INVALID_ARG;
-  if (c.splits < 0 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0) return GEMM_ERR_INVALID_ARG;
+  if (c.splits < 0 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
+      c.reserved != 0)
+    return GEMM_ERR_INVALID_ARG;
   if (c.stages) {
     const int bn = c.block_n ? c.block_n : 256;
-    if (!one_cta_supported(bn, c.stages)) return GEMM_ERR_INVALID_ARG;
+    const bool any = kernel_supported(1, bn, c.stages) || kernel_supported(2, bn, c.stages);
+    if (c.variant ? !kernel_supported(c.variant, bn, c.stages) : !any) return GEMM_ERR_INVALID_ARG;
   }
   h->forced = c;
   return GEMM_OK;
@@ -286,19 +311,23 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(B) % 16)
     return GEMM_ERR_UNSUPPORTED;
 
+  const int out = out_kind(dtype_out);
   Choice ch;
-  gemm_status_t st = choose(h, M, N, K, &ch);
+  gemm_status_t st = choose(h, M, N, K, out, &ch);
   if (st != GEMM_OK) return st;
 
   LaunchSpec s;
   std::memset(&s, 0, sizeof(s));
+  s.cta_group = ch.variant;
   s.bn = ch.bn;
   s.stages = ch.stages;
-  s.out = dtype_out == GEMM_F16 ? kOutF16 : dtype_out == GEMM_BF16 ? kOutBF16 : kOutF32;
+  s.out = out;
   s.grid = ch.grid;
   s.stream = stream;
-  if (!make_operand_map(h, A, M, K, dtype_in, kBlockM, &s.tmA) ||
-      !make_operand_map(h, B, N, K, dtype_in, ch.bn, &s.tmB))
+  const bool c_tma = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0;
+  if (!make_map(h, A, M, K, dtype_in, kBlockM, &s.tmA) ||
+      !make_map(h, B, N, K, dtype_in, ch.bn / ch.variant, &s.tmB) ||
+      (c_tma && !make_map(h, C, M, N, dtype_out, 32, &s.tmC)))
     return GEMM_ERR_CUDA;
 
   GemmParams& p = s.p;
@@ -314,20 +343,24 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.kb_per_split = ch.kb_per_split;
   p.units = (int32_t)ch.units;
   p.group_m = ch.group_m;
-  p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0) ? 1 : 0;
-  p.idesc = idesc_f16_kmajor(kBlockM, ch.bn, dtype_in == GEMM_BF16);
+  p.chain_kb = ch.chain_kb;
+  p.vec_store = c_tma ? 1 : 0;
+  p.tma_store = c_tma ? 1 : 0;
+  p.idesc = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn, dtype_in == GEMM_BF16);
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
   p.test_stall = h->test_stall;
   if (ch.splits > 1) {
-    const size_t ws = (size_t)ch.tiles * ch.splits * kBlockM * ch.bn * sizeof(float);
-    st = ensure_workspace(h, ws, (size_t)ch.tiles * 4);
+    const size_t ws =
+        (size_t)ch.tiles * ch.splits * kBlockM * ch.variant * ch.bn * sizeof(float);
+    st = ensure_workspace(h, ws, (size_t)ch.tiles * ch.variant * 8);
     if (st != GEMM_OK) return st;
     p.workspace = h->d_ws;
     p.counters = h->d_ctr;
   }
-  if (launch_one_cta(s) != cudaSuccess) return GEMM_ERR_CUDA;
-  h->last = gemm_config_t{ch.variant, ch.bn, ch.splits, ch.stages, ch.group_m, ch.grid, 0, 0};
+  if (launch_gemm(s) != cudaSuccess) return GEMM_ERR_CUDA;
+  h->last = gemm_config_t{ch.variant, ch.bn,   ch.splits,   ch.stages,
+                          ch.group_m, ch.grid, ch.chain_kb, 0};
   return GEMM_OK;
 }
 

@@ -2,26 +2,39 @@
 //
 // A is M x K and B is N x K, both K-major (K contiguous), fp16 or bf16; fp32
 // accumulation in Tensor Memory; C is M x N row-major in fp16, bf16 or fp32.
-// ("A Blackwell GEMM by Hand in CuTe DSL", section 1 for the operand convention;
-// section 3 for the warp roles; section 8 for persistence with two TMEM slots.)
+// ("A Blackwell GEMM by Hand in CuTe DSL", section 1 for the operand convention,
+// sections 3 and 8 for the warp roles, the CTA pair and persistence with two TMEM
+// accumulator slots; "Optimizing GEMMs using tcgen05 - Part 1", phases 2-5.)
 //
-// One CTA of 6 warps per SM, looping over work units (tile, K slice):
+// CTA_GROUP = 1: one CTA per 128 x BN tile, tcgen05.mma.cta_group::1 (128 x BN x 16).
+// CTA_GROUP = 2: a cluster of two CTAs on neighbouring SMs computes a 256 x BN tile
+//   with tcgen05.mma.cta_group::2 (256 x BN x 16).  Each CTA loads its own 128 rows of
+//   A and its own BN/2 rows of B; both copies complete on the leader's (rank 0's)
+//   full barrier; only the leader issues MMAs, and its commits arrive on the barriers
+//   of both CTAs (mask 0b11).  Each CTA's Tensor Memory holds its 128 rows.
+//
+// Ten warps per CTA, one CTA per SM, looping over work units (tile, K slice):
 //   warp 0      TMA producer: one thread fills a STAGES-deep ring of 128B-swizzled
-//               A (128 x 64) and B (BN x 64) slices, arming full[s] with the byte count.
-//   warp 1      allocates 2*BN TMEM columns; one thread issues tcgen05.mma
-//               (128 x BN x 16, four per 64-deep stage) into accumulator slot i%2,
-//               commits each stage back to empty[s] and each finished tile to acc_full.
-//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, release acc_empty as soon
-//               as the loads are done, convert (RNE) and store C, so tile i's epilogue
-//               overlaps tile i+1's mainloop.
-// Split-K units write fp32 partials to a workspace; the last of a tile's slices to
-// arrive (per 32-row quarter, by an atomic counter) sums all slices in slice order,
-// so the result does not depend on arrival order ("A Blackwell GEMM by Hand in CuTe
-// DSL", section 9, split-K for decode shapes).
+//               A (128 x 64) and B (BN/CTA_GROUP x 64) slices.
+//   warp 1      allocates 2*BN TMEM columns (two accumulator slots); in the leader one
+//               thread issues the MMAs, four per 64-deep stage, into slot i % 2, commits
+//               each stage back to empty[s] and each finished chain to acc_full[slot].
+//   warps 2..9  epilogue: warp w reads TMEM lane quarter w % 4 and column half
+//               (w - 2) / 4; it loads its 32 x BN/2 block, releases the slot at once
+//               (so the next chain's MMAs overlap this epilogue), adds the chain into
+//               fp32 registers, and after the unit's last chain converts (RNE) and
+//               writes C: through a 128B-swizzled shared staging box and a TMA store,
+//               or with direct stores when C's row pitch is not a multiple of 16 bytes.
+// A unit's K range is accumulated in chains of at most p.chain_kb k-blocks, each in
+// a fresh accumulator; the epilogue sums the chains in order in fp32 registers.
+// Split-K units write fp32 partials to a workspace; the last slice to arrive (per
+// warp's 32 x BN/2 block, by an atomic counter) sums all slices in slice order, so
+// the result does not depend on arrival order ("A Blackwell GEMM by Hand in CuTe
+// DSL", section 9).
 //
 // Every mbarrier wait is bounded by p.wait_limit_ns (globaltimer) and an iteration
-// cap; on expiry the waiting thread records the site in the status word, raises a
-// shared abort flag that makes every role leave its loop, and the CTA drains its own
+// cap; on expiry the waiting thread records the site in the status word and raises a
+// shared abort flag that makes every role leave its loop; the CTA then drains its own
 // outstanding copies and MMAs before freeing TMEM and returning.
 #pragma once
 #include <cuda.h>
@@ -47,7 +60,7 @@ __device__ __forceinline__ void record_timeout(const WaitCtl& c, uint32_t site) 
 
 // Wait for the phase of `bar` with parity `parity` to complete.  Returns false when
 // the CTA is aborting or the limit ran out (then the abort flag is raised).
-__device__ __noinline__ bool wait_parity(uint32_t bar, uint32_t parity, const WaitCtl& c,
+static __device__ __noinline__ bool wait_parity(uint32_t bar, uint32_t parity, const WaitCtl& c,
                                          uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -64,7 +77,7 @@ __device__ __noinline__ bool wait_parity(uint32_t bar, uint32_t parity, const Wa
 }
 
 // Teardown wait: ignores the abort flag (it is used while aborting) but is bounded.
-__device__ __noinline__ bool wait_parity_drain(uint32_t bar, uint32_t parity, const WaitCtl& c) {
+static __device__ __noinline__ bool wait_parity_drain(uint32_t bar, uint32_t parity, const WaitCtl& c) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -72,6 +85,13 @@ __device__ __noinline__ bool wait_parity_drain(uint32_t bar, uint32_t parity, co
       record_timeout(c, kSiteDrain);
       return false;
     }
+  }
+}
+
+// Bounded pause (used by a pair's follower while aborting, so copies it issued can land).
+__device__ __forceinline__ void pause_ns(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) {
   }
 }
 
@@ -99,10 +119,26 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams& p) {
   return w;
 }
 
-// ----------------------------------------------------------------- epilogue stores --
+__device__ __forceinline__ int32_t chains_of(const Unit& w, int32_t chain_kb) {
+  return (w.kb1 - w.kb0 + chain_kb - 1) / chain_kb;
+}
+
+// ------------------------------------------------------------- epilogue helpers --
 template <int OUT>
-__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int32_t m, int32_t n0,
-                                                const float (&v)[32]) {
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (OUT == kOutF16) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// Direct stores of 32 consecutive values of one row (used when C cannot take TMA).
+template <int OUT>
+__device__ __forceinline__ void store_row_direct(const GemmParams& p, int32_t m, int32_t n0,
+                                                 const float* v) {
   if (m >= p.M) return;
   if constexpr (OUT == kOutF32) {
     float* dst = reinterpret_cast<float*>(p.C) + (size_t)m * p.N + n0;
@@ -119,15 +155,7 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, int32_t m, 
   } else {
     uint32_t packed[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if constexpr (OUT == kOutF16) {
-        __half2 h = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
-        packed[j] = *reinterpret_cast<uint32_t*>(&h);
-      } else {
-        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-        packed[j] = *reinterpret_cast<uint32_t*>(&h);
-      }
-    }
+    for (int j = 0; j < 16; ++j) packed[j] = pack2<OUT>(v[2 * j], v[2 * j + 1]);
     uint16_t* dst = reinterpret_cast<uint16_t*>(p.C) + (size_t)m * p.N + n0;
     if (p.vec_store && n0 + 32 <= p.N) {
 #pragma unroll
@@ -141,37 +169,47 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, int32_t m, 
   }
 }
 
-// --------------------------------------------------------------- shared memory map --
-template <int BN, int STAGES>
-struct SmemLayout1 {
-  static constexpr uint32_t kABytes = kBlockM * kBlockK * 2;  // 16 KiB
-  static constexpr uint32_t kBBytes = BN * kBlockK * 2;       // 32 KiB at BN = 256
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+// ------------------------------------------------------------- shared memory map --
+template <int CTA_GROUP, int BN, int STAGES>
+struct Layout {
+  static constexpr int kEpiWarps = 8;
+  static constexpr uint32_t kThreads = 32 * (2 + kEpiWarps);
+  static constexpr int kRowsB = BN / CTA_GROUP;                // B rows loaded per CTA
+  static constexpr uint32_t kABytes = kBlockM * kBlockK * 2;   // 16 KiB
+  static constexpr uint32_t kBBytes = kRowsB * kBlockK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;   // per CTA
+  static constexpr uint32_t kTxBytes = kStageBytes * CTA_GROUP;  // expected on the leader
+  static constexpr uint32_t kStagingBytes = 32 * 128;           // one 32-row x 128 B box
   static constexpr uint32_t kAOff = 0;
   static constexpr uint32_t kBOff = STAGES * kABytes;
-  static constexpr uint32_t kBarOff = kBOff + STAGES * kBBytes;
+  static constexpr uint32_t kCOff = kBOff + STAGES * kBBytes;
+  static constexpr uint32_t kBarOff = kCOff + kEpiWarps * kStagingBytes;
   // full[S], empty[S], acc_full[2], acc_empty[2], drain
   static constexpr uint32_t kNumBars = 2 * STAGES + 5;
   static constexpr uint32_t kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
   static constexpr uint32_t kEnd = kAbortOff + 4;
   static constexpr uint32_t kDynamicBytes = kEnd + 1024;  // slack for 1024-byte alignment
-  static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kABytes % 1024 == 0 &&
-                    kBBytes % 1024 == 0,
-                "every operand stage must start on a 1024-byte boundary (128B swizzle atom)");
+  static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0 && kBOff % 1024 == 0 &&
+                    kCOff % 1024 == 0,
+                "every operand stage and staging box must start on a 1024-byte boundary");
   static_assert(kDynamicBytes <= 227 * 1024, "shared memory over the per-block limit");
 };
 
-constexpr uint32_t kThreads1 = 192;  // warp 0 producer, warp 1 MMA, warps 2..5 epilogue
-
-template <int BN, int STAGES, int OUT>
-__global__ void __launch_bounds__(kThreads1, 1)
-    gemm_1cta_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
-  using L = SmemLayout1<BN, STAGES>;
+template <int CTA_GROUP, int BN, int STAGES, int OUT>
+__global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  using L = Layout<CTA_GROUP, BN, STAGES>;
   static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
-  constexpr uint32_t kTmemCols = 2 * BN;  // two accumulator slots
-  constexpr int kChunks = BN / 32;
+  static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "CTA_GROUP must be 1 or 2");
+  constexpr uint32_t kTmemCols = 2 * BN;       // two accumulator slots
+  constexpr int kHalf = BN / 2;                // columns per epilogue warp
+  constexpr int kPieces = kHalf / 32;          // tcgen05.ld x32 pieces per warp
+  constexpr int kOutBytes = OUT == kOutF32 ? 4 : 2;
+  constexpr int kBoxCols = 128 / kOutBytes;    // columns of one 128-byte staging row
+  constexpr int kBoxes = kHalf / kBoxCols;     // staging boxes per warp
+  constexpr int kRowsTile = kBlockM * CTA_GROUP;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -180,6 +218,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
 
   const uint32_t sA = base + L::kAOff;
   const uint32_t sB = base + L::kBOff;
+  const uint32_t sC = base + L::kCOff;
   const uint32_t bar0 = base + L::kBarOff;
   auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
   auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (STAGES + s); };
@@ -192,29 +231,35 @@ __global__ void __launch_bounds__(kThreads1, 1)
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
   const WaitCtl ctl{p.wait_limit_ns, p.status, abort_flag};
+  const uint32_t rank = CTA_GROUP == 2 ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int32_t first_unit = (int32_t)(blockIdx.x / CTA_GROUP);
+  const int32_t unit_stride = (int32_t)(gridDim.x / CTA_GROUP);
 
   // ---------------------------------------------------------------- setup --
   if (warp == 0 && lane == 0) {
     for (uint32_t s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(full_bar(s), 1);   // the leader's producer arms it; copies complete it
+      mbar_init(empty_bar(s), 1);  // one (multicast) commit per use
     }
     for (uint32_t i = 0; i < 2; ++i) {
       mbar_init(acc_full_bar(i), 1);
-      mbar_init(acc_empty_bar(i), 4);  // one arrival per epilogue warp
+      mbar_init(acc_empty_bar(i), L::kEpiWarps * CTA_GROUP);  // every epilogue warp of the pair
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.tma_store) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc<1>(smem_addr(tmem_slot), kTmemCols);
-    tmem_relinquish<1>();
+    tmem_alloc<CTA_GROUP>(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish<CTA_GROUP>();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CTA_GROUP == 2) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -223,17 +268,27 @@ __global__ void __launch_bounds__(kThreads1, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
-      for (int32_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      for (int32_t u = first_unit; u < p.units && ok; u += unit_stride) {
         const Unit w = decode_unit(u, p);
+        const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
+        const int32_t b_row = w.n_blk * BN + (int32_t)rank * L::kRowsB;
         for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
           if (!wait_parity(empty_bar(stage), phase ^ 1u, ctl, kSiteEmpty)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
-          tma_load_2d(sA + stage * L::kABytes, &tmA, kb * kBlockK, w.m_blk * kBlockM,
-                      full_bar(stage));
-          tma_load_2d(sB + stage * L::kBBytes, &tmB, kb * kBlockK, w.n_blk * BN, full_bar(stage));
+          if constexpr (CTA_GROUP == 1) {
+            mbar_arrive_expect_tx(full_bar(stage), L::kTxBytes);
+            tma_load_2d(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, full_bar(stage));
+            tma_load_2d(sB + stage * L::kBBytes, &tmB, kb * kBlockK, b_row, full_bar(stage));
+          } else {
+            // Both CTAs' copies complete on the leader's full barrier; the leader
+            // arms it with the bytes of the pair.
+            const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), L::kTxBytes);
+            tma_load_2d_pair(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, leader_full);
+            tma_load_2d_pair(sB + stage * L::kBBytes, &tmB, kb * kBlockK, b_row, leader_full);
+          }
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -242,106 +297,136 @@ __global__ void __launch_bounds__(kThreads1, 1)
           }
         }
       }
-      // No copy may still be landing in this CTA's shared memory when it exits.
-      for (uint32_t s = 0; s < STAGES; ++s)
-        if (armed & (1u << s)) wait_parity_drain(full_bar(s), (armed_phase >> s) & 1u, ctl);
+      // No copy may still be landing in shared memory when the CTA exits.
+      if (leader) {
+        for (uint32_t s = 0; s < STAGES; ++s)
+          if (armed & (1u << s)) wait_parity_drain(full_bar(s), (armed_phase >> s) & 1u, ctl);
+      } else if (*abort_flag) {
+        // The follower's copies complete on the leader's barrier, which it cannot poll;
+        // normally every one of them was consumed by an MMA before the teardown.  On an
+        // abort, give any copy still in flight time to land.
+        pause_ns(200000);
+      }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer --
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, iter = 0;
       bool ok = true;
       if (p.test_stall) ok = wait_parity(drain_bar, 0, ctl, kSiteTestStall);
-      for (int32_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      for (int32_t u = first_unit; u < p.units && ok; u += unit_stride) {
         const Unit w = decode_unit(u, p);
-        const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
-        if (!wait_parity(acc_empty_bar(slot), acc_phase ^ 1u, ctl, kSiteAccEmpty)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + slot * BN;
-        for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!wait_parity(full_bar(stage), phase, ctl, kSiteFull)) {
+        for (int32_t c0 = w.kb0; c0 < w.kb1 && ok; c0 += p.chain_kb) {
+          const int32_t c1 = min(c0 + p.chain_kb, w.kb1);
+          const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
+          if (!wait_parity(acc_empty_bar(slot), acc_phase ^ 1u, ctl, kSiteAccEmpty)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = sA + stage * L::kABytes, b0 = sB + stage * L::kBBytes;
+          const uint32_t d_tmem = tmem_base + slot * BN;
+          for (int32_t kb = c0; kb < c1; ++kb) {
+            if (!wait_parity(full_bar(stage), phase, ctl, kSiteFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = sA + stage * L::kABytes, b0 = sB + stage * L::kBBytes;
 #pragma unroll
-          for (uint32_t k = 0; k < kBlockK / 16; ++k)
-            umma_f16<1>(d_tmem, smem_desc_sw128_kmajor(a0 + 32u * k),
-                        smem_desc_sw128_kmajor(b0 + 32u * k), p.idesc,
-                        (kb > w.kb0 || k > 0) ? 1u : 0u);
-          umma_commit(empty_bar(stage));  // stage is free once these MMAs are done
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+            for (uint32_t k = 0; k < kBlockK / 16; ++k)
+              umma_f16<CTA_GROUP>(d_tmem, smem_desc_sw128_kmajor(a0 + 32u * k),
+                                  smem_desc_sw128_kmajor(b0 + 32u * k), p.idesc,
+                                  (kb > c0 || k > 0) ? 1u : 0u);
+            // the stage is free (in both CTAs) once these MMAs are done
+            if constexpr (CTA_GROUP == 1) umma_commit_group<1>(empty_bar(stage));
+            else umma_commit_pair(empty_bar(stage), 0x3);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
+          if (!ok) break;
+          if constexpr (CTA_GROUP == 1) umma_commit_group<1>(acc_full_bar(slot));
+          else umma_commit_pair(acc_full_bar(slot), 0x3);
+          ++iter;
         }
-        if (!ok) break;
-        umma_commit(acc_full_bar(slot));  // accumulator final
-        ++iter;
       }
       // Every issued MMA must finish before TMEM is released.
-      umma_commit(drain_bar);
+      umma_commit_group<CTA_GROUP>(drain_bar);
       wait_parity_drain(drain_bar, 0, ctl);
     }
     __syncwarp();
   } else {
     // -------------------------------------------------------------- epilogue --
-    const uint32_t q = warp & 3u;             // TMEM lane quarter this warp may read
-    const uint32_t row = q * 32u + lane;      // accumulator row held by this thread
+    const uint32_t ew = warp - 2;                // 0..7
+    const uint32_t q = warp & 3u;                // TMEM lane quarter this warp may read
+    const uint32_t h = ew >> 2;                  // column half
+    const uint32_t row = q * 32u + lane;         // accumulator row held by this thread
+    const uint32_t staging = sC + ew * L::kStagingBytes;
     uint32_t iter = 0;
-    for (int32_t u = blockIdx.x; u < p.units; u += gridDim.x) {
+    bool ok = true;
+    for (int32_t u = first_unit; u < p.units && ok; u += unit_stride) {
       const Unit w = decode_unit(u, p);
-      const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
-      // One lane polls; the warp follows its verdict, so tcgen05.ld below is always
-      // executed by the whole, converged warp.
-      uint32_t ok = 1;
-      if (lane == 0) ok = wait_parity(acc_full_bar(slot), acc_phase, ctl, kSiteAccFull) ? 1u : 0u;
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      float acc[kHalf];
+      const int32_t nchains = chains_of(w, p.chain_kb);
+      for (int32_t ch = 0; ch < nchains; ++ch) {
+        const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
+        // One lane polls; the warp follows its verdict, so tcgen05.ld below is always
+        // executed by the whole, converged warp.
+        uint32_t good = 1;
+        if (lane == 0)
+          good = wait_parity(acc_full_bar(slot), acc_phase, ctl, kSiteAccFull) ? 1u : 0u;
+        good = __shfl_sync(0xFFFFFFFFu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * BN + h * kHalf;
+#pragma unroll
+        for (int pc = 0; pc < kPieces; ++pc) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + 32u * pc, r);
+          tmem_ld_wait(r);
+          if (ch == 0) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[32 * pc + j] = __uint_as_float(r[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[32 * pc + j] += __uint_as_float(r[j]);
+          }
+        }
+        // The slot is free for the next chain as soon as the loads are done.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          // the leader's acc_empty, in shared::cluster space (its own, for rank 0)
+          if constexpr (CTA_GROUP == 1) mbar_arrive(acc_empty_bar(slot));
+          else mbar_arrive_cluster(mapa_shared(acc_empty_bar(slot), 0));
+        }
+        ++iter;
+      }
       if (!ok) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * BN;
-      const int32_t m = w.m_blk * kBlockM + (int32_t)row;
-      const int32_t n_base = w.n_blk * BN;
-      if (p.splits == 1) {
-#pragma unroll 1
-        for (int c = 0; c < kChunks; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + 32u * c, r);
-          tmem_ld_wait(r);
-          if (c == kChunks - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty_bar(slot));
-          }
-          float v[32];
+
+      const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;  // first row of this CTA
+      const int32_t n_half = w.n_blk * BN + (int32_t)h * kHalf;          // first column of the half
+      if (p.splits > 1) {
+        // Split-K: this slice's fp32 rows go to the workspace; the last slice of the
+        // block to arrive sums all slices in slice order.
+        const size_t tile_rows = (size_t)kRowsTile;
+        float* ws_tile = p.workspace + (size_t)w.tile * p.splits * tile_rows * BN;
+        const size_t my_row = (size_t)rank * kBlockM + row;
+        float* mine = ws_tile + ((size_t)w.split * tile_rows + my_row) * BN + h * kHalf;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          store_row_chunk<OUT>(p, m, n_base + 32 * c, v);
-        }
-      } else {
-        // Split-K: this slice's fp32 partial rows go to the workspace.
-        float* ws_tile = p.workspace + (size_t)w.tile * p.splits * kBlockM * BN;
-        float* mine = ws_tile + ((size_t)w.split * kBlockM + row) * BN;
-#pragma unroll 1
-        for (int c = 0; c < kChunks; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + 32u * c, r);
-          tmem_ld_wait(r);
-          if (c == kChunks - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty_bar(slot));
-          }
-#pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            st_global_cg_v4(mine + 32 * c + j, r[j], r[j + 1], r[j + 2], r[j + 3]);
-        }
+        for (int j = 0; j < kHalf; j += 4)
+          st_global_cg_v4(mine + j, __float_as_uint(acc[j]), __float_as_uint(acc[j + 1]),
+                          __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
         __threadfence();
         __syncwarp();
         uint32_t last = 0;
         if (lane == 0) {
-          uint32_t* ctr = p.counters + (size_t)w.tile * 4 + q;
+          uint32_t* ctr = p.counters + (((size_t)w.tile * CTA_GROUP + rank) * 4 + q) * 2 + h;
           const uint32_t before = atomicAdd(ctr, 1u);
           last = (before == (uint32_t)p.splits - 1u) ? 1u : 0u;
           if (last) atomicExch(ctr, 0u);  // ready for the next launch
@@ -349,47 +434,83 @@ __global__ void __launch_bounds__(kThreads1, 1)
         }
         last = __shfl_sync(0xFFFFFFFFu, last, 0);
         __syncwarp();
-        if (last) {
-          // Sum the slices in slice order: the result is the same whichever slice
-          // arrived last.
-#pragma unroll 1
-          for (int c = 0; c < kChunks; ++c) {
-            float v[32];
+        if (!last) continue;
+        // Sum the slices in slice order: the result is the same whichever slice
+        // arrived last.
+        for (int32_t s = 0; s < p.splits; ++s) {
+          const float* src = ws_tile + ((size_t)s * tile_rows + my_row) * BN + h * kHalf;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-#pragma unroll 1
-            for (int32_t s = 0; s < p.splits; ++s) {
-              const float* src = ws_tile + ((size_t)s * kBlockM + row) * BN + 32 * c;
-#pragma unroll
-              for (int j = 0; j < 32; j += 4) {
-                const uint4 x = ld_global_cg_v4(src + j);
-                if (s == 0) {
-                  v[j] = __uint_as_float(x.x);
-                  v[j + 1] = __uint_as_float(x.y);
-                  v[j + 2] = __uint_as_float(x.z);
-                  v[j + 3] = __uint_as_float(x.w);
-                } else {
-                  v[j] += __uint_as_float(x.x);
-                  v[j + 1] += __uint_as_float(x.y);
-                  v[j + 2] += __uint_as_float(x.z);
-                  v[j + 3] += __uint_as_float(x.w);
-                }
-              }
+          for (int j = 0; j < kHalf; j += 4) {
+            const uint4 x = ld_global_cg_v4(src + j);
+            if (s == 0) {
+              acc[j] = __uint_as_float(x.x);
+              acc[j + 1] = __uint_as_float(x.y);
+              acc[j + 2] = __uint_as_float(x.z);
+              acc[j + 3] = __uint_as_float(x.w);
+            } else {
+              acc[j] += __uint_as_float(x.x);
+              acc[j + 1] += __uint_as_float(x.y);
+              acc[j + 2] += __uint_as_float(x.z);
+              acc[j + 3] += __uint_as_float(x.w);
             }
-            store_row_chunk<OUT>(p, m, n_base + 32 * c, v);
           }
         }
       }
-      ++iter;
+
+      if (p.tma_store) {
+        // Each 128-byte row of a staging box is written in the 128-byte swizzled order
+        // (16-byte chunk j of row r at chunk j ^ (r % 8)) that the C tensor map's
+        // CU_TENSOR_MAP_SWIZZLE_128B expects ("A Blackwell GEMM by Hand in CuTe DSL",
+        // section 6); the TMA store clips rows >= M and columns >= N.
+        const uint32_t row_addr = staging + lane * 128u;
+#pragma unroll
+        for (int bx = 0; bx < kBoxes; ++bx) {
+          // the previous store from this staging box must have finished reading it
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+#pragma unroll
+          for (int cj = 0; cj < 8; ++cj) {
+            uint32_t w4[4];
+            if constexpr (OUT == kOutF32) {
+#pragma unroll
+              for (int t = 0; t < 4; ++t)
+                w4[t] = __float_as_uint(acc[bx * kBoxCols + cj * 4 + t]);
+            } else {
+#pragma unroll
+              for (int t = 0; t < 4; ++t)
+                w4[t] = pack2<OUT>(acc[bx * kBoxCols + cj * 8 + 2 * t],
+                                   acc[bx * kBoxCols + cj * 8 + 2 * t + 1]);
+            }
+            st_shared_v4(row_addr + ((cj ^ (lane & 7u)) << 4), w4[0], w4[1], w4[2], w4[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          const int32_t box_n = n_half + bx * kBoxCols, box_m = m0 + (int32_t)(q * 32u);
+          // a box wholly outside C (ragged last tiles) is not stored at all
+          if (lane == 0 && box_n < p.N && box_m < p.M) {
+            tma_store_2d(&tmC, staging, box_n, box_m);
+            bulk_commit_group();
+          }
+        }
+      } else {
+        const int32_t m = m0 + (int32_t)row;
+#pragma unroll
+        for (int pc = 0; pc < kPieces; ++pc)
+          store_row_direct<OUT>(p, m, n_half + 32 * pc, acc + 32 * pc);
+      }
     }
+    // Every TMA store of this warp must be complete before the CTA exits.
+    if (p.tma_store && lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
   // --------------------------------------------------------------- teardown --
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CTA_GROUP == 2) cluster_sync();  // no CTA leaves while its pair may still signal it
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc<1>(tmem_base, kTmemCols);
+    tmem_dealloc<CTA_GROUP>(tmem_base, kTmemCols);
   }
 }
 

@@ -46,7 +46,7 @@ using namespace gb300;
 namespace {
 
 constexpr size_t kStatusBytes = 256;                               // status word, padded
-constexpr size_t kCounterWords = 16384;                            // (tile, quarter) counters
+constexpr size_t kCounterWords = 16384;                            // (tile, quarter, half) counters
 constexpr size_t kCounterBytes = kCounterWords * sizeof(uint32_t);
 constexpr size_t kWorkspaceBytes = GEMM_NOALLOC_WORKSPACE_BYTES;   // fp32 partial tiles
 constexpr size_t kScratchBytes = kStatusBytes + kCounterBytes + kWorkspaceBytes;
@@ -99,17 +99,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// rows x cols row-major 16-bit operand, 128-byte swizzle, box {64, box_rows}, zero fill.
-bool encode_operand(const void* ptr, int64_t rows, int64_t cols, gemm_dtype_t dtype, int box_rows,
-                    CUtensorMap* out) {
+// rows x cols row-major matrix, 128-byte swizzle, box {128 bytes of columns, box_rows};
+// loads zero-fill out-of-range elements, stores skip them.
+bool encode_map(const void* ptr, int64_t rows, int64_t cols, gemm_dtype_t dtype, int box_rows,
+                CUtensorMap* out) {
   auto fn = encoder();
   if (!fn) return false;
+  const cuuint64_t esz = dtype == GEMM_F32 ? 4 : 2;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)box_rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * esz};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt =
-      dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt = dtype == GEMM_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dtype == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   return fn(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -165,19 +168,22 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   const int64_t units = tiles * splits;
   if (units > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   const size_t ws_need = splits > 1 ? (size_t)tiles * splits * kBlockM * kBN * sizeof(float) : 0;
-  const size_t ctr_need = splits > 1 ? (size_t)tiles * 4 : 0;
+  const size_t ctr_need = splits > 1 ? (size_t)tiles * 8 : 0;  // (tile, quarter, half)
   // The scratch has a fixed size: a product that would need more is refused.
   if (ws_need > kWorkspaceBytes || ctr_need > kCounterWords) return GEMM_ERR_UNSUPPORTED;
 
   LaunchSpec s;
   std::memset(&s, 0, sizeof(s));
+  s.cta_group = 1;
   s.bn = kBN;
   s.stages = kStages;
   s.out = dtype_out == GEMM_F16 ? kOutF16 : dtype_out == GEMM_BF16 ? kOutBF16 : kOutF32;
   s.grid = (int)(units < ds.sms ? units : ds.sms);
   s.stream = stream;
-  if (!encode_operand(A, M, K, dtype_in, kBlockM, &s.tmA) ||
-      !encode_operand(B, N, K, dtype_in, kBN, &s.tmB))
+  const bool c_tma = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0;
+  if (!encode_map(A, M, K, dtype_in, kBlockM, &s.tmA) ||
+      !encode_map(B, N, K, dtype_in, kBN, &s.tmB) ||
+      (c_tma && !encode_map(C, M, N, dtype_out, 32, &s.tmC)))
     return GEMM_ERR_CUDA;
 
   uint32_t* status = reinterpret_cast<uint32_t*>(ds.scratch);
@@ -202,12 +208,14 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   p.kb_per_split = (int32_t)per;
   p.units = (int32_t)units;
   p.group_m = 16;
-  p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0) ? 1 : 0;
+  p.chain_kb = kChainKBlocks;
+  p.vec_store = c_tma ? 1 : 0;
+  p.tma_store = c_tma ? 1 : 0;
   p.idesc = idesc_f16_kmajor(kBlockM, kBN, dtype_in == GEMM_BF16);
   p.workspace = workspace;
   p.counters = counters;
   p.status = status;
   p.wait_limit_ns = kWaitLimitNs;
   p.test_stall = 0;
-  return launch_one_cta(s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  return launch_gemm(s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

@@ -1,0 +1,34 @@
+// Dispatch over the instantiated kernel menu.
+#include "gemm_kernel.cuh"
+#include "launch.h"
+
+namespace gb300 {
+
+bool kernel_supported(int cg, int bn, int stages) {
+  if (cg == 1) return (bn == 256 && stages == 4) || (bn == 128 && stages == 6);
+  if (cg == 2) return (bn == 256 && stages == 6) || (bn == 128 && stages == 8);
+  return false;
+}
+
+int default_stages(int cg, int bn) {
+  if (cg == 1) return bn == 256 ? 4 : 6;
+  return bn == 256 ? 6 : 8;
+}
+
+size_t kernel_smem_bytes(int cg, int bn, int stages) {
+  if (!kernel_supported(cg, bn, stages)) return 0;
+  if (cg == 1) return bn == 256 ? Layout<1, 256, 4>::kDynamicBytes : Layout<1, 128, 6>::kDynamicBytes;
+  return bn == 256 ? Layout<2, 256, 6>::kDynamicBytes : Layout<2, 128, 8>::kDynamicBytes;
+}
+
+int max_resident_units(int cg, int bn, int stages, int out) {
+  return cg == 1 ? resident_cg1(bn, stages, out) : resident_cg2(bn, stages, out);
+}
+
+cudaError_t launch_gemm(const LaunchSpec& s) {
+  if (s.cta_group == 1) return launch_cg1(s);
+  if (s.cta_group == 2) return launch_cg2(s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gb300

@@ -1,5 +1,5 @@
-// Internal launch interface between the C ABI (gemm_api.cu) and the translation units
-// that instantiate the kernel templates.
+// Internal launch interface between the C ABI (gemm_api.cu, gemm_noalloc.cu) and the
+// translation units that instantiate the kernel templates.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -9,19 +9,31 @@
 namespace gb300 {
 
 struct LaunchSpec {
+  int cta_group;   // 1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile
   int bn;          // columns of C per tile
   int stages;      // operand ring depth
   int out;         // OutKind
-  int grid;        // CTAs (a multiple of 2 for the pair kernel)
-  CUtensorMap tmA; // A: box {64, rows of A per CTA}
-  CUtensorMap tmB; // B: box {64, rows of B per CTA}
+  int grid;        // CTAs (a multiple of cta_group)
+  CUtensorMap tmA; // A: box {64, 128}
+  CUtensorMap tmB; // B: box {64, bn / cta_group}
+  CUtensorMap tmC; // C: box {128 bytes of columns, 32 rows} (used when p.tma_store)
   GemmParams p;
   cudaStream_t stream;
 };
 
-// One CTA per 128-row tile (cta_group::1).
-bool one_cta_supported(int bn, int stages);
-size_t one_cta_smem_bytes(int bn, int stages);
-cudaError_t launch_one_cta(const LaunchSpec& s);
+// The instantiated (cta_group, bn, stages) menu.
+bool kernel_supported(int cta_group, int bn, int stages);
+int default_stages(int cta_group, int bn);
+size_t kernel_smem_bytes(int cta_group, int bn, int stages);
+// Clusters (CTAs for cta_group 1) of this configuration that can be resident at once
+// on the current device; 0 if the query fails.
+int max_resident_units(int cta_group, int bn, int stages, int out);
+cudaError_t launch_gemm(const LaunchSpec& s);
+
+// Per-translation-unit launchers (kernels_cg1.cu, kernels_cg2.cu).
+cudaError_t launch_cg1(const LaunchSpec& s);
+cudaError_t launch_cg2(const LaunchSpec& s);
+int resident_cg1(int bn, int stages, int out);
+int resident_cg2(int bn, int stages, int out);
 
 }  // namespace gb300

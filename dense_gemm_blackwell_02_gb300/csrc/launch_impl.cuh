@@ -1,0 +1,82 @@
+// Template launcher shared by the per-cta_group instantiation files.
+#pragma once
+#include "gemm_kernel.cuh"
+#include "launch.h"
+
+namespace gb300 {
+
+template <int CG, int BN, int STAGES, int OUT>
+cudaError_t launch_one(const LaunchSpec& s) {
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT>;
+  using L = Layout<CG, BN, STAGES>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes);
+  if (e != cudaSuccess) return e;
+  if (CG == 2) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s.grid, 1, 1);
+  cfg.blockDim = dim3(L::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kDynamicBytes;
+  cfg.stream = s.stream;
+  cudaLaunchAttribute attr[1];
+  if (CG == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, s.tmA, s.tmB, s.tmC, s.p);
+}
+
+template <int CG, int BN, int STAGES, int OUT>
+int resident_one() {
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT>;
+  using L = Layout<CG, BN, STAGES>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           L::kDynamicBytes) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * CG, 1, 1);
+  cfg.blockDim = dim3(L::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kDynamicBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int CG, int BN, int STAGES>
+cudaError_t by_out(const LaunchSpec& s) {
+  switch (s.out) {
+    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16>(s);
+    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16>(s);
+    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32>(s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int CG, int BN, int STAGES>
+int resident_by_out(int out) {
+  switch (out) {
+    case kOutF16: return resident_one<CG, BN, STAGES, kOutF16>();
+    case kOutBF16: return resident_one<CG, BN, STAGES, kOutBF16>();
+    case kOutF32: return resident_one<CG, BN, STAGES, kOutF32>();
+    default: return 0;
+  }
+}
+
+}  // namespace gb300

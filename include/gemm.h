@@ -63,6 +63,10 @@ typedef enum {
  *   stages    depth of the shared-memory operand ring
  *   group_m   grouped rasterisation: M tiles per group
  *   max_ctas  cap on the persistent grid (0 = one CTA per SM)
+ *   chain_kblocks  64-deep K blocks accumulated in one Tensor-Memory accumulator
+ *             before the epilogue adds it into its fp32 registers (0 = 64, i.e.
+ *             K 4096: the tensor core's fp32 accumulation error grows with the
+ *             length of one accumulation chain)
  */
 typedef struct {
   int32_t variant;
@@ -71,8 +75,8 @@ typedef struct {
   int32_t stages;
   int32_t group_m;
   int32_t max_ctas;
-  int32_t reserved0;
-  int32_t reserved1;
+  int32_t chain_kblocks;
+  int32_t reserved;
 } gemm_config_t;
 
 /* Create a handle on the current CUDA device.  Fails with GEMM_ERR_UNSUPPORTED

@@ -74,28 +74,59 @@ def test_ragged_shapes(g, M, N):
     _case(g, M, N, 136, F16, F16, seed=25)
 
 
+@pytest.mark.parametrize("variant", [1, 2])
 @pytest.mark.parametrize("bn", [128, 256])
 @pytest.mark.parametrize("splits", [1, 2, 3, 7])
-def test_forced_tiles_and_splits(g, bn, splits):
-    g.set_config(variant=1, block_n=bn, splits=splits)
+def test_forced_tiles_and_splits(g, variant, bn, splits):
+    g.set_config(variant=variant, block_n=bn, splits=splits)
     try:
         _case(g, 300, 700, 1024, F16, F32, seed=26)
         _case(g, 256, 512, 960, BF16, BF16, seed=27)
         cfg = g.last_config()
         kb = 960 // 64                       # k-blocks of the last case
         per = -(-kb // splits)
-        assert cfg["block_n"] == bn and cfg["splits"] == -(-kb // per)
+        assert cfg["variant"] == variant and cfg["block_n"] == bn
+        assert cfg["splits"] == -(-kb // per)
     finally:
         g.reset_config()
 
 
-@pytest.mark.parametrize("max_ctas", [1, 2, 5, 37])
-def test_persistent_loops_many_units_per_cta(g, max_ctas):
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("max_ctas", [2, 4, 10, 38])
+def test_persistent_loops_many_units_per_cta(g, variant, max_ctas):
     # few CTAs: each walks many tiles, so both accumulator slots and the operand
     # ring go through many phases
-    g.set_config(max_ctas=max_ctas, group_m=3)
+    g.set_config(variant=variant, max_ctas=max_ctas, group_m=3)
     try:
         _case(g, 640, 1280, 704, F16, F16, seed=28)
+    finally:
+        g.reset_config()
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("chain", [1, 3, 5, 64])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_accumulation_chains(g, variant, chain, splits):
+    # K split into several TMEM accumulation chains summed by the epilogue in fp32
+    # registers; with split-K on top, and with the chain not dividing the slice
+    g.set_config(variant=variant, chain_kblocks=chain, splits=splits)
+    try:
+        _case(g, 300, 520, 1280, BF16, F32, seed=34)
+        _case(g, 256, 512, 1000, F16, F16, seed=35, exact=True, ints=True)
+        assert g.last_config()["chain_kblocks"] == chain
+    finally:
+        g.reset_config()
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("M,N", [(1, 257), (129, 4097), (383, 136), (256, 264)])
+def test_pair_and_single_on_ragged_edges(g, variant, M, N):
+    # N = 4097 and N = 257 (fp16) are not 16-byte row pitches: direct stores; the
+    # others go through the TMA store, which must clip rows >= M and columns >= N
+    g.set_config(variant=variant)
+    try:
+        _case(g, M, N, 192, F16, F16, seed=36)
+        _case(g, M, N, 200, BF16, F32, seed=37)
     finally:
         g.reset_config()
 
