@@ -23,10 +23,10 @@ EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "gemm_set
 class GemmConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("variant", "block_n", "splits", "stages",
                                                 "group_m", "max_ctas", "chain_kblocks",
-                                                "reserved")]
+                                                "dp_tiles")]
 
     def as_dict(self):
-        return {n: getattr(self, n) for n, _ in self._fields_ if not n.startswith("reserved")}
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 class GemmError(RuntimeError):

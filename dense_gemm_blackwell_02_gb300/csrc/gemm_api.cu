@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -115,7 +116,7 @@ bool valid_dtype(int d) { return d == GEMM_F16 || d == GEMM_BF16 || d == GEMM_F3
 
 struct Choice {
   int variant, bn, stages, splits, kb_per_split, group_m, grid, chain_kb;
-  int64_t tiles, units, k_blocks, num_m, num_n;
+  int64_t tiles, dp_tiles, units, k_blocks, num_m, num_n;
 };
 
 int out_kind(gemm_dtype_t d) { return d == GEMM_F16 ? kOutF16 : d == GEMM_BF16 ? kOutBF16 : kOutF32; }
@@ -144,32 +145,37 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
   c->num_m = ceil_div(M, (int64_t)kBlockM * cg);
   c->num_n = ceil_div(N, c->bn);
   c->tiles = c->num_m * c->num_n;
-  const int slots = resident_units(h, cg, c->bn, c->stages, out);
-  int64_t s;
+  int64_t slots = resident_units(h, cg, c->bn, c->stages, out);
+  if (f.max_ctas) slots = std::min<int64_t>(slots, std::max<int64_t>(f.max_ctas / cg, 1));
+  int64_t s = 1, dp = c->tiles;
   if (f.splits) {
-    s = f.splits;
+    s = f.splits;  // forced: every tile is sliced
+    dp = 0;
   } else if (c->tiles * 2 <= slots && c->k_blocks >= 8) {
-    // Fewer tiles than half the resident units: slice K so every SM has work ("A
-    // Blackwell GEMM by Hand in CuTe DSL", section 9: decode shapes are decided by waves).
-    s = slots / c->tiles;
-    if (s > c->k_blocks / 4) s = c->k_blocks / 4;
-    if (s > 32) s = 32;
-    if (s < 1) s = 1;
-  } else {
-    s = 1;
+    // Fewer tiles than half the resident units: slice every tile along K so all SMs
+    // have work ("A Blackwell GEMM by Hand in CuTe DSL", section 9: decode shapes
+    // are decided by waves).
+    s = std::min<int64_t>({slots / c->tiles, c->k_blocks / 4, 32});
+    dp = 0;
+  } else if (c->tiles > slots && c->tiles % slots != 0 && c->k_blocks >= 8) {
+    // Whole waves run whole tiles; the tiles of the partial last wave are sliced so
+    // that the last wave keeps (nearly) every unit busy.
+    const int64_t rem = c->tiles % slots;
+    s = std::min<int64_t>({slots / rem, c->k_blocks / 4, 8});
+    dp = s >= 2 ? c->tiles - rem : c->tiles;
   }
+  if (s < 1) s = 1;
   if (s > c->k_blocks) s = c->k_blocks;
   const int64_t per = ceil_div(c->k_blocks, s);
   s = ceil_div(c->k_blocks, per);  // no empty slice
+  if (s == 1) dp = c->tiles;
   c->splits = (int)s;
   c->kb_per_split = (int)per;
-  c->units = c->tiles * s;
+  c->dp_tiles = dp;
+  c->units = dp + (c->tiles - dp) * s;
   c->group_m = f.group_m ? f.group_m : 16;
   c->chain_kb = f.chain_kblocks ? f.chain_kblocks : kChainKBlocks;
-  int64_t cap = slots;
-  if (f.max_ctas) cap = f.max_ctas / cg > 0 ? f.max_ctas / cg : 1;
-  if (cap > slots) cap = slots;
-  c->grid = (int)((c->units < cap ? c->units : cap) * cg);
+  c->grid = (int)(std::min<int64_t>(c->units, slots) * cg);
   if (c->units > INT32_MAX || c->tiles * cg * 8 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   return GEMM_OK;
 }
@@ -258,7 +264,7 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
   if (c.variant < 0 || c.variant > 2) return GEMM_ERR_INVALID_ARG;
   if (c.block_n != 0 && c.block_n != 128 && c.block_n != 256) return GEMM_ERR_INVALID_ARG;
   if (c.splits < 0 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
-      c.reserved != 0)
+      c.dp_tiles != 0)
     return GEMM_ERR_INVALID_ARG;
   if (c.stages) {
     const int bn = c.block_n ? c.block_n : 256;
@@ -339,6 +345,7 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.num_n_tiles = (int32_t)ch.num_n;
   p.tiles = (int32_t)ch.tiles;
   p.k_blocks = (int32_t)ch.k_blocks;
+  p.dp_tiles = (int32_t)ch.dp_tiles;
   p.splits = ch.splits;
   p.kb_per_split = ch.kb_per_split;
   p.units = (int32_t)ch.units;
@@ -351,16 +358,16 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.wait_limit_ns = h->wait_limit_ns;
   p.test_stall = h->test_stall;
   if (ch.splits > 1) {
-    const size_t ws =
-        (size_t)ch.tiles * ch.splits * kBlockM * ch.variant * ch.bn * sizeof(float);
-    st = ensure_workspace(h, ws, (size_t)ch.tiles * ch.variant * 8);
+    const size_t sliced = (size_t)(ch.tiles - ch.dp_tiles);
+    const size_t ws = sliced * ch.splits * kBlockM * ch.variant * ch.bn * sizeof(float);
+    st = ensure_workspace(h, ws, sliced * ch.variant * 8);
     if (st != GEMM_OK) return st;
     p.workspace = h->d_ws;
     p.counters = h->d_ctr;
   }
   if (launch_gemm(s) != cudaSuccess) return GEMM_ERR_CUDA;
   h->last = gemm_config_t{ch.variant, ch.bn,   ch.splits,   ch.stages,
-                          ch.group_m, ch.grid, ch.chain_kb, 0};
+                          ch.group_m, ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles};
   return GEMM_OK;
 }
 

@@ -96,17 +96,35 @@ __device__ __forceinline__ void pause_ns(uint64_t ns) {
 }
 
 struct Unit {
-  int32_t tile, split, m_blk, n_blk, kb0, kb1;
+  int32_t tile, split, nsplit, m_blk, n_blk, kb0, kb1;
 };
 
-// Work unit -> (tile, K slice) -> (m block, n block) with grouped rasterisation:
-// tiles are taken group_m M-blocks at a time, walking N inside a group, so units
-// running at the same time share A rows and B columns in L2 ("Matmul on sm_120",
-// block swizzle; "A Blackwell GEMM by Hand in CuTe DSL", section 8).
+// Work unit -> (tile, K slice) -> (m block, n block).
+// Units [0, dp_tiles) are whole tiles; the remaining tiles -- normally the last,
+// partial wave -- are each cut into `splits` K slices, so the tail of the grid is
+// spread over every SM instead of leaving most of them idle ("A Blackwell GEMM by
+// Hand in CuTe DSL", section 9: split-K / stream-K against wave quantisation).
+// With dp_tiles = 0 every tile is sliced (split-K for decode shapes).
+// Tiles map to (m, n) by grouped rasterisation: group_m M-blocks at a time, walking
+// N inside a group, so units running at the same time share A rows and B columns in
+// L2 ("Matmul on sm_120", block swizzle; "A Blackwell GEMM by Hand in CuTe DSL",
+// section 8).
 __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams& p) {
   Unit w;
-  w.tile = u / p.splits;
-  w.split = u - w.tile * p.splits;
+  if (u < p.dp_tiles) {
+    w.tile = u;
+    w.split = 0;
+    w.nsplit = 1;
+    w.kb0 = 0;
+    w.kb1 = p.k_blocks;
+  } else {
+    const int32_t v = u - p.dp_tiles;
+    w.tile = p.dp_tiles + v / p.splits;
+    w.split = v - (w.tile - p.dp_tiles) * p.splits;
+    w.nsplit = p.splits;
+    w.kb0 = w.split * p.kb_per_split;
+    w.kb1 = min(w.kb0 + p.kb_per_split, p.k_blocks);
+  }
   const int32_t group = p.group_m * p.num_n_tiles;
   const int32_t g = w.tile / group;
   const int32_t first_m = g * p.group_m;
@@ -114,8 +132,6 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams& p) {
   const int32_t r = w.tile - g * group;
   w.m_blk = first_m + r % gm;
   w.n_blk = r / gm;
-  w.kb0 = w.split * p.kb_per_split;
-  w.kb1 = min(w.kb0 + p.kb_per_split, p.k_blocks);
   return w;
 }
 
@@ -411,11 +427,12 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
 
       const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;  // first row of this CTA
       const int32_t n_half = w.n_blk * BN + (int32_t)h * kHalf;          // first column of the half
-      if (p.splits > 1) {
+      if (w.nsplit > 1) {
         // Split-K: this slice's fp32 rows go to the workspace; the last slice of the
         // block to arrive sums all slices in slice order.
         const size_t tile_rows = (size_t)kRowsTile;
-        float* ws_tile = p.workspace + (size_t)w.tile * p.splits * tile_rows * BN;
+        const size_t sliced = (size_t)(w.tile - p.dp_tiles);  // index among sliced tiles
+        float* ws_tile = p.workspace + sliced * p.splits * tile_rows * BN;
         const size_t my_row = (size_t)rank * kBlockM + row;
         float* mine = ws_tile + ((size_t)w.split * tile_rows + my_row) * BN + h * kHalf;
 #pragma unroll
@@ -426,7 +443,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         __syncwarp();
         uint32_t last = 0;
         if (lane == 0) {
-          uint32_t* ctr = p.counters + (((size_t)w.tile * CTA_GROUP + rank) * 4 + q) * 2 + h;
+          uint32_t* ctr = p.counters + ((sliced * CTA_GROUP + rank) * 4 + q) * 2 + h;
           const uint32_t before = atomicAdd(ctr, 1u);
           last = (before == (uint32_t)p.splits - 1u) ? 1u : 0u;
           if (last) atomicExch(ctr, 0u);  // ready for the next launch

@@ -204,6 +204,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   p.num_n_tiles = (int32_t)num_n;
   p.tiles = (int32_t)tiles;
   p.k_blocks = (int32_t)k_blocks;
+  p.dp_tiles = splits > 1 ? 0 : (int32_t)tiles;
   p.splits = (int32_t)splits;
   p.kb_per_split = (int32_t)per;
   p.units = (int32_t)units;

@@ -37,9 +37,10 @@ struct GemmParams {
   int32_t num_n_tiles;     // ceil(N / BN)
   int32_t tiles;           // num_m_tiles * num_n_tiles
   int32_t k_blocks;        // ceil(K / 64)
-  int32_t splits;          // K slices per tile (1 = no split)
+  int32_t dp_tiles;        // tiles [0, dp_tiles) run whole, one unit each
+  int32_t splits;          // K slices of each later tile (1 = no split)
   int32_t kb_per_split;    // k-blocks per slice (the last slice may be shorter)
-  int32_t units;           // tiles * splits
+  int32_t units;           // dp_tiles + (tiles - dp_tiles) * splits
   int32_t group_m;         // grouped rasterisation: M-tiles per group
   int32_t chain_kb;        // k-blocks per TMEM accumulation chain
   int32_t vec_store;       // 1 when 16-byte vector stores of C are aligned

@@ -67,6 +67,10 @@ typedef enum {
  *             before the epilogue adds it into its fp32 registers (0 = 64, i.e.
  *             K 4096: the tensor core's fp32 accumulation error grows with the
  *             length of one accumulation chain)
+ *   dp_tiles  reported by gemm_last_config only (must be 0 on input): how many
+ *             tiles ran whole; the rest were cut into `splits` K slices.  A forced
+ *             `splits` slices every tile; automatically, only tiles of a partial
+ *             last wave are sliced (or all tiles, when there are too few for the SMs).
  */
 typedef struct {
   int32_t variant;
@@ -76,7 +80,7 @@ typedef struct {
   int32_t group_m;
   int32_t max_ctas;
   int32_t chain_kblocks;
-  int32_t reserved;
+  int32_t dp_tiles;
 } gemm_config_t;
 
 /* Create a handle on the current CUDA device.  Fails with GEMM_ERR_UNSUPPORTED

@@ -104,6 +104,25 @@ def test_persistent_loops_many_units_per_cta(g, variant, max_ctas):
 
 
 @pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("max_ctas,M,N,K", [(10, 640, 1024, 704), (6, 512, 1280, 2048),
+                                             (14, 300, 2100, 1000)])
+def test_partial_last_wave_is_sliced(g, variant, max_ctas, M, N, K):
+    # more tiles than resident units, not a whole number of waves: the tiles of the
+    # last wave are cut along K and reduced in the kernel, the others run whole
+    g.set_config(variant=variant, max_ctas=max_ctas)
+    try:
+        _case(g, M, N, K, F16, F16, seed=38)
+        _case(g, M, N, K, BF16, F32, seed=39, exact=True, ints=True)
+        cfg = g.last_config()
+        tiles = -(-M // (128 * variant)) * -(-N // 256)
+        units = max_ctas // variant
+        if tiles % units:
+            assert cfg["splits"] > 1 and cfg["dp_tiles"] == tiles - tiles % units, cfg
+    finally:
+        g.reset_config()
+
+
+@pytest.mark.parametrize("variant", [1, 2])
 @pytest.mark.parametrize("chain", [1, 3, 5, 64])
 @pytest.mark.parametrize("splits", [1, 3])
 def test_accumulation_chains(g, variant, chain, splits):
