@@ -116,8 +116,11 @@ def test_partial_last_wave_is_sliced(g, variant, max_ctas, M, N, K):
         cfg = g.last_config()
         tiles = -(-M // (128 * variant)) * -(-N // 256)
         units = max_ctas // variant
-        if tiles % units:
-            assert cfg["splits"] > 1 and cfg["dp_tiles"] == tiles - tiles % units, cfg
+        rem, kb = tiles % units, -(-K // 64)
+        if tiles > units and rem and min(units // rem, kb // 4, 8) >= 2:
+            assert cfg["splits"] > 1 and cfg["dp_tiles"] == tiles - rem, cfg
+        else:
+            assert cfg["splits"] == 1 and cfg["dp_tiles"] == tiles, cfg
     finally:
         g.reset_config()
 
