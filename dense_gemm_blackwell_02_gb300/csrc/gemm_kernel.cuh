@@ -428,22 +428,27 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;  // first row of this CTA
       const int32_t n_half = w.n_blk * BN + (int32_t)h * kHalf;          // first column of the half
       if (w.nsplit > 1) {
-        // Split-K: this slice's fp32 rows go to the workspace; the last slice of the
-        // block to arrive sums all slices in slice order.
-        const size_t tile_rows = (size_t)kRowsTile;
-        const size_t sliced = (size_t)(w.tile - p.dp_tiles);  // index among sliced tiles
-        float* ws_tile = p.workspace + sliced * p.splits * tile_rows * BN;
-        const size_t my_row = (size_t)rank * kBlockM + row;
-        float* mine = ws_tile + ((size_t)w.split * tile_rows + my_row) * BN + h * kHalf;
+        // Split-K: this slice's fp32 block (the warp's 32 rows x BN/2 columns) goes to
+        // the workspace; the last slice of the block to arrive sums all slices in slice
+        // order.  Within a block, each group of 4 columns holds the warp's 32 rows
+        // contiguously (float index (col / 4) * 128 + lane * 4 + col % 4), so every
+        // warp-wide 16-byte access covers 512 contiguous bytes.
+        constexpr size_t kBlockFloats = 32 * kHalf;
+        constexpr size_t kBlocksPerSlice = (size_t)CTA_GROUP * 8;  // (rank, quarter, half)
+        const size_t sliced = (size_t)(w.tile - p.dp_tiles);      // index among sliced tiles
+        const size_t my_block = ((size_t)rank * 4 + q) * 2 + h;
+        float* ws_tile = p.workspace + sliced * p.splits * kBlocksPerSlice * kBlockFloats;
+        float* mine = ws_tile + ((size_t)w.split * kBlocksPerSlice + my_block) * kBlockFloats +
+                      lane * 4;
 #pragma unroll
         for (int j = 0; j < kHalf; j += 4)
-          st_global_cg_v4(mine + j, __float_as_uint(acc[j]), __float_as_uint(acc[j + 1]),
+          st_global_cg_v4(mine + j * 32, __float_as_uint(acc[j]), __float_as_uint(acc[j + 1]),
                           __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
         __threadfence();
         __syncwarp();
         uint32_t last = 0;
         if (lane == 0) {
-          uint32_t* ctr = p.counters + ((sliced * CTA_GROUP + rank) * 4 + q) * 2 + h;
+          uint32_t* ctr = p.counters + sliced * kBlocksPerSlice + my_block;
           const uint32_t before = atomicAdd(ctr, 1u);
           last = (before == (uint32_t)p.splits - 1u) ? 1u : 0u;
           if (last) atomicExch(ctr, 0u);  // ready for the next launch
@@ -455,10 +460,11 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         // Sum the slices in slice order: the result is the same whichever slice
         // arrived last.
         for (int32_t s = 0; s < p.splits; ++s) {
-          const float* src = ws_tile + ((size_t)s * tile_rows + my_row) * BN + h * kHalf;
+          const float* src =
+              ws_tile + ((size_t)s * kBlocksPerSlice + my_block) * kBlockFloats + lane * 4;
 #pragma unroll
           for (int j = 0; j < kHalf; j += 4) {
-            const uint4 x = ld_global_cg_v4(src + j);
+            const uint4 x = ld_global_cg_v4(src + j * 32);
             if (s == 0) {
               acc[j] = __uint_as_float(x.x);
               acc[j + 1] = __uint_as_float(x.y);
