@@ -88,6 +88,14 @@ static __device__ __noinline__ bool wait_parity_drain(uint32_t bar, uint32_t par
   }
 }
 
+// Warp-uniform wait: lane 0 polls, the whole warp follows its verdict.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                          uint32_t site) {
+  uint32_t ok = 0;
+  if (lane_id() == 0) ok = wait_parity(bar, parity, c, site) ? 1u : 0u;
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
 // Bounded pause (used by a pair's follower while aborting, so copies it issued can land).
 __device__ __forceinline__ void pause_ns(uint64_t ns) {
   const uint64_t t0 = globaltimer_ns();
@@ -281,39 +289,40 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer --
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
-      bool ok = true;
-      for (int32_t u = first_unit; u < p.units && ok; u += unit_stride) {
-        const Unit w = decode_unit(u, p);
-        const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
-        const int32_t b_row = w.n_blk * BN + (int32_t)rank * L::kRowsB;
-        for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!wait_parity(empty_bar(stage), phase ^ 1u, ctl, kSiteEmpty)) {
-            ok = false;
-            break;
-          }
-          if constexpr (CTA_GROUP == 1) {
-            mbar_arrive_expect_tx(full_bar(stage), L::kTxBytes);
-            tma_load_2d(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, full_bar(stage));
-            tma_load_2d(sB + stage * L::kBBytes, &tmB, kb * kBlockK, b_row, full_bar(stage));
-          } else {
-            // Both CTAs' copies complete on the leader's full barrier; the leader
-            // arms it with the bytes of the pair.
-            const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
-            if (leader) mbar_arrive_expect_tx(full_bar(stage), L::kTxBytes);
-            tma_load_2d_pair(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, leader_full);
-            tma_load_2d_pair(sB + stage * L::kBBytes, &tmB, kb * kBlockK, b_row, leader_full);
-          }
-          armed |= 1u << stage;
-          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+    // The whole warp runs the loop; one elected lane issues each copy.
+    uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
+    bool ok = true;
+    for (int32_t u = first_unit; u < p.units && ok; u += unit_stride) {
+      const Unit w = decode_unit(u, p);
+      const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
+      const int32_t b_row = w.n_blk * BN + (int32_t)rank * L::kRowsB;
+      for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+        if (!warp_wait(empty_bar(stage), phase ^ 1u, ctl, kSiteEmpty)) {
+          ok = false;
+          break;
+        }
+        if constexpr (CTA_GROUP == 1) {
+          mbar_arrive_expect_tx_elect(full_bar(stage), L::kTxBytes);
+          tma_load_2d_elect(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, full_bar(stage));
+          tma_load_2d_elect(sB + stage * L::kBBytes, &tmB, kb * kBlockK, b_row, full_bar(stage));
+        } else {
+          // Both CTAs' copies complete on the leader's full barrier; the leader arms it
+          // with the bytes of the pair.
+          const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
+          if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), L::kTxBytes);
+          tma_load_2d_pair_elect(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, leader_full);
+          tma_load_2d_pair_elect(sB + stage * L::kBBytes, &tmB, kb * kBlockK, b_row, leader_full);
+        }
+        armed |= 1u << stage;
+        armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      // No copy may still be landing in shared memory when the CTA exits.
+    }
+    // No copy may still be landing in shared memory when the CTA exits.
+    if (lane == 0) {
       if (leader) {
         for (uint32_t s = 0; s < STAGES; ++s)
           if (armed & (1u << s)) wait_parity_drain(full_bar(s), (armed_phase >> s) & 1u, ctl);
@@ -327,50 +336,55 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer --
-    if (lane == 0 && leader) {
+    // In the leader the whole warp runs the loop, one elected lane issues the MMAs
+    // and commits; descriptors advance by adding the stage offset (>> 4) to the
+    // start-address field and 2 (32 bytes) per 16-deep K step.
+    if (leader) {
       uint32_t stage = 0, phase = 0, iter = 0;
       bool ok = true;
-      if (p.test_stall) ok = wait_parity(drain_bar, 0, ctl, kSiteTestStall);
+      const uint64_t desc_a0 = smem_desc_sw128_kmajor(sA);
+      const uint64_t desc_b0 = smem_desc_sw128_kmajor(sB);
+      if (p.test_stall) ok = warp_wait(drain_bar, 0, ctl, kSiteTestStall);
       for (int32_t u = first_unit; u < p.units && ok; u += unit_stride) {
         const Unit w = decode_unit(u, p);
         for (int32_t c0 = w.kb0; c0 < w.kb1 && ok; c0 += p.chain_kb) {
           const int32_t c1 = min(c0 + p.chain_kb, w.kb1);
           const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
-          if (!wait_parity(acc_empty_bar(slot), acc_phase ^ 1u, ctl, kSiteAccEmpty)) {
+          if (!warp_wait(acc_empty_bar(slot), acc_phase ^ 1u, ctl, kSiteAccEmpty)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + slot * BN;
           for (int32_t kb = c0; kb < c1; ++kb) {
-            if (!wait_parity(full_bar(stage), phase, ctl, kSiteFull)) {
+            if (!warp_wait(full_bar(stage), phase, ctl, kSiteFull)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a0 = sA + stage * L::kABytes, b0 = sB + stage * L::kBBytes;
+            const uint64_t da = desc_a0 + ((stage * L::kABytes) >> 4);
+            const uint64_t db = desc_b0 + ((stage * L::kBBytes) >> 4);
 #pragma unroll
             for (uint32_t k = 0; k < kBlockK / 16; ++k)
-              umma_f16<CTA_GROUP>(d_tmem, smem_desc_sw128_kmajor(a0 + 32u * k),
-                                  smem_desc_sw128_kmajor(b0 + 32u * k), p.idesc,
-                                  (kb > c0 || k > 0) ? 1u : 0u);
+              umma_f16_elect<CTA_GROUP>(d_tmem, da + 2u * k, db + 2u * k, p.idesc,
+                                        (kb > c0 || k > 0) ? 1u : 0u);
             // the stage is free (in both CTAs) once these MMAs are done
-            if constexpr (CTA_GROUP == 1) umma_commit_group<1>(empty_bar(stage));
-            else umma_commit_pair(empty_bar(stage), 0x3);
+            if constexpr (CTA_GROUP == 1) umma_commit_elect<1>(empty_bar(stage));
+            else umma_commit_pair_elect(empty_bar(stage), 0x3);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          if constexpr (CTA_GROUP == 1) umma_commit_group<1>(acc_full_bar(slot));
-          else umma_commit_pair(acc_full_bar(slot), 0x3);
+          if constexpr (CTA_GROUP == 1) umma_commit_elect<1>(acc_full_bar(slot));
+          else umma_commit_pair_elect(acc_full_bar(slot), 0x3);
           ++iter;
         }
       }
       // Every issued MMA must finish before TMEM is released.
-      umma_commit_group<CTA_GROUP>(drain_bar);
-      wait_parity_drain(drain_bar, 0, ctl);
+      umma_commit_elect<CTA_GROUP>(drain_bar);
+      if (lane == 0) wait_parity_drain(drain_bar, 0, ctl);
     }
     __syncwarp();
   } else {

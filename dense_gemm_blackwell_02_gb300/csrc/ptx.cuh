@@ -78,6 +78,25 @@ __device__ __forceinline__ bool mbar_try_wait_cluster_acq(uint32_t bar, uint32_t
   return ok != 0;
 }
 
+// ------------------------------------------------- warp-uniform single issue --
+// The producer and MMA warps run their loops with all 32 lanes in lock-step, so the
+// compiler keeps loop state and descriptors warp-uniform; each asynchronous
+// instruction is then issued by exactly one lane, chosen inside the asm block with
+// elect.sync.  (Issuing from a loop that only lane 0 executes measured 227 cycles per
+// tcgen05.mma on sm_103a; the warp-uniform form issues a 128 x 256 x 16 MMA every 128
+// cycles, the tensor core's rate.)
+#define GB300_ELECT "{\n\t.reg .pred e_;\n\t.reg .b32 r_;\n\telect.sync r_|e_, 0xffffffff;\n\t"
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32_t bytes) {
+  asm volatile(GB300_ELECT "@e_ mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_elect(uint32_t bar) {
+  asm volatile(GB300_ELECT "@e_ mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+
 // --------------------------------------------------------------------- fences --
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -126,6 +145,25 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_elect(uint32_t dst, const void* tmap, int32_t c0,
+                                                  int32_t c1, uint32_t bar) {
+  asm volatile(GB300_ELECT
+               "@e_ cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+               " [%0], [%1, {%2, %3}], [%4];\n\t}" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_elect(uint32_t dst, const void* tmap, int32_t c0,
+                                                       int32_t c1, uint32_t cluster_bar) {
+  asm volatile(
+      GB300_ELECT
+      "@e_ cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(cluster_bar)
       : "memory");
 }
 
@@ -222,6 +260,44 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// Warp-uniform forms: every lane executes them, one elected lane issues.
+template <int CTA_GROUP>
+__device__ __forceinline__ void umma_f16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  if constexpr (CTA_GROUP == 1)
+    asm volatile(GB300_ELECT ".reg .pred p_;\n\tsetp.ne.b32 p_, %4, 0;\n\t"
+                 "@e_ tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p_;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+  else
+    asm volatile(GB300_ELECT ".reg .pred p_;\n\tsetp.ne.b32 p_, %4, 0;\n\t"
+                 "@e_ tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p_;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+template <int CTA_GROUP>
+__device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
+  if constexpr (CTA_GROUP == 1)
+    asm volatile(GB300_ELECT
+                 "@e_ tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+                     bar)
+                 : "memory");
+  else
+    asm volatile(GB300_ELECT
+                 "@e_ tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_pair_elect(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(GB300_ELECT
+               "@e_ tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+               " [%0], %1;\n\t}" ::"r"(bar),
+               "h"(cta_mask)
+               : "memory");
 }
 
 // Make `bar` (this CTA) arrive once all previously issued MMAs of this thread completed.
