@@ -88,12 +88,26 @@ static __device__ __noinline__ bool wait_parity_drain(uint32_t bar, uint32_t par
   }
 }
 
-// Warp-uniform wait: lane 0 polls, the whole warp follows its verdict.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& c,
-                                          uint32_t site) {
-  uint32_t ok = 0;
-  if (lane_id() == 0) ok = wait_parity(bar, parity, c, site) ? 1u : 0u;
-  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+// Warp-collective wait: all 32 lanes poll together and leave together (a phase, once
+// complete, stays complete, so one lane seeing it is enough), so the warp never
+// diverges around the wait.  Lane 0's clock decides the timeout for the warp.
+static __device__ __noinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                              uint32_t site) {
+  if (__any_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (__any_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
+    if ((it & 31u) == 0u) {
+      const bool aborting = *c.abort_flag != 0;
+      const bool expired = globaltimer_ns() - t0 > c.limit_ns || it > (1u << 26);
+      if (__shfl_sync(0xFFFFFFFFu, aborting ? 1u : 0u, 0)) return false;
+      if (__shfl_sync(0xFFFFFFFFu, expired ? 1u : 0u, 0)) {
+        if (lane_id() == 0) record_timeout(c, site);
+        __syncwarp();
+        return false;
+      }
+    }
+  }
 }
 
 // Bounded pause (used by a pair's follower while aborting, so copies it issued can land).
