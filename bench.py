@@ -148,6 +148,42 @@ def cpu_rows_sample(A, B, din, dout, M, target_s=10.0):
     return rows, bits, c64, dt, os.cpu_count()
 
 
+def measure_decode(g, dev, stream, flush, peaks, iters=10):
+    """Secondary figures: the M = 256 decode shapes (fp16 -> fp16), HBM-bound, timed
+    like the main workload (events per launch, L2 flushed between launches).  Their
+    parity is covered by the full-size tests; here only time is taken."""
+    wl = si.WORKLOADS["decode_m256"]
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    out = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.seed)
+    for s in wl.shapes:
+        A = (torch.rand(s.M, s.K, generator=gen, device=dev) * 2 - 1).half()
+        B = (torch.rand(s.N, s.K, generator=gen, device=dev) * 2 - 1).half()
+        C = torch.empty(s.M, s.N, dtype=torch.float16, device=dev)
+        for _ in range(3):
+            flush.fill_(0.5)
+            g.run(A, B, C, stream=stream)
+        ev = []
+        for i in range(iters):
+            flush.fill_(float(i))
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.run(A, B, C, stream=stream)
+            e1.record(stream)
+            ev.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = sorted(a.elapsed_time(b) for a, b in ev)[iters // 2]
+        gbs = rl.gemm_bytes(s.M, s.N, s.K, 2, 2) / (ms * 1e-3) / 1e9
+        out[f"{s.M}x{s.N}x{s.K}"] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                                     "frac_of_hbm": round(gbs / hbm, 4),
+                                     "TFLOP/s": round(rl.gemm_flops(s.M, s.N, s.K) / (ms * 1e-3) / 1e12, 1),
+                                     "kernel": g.last_config()}
+        del A, B, C
+    return out
+
+
 def run_reference(args):
     """The oracle as it stands, timed on the host cores on bounded samples."""
     ws, rank, _ = dist_env()
@@ -250,6 +286,7 @@ def run_ours(args):
     if code != 0:
         raise RuntimeError(f"device status after timing: {code} ({word:#x})")
     cfg = g.last_config()
+    decode = measure_decode(g, dev, stream, flush, peaks) if args.decode else None
     flops = rl.gemm_flops(M, N, K)
     ms_per_step = total_ms / args.steps
     value = ws * flops * args.steps / (total_ms * 1e-3) / 1e12
@@ -310,6 +347,8 @@ def run_ours(args):
                                        f" GFLOP) in {cpu_s:.1f} s"},
             "parity": {"rows_checked": len(rows), **metrics},
         }
+        if decode is not None:
+            line["decode"] = decode
         print(json.dumps(line))
     g.close()
     if ws > 1:
@@ -326,6 +365,8 @@ def main():
     ap.add_argument("--workload", default="square_4096", choices=sorted(si.WORKLOADS))
     ap.add_argument("--config", default=None, help="JSON gemm_config_t override (sweeps)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--decode", type=int, default=1,
+                    help="also time the M=256 decode shapes (HBM GB/s) into the line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
