@@ -87,7 +87,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -112,7 +112,7 @@ class ClockSampler:
                              "sw_power": parts[9]})
             except ValueError:
                 continue
-        loaded = [r for r in rows if r["util"] >= 50] or rows
+        loaded = [r for r in rows if r["util"] >= 30] or rows
         if not loaded:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         reasons = []
@@ -256,12 +256,10 @@ def run_ours(args):
 
     sampler = ClockSampler(local)
     sampler.start()
-    # keep the GPU busy for a moment so the sampler sees the clocks under load
-    t_end = time.perf_counter() + 0.6
-    while time.perf_counter() < t_end:
-        for _ in range(20):
-            step()
-        torch.cuda.synchronize()
+    time.sleep(0.25)  # let the sampler take its first reading
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1.0)
+        step()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if ws > 1:
@@ -275,6 +273,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
+    time.sleep(0.1)
     clocks = sampler.stop()
     per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     total_ms = sum(per_ms)
