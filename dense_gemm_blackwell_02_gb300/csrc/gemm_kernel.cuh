@@ -378,13 +378,11 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
             tc_fence_after();
             const uint64_t da = desc_a0 + ((stage * L::kABytes) >> 4);
             const uint64_t db = desc_b0 + ((stage * L::kBBytes) >> 4);
-#pragma unroll
-            for (uint32_t k = 0; k < kBlockK / 16; ++k)
-              umma_f16_elect<CTA_GROUP>(d_tmem, da + 2u * k, db + 2u * k, p.idesc,
-                                        (kb > c0 || k > 0) ? 1u : 0u);
-            // the stage is free (in both CTAs) once these MMAs are done
-            if constexpr (CTA_GROUP == 1) umma_commit_elect<1>(empty_bar(stage));
-            else umma_commit_pair_elect(empty_bar(stage), 0x3);
+            // four K=16 MMAs, then the commit that frees the stage (in both CTAs) once
+            // they are done
+            static_assert(kBlockK == 64, "umma_stage_elect issues four K=16 MMAs");
+            umma_stage_elect<CTA_GROUP>(d_tmem, da, db, p.idesc, kb > c0 ? 1u : 0u,
+                                        empty_bar(stage));
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
