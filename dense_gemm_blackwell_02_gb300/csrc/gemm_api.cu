@@ -115,7 +115,7 @@ size_t out_size(gemm_dtype_t d) { return d == GEMM_F32 ? 4 : 2; }
 bool valid_dtype(int d) { return d == GEMM_F16 || d == GEMM_BF16 || d == GEMM_F32; }
 
 struct Choice {
-  int variant, bn, stages, splits, kb_per_split, group_m, grid, chain_kb;
+  int variant, bn, stages, splits, kb_per_split, group_m, grid, chain_kb, half_tail;
   int64_t tiles, dp_tiles, units, k_blocks, num_m, num_n;
 };
 
@@ -148,6 +148,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
   int64_t slots = resident_units(h, cg, c->bn, c->stages, out);
   if (f.max_ctas) slots = std::min<int64_t>(slots, std::max<int64_t>(f.max_ctas / cg, 1));
   int64_t s = 1, dp = c->tiles;
+  c->half_tail = 0;
   if (f.splits) {
     s = f.splits;  // forced: every tile is sliced
     dp = 0;
@@ -157,22 +158,28 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
     // are decided by waves).
     s = std::min<int64_t>({slots / c->tiles, c->k_blocks / 4, 32});
     dp = 0;
-  } else if (c->tiles > slots && c->tiles % slots != 0 && c->k_blocks >= 8) {
-    // Whole waves run whole tiles; the tiles of the partial last wave are sliced so
-    // that the last wave keeps (nearly) every unit busy.
+  } else if (c->tiles > slots && c->tiles % slots != 0) {
+    // Whole waves run whole tiles; the tiles of the partial last wave are spread over
+    // more units so that the last wave keeps (nearly) every unit busy: as two
+    // 128-column halves when they fit (no reduction), else as K slices.
     const int64_t rem = c->tiles % slots;
-    s = std::min<int64_t>({slots / rem, c->k_blocks / 4, 8});
-    dp = s >= 2 ? c->tiles - rem : c->tiles;
+    if (c->bn == 256 && 2 * rem <= slots) {
+      c->half_tail = 1;
+      dp = c->tiles - rem;
+    } else if (c->k_blocks >= 8) {
+      s = std::min<int64_t>({slots / rem, c->k_blocks / 4, 8});
+      dp = s >= 2 ? c->tiles - rem : c->tiles;
+    }
   }
   if (s < 1) s = 1;
   if (s > c->k_blocks) s = c->k_blocks;
   const int64_t per = ceil_div(c->k_blocks, s);
   s = ceil_div(c->k_blocks, per);  // no empty slice
-  if (s == 1) dp = c->tiles;
+  if (s == 1 && !c->half_tail) dp = c->tiles;
   c->splits = (int)s;
   c->kb_per_split = (int)per;
   c->dp_tiles = dp;
-  c->units = dp + (c->tiles - dp) * s;
+  c->units = dp + (c->tiles - dp) * (c->half_tail ? 2 : s);
   c->group_m = f.group_m ? f.group_m : 16;
   c->chain_kb = f.chain_kblocks ? f.chain_kblocks : kChainKBlocks;
   c->grid = (int)(std::min<int64_t>(c->units, slots) * cg);
@@ -333,8 +340,10 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   const bool c_tma = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0;
   if (!make_map(h, A, M, K, dtype_in, kBlockM, &s.tmA) ||
       !make_map(h, B, N, K, dtype_in, ch.bn / ch.variant, &s.tmB) ||
+      (ch.half_tail && !make_map(h, B, N, K, dtype_in, ch.bn / ch.variant / 2, &s.tmB2)) ||
       (c_tma && !make_map(h, C, M, N, dtype_out, 32, &s.tmC)))
     return GEMM_ERR_CUDA;
+  if (!ch.half_tail) s.tmB2 = s.tmB;
 
   GemmParams& p = s.p;
   p.C = C;
@@ -346,6 +355,7 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.tiles = (int32_t)ch.tiles;
   p.k_blocks = (int32_t)ch.k_blocks;
   p.dp_tiles = (int32_t)ch.dp_tiles;
+  p.half_tail = ch.half_tail;
   p.splits = ch.splits;
   p.kb_per_split = ch.kb_per_split;
   p.units = (int32_t)ch.units;
@@ -354,10 +364,11 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.vec_store = c_tma ? 1 : 0;
   p.tma_store = c_tma ? 1 : 0;
   p.idesc = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn, dtype_in == GEMM_BF16);
+  p.idesc_half = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn / 2, dtype_in == GEMM_BF16);
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
   p.test_stall = h->test_stall;
-  if (ch.splits > 1) {
+  if (ch.splits > 1 && !ch.half_tail) {
     const size_t sliced = (size_t)(ch.tiles - ch.dp_tiles);
     const size_t ws = sliced * ch.splits * kBlockM * ch.variant * ch.bn * sizeof(float);
     st = ensure_workspace(h, ws, sliced * ch.variant * 8);

@@ -119,22 +119,33 @@ __device__ __forceinline__ void pause_ns(uint64_t ns) {
 
 struct Unit {
   int32_t tile, split, nsplit, m_blk, n_blk, kb0, kb1;
+  int32_t half;  // -1: the whole BN columns; 0 / 1: that BN/2-column half of the tile
 };
 
-// Work unit -> (tile, K slice) -> (m block, n block).
-// Units [0, dp_tiles) are whole tiles; the remaining tiles -- normally the last,
-// partial wave -- are each cut into `splits` K slices, so the tail of the grid is
-// spread over every SM instead of leaving most of them idle ("A Blackwell GEMM by
-// Hand in CuTe DSL", section 9: split-K / stream-K against wave quantisation).
-// With dp_tiles = 0 every tile is sliced (split-K for decode shapes).
+// Work unit -> (tile, K slice or column half) -> (m block, n block).
+// Units [0, dp_tiles) are whole tiles.  The remaining tiles -- normally the last,
+// partial wave -- are spread over more SMs instead of leaving most of them idle ("A
+// Blackwell GEMM by Hand in CuTe DSL", section 9, against wave quantisation): either
+// as two BN/2-column halves with the whole K (half_tail; no reduction needed), or as
+// `splits` K slices reduced in the kernel.  With dp_tiles = 0 every tile is sliced
+// along K (split-K for decode shapes).
 // Tiles map to (m, n) by grouped rasterisation: group_m M-blocks at a time, walking
 // N inside a group, so units running at the same time share A rows and B columns in
 // L2 ("Matmul on sm_120", block swizzle; "A Blackwell GEMM by Hand in CuTe DSL",
 // section 8).
 __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams& p) {
   Unit w;
+  w.half = -1;
   if (u < p.dp_tiles) {
     w.tile = u;
+    w.split = 0;
+    w.nsplit = 1;
+    w.kb0 = 0;
+    w.kb1 = p.k_blocks;
+  } else if (p.half_tail) {
+    const int32_t v = u - p.dp_tiles;
+    w.tile = p.dp_tiles + (v >> 1);
+    w.half = v & 1;
     w.split = 0;
     w.nsplit = 1;
     w.kb0 = 0;
@@ -217,6 +228,7 @@ struct Layout {
   static constexpr uint32_t kBBytes = kRowsB * kBlockK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;   // per CTA
   static constexpr uint32_t kTxBytes = kStageBytes * CTA_GROUP;  // expected on the leader
+  static constexpr uint32_t kTxBytesHalf = (kABytes + kBBytes / 2) * CTA_GROUP;  // half-tile unit
   static constexpr uint32_t kStagingBytes = 32 * 128;           // one 32-row x 128 B box
   static constexpr uint32_t kAOff = 0;
   static constexpr uint32_t kBOff = STAGES * kABytes;
@@ -237,7 +249,8 @@ struct Layout {
 template <int CTA_GROUP, int BN, int STAGES, int OUT>
 __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
+                const GemmParams p) {
   using L = Layout<CTA_GROUP, BN, STAGES>;
   static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
   static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "CTA_GROUP must be 1 or 2");
@@ -289,6 +302,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     fence_mbarrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.half_tail) tma_prefetch_desc(&tmB2);
     if (p.tma_store) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
@@ -309,23 +323,29 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     for (int32_t u = first_unit; u < p.units && ok; u += unit_stride) {
       const Unit w = decode_unit(u, p);
       const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
-      const int32_t b_row = w.n_blk * BN + (int32_t)rank * L::kRowsB;
+      // a half-tile unit loads half the B rows (through the half-height map tmB2)
+      const bool half = w.half >= 0;
+      const int32_t b_row = w.n_blk * BN +
+                            (half ? w.half * (BN / 2) + (int32_t)rank * (L::kRowsB / 2)
+                                  : (int32_t)rank * L::kRowsB);
+      const CUtensorMap* mapB = half ? &tmB2 : &tmB;
+      const uint32_t tx = half ? L::kTxBytesHalf : L::kTxBytes;
       for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
         if (!warp_wait(empty_bar(stage), phase ^ 1u, ctl, kSiteEmpty)) {
           ok = false;
           break;
         }
         if constexpr (CTA_GROUP == 1) {
-          mbar_arrive_expect_tx_elect(full_bar(stage), L::kTxBytes);
+          mbar_arrive_expect_tx_elect(full_bar(stage), tx);
           tma_load_2d_elect(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, full_bar(stage));
-          tma_load_2d_elect(sB + stage * L::kBBytes, &tmB, kb * kBlockK, b_row, full_bar(stage));
+          tma_load_2d_elect(sB + stage * L::kBBytes, mapB, kb * kBlockK, b_row, full_bar(stage));
         } else {
           // Both CTAs' copies complete on the leader's full barrier; the leader arms it
           // with the bytes of the pair.
           const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
-          if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), L::kTxBytes);
+          if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), tx);
           tma_load_2d_pair_elect(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, leader_full);
-          tma_load_2d_pair_elect(sB + stage * L::kBBytes, &tmB, kb * kBlockK, b_row, leader_full);
+          tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kBlockK, b_row, leader_full);
         }
         armed |= 1u << stage;
         armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -361,6 +381,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       if (p.test_stall) ok = warp_wait(drain_bar, 0, ctl, kSiteTestStall);
       for (int32_t u = first_unit; u < p.units && ok; u += unit_stride) {
         const Unit w = decode_unit(u, p);
+        const uint32_t idesc = w.half >= 0 ? p.idesc_half : p.idesc;
         for (int32_t c0 = w.kb0; c0 < w.kb1 && ok; c0 += p.chain_kb) {
           const int32_t c1 = min(c0 + p.chain_kb, w.kb1);
           const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
@@ -381,7 +402,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
             // four K=16 MMAs, then the commit that frees the stage (in both CTAs) once
             // they are done
             static_assert(kBlockK == 64, "umma_stage_elect issues four K=16 MMAs");
-            umma_stage_elect<CTA_GROUP>(d_tmem, da, db, p.idesc, kb > c0 ? 1u : 0u,
+            umma_stage_elect<CTA_GROUP>(d_tmem, da, db, idesc, kb > c0 ? 1u : 0u,
                                         empty_bar(stage));
             if (++stage == STAGES) {
               stage = 0;
@@ -410,6 +431,9 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     bool ok = true;
     for (int32_t u = first_unit; u < p.units && ok; u += unit_stride) {
       const Unit w = decode_unit(u, p);
+      // In a half-tile unit the accumulator holds BN/2 columns: the h = 0 warps own
+      // them, the h = 1 warps only take part in the slot hand-over.
+      const bool active = w.half < 0 || h == 0;
       float acc[kHalf];
       const int32_t nchains = chains_of(w, p.chain_kb);
       for (int32_t ch = 0; ch < nchains; ++ch) {
@@ -426,17 +450,19 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * BN + h * kHalf;
+        if (active) {
 #pragma unroll
-        for (int pc = 0; pc < kPieces; ++pc) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + 32u * pc, r);
-          tmem_ld_wait(r);
-          if (ch == 0) {
+          for (int pc = 0; pc < kPieces; ++pc) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + 32u * pc, r);
+            tmem_ld_wait(r);
+            if (ch == 0) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[32 * pc + j] = __uint_as_float(r[j]);
-          } else {
+              for (int j = 0; j < 32; ++j) acc[32 * pc + j] = __uint_as_float(r[j]);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[32 * pc + j] += __uint_as_float(r[j]);
+              for (int j = 0; j < 32; ++j) acc[32 * pc + j] += __uint_as_float(r[j]);
+            }
           }
         }
         // The slot is free for the next chain as soon as the loads are done.
@@ -450,9 +476,11 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         ++iter;
       }
       if (!ok) break;
+      if (!active) continue;
 
       const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;  // first row of this CTA
-      const int32_t n_half = w.n_blk * BN + (int32_t)h * kHalf;          // first column of the half
+      // first column written by this warp
+      const int32_t n_half = w.n_blk * BN + (w.half >= 0 ? w.half : (int32_t)h) * kHalf;
       if (w.nsplit > 1) {
         // Split-K: this slice's fp32 block (the warp's 32 rows x BN/2 columns) goes to
         // the workspace; the last slice of the block to arrive sums all slices in slice

@@ -185,6 +185,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
       !encode_map(B, N, K, dtype_in, kBN, &s.tmB) ||
       (c_tma && !encode_map(C, M, N, dtype_out, 32, &s.tmC)))
     return GEMM_ERR_CUDA;
+  s.tmB2 = s.tmB;  // no half-tile units here
 
   uint32_t* status = reinterpret_cast<uint32_t*>(ds.scratch);
   uint32_t* counters = reinterpret_cast<uint32_t*>(ds.scratch + kStatusBytes);
@@ -205,6 +206,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   p.tiles = (int32_t)tiles;
   p.k_blocks = (int32_t)k_blocks;
   p.dp_tiles = splits > 1 ? 0 : (int32_t)tiles;
+  p.half_tail = 0;
   p.splits = (int32_t)splits;
   p.kb_per_split = (int32_t)per;
   p.units = (int32_t)units;
@@ -213,6 +215,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   p.vec_store = c_tma ? 1 : 0;
   p.tma_store = c_tma ? 1 : 0;
   p.idesc = idesc_f16_kmajor(kBlockM, kBN, dtype_in == GEMM_BF16);
+  p.idesc_half = p.idesc;
   p.workspace = workspace;
   p.counters = counters;
   p.status = status;

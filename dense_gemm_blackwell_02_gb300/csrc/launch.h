@@ -16,6 +16,7 @@ struct LaunchSpec {
   int grid;        // CTAs (a multiple of cta_group)
   CUtensorMap tmA; // A: box {64, 128}
   CUtensorMap tmB; // B: box {64, bn / cta_group}
+  CUtensorMap tmB2; // B: box {64, bn / cta_group / 2} (half-tile units; else a copy of tmB)
   CUtensorMap tmC; // C: box {128 bytes of columns, 32 rows} (used when p.tma_store)
   GemmParams p;
   cudaStream_t stream;

@@ -30,7 +30,7 @@ cudaError_t launch_one(const LaunchSpec& s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, kernel, s.tmA, s.tmB, s.tmC, s.p);
+  return cudaLaunchKernelEx(&cfg, kernel, s.tmA, s.tmB, s.tmB2, s.tmC, s.p);
 }
 
 template <int CG, int BN, int STAGES, int OUT>

@@ -38,14 +38,16 @@ struct GemmParams {
   int32_t tiles;           // num_m_tiles * num_n_tiles
   int32_t k_blocks;        // ceil(K / 64)
   int32_t dp_tiles;        // tiles [0, dp_tiles) run whole, one unit each
-  int32_t splits;          // K slices of each later tile (1 = no split)
+  int32_t half_tail;       // 1: each later tile runs as two BN/2-column halves (full K)
+  int32_t splits;          // otherwise: K slices of each later tile (1 = no split)
   int32_t kb_per_split;    // k-blocks per slice (the last slice may be shorter)
-  int32_t units;           // dp_tiles + (tiles - dp_tiles) * splits
+  int32_t units;           // dp_tiles + (tiles - dp_tiles) * (half_tail ? 2 : splits)
   int32_t group_m;         // grouped rasterisation: M-tiles per group
   int32_t chain_kb;        // k-blocks per TMEM accumulation chain
   int32_t vec_store;       // 1 when 16-byte vector stores of C are aligned
   int32_t tma_store;       // 1 when C is written through the C tensor map
-  uint32_t idesc;          // tcgen05 instruction descriptor
+  uint32_t idesc;          // tcgen05 instruction descriptor (N = BN)
+  uint32_t idesc_half;     // the same for N = BN / 2 (half-tile units)
   float* workspace;        // splits > 1: fp32 partial tiles
   uint32_t* counters;      // splits > 1: per (tile, CTA of the pair, quarter, half) counters
   uint32_t* status;        // device status word

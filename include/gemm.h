@@ -68,9 +68,11 @@ typedef enum {
  *             K 4096: the tensor core's fp32 accumulation error grows with the
  *             length of one accumulation chain)
  *   dp_tiles  reported by gemm_last_config only (must be 0 on input): how many
- *             tiles ran whole; the rest were cut into `splits` K slices.  A forced
- *             `splits` slices every tile; automatically, only tiles of a partial
- *             last wave are sliced (or all tiles, when there are too few for the SMs).
+ *             tiles ran whole.  The rest ran as `splits` K slices each, or, when
+ *             `splits` is 1, as two half-width (block_n / 2 column) units each.  A
+ *             forced `splits` slices every tile; automatically, only the tiles of a
+ *             partial last wave are cut (or all tiles are sliced along K when there
+ *             are too few of them for the SMs).
  */
 typedef struct {
   int32_t variant;

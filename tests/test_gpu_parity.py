@@ -104,21 +104,27 @@ def test_persistent_loops_many_units_per_cta(g, variant, max_ctas):
 
 
 @pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("block_n", [256, 128])
 @pytest.mark.parametrize("max_ctas,M,N,K", [(10, 640, 1024, 704), (6, 512, 1280, 2048),
-                                             (14, 300, 2100, 1000)])
-def test_partial_last_wave_is_sliced(g, variant, max_ctas, M, N, K):
+                                             (14, 300, 2100, 1000), (10, 640, 1100, 704),
+                                             (16, 1000, 1000, 512)])
+def test_partial_last_wave_is_spread(g, variant, block_n, max_ctas, M, N, K):
     # more tiles than resident units, not a whole number of waves: the tiles of the
-    # last wave are cut along K and reduced in the kernel, the others run whole
-    g.set_config(variant=variant, max_ctas=max_ctas)
+    # last wave run as two half-width units (256-column tiles) or as K slices reduced
+    # in the kernel; the others run whole.  N = 1100 leaves the last half tile
+    # entirely outside C.
+    g.set_config(variant=variant, block_n=block_n, max_ctas=max_ctas)
     try:
         _case(g, M, N, K, F16, F16, seed=38)
         _case(g, M, N, K, BF16, F32, seed=39, exact=True, ints=True)
         cfg = g.last_config()
-        tiles = -(-M // (128 * variant)) * -(-N // 256)
+        tiles = -(-M // (128 * variant)) * -(-N // block_n)
         units = max_ctas // variant
         rem, kb = tiles % units, -(-K // 64)
-        if tiles > units and rem and min(units // rem, kb // 4, 8) >= 2:
-            assert cfg["splits"] > 1 and cfg["dp_tiles"] == tiles - rem, cfg
+        if tiles > units and rem and block_n == 256 and 2 * rem <= units:
+            assert cfg["splits"] == 1 and cfg["dp_tiles"] == tiles - rem, cfg   # halves
+        elif tiles > units and rem and min(units // rem, kb // 4, 8) >= 2:
+            assert cfg["splits"] > 1 and cfg["dp_tiles"] == tiles - rem, cfg   # K slices
         else:
             assert cfg["splits"] == 1 and cfg["dp_tiles"] == tiles, cfg
     finally:
