@@ -498,37 +498,53 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         for (int j = 0; j < kHalf; j += 4)
           st_global_cg_v4(mine + j * 32, __float_as_uint(acc[j]), __float_as_uint(acc[j + 1]),
                           __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
-        __threadfence();
+        // The warp's partial is published by lane 0's release-increment of the block's
+        // counter (after the warp barrier); the slice that sees the count reach the
+        // number of slices acquires every other slice's partial the same way.
         __syncwarp();
         uint32_t last = 0;
         if (lane == 0) {
           uint32_t* ctr = p.counters + sliced * kBlocksPerSlice + my_block;
-          const uint32_t before = atomicAdd(ctr, 1u);
+          const uint32_t before = atom_add_acq_rel_gpu(ctr, 1u);
           last = (before == (uint32_t)p.splits - 1u) ? 1u : 0u;
-          if (last) atomicExch(ctr, 0u);  // ready for the next launch
-          __threadfence();
+          if (last) st_relaxed_gpu_u32(ctr, 0u);  // ready for the next launch
         }
         last = __shfl_sync(0xFFFFFFFFu, last, 0);
         __syncwarp();
         if (!last) continue;
-        // Sum the slices in slice order: the result is the same whichever slice
-        // arrived last.
-        for (int32_t s = 0; s < p.splits; ++s) {
-          const float* src =
-              ws_tile + ((size_t)s * kBlocksPerSlice + my_block) * kBlockFloats + lane * 4;
+        // Sum the slices in slice order: the result is the same whichever slice arrived
+        // last.  With two slices the sum is p0 + p1 = p1 + p0 exactly, so the last one
+        // adds the other's partial to its own registers; with more, every partial is
+        // read back and added in order.
+        const float* ws_lane = ws_tile + (size_t)my_block * kBlockFloats + lane * 4;
+        const size_t slice_stride = kBlocksPerSlice * kBlockFloats;
+        if (p.splits == 2) {
+          const float* other = ws_lane + (size_t)(1 - w.split) * slice_stride;
 #pragma unroll
           for (int j = 0; j < kHalf; j += 4) {
-            const uint4 x = ld_global_cg_v4(src + j * 32);
-            if (s == 0) {
-              acc[j] = __uint_as_float(x.x);
-              acc[j + 1] = __uint_as_float(x.y);
-              acc[j + 2] = __uint_as_float(x.z);
-              acc[j + 3] = __uint_as_float(x.w);
-            } else {
-              acc[j] += __uint_as_float(x.x);
-              acc[j + 1] += __uint_as_float(x.y);
-              acc[j + 2] += __uint_as_float(x.z);
-              acc[j + 3] += __uint_as_float(x.w);
+            const uint4 x = ld_global_cg_v4(other + j * 32);
+            acc[j] += __uint_as_float(x.x);
+            acc[j + 1] += __uint_as_float(x.y);
+            acc[j + 2] += __uint_as_float(x.z);
+            acc[j + 3] += __uint_as_float(x.w);
+          }
+        } else {
+          for (int32_t s = 0; s < p.splits; ++s) {
+            const float* src = ws_lane + (size_t)s * slice_stride;
+#pragma unroll
+            for (int j = 0; j < kHalf; j += 4) {
+              const uint4 x = ld_global_cg_v4(src + j * 32);
+              if (s == 0) {
+                acc[j] = __uint_as_float(x.x);
+                acc[j + 1] = __uint_as_float(x.y);
+                acc[j + 2] = __uint_as_float(x.z);
+                acc[j + 3] = __uint_as_float(x.w);
+              } else {
+                acc[j] += __uint_as_float(x.x);
+                acc[j + 1] += __uint_as_float(x.y);
+                acc[j + 2] += __uint_as_float(x.z);
+                acc[j + 3] += __uint_as_float(x.w);
+              }
             }
           }
         }

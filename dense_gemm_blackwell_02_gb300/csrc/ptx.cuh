@@ -410,6 +410,19 @@ __device__ __forceinline__ void st_global_cg_v4(void* p, uint32_t a, uint32_t b,
                : "memory");
 }
 
+// Counter increment that releases this thread's earlier writes (and, through a
+// preceding warp barrier, the warp's) at GPU scope and acquires those released by
+// earlier increments: the hand-over of split-K partial tiles between CTAs.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_global_cg_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.cg.v4.b32 {%0, %1, %2, %3}, [%4];"
