@@ -115,7 +115,7 @@ size_t out_size(gemm_dtype_t d) { return d == GEMM_F32 ? 4 : 2; }
 bool valid_dtype(int d) { return d == GEMM_F16 || d == GEMM_BF16 || d == GEMM_F32; }
 
 struct Choice {
-  int variant, bn, stages, splits, kb_per_split, group_m, grid, chain_kb, half_tail;
+  int variant, bn, stages, splits, kb_per_split, group_m, grid, chain_kb, half_tail, prefetch_kb;
   int64_t tiles, dp_tiles, units, k_blocks, num_m, num_n;
 };
 
@@ -182,6 +182,10 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
   c->units = dp + (c->tiles - dp) * (c->half_tail ? 2 : s);
   c->group_m = f.group_m ? f.group_m : 16;
   c->chain_kb = f.chain_kblocks ? f.chain_kblocks : kChainKBlocks;
+  // Prefetching B into L2 ahead of the ring pays when B streams from DRAM and the
+  // tile count is small (decode shapes: few M tiles, every B byte used by one unit).
+  if (f.prefetch_kblocks) c->prefetch_kb = f.prefetch_kblocks < 0 ? 0 : f.prefetch_kblocks;
+  else c->prefetch_kb = c->num_m <= 1 ? 8 : 0;
   c->grid = (int)(std::min<int64_t>(c->units, slots) * cg);
   if (c->units > INT32_MAX || c->tiles * cg * 8 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   return GEMM_OK;
@@ -271,7 +275,7 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
   if (c.variant < 0 || c.variant > 2) return GEMM_ERR_INVALID_ARG;
   if (c.block_n != 0 && c.block_n != 128 && c.block_n != 256) return GEMM_ERR_INVALID_ARG;
   if (c.splits < 0 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
-      c.dp_tiles != 0)
+      c.dp_tiles != 0 || c.prefetch_kblocks < -1)
     return GEMM_ERR_INVALID_ARG;
   if (c.stages) {
     const int bn = c.block_n ? c.block_n : 256;
@@ -361,6 +365,7 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.units = (int32_t)ch.units;
   p.group_m = ch.group_m;
   p.chain_kb = ch.chain_kb;
+  p.prefetch_kb = ch.prefetch_kb;
   p.vec_store = c_tma ? 1 : 0;
   p.tma_store = c_tma ? 1 : 0;
   p.idesc = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn, dtype_in == GEMM_BF16);
@@ -377,8 +382,9 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
     p.counters = h->d_ctr;
   }
   if (launch_gemm(s) != cudaSuccess) return GEMM_ERR_CUDA;
-  h->last = gemm_config_t{ch.variant, ch.bn,   ch.splits,   ch.stages,
-                          ch.group_m, ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles};
+  h->last = gemm_config_t{ch.variant,  ch.bn,   ch.splits,   ch.stages,
+                          ch.group_m,  ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles,
+                          ch.prefetch_kb ? ch.prefetch_kb : -1};
   return GEMM_OK;
 }
 

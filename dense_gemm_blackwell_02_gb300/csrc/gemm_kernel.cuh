@@ -330,7 +330,15 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
                                   : (int32_t)rank * L::kRowsB);
       const CUtensorMap* mapB = half ? &tmB2 : &tmB;
       const uint32_t tx = half ? L::kTxBytesHalf : L::kTxBytes;
+      // Streaming B from DRAM (decode shapes): keep more requests in flight than the
+      // shared-memory ring holds by prefetching B into L2 prefetch_kb k-blocks ahead
+      // ("A Blackwell GEMM by Hand in CuTe DSL", section 8: TMA prefetch).
+      if (p.prefetch_kb > 0)
+        for (int32_t kb = w.kb0; kb < min(w.kb0 + p.prefetch_kb, w.kb1); ++kb)
+          tma_prefetch_l2_2d_elect(mapB, kb * kBlockK, b_row);
       for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+        if (p.prefetch_kb > 0 && kb + p.prefetch_kb < w.kb1)
+          tma_prefetch_l2_2d_elect(mapB, (kb + p.prefetch_kb) * kBlockK, b_row);
         if (!warp_wait(empty_bar(stage), phase ^ 1u, ctl, kSiteEmpty)) {
           ok = false;
           break;

@@ -212,6 +212,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   p.units = (int32_t)units;
   p.group_m = 16;
   p.chain_kb = kChainKBlocks;
+  p.prefetch_kb = 0;
   p.vec_store = c_tma ? 1 : 0;
   p.tma_store = c_tma ? 1 : 0;
   p.idesc = idesc_f16_kmajor(kBlockM, kBN, dtype_in == GEMM_BF16);

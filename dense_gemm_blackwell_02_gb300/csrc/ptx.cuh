@@ -167,6 +167,14 @@ __device__ __forceinline__ void tma_load_2d_pair_elect(uint32_t dst, const void*
       : "memory");
 }
 
+// Bring a tile of a tensor into L2 without a shared-memory destination (elected lane).
+__device__ __forceinline__ void tma_prefetch_l2_2d_elect(const void* tmap, int32_t c0, int32_t c1) {
+  asm volatile(GB300_ELECT "@e_ cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n\t}" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // Same, with an L2 cache-policy hint.
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap, int32_t c0,
                                                  int32_t c1, uint32_t bar, uint64_t policy) {

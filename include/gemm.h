@@ -73,6 +73,8 @@ typedef enum {
  *             forced `splits` slices every tile; automatically, only the tiles of a
  *             partial last wave are cut (or all tiles are sliced along K when there
  *             are too few of them for the SMs).
+ *   prefetch_kblocks  how many 64-deep K blocks ahead of the shared-memory ring the
+ *             producer prefetches B into L2 (0 = automatic, -1 = never)
  */
 typedef struct {
   int32_t variant;
@@ -83,6 +85,7 @@ typedef struct {
   int32_t max_ctas;
   int32_t chain_kblocks;
   int32_t dp_tiles;
+  int32_t prefetch_kblocks;
 } gemm_config_t;
 
 /* Create a handle on the current CUDA device.  Fails with GEMM_ERR_UNSUPPORTED
