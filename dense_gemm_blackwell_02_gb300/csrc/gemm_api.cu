@@ -117,6 +117,7 @@ bool valid_dtype(int d) { return d == GEMM_F16 || d == GEMM_BF16 || d == GEMM_F3
 struct Choice {
   int variant, bn, stages, splits, kb_per_split, group_m, grid, chain_kb, half_tail, prefetch_kb;
   int64_t tiles, dp_tiles, units, k_blocks, num_m, num_n;
+  int64_t sk_workers, ws_slots;
 };
 
 int out_kind(gemm_dtype_t d) { return d == GEMM_F16 ? kOutF16 : d == GEMM_BF16 ? kOutBF16 : kOutF32; }
@@ -149,15 +150,17 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
   if (f.max_ctas) slots = std::min<int64_t>(slots, std::max<int64_t>(f.max_ctas / cg, 1));
   int64_t s = 1, dp = c->tiles;
   c->half_tail = 0;
+  c->sk_workers = 0;
   if (f.splits) {
     s = f.splits;  // forced: every tile is sliced
     dp = 0;
-  } else if (c->tiles * 2 <= slots && c->k_blocks >= 8) {
-    // Fewer tiles than half the resident units: slice every tile along K so all SMs
-    // have work ("A Blackwell GEMM by Hand in CuTe DSL", section 9: decode shapes
-    // are decided by waves).
-    s = std::min<int64_t>({slots / c->tiles, c->k_blocks / 4, 32});
+  } else if (c->tiles < slots && c->k_blocks >= 8) {
+    // Fewer tiles than resident units: stream-K over all of them, every unit taking an
+    // equal share of the (tile, k-block) iterations ("A Blackwell GEMM by Hand in
+    // CuTe DSL", section 9: decode shapes are decided by waves, and stream-K is the
+    // general answer).
     dp = 0;
+    c->sk_workers = std::min<int64_t>(slots, c->tiles * c->k_blocks);
   } else if (c->tiles > slots && c->tiles % slots != 0) {
     // Whole waves run whole tiles; the tiles of the partial last wave are spread over
     // more units so that the last wave keeps (nearly) every unit busy: as two
@@ -175,18 +178,24 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
   if (s > c->k_blocks) s = c->k_blocks;
   const int64_t per = ceil_div(c->k_blocks, s);
   s = ceil_div(c->k_blocks, per);  // no empty slice
-  if (s == 1 && !c->half_tail) dp = c->tiles;
+  if (s == 1 && !c->half_tail && !c->sk_workers) dp = c->tiles;
   c->splits = (int)s;
   c->kb_per_split = (int)per;
   c->dp_tiles = dp;
-  c->units = dp + (c->tiles - dp) * (c->half_tail ? 2 : s);
+  c->units = c->sk_workers ? dp : dp + (c->tiles - dp) * (c->half_tail ? 2 : s);
+  c->ws_slots = s;
+  if (c->sk_workers) {
+    // A tile meets at most ceil(k_blocks / share) + 1 workers' ranges.
+    const int64_t share = (c->tiles - dp) * c->k_blocks / c->sk_workers;
+    c->ws_slots = ceil_div(c->k_blocks, std::max<int64_t>(share, 1)) + 1;
+  }
   c->group_m = f.group_m ? f.group_m : 16;
   c->chain_kb = f.chain_kblocks ? f.chain_kblocks : kChainKBlocks;
   // Prefetching B into L2 ahead of the ring pays when B streams from DRAM and the
   // tile count is small (decode shapes: few M tiles, every B byte used by one unit).
   if (f.prefetch_kblocks) c->prefetch_kb = f.prefetch_kblocks < 0 ? 0 : f.prefetch_kblocks;
   else c->prefetch_kb = c->num_m <= 1 ? 8 : 0;
-  c->grid = (int)(std::min<int64_t>(c->units, slots) * cg);
+  c->grid = (int)(std::min<int64_t>(std::max(c->units, c->sk_workers), slots) * cg);
   if (c->units > INT32_MAX || c->tiles * cg * 8 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   return GEMM_OK;
 }
@@ -363,6 +372,8 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.splits = ch.splits;
   p.kb_per_split = ch.kb_per_split;
   p.units = (int32_t)ch.units;
+  p.sk_workers = (int32_t)ch.sk_workers;
+  p.ws_slots = (int32_t)ch.ws_slots;
   p.group_m = ch.group_m;
   p.chain_kb = ch.chain_kb;
   p.prefetch_kb = ch.prefetch_kb;
@@ -373,16 +384,17 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
   p.test_stall = h->test_stall;
-  if (ch.splits > 1 && !ch.half_tail) {
+  if ((ch.splits > 1 && !ch.half_tail) || ch.sk_workers) {
     const size_t sliced = (size_t)(ch.tiles - ch.dp_tiles);
-    const size_t ws = sliced * ch.splits * kBlockM * ch.variant * ch.bn * sizeof(float);
+    const size_t ws = sliced * ch.ws_slots * kBlockM * ch.variant * ch.bn * sizeof(float);
     st = ensure_workspace(h, ws, sliced * ch.variant * 8);
     if (st != GEMM_OK) return st;
     p.workspace = h->d_ws;
     p.counters = h->d_ctr;
   }
   if (launch_gemm(s) != cudaSuccess) return GEMM_ERR_CUDA;
-  h->last = gemm_config_t{ch.variant,  ch.bn,   ch.splits,   ch.stages,
+  h->last = gemm_config_t{ch.variant,  ch.bn,   ch.sk_workers ? -(int32_t)ch.sk_workers : ch.splits,
+                          ch.stages,
                           ch.group_m,  ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles,
                           ch.prefetch_kb ? ch.prefetch_kb : -1};
   return GEMM_OK;

@@ -133,6 +133,16 @@ struct Unit {
 // N inside a group, so units running at the same time share A rows and B columns in
 // L2 ("Matmul on sm_120", block swizzle; "A Blackwell GEMM by Hand in CuTe DSL",
 // section 8).
+__device__ __forceinline__ void tile_coords(Unit& w, const GemmParams& p) {
+  const int32_t group = p.group_m * p.num_n_tiles;
+  const int32_t g = w.tile / group;
+  const int32_t first_m = g * p.group_m;
+  const int32_t gm = min(p.num_m_tiles - first_m, p.group_m);
+  const int32_t r = w.tile - g * group;
+  w.m_blk = first_m + r % gm;
+  w.n_blk = r / gm;
+}
+
 __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams& p) {
   Unit w;
   w.half = -1;
@@ -158,14 +168,61 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams& p) {
     w.kb0 = w.split * p.kb_per_split;
     w.kb1 = min(w.kb0 + p.kb_per_split, p.k_blocks);
   }
-  const int32_t group = p.group_m * p.num_n_tiles;
-  const int32_t g = w.tile / group;
-  const int32_t first_m = g * p.group_m;
-  const int32_t gm = min(p.num_m_tiles - first_m, p.group_m);
-  const int32_t r = w.tile - g * group;
-  w.m_blk = first_m + r % gm;
-  w.n_blk = r / gm;
+  tile_coords(w, p);
   return w;
+}
+
+// The sequence of units one CTA (pair) processes.  First the whole tiles (and the
+// half-tile or K-slice units) numbered first, first + stride, ... < p.units; then, in
+// stream-K mode, its own contiguous share of the remaining tiles' (tile, k-block)
+// iterations: worker c of W takes iterations [floor(c T / W), floor((c + 1) T / W)),
+// T = (tiles - dp_tiles) * k_blocks ("Stream-K", cited in "A Blackwell GEMM by Hand
+// in CuTe DSL", section 9 and "CUTLASS Deep Dive", StreamK tile scheduler), cut at
+// tile boundaries into segments.  Segment j of a tile covered by n segments is
+// reduced like K slice j of n.
+struct Walker {
+  int32_t u, stride;    // unit-numbered phase
+  int64_t it, end;      // stream-K phase: remaining iteration range
+};
+
+__device__ __forceinline__ Walker walker_begin(int32_t first, int32_t stride, const GemmParams& p) {
+  Walker k{first, stride, 0, 0};
+  if (p.sk_workers > 0 && first < p.sk_workers) {
+    const int64_t T = (int64_t)(p.tiles - p.dp_tiles) * p.k_blocks;
+    k.it = (int64_t)first * T / p.sk_workers;
+    k.end = (int64_t)(first + 1) * T / p.sk_workers;
+  }
+  return k;
+}
+
+// Stream-K worker holding iteration x (the W-way split above, inverted).
+__device__ __forceinline__ int64_t sk_worker_of(int64_t x, const GemmParams& p) {
+  const int64_t T = (int64_t)(p.tiles - p.dp_tiles) * p.k_blocks;
+  return ((x + 1) * p.sk_workers - 1) / T;
+}
+
+__device__ __forceinline__ bool walker_next(Walker& k, const GemmParams& p, Unit& w) {
+  if (k.u < p.units) {
+    w = decode_unit(k.u, p);
+    k.u += k.stride;
+    return true;
+  }
+  if (k.it >= k.end) return false;
+  const int32_t kb = p.k_blocks;
+  const int64_t t = k.it / kb;                      // stream-K tile (relative to dp_tiles)
+  w.tile = p.dp_tiles + (int32_t)t;
+  w.half = -1;
+  w.kb0 = (int32_t)(k.it - t * kb);
+  const int64_t left = k.end - k.it;
+  w.kb1 = (int32_t)((int64_t)(kb - w.kb0) < left ? kb : w.kb0 + left);
+  const int64_t w_lo = sk_worker_of(t * kb, p);
+  const int64_t w_hi = sk_worker_of(t * kb + kb - 1, p);
+  const int64_t me = sk_worker_of(k.it, p);
+  w.nsplit = (int32_t)(w_hi - w_lo + 1);
+  w.split = (int32_t)(me - w_lo);
+  k.it += w.kb1 - w.kb0;
+  tile_coords(w, p);
+  return true;
 }
 
 __device__ __forceinline__ int32_t chains_of(const Unit& w, int32_t chain_kb) {
@@ -320,8 +377,9 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     // The whole warp runs the loop; one elected lane issues each copy.
     uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
     bool ok = true;
-    for (int32_t u = first_unit; u < p.units && ok; u += unit_stride) {
-      const Unit w = decode_unit(u, p);
+    Walker walk = walker_begin(first_unit, unit_stride, p);
+    Unit w;
+    while (ok && walker_next(walk, p, w)) {
       const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
       // a half-tile unit loads half the B rows (through the half-height map tmB2)
       const bool half = w.half >= 0;
@@ -387,8 +445,9 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       const uint64_t desc_a0 = smem_desc_sw128_kmajor(sA);
       const uint64_t desc_b0 = smem_desc_sw128_kmajor(sB);
       if (p.test_stall) ok = warp_wait(drain_bar, 0, ctl, kSiteTestStall);
-      for (int32_t u = first_unit; u < p.units && ok; u += unit_stride) {
-        const Unit w = decode_unit(u, p);
+      Walker walk = walker_begin(first_unit, unit_stride, p);
+      Unit w;
+      while (ok && walker_next(walk, p, w)) {
         const uint32_t idesc = w.half >= 0 ? p.idesc_half : p.idesc;
         for (int32_t c0 = w.kb0; c0 < w.kb1 && ok; c0 += p.chain_kb) {
           const int32_t c1 = min(c0 + p.chain_kb, w.kb1);
@@ -437,8 +496,9 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     const uint32_t staging = sC + ew * L::kStagingBytes;
     uint32_t iter = 0;
     bool ok = true;
-    for (int32_t u = first_unit; u < p.units && ok; u += unit_stride) {
-      const Unit w = decode_unit(u, p);
+    Walker walk = walker_begin(first_unit, unit_stride, p);
+    Unit w;
+    while (ok && walker_next(walk, p, w)) {
       // In a half-tile unit the accumulator holds BN/2 columns: the h = 0 warps own
       // them, the h = 1 warps only take part in the slot hand-over.
       const bool active = w.half < 0 || h == 0;
@@ -499,7 +559,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         constexpr size_t kBlocksPerSlice = (size_t)CTA_GROUP * 8;  // (rank, quarter, half)
         const size_t sliced = (size_t)(w.tile - p.dp_tiles);      // index among sliced tiles
         const size_t my_block = ((size_t)rank * 4 + q) * 2 + h;
-        float* ws_tile = p.workspace + sliced * p.splits * kBlocksPerSlice * kBlockFloats;
+        float* ws_tile = p.workspace + sliced * p.ws_slots * kBlocksPerSlice * kBlockFloats;
         float* mine = ws_tile + ((size_t)w.split * kBlocksPerSlice + my_block) * kBlockFloats +
                       lane * 4;
 #pragma unroll
@@ -514,7 +574,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         if (lane == 0) {
           uint32_t* ctr = p.counters + sliced * kBlocksPerSlice + my_block;
           const uint32_t before = atom_add_acq_rel_gpu(ctr, 1u);
-          last = (before == (uint32_t)p.splits - 1u) ? 1u : 0u;
+          last = (before == (uint32_t)w.nsplit - 1u) ? 1u : 0u;
           if (last) st_relaxed_gpu_u32(ctr, 0u);  // ready for the next launch
         }
         last = __shfl_sync(0xFFFFFFFFu, last, 0);
@@ -526,7 +586,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         // read back and added in order.
         const float* ws_lane = ws_tile + (size_t)my_block * kBlockFloats + lane * 4;
         const size_t slice_stride = kBlocksPerSlice * kBlockFloats;
-        if (p.splits == 2) {
+        if (w.nsplit == 2) {
           const float* other = ws_lane + (size_t)(1 - w.split) * slice_stride;
 #pragma unroll
           for (int j = 0; j < kHalf; j += 4) {
@@ -537,7 +597,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
             acc[j + 3] += __uint_as_float(x.w);
           }
         } else {
-          for (int32_t s = 0; s < p.splits; ++s) {
+          for (int32_t s = 0; s < w.nsplit; ++s) {
             const float* src = ws_lane + (size_t)s * slice_stride;
 #pragma unroll
             for (int j = 0; j < kHalf; j += 4) {

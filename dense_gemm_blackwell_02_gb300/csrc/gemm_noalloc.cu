@@ -210,6 +210,8 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   p.splits = (int32_t)splits;
   p.kb_per_split = (int32_t)per;
   p.units = (int32_t)units;
+  p.sk_workers = 0;
+  p.ws_slots = (int32_t)splits;
   p.group_m = 16;
   p.chain_kb = kChainKBlocks;
   p.prefetch_kb = 0;

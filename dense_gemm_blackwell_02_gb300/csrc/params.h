@@ -42,6 +42,8 @@ struct GemmParams {
   int32_t splits;          // otherwise: K slices of each later tile (1 = no split)
   int32_t kb_per_split;    // k-blocks per slice (the last slice may be shorter)
   int32_t units;           // dp_tiles + (tiles - dp_tiles) * (half_tail ? 2 : splits)
+  int32_t sk_workers;      // > 0: tiles after dp_tiles go to stream-K over this many units
+  int32_t ws_slots;        // partial-tile slots per cut tile in the workspace
   int32_t group_m;         // grouped rasterisation: M-tiles per group
   int32_t chain_kb;        // k-blocks per TMEM accumulation chain
   int32_t prefetch_kb;     // L2 prefetch of B this many k-blocks ahead of the ring (0: off)

@@ -59,7 +59,8 @@ typedef enum {
  *             2 = a CTA pair per 256-row tile (cta_group::2, cluster of 2)
  *   block_n   128 or 256 columns of C per tile
  *   splits    K slices per tile (1 = no split; >1 = split-K with a deterministic
- *             in-kernel reduction in slice order)
+ *             in-kernel reduction in slice order).  gemm_last_config reports -W when
+ *             the tiles were shared out by stream-K over W units instead.
  *   stages    depth of the shared-memory operand ring
  *   group_m   grouped rasterisation: M tiles per group
  *   max_ctas  cap on the persistent grid (0 = one CTA per SM)

@@ -132,6 +132,33 @@ def test_partial_last_wave_is_spread(g, variant, block_n, max_ctas, M, N, K):
 
 
 @pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("block_n", [128, 256])
+@pytest.mark.parametrize("max_ctas,M,N,K", [(152, 256, 512, 8192), (38, 300, 1100, 2000),
+                                             (20, 256, 2048, 1000), (8, 129, 300, 4096),
+                                             (152, 256, 8192, 512)])
+def test_stream_k(g, variant, block_n, max_ctas, M, N, K):
+    # fewer tiles than resident units: each unit takes an equal share of the
+    # (tile, k-block) iterations, crossing tile boundaries; the segments of a tile are
+    # reduced in K order by whichever arrives last
+    g.set_config(variant=variant, block_n=block_n, max_ctas=max_ctas)
+    try:
+        _case(g, M, N, K, F16, F16, seed=40)
+        _case(g, M, N, K, BF16, F32, seed=41, exact=True, ints=True)
+        cfg = g.last_config()
+        tiles = -(-M // (128 * variant)) * -(-N // block_n)
+        units = max_ctas // variant
+        if tiles < units and -(-K // 64) >= 8:
+            assert cfg["splits"] < 0 and cfg["dp_tiles"] == 0, cfg
+        # deterministic: the same bits on a second run
+        A, B = si.make_operands(M, N, K, F16, "uniform", 42)
+        C1 = parity.run_gpu(g, A, B, F32)
+        C2 = parity.run_gpu(g, A, B, F32)
+        assert torch.equal(C1.view(torch.int32), C2.view(torch.int32))
+    finally:
+        g.reset_config()
+
+
+@pytest.mark.parametrize("variant", [1, 2])
 @pytest.mark.parametrize("chain", [1, 3, 5, 64])
 @pytest.mark.parametrize("splits", [1, 3])
 def test_accumulation_chains(g, variant, chain, splits):
