@@ -123,6 +123,21 @@ def check(got_bits: np.ndarray, want_bits: np.ndarray, dtype_out: int, exact: bo
     return out
 
 
+def check_pair(got_bits, ref_bits, dtype_out, c64, sigma, K, what=""):
+    """Two GPU results of the same product that may accumulate in different orders:
+    each may lie within ulp/2 + tau of the exact sum (and within 1 ulp of its rounding),
+    so they must agree within 2 ulps, or within ulp + 2 tau where the sum cancels."""
+    g = _decode(got_bits, dtype_out)
+    r = _decode(ref_bits, dtype_out)
+    ok = np.abs(g - r) <= ulp_of(c64, dtype_out) + 2 * tau_of(sigma, K)
+    if dtype_out != F32:
+        ok |= ulp_distance(got_bits, ref_bits) <= 2
+    if not ok.all():
+        idx = np.argwhere(~ok)[:5]
+        raise AssertionError(f"{what}: {int((~ok).sum())} elements differ beyond the tolerance; "
+                             f"first at {idx.tolist()}")
+
+
 def oracle_check(got_bits, A, B, dtype_in, dtype_out, rows=None, cols=None, what="",
                  exact=False):
     """Oracle on the same inputs (optionally selected rows/cols), then check()."""

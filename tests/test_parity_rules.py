@@ -53,3 +53,15 @@ def test_ordinal_is_monotone_and_signed_zero_equal():
     x = np.array([-2.0, -1.0, -0.0, 0.0, 1e-7, 1.0, 2.0])
     o = parity.ordinal(_bits(x, F16))
     assert np.all(np.diff(o) >= 0) and o[2] == o[3] == 0
+
+
+def test_check_pair_allows_two_roundings_but_not_more():
+    c64 = np.array([10.0, 1e-4])
+    sigma = np.array([1.0, 15.0])
+    a = _bits([10.0, 1e-4], F16)
+    b = a.copy()
+    b[0] += 2                                    # two ulps apart at 10.0
+    parity.check_pair(a, b, F16, c64, sigma, 64)
+    b[0] += 2                                    # four ulps apart
+    with pytest.raises(AssertionError):
+        parity.check_pair(a, b, F16, c64, sigma, 64)
