@@ -151,16 +151,23 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
   int64_t s = 1, dp = c->tiles;
   c->half_tail = 0;
   c->sk_workers = 0;
-  if (f.splits) {
-    s = f.splits;  // forced: every tile is sliced
-    dp = 0;
-  } else if (c->tiles < slots && c->k_blocks >= 8) {
-    // Fewer tiles than resident units: stream-K over all of them, every unit taking an
-    // equal share of the (tile, k-block) iterations ("A Blackwell GEMM by Hand in
-    // CuTe DSL", section 9: decode shapes are decided by waves, and stream-K is the
-    // general answer).
+  if (f.splits < 0) {
+    // forced stream-K: every resident unit takes an equal share of the (tile, k-block)
+    // iterations ("A Blackwell GEMM by Hand in CuTe DSL", section 9; "CUTLASS Deep
+    // Dive", StreamK).  Measured on the M = 256 decode shapes it lost to split-K (the
+    // three-segment tiles cost more to reduce than the balance saves), so it is not
+    // chosen automatically.
     dp = 0;
     c->sk_workers = std::min<int64_t>(slots, c->tiles * c->k_blocks);
+  } else if (f.splits) {
+    s = f.splits;  // forced: every tile is sliced
+    dp = 0;
+  } else if (c->tiles * 2 <= slots && c->k_blocks >= 8) {
+    // Fewer tiles than half the resident units: slice every tile along K so all SMs
+    // have work ("A Blackwell GEMM by Hand in CuTe DSL", section 9: decode shapes are
+    // decided by waves).
+    s = std::min<int64_t>({slots / c->tiles, c->k_blocks / 4, 32});
+    dp = 0;
   } else if (c->tiles > slots && c->tiles % slots != 0) {
     // Whole waves run whole tiles; the tiles of the partial last wave are spread over
     // more units so that the last wave keeps (nearly) every unit busy: as two
@@ -191,10 +198,9 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
   }
   c->group_m = f.group_m ? f.group_m : 16;
   c->chain_kb = f.chain_kblocks ? f.chain_kblocks : kChainKBlocks;
-  // Prefetching B into L2 ahead of the ring pays when B streams from DRAM and the
-  // tile count is small (decode shapes: few M tiles, every B byte used by one unit).
-  if (f.prefetch_kblocks) c->prefetch_kb = f.prefetch_kblocks < 0 ? 0 : f.prefetch_kblocks;
-  else c->prefetch_kb = c->num_m <= 1 ? 8 : 0;
+  // Prefetching B into L2 ahead of the ring: off unless asked for (measured on the
+  // M = 256 decode shapes and the square ones it did not help).
+  c->prefetch_kb = f.prefetch_kblocks > 0 ? f.prefetch_kblocks : 0;
   c->grid = (int)(std::min<int64_t>(std::max(c->units, c->sk_workers), slots) * cg);
   if (c->units > INT32_MAX || c->tiles * cg * 8 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   return GEMM_OK;
@@ -283,7 +289,7 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
   const gemm_config_t& c = *cfg;
   if (c.variant < 0 || c.variant > 2) return GEMM_ERR_INVALID_ARG;
   if (c.block_n != 0 && c.block_n != 128 && c.block_n != 256) return GEMM_ERR_INVALID_ARG;
-  if (c.splits < 0 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
+  if (c.splits < -1 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
       c.dp_tiles != 0 || c.prefetch_kblocks < -1)
     return GEMM_ERR_INVALID_ARG;
   if (c.stages) {

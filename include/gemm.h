@@ -59,8 +59,9 @@ typedef enum {
  *             2 = a CTA pair per 256-row tile (cta_group::2, cluster of 2)
  *   block_n   128 or 256 columns of C per tile
  *   splits    K slices per tile (1 = no split; >1 = split-K with a deterministic
- *             in-kernel reduction in slice order).  gemm_last_config reports -W when
- *             the tiles were shared out by stream-K over W units instead.
+ *             in-kernel reduction in slice order; -1 = stream-K: every resident unit
+ *             takes an equal share of the (tile, K block) iterations).
+ *             gemm_last_config reports -W for stream-K over W units.
  *   stages    depth of the shared-memory operand ring
  *   group_m   grouped rasterisation: M tiles per group
  *   max_ctas  cap on the persistent grid (0 = one CTA per SM)
@@ -75,7 +76,7 @@ typedef enum {
  *             partial last wave are cut (or all tiles are sliced along K when there
  *             are too few of them for the SMs).
  *   prefetch_kblocks  how many 64-deep K blocks ahead of the shared-memory ring the
- *             producer prefetches B into L2 (0 = automatic, -1 = never)
+ *             producer prefetches B into L2 (0 or -1 = never, the default)
  */
 typedef struct {
   int32_t variant;
