@@ -159,6 +159,8 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
     // chosen automatically.
     dp = 0;
     c->sk_workers = std::min<int64_t>(slots, c->tiles * c->k_blocks);
+    // the kernel splits the iteration range in 32-bit arithmetic
+    if (c->tiles * c->k_blocks * c->sk_workers >= (int64_t(1) << 32)) return GEMM_ERR_UNSUPPORTED;
   } else if (f.splits) {
     s = f.splits;  // forced: every tile is sliced
     dp = 0;

@@ -181,48 +181,55 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams& p) {
 // tile boundaries into segments.  Segment j of a tile covered by n segments is
 // reduced like K slice j of n.
 struct Walker {
-  int32_t u, stride;    // unit-numbered phase
-  int64_t it, end;      // stream-K phase: remaining iteration range
+  int32_t u;        // next unit number (unit-numbered phase)
+  int32_t sk_done;  // stream-K phase: iterations this worker has taken so far
 };
 
-__device__ __forceinline__ Walker walker_begin(int32_t first, int32_t stride, const GemmParams& p) {
-  Walker k{first, stride, 0, 0};
-  if (p.sk_workers > 0 && first < p.sk_workers) {
-    const int64_t T = (int64_t)(p.tiles - p.dp_tiles) * p.k_blocks;
-    k.it = (int64_t)first * T / p.sk_workers;
-    k.end = (int64_t)(first + 1) * T / p.sk_workers;
-  }
-  return k;
+// Stream-K worker holding iteration x (the W-way split above, inverted).  The host
+// takes stream-K only when (T + 1) * W fits in 32 bits.
+__device__ __forceinline__ uint32_t sk_worker_of(uint32_t x, uint32_t T, uint32_t W) {
+  return ((x + 1u) * W - 1u) / T;
 }
 
-// Stream-K worker holding iteration x (the W-way split above, inverted).
-__device__ __forceinline__ int64_t sk_worker_of(int64_t x, const GemmParams& p) {
-  const int64_t T = (int64_t)(p.tiles - p.dp_tiles) * p.k_blocks;
-  return ((x + 1) * p.sk_workers - 1) / T;
-}
-
-__device__ __forceinline__ bool walker_next(Walker& k, const GemmParams& p, Unit& w) {
-  if (k.u < p.units) {
-    w = decode_unit(k.u, p);
-    k.u += k.stride;
-    return true;
-  }
-  if (k.it >= k.end) return false;
-  const int32_t kb = p.k_blocks;
-  const int64_t t = k.it / kb;                      // stream-K tile (relative to dp_tiles)
+// Advance worker `first` to its next stream-K segment (false when its range is used
+// up).  Kept out of line, with the walker and the unit passed by reference: inlined,
+// its divisions raise the register pressure of every role and the epilogue's
+// 128-float accumulator spills, which slowed the whole-tile path by ~4% at 4096^3
+// (measured against this form on the same GPU).
+static __device__ __noinline__ bool sk_next(Walker& k, int32_t first, const GemmParams& p,
+                                            Unit& w) {
+  const uint32_t W = (uint32_t)p.sk_workers;
+  const uint32_t T = (uint32_t)(p.tiles - p.dp_tiles) * (uint32_t)p.k_blocks;
+  const uint32_t it = (uint32_t)first * T / W + (uint32_t)k.sk_done;
+  const uint32_t end = ((uint32_t)first + 1u) * T / W;
+  if (it >= end) return false;
+  const uint32_t kb = (uint32_t)p.k_blocks;
+  const uint32_t t = it / kb;                       // stream-K tile (relative to dp_tiles)
   w.tile = p.dp_tiles + (int32_t)t;
   w.half = -1;
-  w.kb0 = (int32_t)(k.it - t * kb);
-  const int64_t left = k.end - k.it;
-  w.kb1 = (int32_t)((int64_t)(kb - w.kb0) < left ? kb : w.kb0 + left);
-  const int64_t w_lo = sk_worker_of(t * kb, p);
-  const int64_t w_hi = sk_worker_of(t * kb + kb - 1, p);
-  const int64_t me = sk_worker_of(k.it, p);
-  w.nsplit = (int32_t)(w_hi - w_lo + 1);
-  w.split = (int32_t)(me - w_lo);
-  k.it += w.kb1 - w.kb0;
+  w.kb0 = (int32_t)(it - t * kb);
+  const uint32_t left = end - it;
+  w.kb1 = (kb - (uint32_t)w.kb0) < left ? (int32_t)kb : w.kb0 + (int32_t)left;
+  const uint32_t w_lo = sk_worker_of(t * kb, T, W);
+  const uint32_t w_hi = sk_worker_of(t * kb + kb - 1u, T, W);
+  w.nsplit = (int32_t)(w_hi - w_lo + 1u);
+  w.split = first - (int32_t)w_lo;
   tile_coords(w, p);
+  k.sk_done += w.kb1 - w.kb0;
   return true;
+}
+
+// Only two 32-bit counters live across a unit; the stream-K range is recomputed from
+// the worker's index on each call.
+__device__ __forceinline__ bool walker_next(Walker& k, int32_t first, int32_t stride,
+                                            const GemmParams& p, Unit& w) {
+  if (k.u < p.units) {
+    w = decode_unit(k.u, p);
+    k.u += stride;
+    return true;
+  }
+  if (first >= p.sk_workers) return false;
+  return sk_next(k, first, p, w);
 }
 
 __device__ __forceinline__ int32_t chains_of(const Unit& w, int32_t chain_kb) {
@@ -374,12 +381,14 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer --
-    // The whole warp runs the loop; one elected lane issues each copy.
+    // The whole warp runs the loop; one elected lane issues each copy.  B's copy goes
+    // out ahead of A's: on the decode shapes B streams from DRAM while A stays in L2
+    // (1-3% faster there, neutral on square shapes; measured).
     uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
     bool ok = true;
-    Walker walk = walker_begin(first_unit, unit_stride, p);
+    Walker walk{first_unit, 0};
     Unit w;
-    while (ok && walker_next(walk, p, w)) {
+    while (ok && walker_next(walk, first_unit, unit_stride, p, w)) {
       const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
       // a half-tile unit loads half the B rows (through the half-height map tmB2)
       const bool half = w.half >= 0;
@@ -403,15 +412,15 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         }
         if constexpr (CTA_GROUP == 1) {
           mbar_arrive_expect_tx_elect(full_bar(stage), tx);
-          tma_load_2d_elect(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, full_bar(stage));
           tma_load_2d_elect(sB + stage * L::kBBytes, mapB, kb * kBlockK, b_row, full_bar(stage));
+          tma_load_2d_elect(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, full_bar(stage));
         } else {
           // Both CTAs' copies complete on the leader's full barrier; the leader arms it
           // with the bytes of the pair.
           const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
           if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), tx);
-          tma_load_2d_pair_elect(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, leader_full);
           tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kBlockK, b_row, leader_full);
+          tma_load_2d_pair_elect(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, leader_full);
         }
         armed |= 1u << stage;
         armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -445,9 +454,9 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       const uint64_t desc_a0 = smem_desc_sw128_kmajor(sA);
       const uint64_t desc_b0 = smem_desc_sw128_kmajor(sB);
       if (p.test_stall) ok = warp_wait(drain_bar, 0, ctl, kSiteTestStall);
-      Walker walk = walker_begin(first_unit, unit_stride, p);
+      Walker walk{first_unit, 0};
       Unit w;
-      while (ok && walker_next(walk, p, w)) {
+      while (ok && walker_next(walk, first_unit, unit_stride, p, w)) {
         const uint32_t idesc = w.half >= 0 ? p.idesc_half : p.idesc;
         for (int32_t c0 = w.kb0; c0 < w.kb1 && ok; c0 += p.chain_kb) {
           const int32_t c1 = min(c0 + p.chain_kb, w.kb1);
@@ -496,9 +505,9 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     const uint32_t staging = sC + ew * L::kStagingBytes;
     uint32_t iter = 0;
     bool ok = true;
-    Walker walk = walker_begin(first_unit, unit_stride, p);
+    Walker walk{first_unit, 0};
     Unit w;
-    while (ok && walker_next(walk, p, w)) {
+    while (ok && walker_next(walk, first_unit, unit_stride, p, w)) {
       // In a half-tile unit the accumulator holds BN/2 columns: the h = 0 warps own
       // them, the h = 1 warps only take part in the slot hand-over.
       const bool active = w.half < 0 || h == 0;

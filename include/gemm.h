@@ -61,7 +61,9 @@ typedef enum {
  *   splits    K slices per tile (1 = no split; >1 = split-K with a deterministic
  *             in-kernel reduction in slice order; -1 = stream-K: every resident unit
  *             takes an equal share of the (tile, K block) iterations).
- *             gemm_last_config reports -W for stream-K over W units.
+ *             gemm_last_config reports -W for stream-K over W units.  Stream-K
+ *             needs tiles * K blocks * W < 2^32; gemm_run returns
+ *             GEMM_ERR_UNSUPPORTED beyond that.
  *   stages    depth of the shared-memory operand ring
  *   group_m   grouped rasterisation: M tiles per group
  *   max_ctas  cap on the persistent grid (0 = one CTA per SM)
