@@ -68,6 +68,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The job's time is the slowest rank's: max of x over the process group (x itself
+    when there is no group).  Replicas exchange nothing else."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, flops_per_step: float, steps: int, slowest_ms: float) -> float:
+    """Whole-job TFLOP/s of `world` independent replicas, each running `steps` steps of
+    `flops_per_step`, timed by the slowest rank (weak scaling)."""
+    return world * flops_per_step * steps / (slowest_ms * 1e-3) / 1e12
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
@@ -276,11 +293,7 @@ def run_ours(args):
     time.sleep(0.1)
     clocks = sampler.stop()
     per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = sum(per_ms)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(per_ms), dev)
     code, word = g.device_status(stream)
     if code != 0:
         raise RuntimeError(f"device status after timing: {code} ({word:#x})")
@@ -288,7 +301,7 @@ def run_ours(args):
     decode = measure_decode(g, dev, stream, flush, peaks) if args.decode else None
     flops = rl.gemm_flops(M, N, K)
     ms_per_step = total_ms / args.steps
-    value = ws * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = replica_throughput(ws, flops, args.steps, total_ms)
     kernel_tflops = flops / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the C ABI with pinned host buffers
