@@ -4,10 +4,13 @@
                     [--workload square_4096|...]
 
 A step is one GEMM over the workload's synthetic seeded operands (inputs
-resident in HBM).  Between timed steps a 512 MiB buffer is overwritten to
-flush the 129 MB L2, outside the timed events; each step is timed with CUDA
-events on the stream the kernel is launched on.  `value` is TFLOP/s (2MNK per
-step) over all ranks; `e2e` is the same metric through gemm_run_host with
+resident in HBM).  By default a 512 MiB buffer is overwritten before each step
+to flush the 129 MB L2, outside that step's pair of CUDA events on the launching
+stream.  `--l2 rotate` instead cycles through copies of A, B and C totalling at
+least four times the L2 with the K steps launched back to back between two
+events (cold operands in every step, no launch gap; the GPU then runs at its
+power cap throughout).  The decode shapes are always timed the second way.
+`value` is TFLOP/s (2MNK per step) over all ranks; `e2e` is the same metric through gemm_run_host with
 pinned host buffers (host->device copies of A and B and the device->host copy
 of C inside the timed region).  `cpu_baseline` times the CPU oracle on a
 bounded sample of the same product (whole rows of C) on the host cores, and
@@ -41,6 +44,7 @@ METRIC = "GEMM TFLOP/s (4096³ fp16) & % of tensor peak; decode-shape HBM GB/s"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
+L2_NOMINAL_BYTES = 129 * 1000 * 1000
 KERNEL_SOURCES = "dense_gemm_blackwell_02_gb300/csrc/*"
 
 
@@ -165,10 +169,51 @@ def cpu_rows_sample(A, B, din, dout, M, target_s=10.0):
     return rows, bits, c64, dt, os.cpu_count()
 
 
-def measure_decode(g, dev, stream, flush, peaks, iters=10):
-    """Secondary figures: the M = 256 decode shapes (fp16 -> fp16), HBM-bound, timed
-    like the main workload (events per launch, L2 flushed between launches).  Their
-    parity is covered by the full-size tests; here only time is taken."""
+def l2_bytes(dev) -> int:
+    return int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_NOMINAL_BYTES)
+
+
+def operand_sets(A, B, C, dev):
+    """Copies of (A, B, C) totalling at least 4x the L2, used in turn so that every
+    step's operands were evicted by the steps before it."""
+    per = A.numel() * A.element_size() + B.numel() * B.element_size() + C.numel() * C.element_size()
+    n = max(2, -(-4 * l2_bytes(dev) // per))
+    return [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C)) for _ in range(n - 1)], n * per
+
+
+def time_steps(run, sets, stream, steps, flush=None):
+    """ms for `steps` launches: back to back between two events, cycling through
+    `sets`; or, with `flush`, one event pair per step after overwriting the flush
+    buffer (summed)."""
+    if flush is None:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            run(*sets[i % len(sets)])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+    ev = []
+    for i in range(steps):
+        flush.fill_(float(i))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run(*sets[0])
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev)
+
+
+def measure_decode(g, dev, stream, peaks, iters=20):
+    """Secondary figures: the M = 256 decode shapes (fp16 -> fp16), HBM-bound.  Each is
+    timed over `iters` launches back to back, cycling through operand copies at least
+    four times the L2 (cold operands in every launch, as when a model's layers stream
+    their weights).  Their parity is covered by the full-size tests; here only time is
+    taken."""
+    flush = None
     wl = si.WORKLOADS["decode_m256"]
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     out = {}
@@ -178,26 +223,23 @@ def measure_decode(g, dev, stream, flush, peaks, iters=10):
         A = (torch.rand(s.M, s.K, generator=gen, device=dev) * 2 - 1).half()
         B = (torch.rand(s.N, s.K, generator=gen, device=dev) * 2 - 1).half()
         C = torch.empty(s.M, s.N, dtype=torch.float16, device=dev)
-        for _ in range(3):
-            flush.fill_(0.5)
-            g.run(A, B, C, stream=stream)
-        ev = []
-        for i in range(iters):
-            flush.fill_(float(i))
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            g.run(A, B, C, stream=stream)
-            e1.record(stream)
-            ev.append((e0, e1))
+        sets, _ = operand_sets(A, B, C, dev) if flush is None else ([(A, B, C)], 0)
+
+        def run(a, b, c):
+            g.run(a, b, c, stream=stream)
+
+        for i in range(3 * len(sets)):
+            if flush is not None:
+                flush.fill_(0.5)
+            run(*sets[i % len(sets)])
         torch.cuda.synchronize()
-        ms = sorted(a.elapsed_time(b) for a, b in ev)[iters // 2]
+        ms = time_steps(run, sets, stream, iters, flush) / iters
         gbs = rl.gemm_bytes(s.M, s.N, s.K, 2, 2) / (ms * 1e-3) / 1e9
         out[f"{s.M}x{s.N}x{s.K}"] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
                                      "frac_of_hbm": round(gbs / hbm, 4),
                                      "TFLOP/s": round(rl.gemm_flops(s.M, s.N, s.K) / (ms * 1e-3) / 1e12, 1),
                                      "kernel": g.last_config()}
-        del A, B, C
+        del A, B, C, sets
     return out
 
 
@@ -254,18 +296,27 @@ def run_ours(args):
     A_cpu, B_cpu = si.make_operands(M, N, K, din, wl.dist, wl.seed)
     A, B = A_cpu.to(dev), B_cpu.to(dev)
     C = torch.empty(M, N, dtype=si.TORCH_DTYPE[dout], device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = (torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+             if args.l2 == "flush" else None)
+    if flush is None:
+        sets, set_bytes = operand_sets(A, B, C, dev)
+        l2_note = (f"inputs larger than L2: {len(sets)} copies of A, B, C ({set_bytes >> 20} MiB in all,"
+                   f" L2 {l2_bytes(dev) / 1e6:.0f} MB) used in turn, launches back to back")
+    else:
+        sets = [(A, B, C)]
+        l2_note = "flushed (512 MiB write before each step, outside its events)"
     stream = torch.cuda.current_stream(dev)
     g = Gemm()
     if args.config:
         g.set_config(**json.loads(args.config))
 
-    def step():
-        g.run(A, B, C, stream=stream)
+    def run(a, b, c):
+        g.run(a, b, c, stream=stream)
 
-    for _ in range(max(args.warmup, 3)):
-        flush.fill_(1.0)
-        step()
+    for i in range(max(args.warmup, 3, len(sets))):
+        if flush is not None:
+            flush.fill_(1.0)
+        run(*sets[i % len(sets)])
     torch.cuda.synchronize()
     code, word = g.device_status(stream)
     if code != 0:
@@ -274,31 +325,24 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.25)  # let the sampler take its first reading
-    for _ in range(max(args.warmup, 3)):
-        flush.fill_(1.0)
-        step()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(max(args.warmup, 3)):
+        if flush is not None:
+            flush.fill_(1.0)
+        run(*sets[i % len(sets)])
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    local_ms = time_steps(run, sets, stream, args.steps, flush)
     if ws > 1:
         torch.distributed.barrier()
     time.sleep(0.1)
     clocks = sampler.stop()
-    per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = max_over_ranks(sum(per_ms), dev)
+    total_ms = max_over_ranks(local_ms, dev)
     code, word = g.device_status(stream)
     if code != 0:
         raise RuntimeError(f"device status after timing: {code} ({word:#x})")
     cfg = g.last_config()
-    decode = measure_decode(g, dev, stream, flush, peaks) if args.decode else None
+    decode = measure_decode(g, dev, stream, peaks) if args.decode else None
     flops = rl.gemm_flops(M, N, K)
     ms_per_step = total_ms / args.steps
     value = replica_throughput(ws, flops, args.steps, total_ms)
@@ -345,7 +389,7 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": si.DTYPE_NAME[din], "data": "synthetic",
             "config": {"workload": args.workload, "M": M, "N": N, "K": K,
                        "dtype_in": si.DTYPE_NAME[din], "dtype_out": si.DTYPE_NAME[dout],
-                       "dist": wl.dist, "seed": wl.seed, "l2": "flushed (512 MiB write between steps)",
+                       "dist": wl.dist, "seed": wl.seed, "l2": l2_note,
                        "kernel": cfg, "parallelism": "replicas" if ws > 1 else "single-gpu"},
             "clocks": clocks,
             "e2e": e2e,
@@ -379,6 +423,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--decode", type=int, default=1,
                     help="also time the M=256 decode shapes (HBM GB/s) into the line")
+    ap.add_argument("--l2", default="flush", choices=["rotate", "flush"],
+                    help="main workload: flush L2 before each separately timed step (default), "
+                         "or cycle operand copies larger than L2 with launches back to back")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
