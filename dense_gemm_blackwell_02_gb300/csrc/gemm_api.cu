@@ -116,6 +116,7 @@ bool valid_dtype(int d) { return d == GEMM_F16 || d == GEMM_BF16 || d == GEMM_F3
 
 struct Choice {
   int variant, bn, stages, splits, kb_per_split, group_m, grid, chain_kb, half_tail, prefetch_kb;
+  bool one_chain;
   int64_t tiles, dp_tiles, units, k_blocks, num_m, num_n;
   int64_t sk_workers, ws_slots;
 };
@@ -204,6 +205,16 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
   // M = 256 decode shapes and the square ones it did not help).
   c->prefetch_kb = f.prefetch_kblocks > 0 ? f.prefetch_kblocks : 0;
   c->grid = (int)(std::min<int64_t>(std::max(c->units, c->sk_workers), slots) * cg);
+  // The single-chain epilogue needs every unit to be one accumulation chain.
+  int64_t longest = c->k_blocks;  // whole tiles and half-tile units
+  if (c->sk_workers)
+    longest = std::min<int64_t>(c->k_blocks,
+                                ceil_div((c->tiles - dp) * c->k_blocks, c->sk_workers));
+  else if (!c->half_tail && s > 1 && dp == 0)
+    longest = c->kb_per_split;
+  const bool one_ok = longest <= c->chain_kb;
+  if (f.epilogue == 2 && !one_ok) return GEMM_ERR_UNSUPPORTED;
+  c->one_chain = f.epilogue == 1 ? false : one_ok;
   if (c->units > INT32_MAX || c->tiles * cg * 8 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   return GEMM_OK;
 }
@@ -292,7 +303,7 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
   if (c.variant < 0 || c.variant > 2) return GEMM_ERR_INVALID_ARG;
   if (c.block_n != 0 && c.block_n != 128 && c.block_n != 256) return GEMM_ERR_INVALID_ARG;
   if (c.splits < -1 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
-      c.dp_tiles != 0 || c.prefetch_kblocks < -1)
+      c.dp_tiles != 0 || c.prefetch_kblocks < -1 || c.epilogue < 0 || c.epilogue > 2)
     return GEMM_ERR_INVALID_ARG;
   if (c.stages) {
     const int bn = c.block_n ? c.block_n : 256;
@@ -357,6 +368,7 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   s.stages = ch.stages;
   s.out = out;
   s.grid = ch.grid;
+  s.one_chain = ch.one_chain;
   s.stream = stream;
   const bool c_tma = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0;
   if (!make_map(h, A, M, K, dtype_in, kBlockM, &s.tmA) ||
@@ -404,7 +416,7 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   h->last = gemm_config_t{ch.variant,  ch.bn,   ch.sk_workers ? -(int32_t)ch.sk_workers : ch.splits,
                           ch.stages,
                           ch.group_m,  ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles,
-                          ch.prefetch_kb ? ch.prefetch_kb : -1};
+                          ch.prefetch_kb ? ch.prefetch_kb : -1, ch.one_chain ? 2 : 1};
   return GEMM_OK;
 }
 

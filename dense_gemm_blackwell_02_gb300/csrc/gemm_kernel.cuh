@@ -282,6 +282,53 @@ __device__ __forceinline__ void store_row_direct(const GemmParams& p, int32_t m,
   }
 }
 
+// One 32-column piece of a single-chain unit's output, for the warp's rows: the TMEM
+// accumulator at `taddr`, or for a split tile the slices summed in slice order (the
+// own slice's partial is the TMEM value itself; two slices add in either order to the
+// same bits).  `ws_lane` is this lane's start of the tile's workspace block, `col` the
+// piece's first column within the warp's block.
+__device__ __forceinline__ void one_chain_piece(uint32_t taddr, const Unit& w, const float* ws_lane,
+                                                size_t slice_stride, int col, float (&v)[32]) {
+  uint32_t r[32];
+  tmem_ld_32x32b_x32(taddr, r);
+  tmem_ld_wait(r);
+  if (w.nsplit <= 1) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  } else if (w.nsplit == 2) {
+    const float* other = ws_lane + (size_t)(1 - w.split) * slice_stride;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const uint4 x = ld_global_cg_v4(other + (col + j) * 32);
+      v[j] = __uint_as_float(r[j]) + __uint_as_float(x.x);
+      v[j + 1] = __uint_as_float(r[j + 1]) + __uint_as_float(x.y);
+      v[j + 2] = __uint_as_float(r[j + 2]) + __uint_as_float(x.z);
+      v[j + 3] = __uint_as_float(r[j + 3]) + __uint_as_float(x.w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+    for (int32_t sl = 0; sl < w.nsplit; ++sl) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        float t[4];
+        if (sl == w.split) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) t[u] = __uint_as_float(r[j + u]);
+        } else {
+          const uint4 x = ld_global_cg_v4(ws_lane + (size_t)sl * slice_stride + (col + j) * 32);
+          t[0] = __uint_as_float(x.x);
+          t[1] = __uint_as_float(x.y);
+          t[2] = __uint_as_float(x.z);
+          t[3] = __uint_as_float(x.w);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[j + u] = sl == 0 ? t[u] : v[j + u] + t[u];
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------- shared memory map --
 template <int CTA_GROUP, int BN, int STAGES>
 struct Layout {
@@ -310,7 +357,11 @@ struct Layout {
   static_assert(kDynamicBytes <= 227 * 1024, "shared memory over the per-block limit");
 };
 
-template <int CTA_GROUP, int BN, int STAGES, int OUT>
+// ONE_CHAIN: every work unit is a single accumulation chain (at most p.chain_kb
+// k-blocks), so the epilogue streams the accumulator out of TMEM in 32-column pieces
+// instead of first copying the warp's whole 32 x BN/2 block into registers; the
+// registers this frees go to loads in flight in the split-K hand-over.
+template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN>
 __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
@@ -507,6 +558,116 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     bool ok = true;
     Walker walk{first_unit, 0};
     Unit w;
+    if constexpr (ONE_CHAIN) {
+      constexpr size_t kBlockFloats = 32 * kHalf;
+      constexpr size_t kBlocksPerSlice = (size_t)CTA_GROUP * 8;  // (rank, quarter, half)
+      constexpr size_t kSliceStride = kBlocksPerSlice * kBlockFloats;
+      const size_t my_block = ((size_t)rank * 4 + q) * 2 + h;
+      while (ok && walker_next(walk, first_unit, unit_stride, p, w)) {
+        // in a half-tile unit the h = 1 warps only take part in the slot hand-over
+        const bool active = w.half < 0 || h == 0;
+        const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
+        uint32_t good = 1;
+        if (lane == 0)
+          good = wait_parity(acc_full_bar(slot), acc_phase, ctl, kSiteAccFull) ? 1u : 0u;
+        good = __shfl_sync(0xFFFFFFFFu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * BN + h * kHalf;
+        const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
+        const int32_t n_half = w.n_blk * BN + (w.half >= 0 ? w.half : (int32_t)h) * kHalf;
+        bool emit = active;
+        const float* ws_lane = nullptr;
+        if (active && w.nsplit > 1) {
+          // Split-K: this slice's partial goes to the workspace straight from TMEM
+          // (the same block layout as the general epilogue); the last slice to arrive
+          // emits C, summing the slices in slice order.
+          const size_t sliced = (size_t)(w.tile - p.dp_tiles);
+          const float* ws_tile = p.workspace + sliced * p.ws_slots * kSliceStride;
+          ws_lane = ws_tile + my_block * kBlockFloats + lane * 4;
+          float* mine = p.workspace + sliced * p.ws_slots * kSliceStride +
+                        ((size_t)w.split * kBlocksPerSlice + my_block) * kBlockFloats + lane * 4;
+#pragma unroll
+          for (int pc = 0; pc < kPieces; ++pc) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + 32u * pc, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              st_global_cg_v4(mine + (32 * pc + j) * 32, r[j], r[j + 1], r[j + 2], r[j + 3]);
+          }
+          __syncwarp();
+          uint32_t last = 0;
+          if (lane == 0) {
+            uint32_t* ctr = p.counters + sliced * kBlocksPerSlice + my_block;
+            const uint32_t before = atom_add_acq_rel_gpu(ctr, 1u);
+            last = (before == (uint32_t)w.nsplit - 1u) ? 1u : 0u;
+            if (last) st_relaxed_gpu_u32(ctr, 0u);  // ready for the next launch
+          }
+          emit = __shfl_sync(0xFFFFFFFFu, last, 0) != 0;
+          __syncwarp();
+        }
+        if (emit) {
+          if (p.tma_store) {
+            constexpr int kPiecesPerBox = kBoxCols / 32;
+            const uint32_t row_addr = staging + lane * 128u;
+#pragma unroll
+            for (int bx = 0; bx < kBoxes; ++bx) {
+              // the previous store from this staging box must have finished reading it
+              if (lane == 0) bulk_wait_group_read<0>();
+              __syncwarp();
+#pragma unroll
+              for (int pp = 0; pp < kPiecesPerBox; ++pp) {
+                float v[32];
+                const int pc = bx * kPiecesPerBox + pp;
+                one_chain_piece(taddr + 32u * pc, w, ws_lane, kSliceStride, 32 * pc, v);
+                // 16-byte chunks of the 128-byte row, in the 128-byte swizzled order
+                constexpr int kChunks = 8 / kPiecesPerBox;
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                  const uint32_t cj = (uint32_t)(pp * kChunks + c);
+                  uint32_t w4[4];
+                  if constexpr (OUT == kOutF32) {
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) w4[t] = __float_as_uint(v[c * 4 + t]);
+                  } else {
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) w4[t] = pack2<OUT>(v[c * 8 + 2 * t], v[c * 8 + 2 * t + 1]);
+                  }
+                  st_shared_v4(row_addr + ((cj ^ (lane & 7u)) << 4), w4[0], w4[1], w4[2], w4[3]);
+                }
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              const int32_t box_n = n_half + bx * kBoxCols, box_m = m0 + (int32_t)(q * 32u);
+              if (lane == 0 && box_n < p.N && box_m < p.M) {
+                tma_store_2d(&tmC, staging, box_n, box_m);
+                bulk_commit_group();
+              }
+            }
+          } else {
+            const int32_t m = m0 + (int32_t)row;
+#pragma unroll
+            for (int pc = 0; pc < kPieces; ++pc) {
+              float v[32];
+              one_chain_piece(taddr + 32u * pc, w, ws_lane, kSliceStride, 32 * pc, v);
+              store_row_direct<OUT>(p, m, n_half + 32 * pc, v);
+            }
+          }
+        }
+        // The slot goes back to the MMA warp once this warp's last TMEM read is done.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CTA_GROUP == 1) mbar_arrive(acc_empty_bar(slot));
+          else mbar_arrive_cluster(mapa_shared(acc_empty_bar(slot), 0));
+        }
+        ++iter;
+      }
+    } else {
     while (ok && walker_next(walk, first_unit, unit_stride, p, w)) {
       // In a half-tile unit the accumulator holds BN/2 columns: the h = 0 warps own
       // them, the h = 1 warps only take part in the slot hand-over.
@@ -669,6 +830,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
           store_row_direct<OUT>(p, m, n_half + 32 * pc, acc + 32 * pc);
       }
     }
+    }  // general epilogue
     // Every TMA store of this warp must be complete before the CTA exits.
     if (p.tma_store && lane == 0) bulk_wait_group<0>();
     __syncwarp();

@@ -14,6 +14,7 @@ struct LaunchSpec {
   int stages;      // operand ring depth
   int out;         // OutKind
   int grid;        // CTAs (a multiple of cta_group)
+  bool one_chain;  // every unit is one accumulation chain (streaming epilogue)
   CUtensorMap tmA; // A: box {64, 128}
   CUtensorMap tmB; // B: box {64, bn / cta_group}
   CUtensorMap tmB2; // B: box {64, bn / cta_group / 2} (half-tile units; else a copy of tmB)
@@ -31,9 +32,12 @@ size_t kernel_smem_bytes(int cta_group, int bn, int stages);
 int max_resident_units(int cta_group, int bn, int stages, int out);
 cudaError_t launch_gemm(const LaunchSpec& s);
 
-// Per-translation-unit launchers (kernels_cg1.cu, kernels_cg2.cu).
+// Per-translation-unit launchers (kernels_cg1.cu, kernels_cg2.cu: the general
+// epilogue; kernels_cg1_one.cu, kernels_cg2_one.cu: single-chain units).
 cudaError_t launch_cg1(const LaunchSpec& s);
 cudaError_t launch_cg2(const LaunchSpec& s);
+cudaError_t launch_cg1_one(const LaunchSpec& s);
+cudaError_t launch_cg2_one(const LaunchSpec& s);
 int resident_cg1(int bn, int stages, int out);
 int resident_cg2(int bn, int stages, int out);
 

@@ -5,9 +5,9 @@
 
 namespace gb300 {
 
-template <int CG, int BN, int STAGES, int OUT>
+template <int CG, int BN, int STAGES, int OUT, bool ONE>
 cudaError_t launch_one(const LaunchSpec& s) {
-  auto kernel = gemm_kernel<CG, BN, STAGES, OUT>;
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE>;
   using L = Layout<CG, BN, STAGES>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes);
@@ -35,7 +35,7 @@ cudaError_t launch_one(const LaunchSpec& s) {
 
 template <int CG, int BN, int STAGES, int OUT>
 int resident_one() {
-  auto kernel = gemm_kernel<CG, BN, STAGES, OUT>;
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, false>;
   using L = Layout<CG, BN, STAGES>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            L::kDynamicBytes) != cudaSuccess)
@@ -59,12 +59,12 @@ int resident_one() {
   return n;
 }
 
-template <int CG, int BN, int STAGES>
+template <int CG, int BN, int STAGES, bool ONE>
 cudaError_t by_out(const LaunchSpec& s) {
   switch (s.out) {
-    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16>(s);
-    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16>(s);
-    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32>(s);
+    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE>(s);
+    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE>(s);
+    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE>(s);
     default: return cudaErrorInvalidValue;
   }
 }

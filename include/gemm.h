@@ -79,6 +79,11 @@ typedef enum {
  *             are too few of them for the SMs).
  *   prefetch_kblocks  how many 64-deep K blocks ahead of the shared-memory ring the
  *             producer prefetches B into L2 (0 or -1 = never, the default)
+ *   epilogue  1 = general (the accumulator is copied to registers, chains summed
+ *             there); 2 = single-chain (streamed out of Tensor Memory in 32-column
+ *             pieces), valid only when every work unit spans at most chain_kblocks K
+ *             blocks (else gemm_run returns GEMM_ERR_UNSUPPORTED); 0 = 2 when valid.
+ *             gemm_last_config reports the one used.
  */
 typedef struct {
   int32_t variant;
@@ -90,6 +95,7 @@ typedef struct {
   int32_t chain_kblocks;
   int32_t dp_tiles;
   int32_t prefetch_kblocks;
+  int32_t epilogue;
 } gemm_config_t;
 
 /* Create a handle on the current CUDA device.  Fails with GEMM_ERR_UNSUPPORTED

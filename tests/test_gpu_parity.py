@@ -268,3 +268,53 @@ def test_run_host_matches_device(g):
     Ch = torch.empty(300, 500, dtype=torch.float16).pin_memory()
     g.run_host(A.pin_memory(), B.pin_memory(), Ch, F16, F16)
     assert torch.equal(Ch.view(torch.int16), Cd.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("cfg,M,N,K,dtype_out", [
+    ({"variant": 2, "block_n": 256}, 512, 768, 1024, F16),                  # whole tiles
+    ({"variant": 2, "block_n": 256, "splits": 2}, 256, 1024, 4096, BF16),   # two K slices
+    ({"variant": 1, "block_n": 256, "splits": 3}, 300, 1100, 2000, F32),    # three K slices
+    ({"variant": 2, "block_n": 128, "splits": -1, "max_ctas": 38}, 300, 1100, 2000, F16),  # stream-K
+    ({"variant": 2, "block_n": 256, "max_ctas": 10}, 640, 1024, 704, F16),  # half-tile tail
+    ({"variant": 1, "block_n": 128, "max_ctas": 6}, 512, 1280, 2048, BF16),  # K-sliced tail
+    ({"variant": 2, "block_n": 256}, 129, 4097, 512, F16),                  # direct stores
+    ({"variant": 1, "block_n": 256, "splits": 2}, 131, 1001, 1024, F32),    # direct, split
+])
+def test_single_chain_epilogue_matches_general(g, cfg, M, N, K, dtype_out):
+    # Every unit here is one accumulation chain, so the streaming epilogue applies; it
+    # performs the same additions in the same order as the general one (the own slice's
+    # partial is read from TMEM instead of the workspace, the same bits), so the two
+    # must agree bit for bit, and both with the oracle.
+    A, B = si.make_operands(M, N, K, F16, "uniform", 50)
+    out = {}
+    try:
+        for epi in (1, 2):
+            g.set_config(epilogue=epi, **cfg)
+            out[epi] = parity.run_gpu(g, A, B, dtype_out)
+            assert g.device_status()[0] == 0
+            assert g.last_config()["epilogue"] == epi
+        g.set_config(**cfg)
+        auto = parity.run_gpu(g, A, B, dtype_out)
+        assert g.last_config()["epilogue"] == 2        # chosen automatically
+    finally:
+        g.reset_config()
+    assert np.array_equal(parity.bits_of(out[1]), parity.bits_of(out[2]))
+    assert np.array_equal(parity.bits_of(out[2]), parity.bits_of(auto))
+    parity.oracle_check(parity.bits_of(out[2]), A, B, F16, dtype_out,
+                        what=f"single-chain epilogue {cfg} {M}x{N}x{K}")
+
+
+def test_single_chain_epilogue_needs_single_chain_units(g):
+    from dense_gemm_blackwell_02_gb300.binding import GemmError
+    A, B = si.make_operands(256, 256, 8192, F16, "uniform", 51)
+    try:
+        g.set_config(variant=2, splits=1, epilogue=2)          # 128 k-blocks in one unit
+        with pytest.raises(GemmError) as e:
+            parity.run_gpu(g, A, B, F32)
+        assert e.value.code == 2
+        g.set_config(variant=2, splits=1)
+        C = parity.run_gpu(g, A, B, F32)
+        assert g.last_config()["epilogue"] == 1
+    finally:
+        g.reset_config()
+    parity.oracle_check(parity.bits_of(C), A, B, F16, F32, what="two chains, general epilogue")
