@@ -45,12 +45,18 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
 L2_NOMINAL_BYTES = 129 * 1000 * 1000
-KERNEL_SOURCES = "dense_gemm_blackwell_02_gb300/csrc/*"
+# The device code of the kernels (the host-side files -- the C ABI, the launch table --
+# do not change what a launch of a given configuration moves).
+KERNEL_SOURCES = ("dense_gemm_blackwell_02_gb300/csrc/gemm_kernel.cuh",
+                  "dense_gemm_blackwell_02_gb300/csrc/ptx.cuh",
+                  "dense_gemm_blackwell_02_gb300/csrc/umma.cuh",
+                  "dense_gemm_blackwell_02_gb300/csrc/params.h",
+                  "dense_gemm_blackwell_02_gb300/csrc/launch_impl.cuh")
 
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, KERNEL_SOURCES))):
+    for f in sorted(os.path.join(ROOT, k) for k in KERNEL_SOURCES):
         h.update(os.path.basename(f).encode())
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
@@ -381,7 +387,9 @@ def run_ours(args):
         tf_path = os.path.join(ROOT, "profiles", "traffic.json")
         if os.path.exists(tf_path):
             rec = json.load(open(tf_path)).get(args.workload)
-            if rec and rec.get("source_hash") == kernel_source_hash():
+            # valid only for the same kernel source and the same launch configuration
+            if (rec and rec.get("source_hash") == kernel_source_hash()
+                    and rec.get("config") == cfg):
                 traffic = rec.get("bytes_per_launch")
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,

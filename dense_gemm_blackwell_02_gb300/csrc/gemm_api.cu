@@ -149,6 +149,28 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
   c->tiles = c->num_m * c->num_n;
   int64_t slots = resident_units(h, cg, c->bn, c->stages, out);
   if (f.max_ctas) slots = std::min<int64_t>(slots, std::max<int64_t>(f.max_ctas / cg, 1));
+  // Too few 256-column tiles for the SMs, but 128-column tiles fill more than half of
+  // one wave:
+  // with K of at most 8192 the narrower tiles without a K split beat splitting K
+  // (measured, 256 x 8192 x 8192: 38.3 us against 40.5 us for two K slices, whose
+  // hand-over of fp32 partials costs several microseconds at the end).  For longer K the
+  // hand-over is amortised and split-K wins (256 x 8192 x 28672: 98 against 110 us).
+  if (!f.block_n && !f.splits && !f.stages && c->bn == 256 && c->tiles * 2 <= slots &&
+      c->k_blocks <= 128) {
+    const int64_t tiles128 = c->num_m * ceil_div(N, (int64_t)128);
+    const int64_t slots128 = [&] {
+      int64_t n = resident_units(h, cg, 128, default_stages(cg, 128), out);
+      if (f.max_ctas) n = std::min<int64_t>(n, std::max<int64_t>(f.max_ctas / cg, 1));
+      return n;
+    }();
+    if (tiles128 <= slots128 && tiles128 * 2 > slots128) {
+      c->bn = 128;
+      c->stages = default_stages(cg, 128);
+      c->num_n = ceil_div(N, (int64_t)128);
+      c->tiles = tiles128;
+      slots = slots128;
+    }
+  }
   int64_t s = 1, dp = c->tiles;
   c->half_tail = 0;
   c->sk_workers = 0;
