@@ -429,6 +429,12 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched with programmatic stream serialisation: the setup above overlaps the tail
+  // of the preceding kernel; nothing in global memory (A, B, C, the workspace, the
+  // status word) is touched before that kernel has completed.  The next kernel may
+  // then be scheduled as this one's CTAs exit.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer --

@@ -97,6 +97,16 @@ __device__ __forceinline__ void mbar_arrive_elect(uint32_t bar) {
   asm volatile(GB300_ELECT "@e_ mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar) : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on (the
+// preceding work in the stream) have completed and their memory is visible; and let
+// the next grid launch early (its blocks wait in their own grid_dependency_wait).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- fences --
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
