@@ -45,6 +45,9 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
 L2_NOMINAL_BYTES = 129 * 1000 * 1000
+# Nominal GB300 figures, reported as context beside the measured peaks.
+NOMINAL_TFLOPS = 2250.0   # dense fp16/bf16
+NOMINAL_HBM_GBS = 7900.0
 # The device code of the kernels (the host-side files -- the C ABI, the launch table --
 # do not change what a launch of a given configuration moves).
 KERNEL_SOURCES = ("dense_gemm_blackwell_02_gb300/csrc/gemm_kernel.cuh",
@@ -187,19 +190,26 @@ def operand_sets(A, B, C, dev):
     return [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C)) for _ in range(n - 1)], n * per
 
 
-def time_steps(run, sets, stream, steps, flush=None):
+def time_steps(run, sets, stream, steps, flush=None, per_step=False):
     """ms for `steps` launches: back to back between two events, cycling through
     `sets`; or, with `flush`, one event pair per step after overwriting the flush
-    buffer (summed)."""
+    buffer (summed).  With per_step, also the list of per-launch ms (back to back:
+    between consecutive events recorded between the launches)."""
     if flush is None:
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        # events between the launches only when asked for: a stream event between two
+        # launches would also stop the second from starting early (programmatic
+        # dependent launch)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
         for i in range(steps):
             run(*sets[i % len(sets)])
-        e1.record(stream)
+            if per_step or i == steps - 1:
+                ev[i + 1].record(stream)
         torch.cuda.synchronize()
-        return e0.elapsed_time(e1)
+        total = ev[0].elapsed_time(ev[-1])
+        if not per_step:
+            return total
+        return total, [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
     ev = []
     for i in range(steps):
         flush.fill_(float(i))
@@ -210,7 +220,8 @@ def time_steps(run, sets, stream, steps, flush=None):
         e1.record(stream)
         ev.append((e0, e1))
     torch.cuda.synchronize()
-    return sum(a.elapsed_time(b) for a, b in ev)
+    each = [a.elapsed_time(b) for a, b in ev]
+    return (sum(each), each) if per_step else sum(each)
 
 
 def measure_decode(g, dev, stream, peaks, iters=20):
@@ -243,6 +254,7 @@ def measure_decode(g, dev, stream, peaks, iters=20):
         gbs = rl.gemm_bytes(s.M, s.N, s.K, 2, 2) / (ms * 1e-3) / 1e9
         out[f"{s.M}x{s.N}x{s.K}"] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
                                      "frac_of_hbm": round(gbs / hbm, 4),
+                                     "frac_of_nominal_hbm": round(gbs / NOMINAL_HBM_GBS, 4),
                                      "TFLOP/s": round(rl.gemm_flops(s.M, s.N, s.K) / (ms * 1e-3) / 1e12, 1),
                                      "kernel": g.last_config()}
         del A, B, C, sets
@@ -338,7 +350,13 @@ def run_ours(args):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    local_ms = time_steps(run, sets, stream, args.steps, flush)
+    # Per-step events only in the flushed form: between back-to-back launches they would
+    # also stop each launch from starting early (programmatic dependent launch).
+    if flush is not None:
+        local_ms, each_ms = time_steps(run, sets, stream, args.steps, flush, per_step=True)
+    else:
+        local_ms = time_steps(run, sets, stream, args.steps)
+        each_ms = [local_ms / args.steps]
     if ws > 1:
         torch.distributed.barrier()
     time.sleep(0.1)
@@ -348,6 +366,20 @@ def run_ours(args):
     if code != 0:
         raise RuntimeError(f"device status after timing: {code} ({word:#x})")
     cfg = g.last_config()
+    # The same workload timed the other way (compute-bound shapes are reported both
+    # ways): back to back over operand copies larger than L2, or flushed per step.
+    if flush is not None:
+        other_sets, _ = operand_sets(A, B, C, dev)
+        other_flush, other_how = None, "back to back over operand copies >= 4x L2"
+    else:
+        other_sets = [(A, B, C)]
+        other_flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        other_how = "L2 flushed before each step"
+    for i in range(2 * len(other_sets)):
+        run(*other_sets[i % len(other_sets)])
+    other_steps = min(args.steps, 20)
+    other_ms = time_steps(run, other_sets, stream, other_steps, other_flush) / other_steps
+    del other_sets, other_flush
     decode = measure_decode(g, dev, stream, peaks) if args.decode else None
     flops = rl.gemm_flops(M, N, K)
     ms_per_step = total_ms / args.steps
@@ -406,6 +438,12 @@ def run_ours(args):
                          "unit": "TFLOP/s", "frac": kernel_tflops / peak, "traffic": traffic,
                          "peak_source": f"{peak_src} bf16_tflops (burst; fp16 has the same dense rate)",
                          "algorithmic_flops_per_launch": flops},
+            "per_step_us": {"median": 1e3 * statistics.median(each_ms), "best": 1e3 * min(each_ms),
+                            "mean": 1e3 * ms_per_step},
+            "timed_other_way": {"how": other_how, "us": 1e3 * other_ms,
+                                "TFLOP/s": flops / (other_ms * 1e-3) / 1e12},
+            "nominal_context": {"tensor_tflops": NOMINAL_TFLOPS, "hbm_gbs": NOMINAL_HBM_GBS,
+                                "frac_of_nominal_tensor": kernel_tflops / NOMINAL_TFLOPS},
             "cpu_baseline": {"value": cpu_value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"{len(rows)} whole rows of C ({2.0 * len(rows) * N * K / 1e9:.1f}"
                                        f" GFLOP) in {cpu_s:.1f} s"},
