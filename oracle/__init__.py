@@ -70,6 +70,10 @@ def load_library(path: str):
     lib.oracle_decode.restype = i32
     lib.oracle_round.argtypes = [vp, vp, i64, i32]
     lib.oracle_round.restype = i32
+    if hasattr(lib, "oracle_gemm_epilogue"):
+        lib.oracle_gemm_epilogue.argtypes = [vp, vp, vp, vp, ctypes.c_double, ctypes.c_double,
+                                             i32, vp, i64, i64, i64, i32, i32, i32]
+        lib.oracle_gemm_epilogue.restype = i32
     return lib
 
 
@@ -143,6 +147,31 @@ def gemm_select(A, B, rows, cols, dtype_in: int, dtype_out: int, nthreads: int =
         None if r is None else r.ctypes.data, nr,
         None if c is None else c.ctypes.data, nc, dtype_in, dtype_out, nthreads))
     return (out, f64) if want_f64 else out
+
+
+def gemm_epilogue(A, B, dtype_in: int, dtype_out: int, alpha=1.0, beta=0.0, cprev=None,
+                  bias=None, relu=False, nthreads: int = 0, lib=None) -> np.ndarray:
+    """D = act(alpha * A . B^T + beta * cprev + bias[j]) as output-format bit patterns
+    (M x N): cprev is M x N output-format bit patterns (needed when beta != 0), bias N
+    binary32 values, act ReLU when relu.  Evaluated in binary64, rounded once."""
+    a, b = _bits16(A), _bits16(B)
+    M, K = a.shape
+    N, K2 = b.shape
+    if K != K2:
+        raise ValueError("A and B disagree on K")
+    cp = None
+    if beta != 0.0:
+        if cprev is None:
+            raise ValueError("beta != 0 needs the previous output")
+        want = np.uint32 if dtype_out == F32 else np.uint16
+        cp = np.ascontiguousarray(np.asarray(cprev).view(want).reshape(M, N))
+    bs = None if bias is None else np.ascontiguousarray(np.asarray(bias, dtype=np.float32).reshape(N))
+    D = _out_array((M, N), dtype_out)
+    _check(_load(lib).oracle_gemm_epilogue(
+        a.ctypes.data, b.ctypes.data, None if cp is None else cp.ctypes.data,
+        None if bs is None else bs.ctypes.data, float(alpha), float(beta), 1 if relu else 0,
+        D.ctypes.data, M, N, K, dtype_in, dtype_out, nthreads))
+    return D
 
 
 def decode(bits: np.ndarray, dtype: int, lib=None) -> np.ndarray:

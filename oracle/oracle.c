@@ -23,6 +23,16 @@
  *   - Subnormal inputs are decoded exactly.
  *   - K == 0 gives the empty sum, +0.
  *
+ * Fused epilogue (oracle_gemm_epilogue): "CUTLASS Deep Dive: From CuTe Layouts
+ * to Blackwell tcgen05", Part 6, Epilogue Visitor Trees (D = alpha * acc +
+ * beta * C) and Classic Fused Epilogue: Bias + ReLU (d = max(0, alpha * acc +
+ * bias)), taken together:
+ *       D[i][j] = act( alpha * S[i][j] + beta * Cprev[i][j] + bias[j] )
+ *   with S the sum above, Cprev the previous output (dtype_out bit patterns),
+ *   bias one binary32 value per column, act the identity or ReLU (max(x, 0));
+ *   alpha, beta and bias are taken exactly, the expression is evaluated in
+ *   binary64 and rounded once to dtype_out.
+ *
  * The format decoders and the rounding routine below are written from the
  * IEEE 754 / bfloat16 format definitions (sign, biased exponent, fraction).
  *
@@ -177,6 +187,13 @@ typedef struct {
   const double* lut;
   int64_t next_row;    /* shared work counter */
   pthread_mutex_t mu;
+  /* fused epilogue (all zero: none) */
+  int epi;
+  double alpha, beta;
+  const void* cprev;   /* M x N, dtype_out bit patterns, or NULL */
+  int64_t ldc;         /* row length of cprev (N) */
+  const float* bias;   /* N values, or NULL */
+  int relu;
 } job_t;
 
 static void* worker(void* arg) {
@@ -190,7 +207,20 @@ static void* worker(void* arg) {
     const uint16_t* a_row = jb->A + i * jb->K;
     for (int64_t c = 0; c < jb->ncols; ++c) {
       const int64_t j = jb->cols ? jb->cols[c] : c;
-      const double v = dot_row(a_row, jb->B + j * jb->K, jb->K, jb->lut);
+      double v = dot_row(a_row, jb->B + j * jb->K, jb->K, jb->lut);
+      if (jb->epi) {
+        v = jb->alpha * v;
+        if (jb->cprev) {
+          const fmt_t* f = fmt_of(jb->dtype_out);
+          const int64_t idx = i * jb->ldc + j;
+          const uint32_t bits = jb->dtype_out == ORACLE_F32
+                                    ? ((const uint32_t*)jb->cprev)[idx]
+                                    : ((const uint16_t*)jb->cprev)[idx];
+          v += jb->beta * decode_bits(bits, f);
+        }
+        if (jb->bias) v += (double)jb->bias[j];
+        if (jb->relu && !(v > 0.0)) v = 0.0;
+      }
       const int64_t out = r * jb->ncols + c;
       if (jb->C64) jb->C64[out] = v;
       if (jb->C) store_out(jb->C, out, v, jb->dtype_out);
@@ -249,6 +279,26 @@ int oracle_gemm_select(const uint16_t* A, const uint16_t* B, void* C_out, double
   if (check_types(dtype_in, dtype_out) || K < 0 || nrows < 0 || ncols < 0) return -1;
   job_t jb = {A, B, C_out, C64_out, K, rows, nrows, cols, ncols, dtype_out,
               lut_of(dtype_in), 0};
+  return run_job(&jb, nthreads);
+}
+
+/* Full D (M x N) with the fused epilogue described at the top: cprev (M x N,
+ * dtype_out patterns) may be NULL when beta is 0, bias (N floats) may be NULL,
+ * relu is 0 or 1.  D may be the same buffer as cprev only if nthreads == 1. */
+int oracle_gemm_epilogue(const uint16_t* A, const uint16_t* B, const void* cprev,
+                         const float* bias, double alpha, double beta, int relu, void* D,
+                         int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out,
+                         int nthreads) {
+  if (check_types(dtype_in, dtype_out) || M < 0 || N < 0 || K < 0) return -1;
+  if (beta != 0.0 && !cprev) return -1;
+  job_t jb = {A, B, D, NULL, K, NULL, M, NULL, N, dtype_out, lut_of(dtype_in), 0};
+  jb.epi = 1;
+  jb.alpha = alpha;
+  jb.beta = beta;
+  jb.cprev = beta != 0.0 ? cprev : NULL;
+  jb.ldc = N;
+  jb.bias = bias;
+  jb.relu = relu ? 1 : 0;
   return run_job(&jb, nthreads);
 }
 

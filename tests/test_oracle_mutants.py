@@ -40,6 +40,13 @@ MUTANTS = {
     "no_overflow": ("if (ee > f->emax) return inf_bits;", "if (ee > f->emax + 1) return inf_bits;"),
     "bf16_as_f16_in": ("g_lut[ORACLE_BF16][b] = decode_bits(b, &FMT_BF16);",
                        "g_lut[ORACLE_BF16][b] = decode_bits(b, &FMT_F16);"),
+    # fused epilogue
+    "epi_alpha_dropped": ("v = jb->alpha * v;", "v = v;"),
+    "epi_beta_as_one": ("v += jb->beta * decode_bits(bits, f);", "v += decode_bits(bits, f);"),
+    "epi_bias_by_row": ("if (jb->bias) v += (double)jb->bias[j];",
+                        "if (jb->bias) v += (double)jb->bias[i];"),
+    "epi_relu_before_bias": ("if (jb->bias) v += (double)jb->bias[j];\n        if (jb->relu && !(v > 0.0)) v = 0.0;",
+                             "if (jb->relu && !(v > 0.0)) v = 0.0;\n        if (jb->bias) v += (double)jb->bias[j];"),
 }
 
 
@@ -84,6 +91,24 @@ def _pins_pass(lib) -> bool:
         for j in range(3):
             if Fraction(float(got[i, j])) != exact.round_exact(ex[i][j], F16):
                 return False
+    # fused epilogue, exact rational: alpha, beta, per-column bias, ReLU
+    M, N, K = 3, 5, 16
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=3)
+    bias = np.array([0.75, -1.5, 0.25, -0.125, 2.0], dtype=np.float32)
+    prev = oracle.round_to(np.linspace(-2, 2, M * N).reshape(M, N), F32, lib=lib)
+    S = exact.exact_gemm(A, B)
+    prev_exact = oracle.decode(prev, F32, lib=lib)
+    for relu in (False, True):
+        got = oracle.decode(oracle.gemm_epilogue(A, B, F16, F32, alpha=-1.5, beta=0.75, cprev=prev,
+                                                 bias=bias, relu=relu, lib=lib), F32, lib=lib)
+        for i in range(M):
+            for j in range(N):
+                q = (Fraction(-3, 2) * S[i][j] + Fraction(3, 4) * Fraction(float(prev_exact[i, j]))
+                     + Fraction(float(bias[j])))
+                if relu and q < 0:
+                    q = Fraction(0)
+                if Fraction(float(got[i, j])) != exact.round_exact(q, F32):
+                    return False
     # rounding routine against numpy on ties and overflow
     x = np.array([1.0 + 2.0**-11, 1.0 + 3 * 2.0**-11, 65520.0, 70000.0, 2.0**-25 * 3])
     with np.errstate(over="ignore"):

@@ -267,3 +267,80 @@ def test_rejects_bad_dtype(oracle_lib):
     A = torch.zeros(2, 2, dtype=torch.float16)
     with pytest.raises(ValueError):
         oracle_lib.gemm(A, A, 2, 0)
+
+
+# ---------------------------------------------------------------------------------------
+# Fused epilogue: D = act(alpha * S + beta * Cprev + bias[j])  ("CUTLASS Deep Dive: From
+# CuTe Layouts to Blackwell tcgen05", Part 6: Epilogue Visitor Trees; Classic Fused
+# Epilogue: Bias + ReLU).
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype_in", [F16, BF16])
+@pytest.mark.parametrize("dtype_out", [F16, BF16, F32])
+def test_epilogue_identity_is_the_plain_product(oracle_lib, dtype_in, dtype_out):
+    A, B = si.make_operands(9, 11, 40, dtype_in, "uniform", seed=60)
+    assert np.array_equal(oracle_lib.gemm_epilogue(A, B, dtype_in, dtype_out),
+                          oracle_lib.gemm(A, B, dtype_in, dtype_out))
+
+
+def _f32(x):
+    return np.float32(x)
+
+
+@pytest.mark.parametrize("dtype_out", [F16, BF16, F32])
+@pytest.mark.parametrize("relu", [False, True])
+def test_epilogue_exact_rational(oracle_lib, dtype_out, relu):
+    # every term exact in rational arithmetic (alpha, beta, bias are binary32 values,
+    # Cprev the decoded output patterns), ReLU applied, then one round-to-nearest-even
+    g = torch.Generator().manual_seed(61 + dtype_out + 3 * relu)
+    M, N, K = 4, 5, 24
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=62)
+    alpha, beta = _f32(-0.7109375), _f32(1.3125)
+    bias = (torch.rand(N, generator=g) * 4 - 2).numpy().astype(np.float32)
+    prev_vals = (torch.rand(M, N, generator=g) * 6 - 3)
+    prev = oracle_lib.round_to(prev_vals.numpy().astype(np.float64), dtype_out)
+    got = oracle_lib.decode(oracle_lib.gemm_epilogue(A, B, F16, dtype_out, alpha, beta, prev, bias,
+                                                     relu), dtype_out)
+    S = exact.exact_gemm(A, B)
+    prev_exact = oracle_lib.decode(prev, dtype_out)
+    for i in range(M):
+        for j in range(N):
+            q = (Fraction(float(alpha)) * S[i][j] + Fraction(float(beta)) * Fraction(float(prev_exact[i, j]))
+                 + Fraction(float(bias[j])))
+            if relu and q < 0:
+                q = Fraction(0)
+            assert Fraction(float(got[i, j])) == exact.round_exact(q, dtype_out), (i, j)
+
+
+def test_epilogue_closed_forms(oracle_lib):
+    M, N = 3, 6
+    # K = 0: D = round(beta * Cprev + bias); numpy's float64 -> float16 cast rounds to even
+    A = torch.empty(M, 0, dtype=torch.float16)
+    B = torch.empty(N, 0, dtype=torch.float16)
+    prev = np.arange(M * N, dtype=np.float16).reshape(M, N).view(np.uint16)
+    bias = np.linspace(-1.0, 1.0, N).astype(np.float32)
+    got = oracle_lib.gemm_epilogue(A, B, F16, F16, beta=0.5, cprev=prev, bias=bias)
+    want = (0.5 * prev.view(np.float16).astype(np.float64) + bias.astype(np.float64)).astype(np.float16)
+    assert np.array_equal(got, want.view(np.uint16))
+    # alpha a power of two scales the plain result exactly (no overflow or subnormals here)
+    A, B = si.make_operands(M, N, 64, F16, "uniform", seed=63)
+    plain = oracle_lib.decode(oracle_lib.gemm(A, B, F16, F32), F32)
+    got = oracle_lib.decode(oracle_lib.gemm_epilogue(A, B, F16, F32, alpha=4.0), F32)
+    assert np.array_equal(got, 4.0 * plain)
+    # ReLU: negatives become +0, the rest is untouched
+    got = oracle_lib.gemm_epilogue(A, B, F16, F32, relu=True)
+    want = np.where(plain > 0, plain, 0.0)
+    assert np.array_equal(oracle_lib.decode(got, F32), want)
+    assert np.all(got[plain <= 0] == 0)                        # +0, not -0
+    # the bias is per column: a bias on column 2 only changes column 2
+    bias = np.zeros(N, dtype=np.float32)
+    bias[2] = 1024.0
+    got = oracle_lib.decode(oracle_lib.gemm_epilogue(A, B, F16, F32, bias=bias), F32)
+    assert np.array_equal(got[:, [0, 1, 3, 4, 5]], plain[:, [0, 1, 3, 4, 5]])
+    assert np.all(got[:, 2] != plain[:, 2])
+
+
+def test_epilogue_rejects_beta_without_prev(oracle_lib):
+    A, B = si.make_operands(2, 2, 8, F16, "uniform", seed=64)
+    with pytest.raises(ValueError):
+        oracle_lib.gemm_epilogue(A, B, F16, F16, beta=1.0, cprev=None)
