@@ -15,7 +15,8 @@ STATUS_NAMES = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTE
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgemm.so")
 
 # Every function include/gemm.h declares (checked against the header by the tests).
-EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_host", "gemm_set_config",
+EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_epilogue", "gemm_run_host",
+           "gemm_set_config",
            "gemm_last_config", "gemm_device_status", "gemm_set_wait_limit",
            "gemm_set_test_stall", "gemm_sm_count", "gemm_status_string", "gemm_run_noalloc")
 
@@ -27,6 +28,15 @@ class GemmConfig(ctypes.Structure):
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+ACT_NONE, ACT_RELU = 0, 1
+
+
+class GemmEpilogue(ctypes.Structure):
+    """gemm_epilogue_t: C = act(alpha * A . B^T + beta * C_prev + bias)."""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
+                ("activation", ctypes.c_int32)]
 
 
 class GemmError(RuntimeError):
@@ -61,6 +71,8 @@ def lib():
     L.gemm_sm_count.argtypes = [vp]
     L.gemm_sm_count.restype = i32
     L.gemm_run_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i32, i32, vp]
+    L.gemm_run_epilogue.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32,
+                                    ctypes.POINTER(GemmEpilogue), vp]
     L.gemm_status_string.argtypes = [i32]
     L.gemm_status_string.restype = ctypes.c_char_p
     for name in EXPORTS:
@@ -73,6 +85,11 @@ def lib():
 def _check(code: int, what: str = ""):
     if code != 0:
         raise GemmError(code, what)
+
+
+def torch_float32():
+    import torch
+    return torch.float32
 
 
 def torch_dtype_code(dt) -> int:
@@ -146,6 +163,27 @@ class Gemm:
                             torch_dtype_code(A.dtype), torch_dtype_code(C.dtype),
                             _stream_ptr(stream, A.device))
         _check(code, f"gemm_run M={M} N={N} K={K}")
+        return C
+
+    def run_epilogue(self, A, B, C, alpha=1.0, beta=0.0, bias=None, relu=False, stream=None):
+        """C = act(alpha * A @ B.T + beta * C + bias) in the GEMM's epilogue: bias a CUDA
+        float32 tensor of N values (or None), act ReLU when relu."""
+        M, K = A.shape
+        N = B.shape[0]
+        if bias is not None:
+            if not (bias.is_cuda and bias.dtype == torch_float32() and bias.is_contiguous()
+                    and bias.numel() == N):
+                raise ValueError("bias must be a contiguous float32 CUDA tensor of N values")
+        if not (A.is_cuda and B.is_cuda and C.is_cuda and A.is_contiguous() and B.is_contiguous()
+                and C.is_contiguous() and B.shape[1] == K and tuple(C.shape) == (M, N)
+                and A.dtype == B.dtype):
+            raise ValueError("A (M,K), B (N,K), C (M,N): contiguous CUDA tensors, A and B of one dtype")
+        epi = GemmEpilogue(float(alpha), float(beta), None if bias is None else bias.data_ptr(),
+                           ACT_RELU if relu else ACT_NONE)
+        code = lib().gemm_run_epilogue(self._h, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                                       torch_dtype_code(A.dtype), torch_dtype_code(C.dtype),
+                                       ctypes.byref(epi), _stream_ptr(stream, A.device))
+        _check(code, f"gemm_run_epilogue M={M} N={N} K={K}")
         return C
 
     def run_host(self, A, B, C, dtype_in, dtype_out, stream=None):

@@ -356,10 +356,18 @@ gemm_status_t gemm_set_test_stall(gemm_handle_t h, int32_t enable) {
 
 int32_t gemm_sm_count(gemm_handle_t h) { return h ? h->sms : 0; }
 
-gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M,
+namespace {
+
+gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M,
                        int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
-                       gemm_stream_t stream_) {
+                       const gemm_epilogue_t* epi, gemm_stream_t stream_) {
   if (!h) return GEMM_ERR_INVALID_ARG;
+  const bool fused = epi && (epi->alpha != 1.0f || epi->beta != 0.0f || epi->bias ||
+                             epi->activation != GEMM_ACT_NONE);
+  if (epi && epi->activation != GEMM_ACT_NONE && epi->activation != GEMM_ACT_RELU)
+    return GEMM_ERR_INVALID_ARG;
+  if (fused && epi->bias && reinterpret_cast<uintptr_t>(epi->bias) % 16)
+    return GEMM_ERR_UNSUPPORTED;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   if (!valid_dtype(dtype_in) || !valid_dtype(dtype_out)) return GEMM_ERR_INVALID_ARG;
   if (dtype_in == GEMM_F32) return GEMM_ERR_UNSUPPORTED;
@@ -370,6 +378,7 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   const size_t osz = out_size(dtype_out);
   if (reinterpret_cast<uintptr_t>(C) % osz) return GEMM_ERR_UNSUPPORTED;
   if (K == 0) {  // the empty sum: C = 0 (all-zero bits in every output format)
+    if (fused) return GEMM_ERR_UNSUPPORTED;
     if (cudaMemsetAsync(C, 0, (size_t)M * (size_t)N * osz, stream) != cudaSuccess)
       return GEMM_ERR_CUDA;
     return GEMM_OK;
@@ -391,6 +400,7 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
   s.out = out;
   s.grid = ch.grid;
   s.one_chain = ch.one_chain;
+  s.fused = fused;
   s.stream = stream;
   const bool c_tma = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0;
   if (!make_map(h, A, M, K, dtype_in, kBlockM, &s.tmA) ||
@@ -402,6 +412,11 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
 
   GemmParams& p = s.p;
   p.C = C;
+  p.fused = fused ? 1 : 0;
+  p.relu = fused && epi->activation == GEMM_ACT_RELU ? 1 : 0;
+  p.alpha = fused ? epi->alpha : 1.0f;
+  p.beta = fused ? epi->beta : 0.0f;
+  p.bias = fused ? epi->bias : nullptr;
   p.M = (int32_t)M;
   p.N = (int32_t)N;
   p.K = (int32_t)K;
@@ -440,6 +455,21 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
                           ch.group_m,  ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles,
                           ch.prefetch_kb ? ch.prefetch_kb : -1, ch.one_chain ? 2 : 1};
   return GEMM_OK;
+}
+
+}  // namespace
+
+gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M,
+                       int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                       gemm_stream_t stream) {
+  return run_impl(h, A, B, C, M, N, K, dtype_in, dtype_out, nullptr, stream);
+}
+
+gemm_status_t gemm_run_epilogue(gemm_handle_t h, const void* A, const void* B, void* C,
+                                int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in,
+                                gemm_dtype_t dtype_out, const gemm_epilogue_t* epilogue,
+                                gemm_stream_t stream) {
+  return run_impl(h, A, B, C, M, N, K, dtype_in, dtype_out, epilogue, stream);
 }
 
 gemm_status_t gemm_device_status(gemm_handle_t h, gemm_stream_t stream_, uint32_t* detail) {

@@ -248,6 +248,79 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
+// Fused epilogue on 32 consecutive values of row m starting at column n0, before they
+// are rounded to the output type: v = act(alpha * v + beta * C[m][n] + bias[n])
+// ("CUTLASS Deep Dive: From CuTe Layouts to Blackwell tcgen05", Part 6: Epilogue
+// Visitor Trees, D = alpha * acc + beta * C; Classic Fused Epilogue: Bias + ReLU).
+// C is read in its own type before this warp writes it; out-of-range columns (and rows)
+// read as zero and are not stored.
+template <int OUT>
+__device__ __forceinline__ void fuse_piece(const GemmParams& p, int32_t m, int32_t n0, float* v) {
+  const bool row_ok = m < p.M;
+  const bool vec = p.vec_store && n0 + 32 <= p.N;  // C rows and this piece 16-byte aligned
+#pragma unroll
+  for (int j0 = 0; j0 < 32; j0 += 8) {
+    float c[8], b[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) c[t] = 0.0f;
+    if (p.beta != 0.0f && row_ok) {
+      if constexpr (OUT == kOutF32) {
+        const float* src = reinterpret_cast<const float*>(p.C) + (size_t)m * p.N + n0 + j0;
+        if (vec) {
+          const uint4 x = ld_global_cg_v4(src), y = ld_global_cg_v4(src + 4);
+          c[0] = __uint_as_float(x.x); c[1] = __uint_as_float(x.y);
+          c[2] = __uint_as_float(x.z); c[3] = __uint_as_float(x.w);
+          c[4] = __uint_as_float(y.x); c[5] = __uint_as_float(y.y);
+          c[6] = __uint_as_float(y.z); c[7] = __uint_as_float(y.w);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            if (n0 + j0 + t < p.N) c[t] = src[t];
+        }
+      } else {
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(p.C) + (size_t)m * p.N + n0 + j0;
+        uint16_t h[8];
+        if (vec) {
+          const uint4 x = ld_global_cg_v4(src);
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int t = 0; t < 8; ++t) h[t] = (uint16_t)(w[t >> 1] >> ((t & 1) * 16));
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) h[t] = n0 + j0 + t < p.N ? src[t] : (uint16_t)0;
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          if constexpr (OUT == kOutF16) c[t] = __half2float(__ushort_as_half(h[t]));
+          else c[t] = __bfloat162float(__ushort_as_bfloat16(h[t]));
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) b[t] = 0.0f;
+    if (p.bias) {
+      const float* src = p.bias + n0 + j0;
+      if (n0 + j0 + 8 <= p.N) {
+        const uint4 x = ld_global_cg_v4(src), y = ld_global_cg_v4(src + 4);
+        b[0] = __uint_as_float(x.x); b[1] = __uint_as_float(x.y);
+        b[2] = __uint_as_float(x.z); b[3] = __uint_as_float(x.w);
+        b[4] = __uint_as_float(y.x); b[5] = __uint_as_float(y.y);
+        b[6] = __uint_as_float(y.z); b[7] = __uint_as_float(y.w);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          if (n0 + j0 + t < p.N) b[t] = src[t];
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      float x = fmaf(p.beta, c[t], p.alpha * v[j0 + t]) + b[t];
+      if (p.relu) x = x > 0.0f ? x : 0.0f;  // NaN and -0 become +0, as max(x, 0) reads
+      v[j0 + t] = x;
+    }
+  }
+}
+
 // Direct stores of 32 consecutive values of one row (used when C cannot take TMA).
 template <int OUT>
 __device__ __forceinline__ void store_row_direct(const GemmParams& p, int32_t m, int32_t n0,
@@ -361,7 +434,9 @@ struct Layout {
 // k-blocks), so the epilogue streams the accumulator out of TMEM in 32-column pieces
 // instead of first copying the warp's whole 32 x BN/2 block into registers; the
 // registers this frees go to loads in flight in the split-K hand-over.
-template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN>
+// FUSED: the fused epilogue (alpha, beta * C, bias, ReLU) is compiled in; kept out of
+// the plain kernels, whose general epilogue it would push into more register spills.
+template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN, bool FUSED>
 __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
@@ -630,6 +705,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
                 float v[32];
                 const int pc = bx * kPiecesPerBox + pp;
                 one_chain_piece(taddr + 32u * pc, w, ws_lane, kSliceStride, 32 * pc, v);
+                if constexpr (FUSED) fuse_piece<OUT>(p, m0 + (int32_t)row, n_half + 32 * pc, v);
                 // 16-byte chunks of the 128-byte row, in the 128-byte swizzled order
                 constexpr int kChunks = 8 / kPiecesPerBox;
 #pragma unroll
@@ -660,6 +736,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
             for (int pc = 0; pc < kPieces; ++pc) {
               float v[32];
               one_chain_piece(taddr + 32u * pc, w, ws_lane, kSliceStride, 32 * pc, v);
+                if constexpr (FUSED) fuse_piece<OUT>(p, m0 + (int32_t)row, n_half + 32 * pc, v);
               store_row_direct<OUT>(p, m, n_half + 32 * pc, v);
             }
           }
@@ -794,6 +871,11 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         }
       }
 
+      if constexpr (FUSED) {
+        const int32_t m = m0 + (int32_t)row;
+#pragma unroll
+        for (int pc = 0; pc < kPieces; ++pc) fuse_piece<OUT>(p, m, n_half + 32 * pc, acc + 32 * pc);
+      }
       if (p.tma_store) {
         // Each 128-byte row of a staging box is written in the 128-byte swizzled order
         // (16-byte chunk j of row r at chunk j ^ (r % 8)) that the C tensor map's

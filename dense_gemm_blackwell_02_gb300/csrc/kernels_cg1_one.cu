@@ -6,8 +6,8 @@
 namespace gb300 {
 
 cudaError_t launch_cg1_one(const LaunchSpec& s) {
-  if (s.bn == 256 && s.stages == 4) return by_out<1, 256, 4, true>(s);
-  if (s.bn == 128 && s.stages == 6) return by_out<1, 128, 6, true>(s);
+  if (s.bn == 256 && s.stages == 4) return by_out<1, 256, 4, true, false>(s);
+  if (s.bn == 128 && s.stages == 6) return by_out<1, 128, 6, true, false>(s);
   return cudaErrorInvalidValue;
 }
 

@@ -5,8 +5,8 @@
 namespace gb300 {
 
 cudaError_t launch_cg2(const LaunchSpec& s) {
-  if (s.bn == 256 && s.stages == 6) return by_out<2, 256, 6, false>(s);
-  if (s.bn == 128 && s.stages == 8) return by_out<2, 128, 8, false>(s);
+  if (s.bn == 256 && s.stages == 6) return by_out<2, 256, 6, false, false>(s);
+  if (s.bn == 128 && s.stages == 8) return by_out<2, 128, 8, false, false>(s);
   return cudaErrorInvalidValue;
 }
 

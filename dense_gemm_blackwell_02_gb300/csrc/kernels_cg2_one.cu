@@ -6,8 +6,8 @@
 namespace gb300 {
 
 cudaError_t launch_cg2_one(const LaunchSpec& s) {
-  if (s.bn == 256 && s.stages == 6) return by_out<2, 256, 6, true>(s);
-  if (s.bn == 128 && s.stages == 8) return by_out<2, 128, 8, true>(s);
+  if (s.bn == 256 && s.stages == 6) return by_out<2, 256, 6, true, false>(s);
+  if (s.bn == 128 && s.stages == 8) return by_out<2, 128, 8, true, false>(s);
   return cudaErrorInvalidValue;
 }
 

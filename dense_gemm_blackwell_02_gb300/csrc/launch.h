@@ -15,6 +15,7 @@ struct LaunchSpec {
   int out;         // OutKind
   int grid;        // CTAs (a multiple of cta_group)
   bool one_chain;  // every unit is one accumulation chain (streaming epilogue)
+  bool fused;      // the fused epilogue (p.fused) is compiled in
   CUtensorMap tmA; // A: box {64, 128}
   CUtensorMap tmB; // B: box {64, bn / cta_group}
   CUtensorMap tmB2; // B: box {64, bn / cta_group / 2} (half-tile units; else a copy of tmB)
@@ -38,6 +39,11 @@ cudaError_t launch_cg1(const LaunchSpec& s);
 cudaError_t launch_cg2(const LaunchSpec& s);
 cudaError_t launch_cg1_one(const LaunchSpec& s);
 cudaError_t launch_cg2_one(const LaunchSpec& s);
+// ... and with the fused epilogue (kernels_cg*_fused.cu)
+cudaError_t launch_cg1_fused(const LaunchSpec& s);
+cudaError_t launch_cg2_fused(const LaunchSpec& s);
+cudaError_t launch_cg1_one_fused(const LaunchSpec& s);
+cudaError_t launch_cg2_one_fused(const LaunchSpec& s);
 int resident_cg1(int bn, int stages, int out);
 int resident_cg2(int bn, int stages, int out);
 

@@ -5,9 +5,9 @@
 
 namespace gb300 {
 
-template <int CG, int BN, int STAGES, int OUT, bool ONE>
+template <int CG, int BN, int STAGES, int OUT, bool ONE, bool FUSED>
 cudaError_t launch_one(const LaunchSpec& s) {
-  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE>;
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED>;
   using L = Layout<CG, BN, STAGES>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes);
@@ -43,7 +43,7 @@ cudaError_t launch_one(const LaunchSpec& s) {
 
 template <int CG, int BN, int STAGES, int OUT>
 int resident_one() {
-  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, false>;
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, false, false>;
   using L = Layout<CG, BN, STAGES>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            L::kDynamicBytes) != cudaSuccess)
@@ -67,12 +67,12 @@ int resident_one() {
   return n;
 }
 
-template <int CG, int BN, int STAGES, bool ONE>
+template <int CG, int BN, int STAGES, bool ONE, bool FUSED>
 cudaError_t by_out(const LaunchSpec& s) {
   switch (s.out) {
-    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE>(s);
-    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE>(s);
-    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE>(s);
+    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED>(s);
+    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED>(s);
+    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED>(s);
     default: return cudaErrorInvalidValue;
   }
 }

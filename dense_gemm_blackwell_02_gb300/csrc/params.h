@@ -54,6 +54,11 @@ struct GemmParams {
   float* workspace;        // splits > 1: fp32 partial tiles
   uint32_t* counters;      // splits > 1: per (tile, CTA of the pair, quarter, half) counters
   uint32_t* status;        // device status word
+  // fused epilogue, fused = 0: C = A . B^T; else C = act(alpha * A . B^T + beta * C + bias)
+  int32_t fused;
+  int32_t relu;            // act: ReLU when 1, the identity when 0
+  float alpha, beta;
+  const float* bias;       // N values (16-byte aligned), or nullptr
   uint64_t wait_limit_ns;  // bound on every mbarrier wait
   int32_t test_stall;      // 1: the MMA issuer waits on a barrier that never completes
 };

@@ -122,6 +122,39 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
                        gemm_stream_t stream);
 
 /*
+ * Fused epilogue ("CUTLASS Deep Dive: From CuTe Layouts to Blackwell tcgen05",
+ * Part 6: Epilogue Visitor Trees, D = alpha * acc + beta * C; Classic Fused
+ * Epilogue: Bias + ReLU).  Applied to the fp32 accumulator before the single
+ * rounding to dtype_out:
+ *     C[i][j] = act( alpha * sum_k A[i][k] B[j][k] + beta * C_prev[i][j] + bias[j] )
+ *   alpha, beta  binary32 scales (alpha = 1, beta = 0: the plain product)
+ *   C_prev       the contents of C before the call (read in dtype_out, only when
+ *                beta != 0; C is then read and overwritten in place)
+ *   bias         N binary32 values, one per column of C, 16-byte aligned; or NULL
+ *   activation   GEMM_ACT_NONE (identity) or GEMM_ACT_RELU (max(x, 0); NaN and -0
+ *                give +0)
+ * The caller owns bias.  Split-K and stream-K tiles apply it once, to the reduced
+ * sum.
+ */
+typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1 } gemm_activation_t;
+typedef struct {
+  float alpha;
+  float beta;
+  const float* bias;
+  int32_t activation;
+} gemm_epilogue_t;
+
+/* gemm_run with a fused epilogue.  epilogue == NULL (or alpha 1, beta 0, no bias,
+ * no activation) is exactly gemm_run.  Errors as gemm_run, and:
+ *   GEMM_ERR_INVALID_ARG   an activation other than the two above;
+ *   GEMM_ERR_UNSUPPORTED   bias not 16-byte aligned, or K == 0 with a non-trivial
+ *                          epilogue. */
+gemm_status_t gemm_run_epilogue(gemm_handle_t h, const void* A, const void* B, void* C,
+                                int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in,
+                                gemm_dtype_t dtype_out, const gemm_epilogue_t* epilogue,
+                                gemm_stream_t stream);
+
+/*
  * The same product with HOST buffers: copies A and B to device staging buffers
  * owned by the handle, runs the GEMM and copies C back, all on `stream`, then
  * synchronises `stream` and reports kernel timeouts like gemm_device_status.
