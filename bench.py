@@ -224,14 +224,14 @@ def time_steps(run, sets, stream, steps, flush=None, per_step=False):
     return (sum(each), each) if per_step else sum(each)
 
 
-def measure_decode(g, dev, stream, peaks, iters=20):
-    """Secondary figures: the M = 256 decode shapes (fp16 -> fp16), HBM-bound.  Each is
-    timed over `iters` launches back to back, cycling through operand copies at least
-    four times the L2 (cold operands in every launch, as when a model's layers stream
-    their weights).  Their parity is covered by the full-size tests; here only time is
-    taken."""
+def measure_decode(g, dev, stream, peaks, iters=20, name="decode_m256"):
+    """Secondary figures: the decode shapes (fp16 -> fp16, M = 256 or M = 1..128),
+    HBM-bound.  Each is timed over `iters` launches back to back, cycling through
+    operand copies at least four times the L2 (cold operands in every launch, as when a
+    model's layers stream their weights).  Their parity is covered by the full-size
+    tests; here only time is taken."""
     flush = None
-    wl = si.WORKLOADS["decode_m256"]
+    wl = si.WORKLOADS[name]
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     out = {}
     gen = torch.Generator(device=dev)
@@ -381,6 +381,8 @@ def run_ours(args):
     other_ms = time_steps(run, other_sets, stream, other_steps, other_flush) / other_steps
     del other_sets, other_flush
     decode = measure_decode(g, dev, stream, peaks) if args.decode else None
+    decode_small = (measure_decode(g, dev, stream, peaks, name="decode_small_m")
+                    if args.decode > 1 else None)
     flops = rl.gemm_flops(M, N, K)
     ms_per_step = total_ms / args.steps
     value = replica_throughput(ws, flops, args.steps, total_ms)
@@ -451,6 +453,8 @@ def run_ours(args):
         }
         if decode is not None:
             line["decode"] = decode
+        if decode_small is not None:
+            line["decode_small_m"] = decode_small
         print(json.dumps(line))
     g.close()
     if ws > 1:
@@ -467,8 +471,9 @@ def main():
     ap.add_argument("--workload", default="square_4096", choices=sorted(si.WORKLOADS))
     ap.add_argument("--config", default=None, help="JSON gemm_config_t override (sweeps)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--decode", type=int, default=1,
-                    help="also time the M=256 decode shapes (HBM GB/s) into the line")
+    ap.add_argument("--decode", type=int, default=2,
+                    help="also time the M=256 decode shapes (HBM GB/s) into the line; "
+                         "2 adds the M=1..128 decode shapes")
     ap.add_argument("--l2", default="flush", choices=["rotate", "flush"],
                     help="main workload: flush L2 before each separately timed step (default), "
                          "or cycle operand copies larger than L2 with launches back to back")

@@ -155,15 +155,23 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
   // (measured, 256 x 8192 x 8192: 38.3 us against 40.5 us for two K slices, whose
   // hand-over of fp32 partials costs several microseconds at the end).  For longer K the
   // hand-over is amortised and split-K wins (256 x 8192 x 28672: 98 against 110 us).
+  // With one CTA per 128-row tile (M <= 128), 128-column tiles are taken whenever they
+  // need fewer K slices than 256-column ones, for any K (measured, M = 8..128,
+  // N = 8192: K 8192, 32 against 38 us; K 28672, 84 against 91 us).
   if (!f.block_n && !f.splits && !f.stages && c->bn == 256 && c->tiles * 2 <= slots &&
-      c->k_blocks <= 128) {
+      (c->k_blocks <= 128 || cg == 1)) {
     const int64_t tiles128 = c->num_m * ceil_div(N, (int64_t)128);
     const int64_t slots128 = [&] {
       int64_t n = resident_units(h, cg, 128, default_stages(cg, 128), out);
       if (f.max_ctas) n = std::min<int64_t>(n, std::max<int64_t>(f.max_ctas / cg, 1));
       return n;
     }();
-    if (tiles128 <= slots128 && tiles128 * 2 > slots128) {
+    const auto slices = [&](int64_t tiles, int64_t sl) {
+      return tiles * 2 <= sl ? std::min<int64_t>({sl / tiles, c->k_blocks / 4, 32}) : 1;
+    };
+    const bool fewer = cg == 1 ? slices(tiles128, slots128) < slices(c->tiles, slots)
+                               : tiles128 * 2 > slots128;
+    if (tiles128 <= slots128 && fewer) {
       c->bn = 128;
       c->stages = default_stages(cg, 128);
       c->num_n = ceil_div(N, (int64_t)128);
@@ -403,7 +411,12 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   s.fused = fused;
   s.stream = stream;
   const bool c_tma = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0;
-  if (!make_map(h, A, M, K, dtype_in, kBlockM, &s.tmA) ||
+  // A single one-CTA row tile of M < 128 rows loads A as an M-row box: the stage's
+  // rows M..127 are never written and only feed accumulator rows that are never
+  // stored.  (A 128-row box over fewer than 8 rows of A ran up to 1.5x slower on the
+  // decode shapes than over 8 or more, measured.)
+  const int a_box = (ch.variant == 1 && M < kBlockM) ? (int)M : kBlockM;
+  if (!make_map(h, A, M, K, dtype_in, a_box, &s.tmA) ||
       !make_map(h, B, N, K, dtype_in, ch.bn / ch.variant, &s.tmB) ||
       (ch.half_tail && !make_map(h, B, N, K, dtype_in, ch.bn / ch.variant / 2, &s.tmB2)) ||
       (c_tma && !make_map(h, C, M, N, dtype_out, 32, &s.tmC)))
@@ -434,6 +447,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.group_m = ch.group_m;
   p.chain_kb = ch.chain_kb;
   p.prefetch_kb = ch.prefetch_kb;
+  p.a_tx_short = (uint32_t)(kBlockM - a_box) * 128u;
   p.vec_store = c_tma ? 1 : 0;
   p.tma_store = c_tma ? 1 : 0;
   p.idesc = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn, dtype_in == GEMM_BF16);

@@ -528,7 +528,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
                             (half ? w.half * (BN / 2) + (int32_t)rank * (L::kRowsB / 2)
                                   : (int32_t)rank * L::kRowsB);
       const CUtensorMap* mapB = half ? &tmB2 : &tmB;
-      const uint32_t tx = half ? L::kTxBytesHalf : L::kTxBytes;
+      const uint32_t tx = (half ? L::kTxBytesHalf : L::kTxBytes) - p.a_tx_short;
       // Streaming B from DRAM (decode shapes): keep more requests in flight than the
       // shared-memory ring holds by prefetching B into L2 prefetch_kb k-blocks ahead
       // ("A Blackwell GEMM by Hand in CuTe DSL", section 8: TMA prefetch).
@@ -645,8 +645,10 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       constexpr size_t kSliceStride = kBlocksPerSlice * kBlockFloats;
       const size_t my_block = ((size_t)rank * 4 + q) * 2 + h;
       while (ok && walker_next(walk, first_unit, unit_stride, p, w)) {
-        // in a half-tile unit the h = 1 warps only take part in the slot hand-over
-        const bool active = w.half < 0 || h == 0;
+        // in a half-tile unit the h = 1 warps only take part in the slot hand-over, and
+        // so do warps whose 32 rows all lie at or past M (no partial, no store)
+        const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
+        const bool active = (w.half < 0 || h == 0) && m0 + (int32_t)(q * 32u) < p.M;
         const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
         uint32_t good = 1;
         if (lane == 0)
@@ -658,7 +660,6 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * BN + h * kHalf;
-        const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
         const int32_t n_half = w.n_blk * BN + (w.half >= 0 ? w.half : (int32_t)h) * kHalf;
         bool emit = active;
         const float* ws_lane = nullptr;

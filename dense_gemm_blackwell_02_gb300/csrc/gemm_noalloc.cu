@@ -181,7 +181,9 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   s.grid = (int)(units < ds.sms ? units : ds.sms);
   s.stream = stream;
   const bool c_tma = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0;
-  if (!encode_map(A, M, K, dtype_in, kBlockM, &s.tmA) ||
+  // one row tile of M < 128 rows: A's box is M rows (see gemm_run)
+  const int a_box = M < kBlockM ? (int)M : kBlockM;
+  if (!encode_map(A, M, K, dtype_in, a_box, &s.tmA) ||
       !encode_map(B, N, K, dtype_in, kBN, &s.tmB) ||
       (c_tma && !encode_map(C, M, N, dtype_out, 32, &s.tmC)))
     return GEMM_ERR_CUDA;
@@ -215,6 +217,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   p.group_m = 16;
   p.chain_kb = kChainKBlocks;
   p.prefetch_kb = 0;
+  p.a_tx_short = (uint32_t)(kBlockM - a_box) * 128u;
   p.vec_store = c_tma ? 1 : 0;
   p.tma_store = c_tma ? 1 : 0;
   p.idesc = idesc_f16_kmajor(kBlockM, kBN, dtype_in == GEMM_BF16);

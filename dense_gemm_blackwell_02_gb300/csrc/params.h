@@ -47,6 +47,8 @@ struct GemmParams {
   int32_t group_m;         // grouped rasterisation: M-tiles per group
   int32_t chain_kb;        // k-blocks per TMEM accumulation chain
   int32_t prefetch_kb;     // L2 prefetch of B this many k-blocks ahead of the ring (0: off)
+  uint32_t a_tx_short;     // bytes of A's 128-row box that A's tensor map does not load:
+                           // (128 - M) * 128 when a one-CTA tile's A box is M < 128 rows
   int32_t vec_store;       // 1 when 16-byte vector stores of C are aligned
   int32_t tma_store;       // 1 when C is written through the C tensor map
   uint32_t idesc;          // tcgen05 instruction descriptor (N = BN)

@@ -318,3 +318,34 @@ def test_single_chain_epilogue_needs_single_chain_units(g):
     finally:
         g.reset_config()
     parity.oracle_check(parity.bits_of(C), A, B, F16, F32, what="two chains, general epilogue")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 7, 8, 31, 33, 100])
+@pytest.mark.parametrize("cfg,N,K", [
+    ({}, 1000, 2048),                                                   # auto: K slices
+    ({"variant": 1, "block_n": 256, "splits": 3}, 700, 1024),           # general epilogue, split
+    ({"variant": 1, "block_n": 128, "splits": 2, "epilogue": 2}, 520, 4096),  # single chain, split
+    ({"variant": 1, "block_n": 256, "max_ctas": 5}, 3000, 640),         # half-tile tail
+    ({"variant": 1, "block_n": 128, "splits": -1, "max_ctas": 38}, 900, 1504),  # stream-K
+])
+def test_one_row_tile_of_few_rows(g, M, cfg, N, K):
+    # M < 128 in one-CTA tiles: A is loaded as an M-row box (the stage's other rows are
+    # never written) and epilogue warps whose 32 rows lie past M skip their partials
+    if cfg:
+        g.set_config(**cfg)
+    try:
+        _case(g, M, N, K, F16, F16, seed=90 + M)
+        _case(g, M, N, K, BF16, F32, seed=91 + M, exact=True, ints=True)
+        assert g.last_config()["variant"] == 1
+    finally:
+        g.reset_config()
+
+
+@pytest.mark.parametrize("M", [1, 8, 64, 128])
+def test_small_m_decode_takes_narrow_tiles(g, M):
+    # M <= 128, N = 8192: 64 tiles of 128 columns in two K slices beat 32 tiles of 256
+    # columns in four (fewer slices to reduce)
+    _case(g, M, 8192, 1024, F16, F16, seed=95)
+    cfg = g.last_config()
+    assert cfg["variant"] == 1 and cfg["block_n"] == 128, cfg
+    assert cfg["splits"] == min(g.sm_count // 64, 1024 // 64 // 4), cfg
