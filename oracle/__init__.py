@@ -19,6 +19,10 @@ with A (M x K) and B (N x K) K-major, k summed in increasing order in
 binary64, and round_out a single round-to-nearest-even step from binary64 to
 the output format.
 
+FP8 operands (codes E4M3 = 3, E5M2 = 4; OCP 8-bit formats) and the blockwise-scaled
+product ("CUTLASS Deep Dive: From CuTe Layouts to Blackwell tcgen05", Part 6, FP8 and
+Blockwise Scaling) are described at the top of oracle.c.
+
 Pins (tests/test_oracle_pins.py): exact rational brute force on tiny shapes,
 all-ones (C = K), identity B (C = A), small-integer operands (exact integer
 products), rank-1 operands (C = u v^T (a.b)), and the converters against
@@ -33,7 +37,8 @@ import subprocess
 
 import numpy as np
 
-F16, BF16, F32 = 0, 1, 2
+F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
+FP8 = (E4M3, E5M2)
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
@@ -70,6 +75,10 @@ def load_library(path: str):
     lib.oracle_decode.restype = i32
     lib.oracle_round.argtypes = [vp, vp, i64, i32]
     lib.oracle_round.restype = i32
+    if hasattr(lib, "oracle_gemm_blockwise"):
+        lib.oracle_gemm_blockwise.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, i64,
+                                              vp, i64, vp, i64, i32, i32, i32]
+        lib.oracle_gemm_blockwise.restype = i32
     if hasattr(lib, "oracle_gemm_epilogue"):
         lib.oracle_gemm_epilogue.argtypes = [vp, vp, vp, vp, ctypes.c_double, ctypes.c_double,
                                              i32, vp, i64, i64, i64, i32, i32, i32]
@@ -86,16 +95,22 @@ def _load(lib=None):
     return _lib
 
 
-def _bits16(x) -> np.ndarray:
-    """Accept a numpy uint16/float16 array or a CPU torch fp16/bf16 tensor and
-    return a C-contiguous uint16 view of its bit patterns."""
+def _bits16(x, dtype_in: int = F16) -> np.ndarray:
+    """Accept a numpy array of bit patterns or a CPU torch tensor (fp16/bf16, or
+    fp8 for the E4M3/E5M2 codes) and return a C-contiguous view of its bit
+    patterns: uint16, or uint8 for fp8."""
+    width = 1 if dtype_in in FP8 else 2
     if hasattr(x, "detach"):  # torch tensor (CPU); reinterpret without copying values
         import torch
-        x = x.detach().contiguous().view(torch.int16).numpy()
+        if x.element_size() != width:
+            raise TypeError(f"oracle operands for dtype {dtype_in} must be {8 * width}-bit, "
+                            f"got {x.dtype}")
+        x = x.detach().contiguous().view(torch.uint8 if width == 1 else torch.int16).numpy()
     a = np.ascontiguousarray(x)
-    if a.dtype.itemsize != 2:
-        raise TypeError(f"oracle operands must be 16-bit patterns, got {a.dtype}")
-    return a.view(np.uint16)
+    if a.dtype.itemsize != width:
+        raise TypeError(f"oracle operands for dtype {dtype_in} must be {8 * width}-bit "
+                        f"patterns, got {a.dtype}")
+    return a.view(np.uint8 if width == 1 else np.uint16)
 
 
 def _out_array(shape, dtype_out):
@@ -110,7 +125,7 @@ def _check(rc):
 
 def gemm(A, B, dtype_in: int, dtype_out: int, nthreads: int = 0, lib=None) -> np.ndarray:
     """Full C = A . B^T as output-format bit patterns (uint16 or uint32), M x N."""
-    a, b = _bits16(A), _bits16(B)
+    a, b = _bits16(A, dtype_in), _bits16(B, dtype_in)
     M, K = a.shape
     N, K2 = b.shape
     if K != K2:
@@ -126,7 +141,7 @@ def gemm_select(A, B, rows, cols, dtype_in: int, dtype_out: int, nthreads: int =
     """Outputs C[rows][:, cols] (len(rows) x len(cols)); rows/cols None = all.
 
     Returns the rounded bit patterns, or (bits, binary64 sums) if want_f64."""
-    a, b = _bits16(A), _bits16(B)
+    a, b = _bits16(A, dtype_in), _bits16(B, dtype_in)
     M, K = a.shape
     N, K2 = b.shape
     if K != K2:
@@ -154,7 +169,7 @@ def gemm_epilogue(A, B, dtype_in: int, dtype_out: int, alpha=1.0, beta=0.0, cpre
     """D = act(alpha * A . B^T + beta * cprev + bias[j]) as output-format bit patterns
     (M x N): cprev is M x N output-format bit patterns (needed when beta != 0), bias N
     binary32 values, act ReLU when relu.  Evaluated in binary64, rounded once."""
-    a, b = _bits16(A), _bits16(B)
+    a, b = _bits16(A, dtype_in), _bits16(B, dtype_in)
     M, K = a.shape
     N, K2 = b.shape
     if K != K2:
@@ -174,9 +189,45 @@ def gemm_epilogue(A, B, dtype_in: int, dtype_out: int, alpha=1.0, beta=0.0, cpre
     return D
 
 
+def gemm_blockwise(A, B, sfa, sfb, bm: int, bn: int, bk: int, dtype_in: int, dtype_out: int,
+                   rows=None, cols=None, nthreads: int = 0, want_f64: bool = False, lib=None):
+    """Outputs C[rows][:, cols] of the blockwise-scaled product
+        C[i, j] = sum_kb sfa[i // bm, kb] * sfb[j // bn, kb] * sum_{k in block kb} A[i, k] B[j, k]
+    (blocks of bk along K), as output-format bit patterns; sfa is ceil(M/bm) x
+    ceil(K/bk) and sfb ceil(N/bn) x ceil(K/bk) binary32 scales.  rows/cols None = all.
+    Returns the bits, or (bits, binary64 values) if want_f64."""
+    a, b = _bits16(A, dtype_in), _bits16(B, dtype_in)
+    M, K = a.shape
+    N, K2 = b.shape
+    if K != K2:
+        raise ValueError("A and B disagree on K")
+    nkb = -(-K // bk) if bk > 0 else 0
+    fa = np.ascontiguousarray(np.asarray(sfa, dtype=np.float32))
+    fb = np.ascontiguousarray(np.asarray(sfb, dtype=np.float32))
+    if fa.shape != (-(-M // bm), nkb) or fb.shape != (-(-N // bn), nkb):
+        raise ValueError(f"scale shapes {fa.shape}, {fb.shape} do not match the blocks")
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nr = M if r is None else len(r)
+    nc = N if c is None else len(c)
+    if r is not None and len(r) and (r.min() < 0 or r.max() >= M):
+        raise IndexError("row index out of range")
+    if c is not None and len(c) and (c.min() < 0 or c.max() >= N):
+        raise IndexError("column index out of range")
+    out = _out_array((nr, nc), dtype_out)
+    f64 = np.empty((nr, nc), dtype=np.float64) if want_f64 else None
+    _check(_load(lib).oracle_gemm_blockwise(
+        a.ctypes.data, b.ctypes.data, fa.ctypes.data, fb.ctypes.data, bm, bn, bk,
+        out.ctypes.data, None if f64 is None else f64.ctypes.data, M, K,
+        None if r is None else r.ctypes.data, nr, None if c is None else c.ctypes.data, nc,
+        dtype_in, dtype_out, nthreads))
+    return (out, f64) if want_f64 else out
+
+
 def decode(bits: np.ndarray, dtype: int, lib=None) -> np.ndarray:
-    """Exact binary64 values of fp16/bf16 (uint16) or fp32 (uint32) patterns."""
-    want = np.uint32 if dtype == F32 else np.uint16
+    """Exact binary64 values of fp16/bf16 (uint16), fp32 (uint32) or fp8 E4M3/E5M2
+    (uint8) patterns."""
+    want = np.uint32 if dtype == F32 else np.uint8 if dtype in FP8 else np.uint16
     b = np.ascontiguousarray(bits).view(want)
     out = np.empty(b.shape, dtype=np.float64)
     _check(_load(lib).oracle_decode(b.ctypes.data, out.ctypes.data, b.size, dtype))

@@ -33,8 +33,30 @@
  *   alpha, beta and bias are taken exactly, the expression is evaluated in
  *   binary64 and rounded once to dtype_out.
  *
+ * FP8 inputs ("CUTLASS Deep Dive: From CuTe Layouts to Blackwell tcgen05",
+ * Part 6, FP8 and Blockwise Scaling: E4M3 input): A and B may instead hold
+ * 8-bit E4M3 or E5M2 patterns, one byte per element.  The pages name E4M3 but do
+ * not define it; the definitions taken are the OCP 8-bit floating point ones:
+ *   E4M3: 1 sign, 4 exponent bits (bias 7), 3 fraction bits; no infinities;
+ *         exponent 1111 is a normal binade except fraction 111, which is NaN
+ *         (largest finite 448); exponent 0000 is subnormal, frac * 2^-9.
+ *   E5M2: 1 sign, 5 exponent bits (bias 15), 2 fraction bits, IEEE-style
+ *         (exponent 11111: infinity or NaN; largest finite 57344).
+ * Products of two such values are exact in binary64, as above.
+ *
+ * Blockwise scaling (oracle_gemm_blockwise; same page and section: one scale
+ * per (block_m, block_k) tile of A and one per (block_n, block_k) tile of B,
+ * applied during accumulation):
+ *       C[i][j] = round_out( sum_kb  sfa[i / bm][kb] * sfb[j / bn][kb] * P_kb[i][j] )
+ *       P_kb[i][j] = sum_{k = kb*bk}^{min(K, (kb+1)*bk) - 1} A[i][k] * B[j][k]
+ *   with sfa (ceil(M/bm) x ceil(K/bk)) and sfb (ceil(N/bn) x ceil(K/bk))
+ *   row-major binary32 scales.  Each block's partial sum runs over k in
+ *   increasing order in binary64; the scale product (exact in binary64) then
+ *   multiplies it, and the blocks are summed in increasing kb.
+ *
  * The format decoders and the rounding routine below are written from the
- * IEEE 754 / bfloat16 format definitions (sign, biased exponent, fraction).
+ * IEEE 754 / bfloat16 / OCP FP8 format definitions (sign, biased exponent,
+ * fraction).
  *
  * Build: gcc -O2 -ffp-contract=off -fPIC -shared -pthread oracle.c -o liboracle.so
  * (-ffp-contract=off keeps "sum += a*b" as a multiply then an add on every
@@ -47,7 +69,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_F32 = 2 };
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_F32 = 2, ORACLE_E4M3 = 3, ORACLE_E5M2 = 4 };
 
 /* ---------------------------------------------------------------------- */
 /* Format parameters: fraction bits, minimum normal exponent, maximum       */
@@ -64,6 +86,7 @@ typedef struct {
 static const fmt_t FMT_F16 = {10, -14, 15, 15, 5};
 static const fmt_t FMT_BF16 = {7, -126, 127, 127, 8};
 static const fmt_t FMT_F32 = {23, -126, 127, 127, 8};
+static const fmt_t FMT_E5M2 = {2, -14, 15, 15, 5};
 
 static const fmt_t* fmt_of(int dtype) {
   switch (dtype) {
@@ -90,6 +113,20 @@ static double decode_bits(uint32_t bits, const fmt_t* f) {
     /* normal: (2^frac_bits + frac) * 2^(e - bias - frac_bits) */
     v = ldexp((double)((1u << f->frac_bits) + frac), (int)e - f->bias - f->frac_bits);
   }
+  return sign ? -v : v;
+}
+
+/* E4M3 (OCP): like an IEEE format of 4 exponent bits (bias 7) and 3 fraction
+ * bits, except that the all-ones exponent holds normal numbers and only the
+ * all-ones exponent with the all-ones fraction is NaN (there is no infinity). */
+static double decode_e4m3(uint32_t bits) {
+  const uint32_t sign = (bits >> 7) & 1u;
+  const uint32_t e = (bits >> 3) & 15u;
+  const uint32_t frac = bits & 7u;
+  double v;
+  if (e == 15u && frac == 7u) return NAN;
+  if (e == 0) v = ldexp((double)frac, 1 - 7 - 3);  /* subnormal: frac * 2^-9 */
+  else v = ldexp((double)(8u + frac), (int)e - 7 - 3);
   return sign ? -v : v;
 }
 
@@ -139,6 +176,7 @@ static uint32_t round_to_bits(double x, const fmt_t* f) {
 /* Decode tables (one per 16-bit input format), built once.                 */
 /* ---------------------------------------------------------------------- */
 static double g_lut[2][65536];
+static double g_lut8[2][256];  /* [0]: E4M3, [1]: E5M2 */
 static pthread_once_t g_lut_once = PTHREAD_ONCE_INIT;
 
 static void build_luts(void) {
@@ -146,19 +184,37 @@ static void build_luts(void) {
     g_lut[ORACLE_F16][b] = decode_bits(b, &FMT_F16);
     g_lut[ORACLE_BF16][b] = decode_bits(b, &FMT_BF16);
   }
+  for (uint32_t b = 0; b < 256u; ++b) {
+    g_lut8[0][b] = decode_e4m3(b);
+    g_lut8[1][b] = decode_bits(b, &FMT_E5M2);
+  }
 }
 
 static const double* lut_of(int dtype_in) {
   pthread_once(&g_lut_once, build_luts);
+  if (dtype_in == ORACLE_E4M3) return g_lut8[0];
+  if (dtype_in == ORACLE_E5M2) return g_lut8[1];
   return g_lut[dtype_in];
 }
 
-/* One output element: the sequential binary64 dot product of row i of A and
- * row j of B. */
-static double dot_row(const uint16_t* a_row, const uint16_t* b_row, int64_t K,
-                      const double* lut) {
+static int in_bytes_of(int dtype_in) {
+  return dtype_in == ORACLE_E4M3 || dtype_in == ORACLE_E5M2 ? 1 : 2;
+}
+
+/* The sequential binary64 dot product of row i of A and row j of B over
+ * k = k0 .. k1-1 (elements of in_bytes bytes, decoded through lut). */
+static double dot_row(const void* a_row, const void* b_row, int64_t k0, int64_t k1,
+                      int in_bytes, const double* lut) {
   double s = 0.0;
-  for (int64_t k = 0; k < K; ++k) s += lut[a_row[k]] * lut[b_row[k]];
+  if (in_bytes == 1) {
+    const uint8_t* a8 = (const uint8_t*)a_row;
+    const uint8_t* b8 = (const uint8_t*)b_row;
+    for (int64_t k = k0; k < k1; ++k) s += lut[a8[k]] * lut[b8[k]];
+  } else {
+    const uint16_t* a16 = (const uint16_t*)a_row;
+    const uint16_t* b16 = (const uint16_t*)b_row;
+    for (int64_t k = k0; k < k1; ++k) s += lut[a16[k]] * lut[b16[k]];
+  }
   return s;
 }
 
@@ -174,8 +230,8 @@ static void store_out(void* C, int64_t idx, double v, int dtype_out) {
 /* row list and a column list; workers take whole rows of that product.     */
 /* ---------------------------------------------------------------------- */
 typedef struct {
-  const uint16_t* A;
-  const uint16_t* B;
+  const void* A;
+  const void* B;
   void* C;            /* rounded output, or NULL */
   double* C64;        /* unrounded binary64 output, or NULL */
   int64_t K;
@@ -194,6 +250,11 @@ typedef struct {
   int64_t ldc;         /* row length of cprev (N) */
   const float* bias;   /* N values, or NULL */
   int relu;
+  int in_bytes;        /* 2: fp16/bf16 operands, 1: fp8 */
+  /* blockwise scales (sfa NULL: none) */
+  const float* sfa;    /* ceil(M/bm) x nkb */
+  const float* sfb;    /* ceil(N/bn) x nkb */
+  int64_t bm, bn, bk, nkb;
 } job_t;
 
 static void* worker(void* arg) {
@@ -204,10 +265,23 @@ static void* worker(void* arg) {
     pthread_mutex_unlock(&jb->mu);
     if (r >= jb->nrows) break;
     const int64_t i = jb->rows ? jb->rows[r] : r;
-    const uint16_t* a_row = jb->A + i * jb->K;
+    const char* a_row = (const char*)jb->A + i * jb->K * jb->in_bytes;
     for (int64_t c = 0; c < jb->ncols; ++c) {
       const int64_t j = jb->cols ? jb->cols[c] : c;
-      double v = dot_row(a_row, jb->B + j * jb->K, jb->K, jb->lut);
+      const char* b_row = (const char*)jb->B + j * jb->K * jb->in_bytes;
+      double v;
+      if (jb->sfa) {
+        v = 0.0;
+        for (int64_t kb = 0; kb < jb->nkb; ++kb) {
+          const int64_t k0 = kb * jb->bk;
+          const int64_t k1 = k0 + jb->bk < jb->K ? k0 + jb->bk : jb->K;
+          const double scale = (double)jb->sfa[(i / jb->bm) * jb->nkb + kb] *
+                               (double)jb->sfb[(j / jb->bn) * jb->nkb + kb];
+          v += scale * dot_row(a_row, b_row, k0, k1, jb->in_bytes, jb->lut);
+        }
+      } else {
+        v = dot_row(a_row, b_row, 0, jb->K, jb->in_bytes, jb->lut);
+      }
       if (jb->epi) {
         v = jb->alpha * v;
         if (jb->cprev) {
@@ -251,7 +325,9 @@ static int run_job(job_t* jb, int nthreads) {
 }
 
 static int check_types(int dtype_in, int dtype_out) {
-  if (dtype_in != ORACLE_F16 && dtype_in != ORACLE_BF16) return -1;
+  if (dtype_in != ORACLE_F16 && dtype_in != ORACLE_BF16 && dtype_in != ORACLE_E4M3 &&
+      dtype_in != ORACLE_E5M2)
+    return -1;
   if (!fmt_of(dtype_out)) return -1;
   return 0;
 }
@@ -262,36 +338,39 @@ static int check_types(int dtype_in, int dtype_out) {
 /* ---------------------------------------------------------------------- */
 
 /* Full C (M x N, row-major), rounded to dtype_out. */
-int oracle_gemm(const uint16_t* A, const uint16_t* B, void* C, int64_t M, int64_t N,
+int oracle_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N,
                 int64_t K, int dtype_in, int dtype_out, int nthreads) {
   if (check_types(dtype_in, dtype_out) || M < 0 || N < 0 || K < 0) return -1;
   job_t jb = {A, B, C, NULL, K, NULL, M, NULL, N, dtype_out, lut_of(dtype_in), 0};
+  jb.in_bytes = in_bytes_of(dtype_in);
   return run_job(&jb, nthreads);
 }
 
 /* Selected outputs: out[r][c] = C[rows[r]][cols[c]] (nrows x ncols,
  * row-major).  rows == NULL selects 0..nrows-1, cols == NULL 0..ncols-1.
  * Either C_out (rounded) or C64_out (unrounded binary64 sum) may be NULL. */
-int oracle_gemm_select(const uint16_t* A, const uint16_t* B, void* C_out, double* C64_out,
+int oracle_gemm_select(const void* A, const void* B, void* C_out, double* C64_out,
                        int64_t K, const int64_t* rows, int64_t nrows,
                        const int64_t* cols, int64_t ncols, int dtype_in, int dtype_out,
                        int nthreads) {
   if (check_types(dtype_in, dtype_out) || K < 0 || nrows < 0 || ncols < 0) return -1;
   job_t jb = {A, B, C_out, C64_out, K, rows, nrows, cols, ncols, dtype_out,
               lut_of(dtype_in), 0};
+  jb.in_bytes = in_bytes_of(dtype_in);
   return run_job(&jb, nthreads);
 }
 
 /* Full D (M x N) with the fused epilogue described at the top: cprev (M x N,
  * dtype_out patterns) may be NULL when beta is 0, bias (N floats) may be NULL,
  * relu is 0 or 1.  D may be the same buffer as cprev only if nthreads == 1. */
-int oracle_gemm_epilogue(const uint16_t* A, const uint16_t* B, const void* cprev,
+int oracle_gemm_epilogue(const void* A, const void* B, const void* cprev,
                          const float* bias, double alpha, double beta, int relu, void* D,
                          int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out,
                          int nthreads) {
   if (check_types(dtype_in, dtype_out) || M < 0 || N < 0 || K < 0) return -1;
   if (beta != 0.0 && !cprev) return -1;
   job_t jb = {A, B, D, NULL, K, NULL, M, NULL, N, dtype_out, lut_of(dtype_in), 0};
+  jb.in_bytes = in_bytes_of(dtype_in);
   jb.epi = 1;
   jb.alpha = alpha;
   jb.beta = beta;
@@ -302,8 +381,35 @@ int oracle_gemm_epilogue(const uint16_t* A, const uint16_t* B, const void* cprev
   return run_job(&jb, nthreads);
 }
 
+/* Selected outputs (as oracle_gemm_select) of the blockwise-scaled product
+ * described at the top: sfa holds ceil(M/bm) x ceil(K/bk) and sfb
+ * ceil(N/bn) x ceil(K/bk) binary32 scales, row-major; M is the row count of A. */
+int oracle_gemm_blockwise(const void* A, const void* B, const float* sfa, const float* sfb,
+                          int64_t bm, int64_t bn, int64_t bk, void* C_out, double* C64_out,
+                          int64_t M, int64_t K, const int64_t* rows, int64_t nrows,
+                          const int64_t* cols, int64_t ncols, int dtype_in, int dtype_out,
+                          int nthreads) {
+  if (check_types(dtype_in, dtype_out) || M < 0 || K < 0 || nrows < 0 || ncols < 0) return -1;
+  if (!sfa || !sfb || bm <= 0 || bn <= 0 || bk <= 0) return -1;
+  job_t jb = {A, B, C_out, C64_out, K, rows, nrows, cols, ncols, dtype_out,
+              lut_of(dtype_in), 0};
+  jb.in_bytes = in_bytes_of(dtype_in);
+  jb.sfa = sfa;
+  jb.sfb = sfb;
+  jb.bm = bm;
+  jb.bn = bn;
+  jb.bk = bk;
+  jb.nkb = (K + bk - 1) / bk;
+  (void)M;
+  return run_job(&jb, nthreads);
+}
+
 /* Exposed for the pins: decode n patterns of dtype to binary64. */
 int oracle_decode(const void* bits, double* out, int64_t n, int dtype) {
+  if (dtype == ORACLE_E4M3 || dtype == ORACLE_E5M2) {
+    for (int64_t t = 0; t < n; ++t) out[t] = lut_of(dtype)[((const uint8_t*)bits)[t]];
+    return 0;
+  }
   const fmt_t* f = fmt_of(dtype);
   if (!f) return -1;
   for (int64_t t = 0; t < n; ++t) {

@@ -7,7 +7,7 @@ their inputs from it without sharing any part of the method.
 
 Recipe (one CPU ``torch.Generator`` per shape, seeded with the workload's
 seed; A is drawn first, then B; values are drawn in fp32 and cast to the
-input dtype by torch with round-to-nearest-even):
+input dtype by torch with round-to-nearest-even; FP8 inputs are E4M3 or E5M2):
   * ``uniform``: iid U[-1, 1) as ``rand * 2 - 1``;
   * ``normal``:  iid N(0, 1/K) as ``randn * K**-0.5`` (the standard deviation
     is read as 1/sqrt(K)).
@@ -21,9 +21,10 @@ from dataclasses import dataclass
 
 import torch
 
-F16, BF16, F32 = 0, 1, 2
-TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32}
-DTYPE_NAME = {F16: "f16", BF16: "bf16", F32: "f32"}
+F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
+TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32,
+               E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
+DTYPE_NAME = {F16: "f16", BF16: "bf16", F32: "f32", E4M3: "e4m3", E5M2: "e5m2"}
 
 
 @dataclass(frozen=True)
@@ -88,6 +89,14 @@ def make_small_int_operands(M: int, N: int, K: int, dtype_in: int, seed: int = 0
     A = torch.randint(lo, hi + 1, (M, K), generator=g).to(td)
     B = torch.randint(lo, hi + 1, (N, K), generator=g).to(td)
     return A, B
+
+
+def make_block_scales(rows: int, cols: int, seed: int = 0, lo: float = -3.0, hi: float = 3.0):
+    """A rows x cols float32 array of positive scales 2**u, u iid uniform in [lo, hi)
+    (one per (row block, k block), as blockwise-scaled operands carry)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return torch.exp2(torch.rand(rows, cols, generator=g) * (hi - lo) + lo).float()
 
 
 def sample_indices(n: int, count: int, seed: int, must=()):

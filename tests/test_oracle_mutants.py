@@ -18,21 +18,21 @@ import oracle
 import seeded_inputs as si
 from tests import exact
 
-F16, BF16, F32 = 0, 1, 2
+F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
 TD = {F16: torch.float16, BF16: torch.bfloat16}
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 MUTANTS = {
-    "drop_last_term": ("for (int64_t k = 0; k < K; ++k) s +=",
-                       "for (int64_t k = 0; k < K - 1; ++k) s +="),
-    "wrong_sign": ("s += lut[a_row[k]] * lut[b_row[k]];", "s -= lut[a_row[k]] * lut[b_row[k]];"),
-    "reversed_index": ("s += lut[a_row[k]] * lut[b_row[k]];",
-                       "s += lut[a_row[k]] * lut[b_row[K - 1 - k]];"),
+    "drop_last_term": ("for (int64_t k = k0; k < k1; ++k) s += lut[a16[k]]",
+                       "for (int64_t k = k0; k < k1 - 1; ++k) s += lut[a16[k]]"),
+    "wrong_sign": ("s += lut[a16[k]] * lut[b16[k]];", "s -= lut[a16[k]] * lut[b16[k]];"),
+    "reversed_index": ("s += lut[a16[k]] * lut[b16[k]];",
+                       "s += lut[a16[k]] * lut[b16[k1 - 1 - (k - k0)]];"),
     # B walked with unit stride across j, as if it were stored transposed
-    "transposed_B": ("dot_row(a_row, jb->B + j * jb->K, jb->K, jb->lut)",
-                     "dot_row(a_row, jb->B + j, jb->K, jb->lut)"),
-    "A_for_B": ("dot_row(a_row, jb->B + j * jb->K, jb->K, jb->lut)",
-                "dot_row(a_row, jb->A + j * jb->K, jb->K, jb->lut)"),
+    "transposed_B": ("const char* b_row = (const char*)jb->B + j * jb->K * jb->in_bytes;",
+                     "const char* b_row = (const char*)jb->B + j * jb->in_bytes;"),
+    "A_for_B": ("const char* b_row = (const char*)jb->B + j * jb->K * jb->in_bytes;",
+                "const char* b_row = (const char*)jb->A + j * jb->K * jb->in_bytes;"),
     "ties_away": ("(rem == 0.5 && fmod(n, 2.0) != 0.0)", "(rem == 0.5)"),
     "truncate": ("if (rem > 0.5 ||", "if (rem > 2.0 ||"),
     "subnormal_scale": ("v = ldexp((double)frac, f->emin - f->frac_bits);",
@@ -45,6 +45,24 @@ MUTANTS = {
     "epi_beta_as_one": ("v += jb->beta * decode_bits(bits, f);", "v += decode_bits(bits, f);"),
     "epi_bias_by_row": ("if (jb->bias) v += (double)jb->bias[j];",
                         "if (jb->bias) v += (double)jb->bias[i];"),
+    # FP8 operands
+    "e4m3_bias_8": ("else v = ldexp((double)(8u + frac), (int)e - 7 - 3);",
+                    "else v = ldexp((double)(8u + frac), (int)e - 8 - 3);"),
+    "e4m3_top_binade_as_nan": ("if (e == 15u && frac == 7u) return NAN;",
+                               "if (e == 15u) return NAN;"),
+    "e4m3_subnormal_scale": ("if (e == 0) v = ldexp((double)frac, 1 - 7 - 3);",
+                             "if (e == 0) v = ldexp((double)frac, 0 - 7 - 3);"),
+    "e5m2_as_e4m3": ("g_lut8[1][b] = decode_bits(b, &FMT_E5M2);", "g_lut8[1][b] = decode_e4m3(b);"),
+    "fp8_wrong_index": ("s += lut[a8[k]] * lut[b8[k]];", "s += lut[a8[k]] * lut[b8[k1 - 1 - (k - k0)]];"),
+    # blockwise scales
+    "bw_sfb_by_row_block": ("(double)jb->sfb[(j / jb->bn) * jb->nkb + kb];",
+                            "(double)jb->sfb[(i / jb->bn) * jb->nkb + kb];"),
+    "bw_first_scale_only": ("const double scale = (double)jb->sfa[(i / jb->bm) * jb->nkb + kb] *",
+                            "const double scale = (double)jb->sfa[(i / jb->bm) * jb->nkb + 0] *"),
+    "bw_short_block": ("const int64_t k1 = k0 + jb->bk < jb->K ? k0 + jb->bk : jb->K;",
+                       "const int64_t k1 = k0 + jb->bk - 1 < jb->K ? k0 + jb->bk - 1 : jb->K;"),
+    "bw_sfa_by_col_block": ("const double scale = (double)jb->sfa[(i / jb->bm) * jb->nkb + kb] *",
+                            "const double scale = (double)jb->sfa[(j / jb->bm) * jb->nkb + kb] *"),
     "epi_relu_before_bias": ("if (jb->bias) v += (double)jb->bias[j];\n        if (jb->relu && !(v > 0.0)) v = 0.0;",
                              "if (jb->relu && !(v > 0.0)) v = 0.0;\n        if (jb->bias) v += (double)jb->bias[j];"),
 }
@@ -109,6 +127,39 @@ def _pins_pass(lib) -> bool:
                     q = Fraction(0)
                 if Fraction(float(got[i, j])) != exact.round_exact(q, F32):
                     return False
+    # FP8 decoders against torch's widening, all 256 patterns
+    for dt, td in ((E4M3, torch.float8_e4m3fn), (E5M2, torch.float8_e5m2)):
+        bits = np.arange(256, dtype=np.uint8)
+        got = oracle.decode(bits, dt, lib=lib)
+        want = torch.from_numpy(bits.copy()).view(td).to(torch.float64).numpy()
+        nan = np.isnan(want)
+        if not (np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], want[~nan])):
+            return False
+    # FP8 product, exact rational (non-square, non-symmetric)
+    for dt in (E4M3, E5M2):
+        A, B = si.make_operands(4, 3, 24, dt, "uniform", seed=4)
+        ex = exact.exact_gemm(A, B)
+        got = oracle.decode(oracle.gemm(A, B, dt, F32, lib=lib), F32, lib=lib)
+        for i in range(4):
+            for j in range(3):
+                if Fraction(float(got[i, j])) != exact.round_exact(ex[i][j], F32):
+                    return False
+    # blockwise scales, exact rational: M == N keeps a mis-indexed scale in bounds
+    M = N = 5
+    K, bm, bn, bk = 13, 2, 3, 4
+    A, B = si.make_small_int_operands(M, N, K, E4M3, seed=5)
+    g = torch.Generator().manual_seed(6)
+    sfa = torch.exp2(torch.randint(-3, 4, (3, 4), generator=g).float()).numpy()
+    sfb = torch.exp2(torch.randint(-3, 4, (2, 4), generator=g).float()).numpy()
+    av, bv = exact.exact_values(A), exact.exact_values(B)
+    got = oracle.decode(oracle.gemm_blockwise(A, B, sfa, sfb, bm, bn, bk, E4M3, F32, lib=lib),
+                        F32, lib=lib)
+    for i in range(M):
+        for j in range(N):
+            q = sum((Fraction(float(sfa[i // bm, k // bk])) * Fraction(float(sfb[j // bn, k // bk]))
+                     * av[i][k] * bv[j][k] for k in range(K)), Fraction(0))
+            if Fraction(float(got[i, j])) != exact.round_exact(q, F32):
+                return False
     # rounding routine against numpy on ties and overflow
     x = np.array([1.0 + 2.0**-11, 1.0 + 3 * 2.0**-11, 65520.0, 70000.0, 2.0**-25 * 3])
     with np.errstate(over="ignore"):
