@@ -48,6 +48,7 @@ L2_NOMINAL_BYTES = 129 * 1000 * 1000
 # Nominal GB300 figures, reported as context beside the measured peaks.
 NOMINAL_TFLOPS = 2250.0   # dense fp16/bf16
 NOMINAL_HBM_GBS = 7900.0
+NOMINAL_FP8_RATIO = 2.0  # dense FP8 / dense bf16 (4.5 / 2.25 PFLOP/s nominal)
 # The device code of the kernels (the host-side files -- the C ABI, the launch table --
 # do not change what a launch of a given configuration moves).
 KERNEL_SOURCES = ("dense_gemm_blackwell_02_gb300/csrc/gemm_kernel.cuh",
@@ -261,6 +262,49 @@ def measure_decode(g, dev, stream, peaks, iters=20, name="decode_m256"):
     return out
 
 
+def fp8_peak(peaks):
+    """The FP8 dense peak: the measured bf16 peak times the nominal FP8 / bf16 ratio."""
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    return bf16 * NOMINAL_FP8_RATIO
+
+
+def measure_fp8(g, dev, stream, peaks, iters=20):
+    """Secondary figures: the FP8 (E4M3 -> bf16) square shapes, tensor-bound.  Each is
+    timed like the main workload, one launch per event pair after an L2 flush.  Their
+    parity is covered by the full-size tests; here only time is taken."""
+    wl = si.WORKLOADS["fp8"]
+    peak = fp8_peak(peaks)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    out = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.seed)
+    for s in wl.shapes:
+        td = si.TORCH_DTYPE[wl.dtype_in]
+        A = (torch.rand(s.M, s.K, generator=gen, device=dev) * 2 - 1).to(td)
+        B = (torch.rand(s.N, s.K, generator=gen, device=dev) * 2 - 1).to(td)
+        C = torch.empty(s.M, s.N, dtype=si.TORCH_DTYPE[wl.dtype_out], device=dev)
+
+        def run(a, b, c):
+            g.run(a, b, c, stream=stream)
+
+        for _ in range(3):
+            flush.fill_(0.5)
+            run(A, B, C)
+        torch.cuda.synchronize()
+        total, each = time_steps(run, [(A, B, C)], stream, iters, flush, per_step=True)
+        ms = total / iters
+        tf = rl.gemm_flops(s.M, s.N, s.K) / (ms * 1e-3) / 1e12
+        out[f"{s.M}x{s.N}x{s.K}"] = {"us": round(ms * 1e3, 2),
+                                     "median_us": round(1e3 * statistics.median(each), 2),
+                                     "TFLOP/s": round(tf, 1), "frac_of_peak": round(tf / peak, 4),
+                                     "peak": round(peak, 1),
+                                     "dtype_in": si.DTYPE_NAME[wl.dtype_in],
+                                     "dtype_out": si.DTYPE_NAME[wl.dtype_out],
+                                     "kernel": g.last_config()}
+        del A, B, C
+    return out
+
+
 def run_reference(args):
     """The oracle as it stands, timed on the host cores on bounded samples."""
     ws, rank, _ = dist_env()
@@ -383,6 +427,7 @@ def run_ours(args):
     decode = measure_decode(g, dev, stream, peaks) if args.decode else None
     decode_small = (measure_decode(g, dev, stream, peaks, name="decode_small_m")
                     if args.decode > 1 else None)
+    fp8 = measure_fp8(g, dev, stream, peaks) if args.fp8 else None
     flops = rl.gemm_flops(M, N, K)
     ms_per_step = total_ms / args.steps
     value = replica_throughput(ws, flops, args.steps, total_ms)
@@ -399,8 +444,9 @@ def run_ours(args):
         g.run_host(A_h, B_h, C_h, din, dout, stream=stream)
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     out_b = 4 if dout == si.F32 else 2
+    in_b = 1 if din in (si.E4M3, si.E5M2) else 2
     e2e = {"value": flops / e2e_s / 1e12, "unit": UNIT,
-           "h2d_bytes_per_step": 2 * (M * K + N * K), "d2h_bytes_per_step": out_b * M * N}
+           "h2d_bytes_per_step": in_b * (M * K + N * K), "d2h_bytes_per_step": out_b * M * N}
 
     line = None
     if rank == 0:
@@ -417,6 +463,11 @@ def run_ours(args):
         cpu_value = 2.0 * len(rows) * N * K / cpu_s / 1e12
 
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        peak_note = f"{peak_src} bf16_tflops (burst; fp16 has the same dense rate)"
+        if in_b == 1:
+            peak = fp8_peak(peaks)
+            peak_note = (f"{peak_src} bf16_tflops (burst) x {NOMINAL_FP8_RATIO:g}, the nominal "
+                         f"FP8 / bf16 dense ratio")
         traffic = None
         tf_path = os.path.join(ROOT, "profiles", "traffic.json")
         if os.path.exists(tf_path):
@@ -438,7 +489,7 @@ def run_ours(args):
             "gpu_launches": args.steps,
             "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak,
                          "unit": "TFLOP/s", "frac": kernel_tflops / peak, "traffic": traffic,
-                         "peak_source": f"{peak_src} bf16_tflops (burst; fp16 has the same dense rate)",
+                         "peak_source": peak_note,
                          "algorithmic_flops_per_launch": flops},
             "per_step_us": {"median": 1e3 * statistics.median(each_ms), "best": 1e3 * min(each_ms),
                             "mean": 1e3 * ms_per_step},
@@ -455,6 +506,8 @@ def run_ours(args):
             line["decode"] = decode
         if decode_small is not None:
             line["decode_small_m"] = decode_small
+        if fp8 is not None:
+            line["fp8"] = fp8
         print(json.dumps(line))
     g.close()
     if ws > 1:
@@ -474,6 +527,8 @@ def main():
     ap.add_argument("--decode", type=int, default=2,
                     help="also time the M=256 decode shapes (HBM GB/s) into the line; "
                          "2 adds the M=1..128 decode shapes")
+    ap.add_argument("--fp8", type=int, default=1,
+                    help="also time the FP8 (E4M3 -> bf16) square shapes into the line")
     ap.add_argument("--l2", default="flush", choices=["rotate", "flush"],
                     help="main workload: flush L2 before each separately timed step (default), "
                          "or cycle operand copies larger than L2 with launches back to back")

@@ -9,7 +9,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-F16, BF16, F32 = 0, 1, 2
+F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
 STATUS_NAMES = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
                 3: "GEMM_ERR_CUDA", 4: "GEMM_ERR_OOM", 5: "GEMM_ERR_TIMEOUT"}
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgemm.so")
@@ -94,7 +94,8 @@ def torch_float32():
 
 def torch_dtype_code(dt) -> int:
     import torch
-    return {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32}[dt]
+    return {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
+            torch.float8_e4m3fn: E4M3, torch.float8_e5m2: E5M2}[dt]
 
 
 def _stream_ptr(stream, device):

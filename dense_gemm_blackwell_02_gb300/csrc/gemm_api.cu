@@ -73,6 +73,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+bool is_fp8(int d) { return d == GEMM_E4M3 || d == GEMM_E5M2; }
+
 // 2-D tensor map over a row-major rows x cols matrix, 128-byte swizzle, box of 128
 // bytes of columns x box_rows rows.  Loads read out-of-range elements as zero (M, N and
 // K tails); stores skip them.
@@ -87,13 +89,14 @@ bool make_map(gemm_ctx* h, const void* ptr, int64_t rows, int64_t cols, int dtyp
   auto fn = encode_fn();
   if (!fn) return false;
   CUtensorMap m;
-  const cuuint64_t esz = dtype == GEMM_F32 ? 4 : 2;
+  const cuuint64_t esz = dtype == GEMM_F32 ? 4 : is_fp8(dtype) ? 1 : 2;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols * esz};
   const cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = dtype == GEMM_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                  : dtype == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : is_fp8(dtype)     ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUresult r = fn(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -112,7 +115,9 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 size_t out_size(gemm_dtype_t d) { return d == GEMM_F32 ? 4 : 2; }
 
-bool valid_dtype(int d) { return d == GEMM_F16 || d == GEMM_BF16 || d == GEMM_F32; }
+bool valid_dtype(int d) { return d >= GEMM_F16 && d <= GEMM_E5M2; }
+
+size_t in_size(gemm_dtype_t d) { return is_fp8(d) ? 1 : 2; }
 
 struct Choice {
   int variant, bn, stages, splits, kb_per_split, group_m, grid, chain_kb, half_tail, prefetch_kb;
@@ -135,7 +140,9 @@ int resident_units(gemm_ctx* h, int cg, int bn, int stages, int out) {
   return slot;
 }
 
-gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choice* c) {
+// kb_elems: K elements per 128-byte K block (64 fp16/bf16, 128 FP8).
+gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int kb_elems,
+                     Choice* c) {
   const gemm_config_t& f = h->forced;
   // A CTA pair (256-row tiles, each CTA loading half of B) whenever M fills one.
   c->variant = f.variant ? f.variant : (M > kBlockM ? 2 : 1);
@@ -143,7 +150,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
   c->bn = f.block_n ? f.block_n : (N <= 128 ? 128 : 256);
   c->stages = f.stages ? f.stages : default_stages(cg, c->bn);
   if (!kernel_supported(cg, c->bn, c->stages)) return GEMM_ERR_INVALID_ARG;
-  c->k_blocks = ceil_div(K, kBlockK);
+  c->k_blocks = ceil_div(K, (int64_t)kb_elems);
   c->num_m = ceil_div(M, (int64_t)kBlockM * cg);
   c->num_n = ceil_div(N, c->bn);
   c->tiles = c->num_m * c->num_n;
@@ -230,7 +237,8 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, Choi
     c->ws_slots = ceil_div(c->k_blocks, std::max<int64_t>(share, 1)) + 1;
   }
   c->group_m = f.group_m ? f.group_m : 16;
-  c->chain_kb = f.chain_kblocks ? f.chain_kblocks : kChainKBlocks;
+  // a chain of K 4096 elements: 64 blocks of fp16/bf16, 32 of FP8
+  c->chain_kb = f.chain_kblocks ? f.chain_kblocks : kChainKBlocks * kBlockK / kb_elems;
   // Prefetching B into L2 ahead of the ring: off unless asked for (measured on the
   // M = 256 decode shapes and the square ones it did not help).
   c->prefetch_kb = f.prefetch_kblocks > 0 ? f.prefetch_kblocks : 0;
@@ -276,7 +284,7 @@ const char* gemm_status_string(gemm_status_t s) {
   switch (s) {
     case GEMM_OK: return "ok";
     case GEMM_ERR_INVALID_ARG: return "invalid argument";
-    case GEMM_ERR_UNSUPPORTED: return "unsupported (dtype, alignment, K % 8, or device)";
+    case GEMM_ERR_UNSUPPORTED: return "unsupported (dtype, alignment, K row pitch, or device)";
     case GEMM_ERR_CUDA: return "CUDA error";
     case GEMM_ERR_OOM: return "out of memory";
     case GEMM_ERR_TIMEOUT: return "kernel wait timed out";
@@ -378,7 +386,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
     return GEMM_ERR_UNSUPPORTED;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   if (!valid_dtype(dtype_in) || !valid_dtype(dtype_out)) return GEMM_ERR_INVALID_ARG;
-  if (dtype_in == GEMM_F32) return GEMM_ERR_UNSUPPORTED;
+  if (dtype_in == GEMM_F32 || is_fp8(dtype_out)) return GEMM_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return GEMM_OK;
   if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
   if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
@@ -391,13 +399,14 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
       return GEMM_ERR_CUDA;
     return GEMM_OK;
   }
-  if (K % 8) return GEMM_ERR_UNSUPPORTED;
+  if ((K * (int64_t)in_size(dtype_in)) % 16) return GEMM_ERR_UNSUPPORTED;  // TMA row pitch
   if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(B) % 16)
     return GEMM_ERR_UNSUPPORTED;
 
   const int out = out_kind(dtype_out);
   Choice ch;
-  gemm_status_t st = choose(h, M, N, K, out, &ch);
+  const bool fp8 = is_fp8(dtype_in);
+  gemm_status_t st = choose(h, M, N, K, out, fp8 ? 2 * kBlockK : kBlockK, &ch);
   if (st != GEMM_OK) return st;
 
   LaunchSpec s;
@@ -408,7 +417,9 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   s.out = out;
   s.grid = ch.grid;
   s.one_chain = ch.one_chain;
-  s.fused = fused;
+  // FP8 kernels always carry the epilogue: the per-tensor scales arrive as alpha
+  s.fused = fused || fp8;
+  s.kind = fp8 ? 1 : 0;
   s.stream = stream;
   const bool c_tma = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0;
   // A single one-CTA row tile of M < 128 rows loads A as an M-row box: the stage's
@@ -425,7 +436,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
 
   GemmParams& p = s.p;
   p.C = C;
-  p.fused = fused ? 1 : 0;
+  p.fused = s.fused ? 1 : 0;
   p.relu = fused && epi->activation == GEMM_ACT_RELU ? 1 : 0;
   p.alpha = fused ? epi->alpha : 1.0f;
   p.beta = fused ? epi->beta : 0.0f;
@@ -450,8 +461,13 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.a_tx_short = (uint32_t)(kBlockM - a_box) * 128u;
   p.vec_store = c_tma ? 1 : 0;
   p.tma_store = c_tma ? 1 : 0;
-  p.idesc = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn, dtype_in == GEMM_BF16);
-  p.idesc_half = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn / 2, dtype_in == GEMM_BF16);
+  if (fp8) {
+    p.idesc = idesc_f8_kmajor(kBlockM * ch.variant, ch.bn, dtype_in == GEMM_E5M2);
+    p.idesc_half = idesc_f8_kmajor(kBlockM * ch.variant, ch.bn / 2, dtype_in == GEMM_E5M2);
+  } else {
+    p.idesc = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn, dtype_in == GEMM_BF16);
+    p.idesc_half = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn / 2, dtype_in == GEMM_BF16);
+  }
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
   p.test_stall = h->test_stall;
@@ -508,11 +524,13 @@ gemm_status_t gemm_run_host(gemm_handle_t h, const void* A_host, const void* B_h
   if (!h) return GEMM_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   if (!valid_dtype(dtype_in) || !valid_dtype(dtype_out)) return GEMM_ERR_INVALID_ARG;
-  if (dtype_in == GEMM_F32) return GEMM_ERR_UNSUPPORTED;
+  if (dtype_in == GEMM_F32 || is_fp8(dtype_out)) return GEMM_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return GEMM_OK;
   if (!C_host || (K > 0 && (!A_host || !B_host))) return GEMM_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  const size_t bytes[3] = {(size_t)M * K * 2, (size_t)N * K * 2, (size_t)M * N * out_size(dtype_out)};
+  const size_t isz = in_size(dtype_in);
+  const size_t bytes[3] = {(size_t)M * K * isz, (size_t)N * K * isz,
+                           (size_t)M * N * out_size(dtype_out)};
   for (int i = 0; i < 3; ++i) {
     if (bytes[i] > h->stage_bytes[i]) {
       if (h->d_stage[i]) cudaFree(h->d_stage[i]);

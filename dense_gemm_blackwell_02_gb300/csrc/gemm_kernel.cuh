@@ -436,7 +436,9 @@ struct Layout {
 // registers this frees go to loads in flight in the split-K hand-over.
 // FUSED: the fused epilogue (alpha, beta * C, bias, ReLU) is compiled in; kept out of
 // the plain kernels, whose general epilogue it would push into more register spills.
-template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN, bool FUSED>
+// KIND 0: fp16/bf16 operands (tcgen05.mma kind::f16); KIND 1: FP8 operands (kind::f8f6f4).
+// Either way a K block is one 128-byte row of the swizzle atom: 64 or 128 elements.
+template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN, bool FUSED, int KIND = 0>
 __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
@@ -451,6 +453,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
   constexpr int kBoxCols = 128 / kOutBytes;    // columns of one 128-byte staging row
   constexpr int kBoxes = kHalf / kBoxCols;     // staging boxes per warp
   constexpr int kRowsTile = kBlockM * CTA_GROUP;
+  constexpr int kKbElems = KIND == 0 ? kBlockK : 2 * kBlockK;  // K elements per K block
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -534,25 +537,25 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       // ("A Blackwell GEMM by Hand in CuTe DSL", section 8: TMA prefetch).
       if (p.prefetch_kb > 0)
         for (int32_t kb = w.kb0; kb < min(w.kb0 + p.prefetch_kb, w.kb1); ++kb)
-          tma_prefetch_l2_2d_elect(mapB, kb * kBlockK, b_row);
+          tma_prefetch_l2_2d_elect(mapB, kb * kKbElems, b_row);
       for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
         if (p.prefetch_kb > 0 && kb + p.prefetch_kb < w.kb1)
-          tma_prefetch_l2_2d_elect(mapB, (kb + p.prefetch_kb) * kBlockK, b_row);
+          tma_prefetch_l2_2d_elect(mapB, (kb + p.prefetch_kb) * kKbElems, b_row);
         if (!warp_wait(empty_bar(stage), phase ^ 1u, ctl, kSiteEmpty)) {
           ok = false;
           break;
         }
         if constexpr (CTA_GROUP == 1) {
           mbar_arrive_expect_tx_elect(full_bar(stage), tx);
-          tma_load_2d_elect(sB + stage * L::kBBytes, mapB, kb * kBlockK, b_row, full_bar(stage));
-          tma_load_2d_elect(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, full_bar(stage));
+          tma_load_2d_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row, full_bar(stage));
+          tma_load_2d_elect(sA + stage * L::kABytes, &tmA, kb * kKbElems, a_row, full_bar(stage));
         } else {
           // Both CTAs' copies complete on the leader's full barrier; the leader arms it
           // with the bytes of the pair.
           const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
           if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), tx);
-          tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kBlockK, b_row, leader_full);
-          tma_load_2d_pair_elect(sA + stage * L::kABytes, &tmA, kb * kBlockK, a_row, leader_full);
+          tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row, leader_full);
+          tma_load_2d_pair_elect(sA + stage * L::kABytes, &tmA, kb * kKbElems, a_row, leader_full);
         }
         armed |= 1u << stage;
         armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -607,11 +610,11 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
             tc_fence_after();
             const uint64_t da = desc_a0 + ((stage * L::kABytes) >> 4);
             const uint64_t db = desc_b0 + ((stage * L::kBBytes) >> 4);
-            // four K=16 MMAs, then the commit that frees the stage (in both CTAs) once
-            // they are done
-            static_assert(kBlockK == 64, "umma_stage_elect issues four K=16 MMAs");
-            umma_stage_elect<CTA_GROUP>(d_tmem, da, db, idesc, kb > c0 ? 1u : 0u,
-                                        empty_bar(stage));
+            // four MMAs of 32 bytes of K, then the commit that frees the stage (in both
+            // CTAs) once they are done
+            static_assert(kBlockK * 2 == 128, "umma_stage_elect covers 128 bytes of K");
+            umma_stage_elect<CTA_GROUP, KIND>(d_tmem, da, db, idesc, kb > c0 ? 1u : 0u,
+                                              empty_bar(stage));
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;

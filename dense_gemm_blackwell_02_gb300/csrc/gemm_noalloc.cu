@@ -128,7 +128,9 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   const bool in_ok = dtype_in == GEMM_F16 || dtype_in == GEMM_BF16;
   const bool out_ok = dtype_out == GEMM_F16 || dtype_out == GEMM_BF16 || dtype_out == GEMM_F32;
-  if (!out_ok || (!in_ok && dtype_in != GEMM_F32)) return GEMM_ERR_INVALID_ARG;
+  const bool in_known = in_ok || dtype_in == GEMM_F32 || dtype_in == GEMM_E4M3 ||
+                        dtype_in == GEMM_E5M2;  // known types this entry point does not take
+  if (!out_ok || !in_known) return GEMM_ERR_INVALID_ARG;
   if (!in_ok) return GEMM_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return GEMM_OK;
   if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;

@@ -16,9 +16,10 @@ struct LaunchSpec {
   int grid;        // CTAs (a multiple of cta_group)
   bool one_chain;  // every unit is one accumulation chain (streaming epilogue)
   bool fused;      // the fused epilogue (p.fused) is compiled in
-  CUtensorMap tmA; // A: box {64, 128}
-  CUtensorMap tmB; // B: box {64, bn / cta_group}
-  CUtensorMap tmB2; // B: box {64, bn / cta_group / 2} (half-tile units; else a copy of tmB)
+  int kind;        // 0: fp16/bf16 operands (kind::f16); 1: FP8 (kind::f8f6f4, always fused)
+  CUtensorMap tmA; // A: box {128 bytes of K, 128 (or M < 128) rows}
+  CUtensorMap tmB; // B: box {128 bytes of K, bn / cta_group}
+  CUtensorMap tmB2; // B: box {128 bytes of K, bn / cta_group / 2} (half-tile units; else tmB)
   CUtensorMap tmC; // C: box {128 bytes of columns, 32 rows} (used when p.tma_store)
   GemmParams p;
   cudaStream_t stream;
@@ -44,6 +45,11 @@ cudaError_t launch_cg1_fused(const LaunchSpec& s);
 cudaError_t launch_cg2_fused(const LaunchSpec& s);
 cudaError_t launch_cg1_one_fused(const LaunchSpec& s);
 cudaError_t launch_cg2_one_fused(const LaunchSpec& s);
+// ... and with FP8 operands (kernels_cg*_fp8.cu; the fused epilogue carries the scales)
+cudaError_t launch_cg1_fp8(const LaunchSpec& s);
+cudaError_t launch_cg2_fp8(const LaunchSpec& s);
+cudaError_t launch_cg1_one_fp8(const LaunchSpec& s);
+cudaError_t launch_cg2_one_fp8(const LaunchSpec& s);
 int resident_cg1(int bn, int stages, int out);
 int resident_cg2(int bn, int stages, int out);
 

@@ -5,9 +5,9 @@
 
 namespace gb300 {
 
-template <int CG, int BN, int STAGES, int OUT, bool ONE, bool FUSED>
+template <int CG, int BN, int STAGES, int OUT, bool ONE, bool FUSED, int KIND = 0>
 cudaError_t launch_one(const LaunchSpec& s) {
-  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED>;
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED, KIND>;
   using L = Layout<CG, BN, STAGES>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes);
@@ -67,12 +67,12 @@ int resident_one() {
   return n;
 }
 
-template <int CG, int BN, int STAGES, bool ONE, bool FUSED>
+template <int CG, int BN, int STAGES, bool ONE, bool FUSED, int KIND = 0>
 cudaError_t by_out(const LaunchSpec& s) {
   switch (s.out) {
-    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED>(s);
-    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED>(s);
-    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED>(s);
+    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED, KIND>(s);
+    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED, KIND>(s);
+    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED, KIND>(s);
     default: return cudaErrorInvalidValue;
   }
 }

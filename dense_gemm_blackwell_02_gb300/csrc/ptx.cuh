@@ -296,44 +296,42 @@ __device__ __forceinline__ void umma_f16_elect(uint32_t d_tmem, uint64_t a_desc,
                  : "memory");
 }
 
-// One 64-deep stage: four K=16 MMAs (descriptor start addresses advance by 32 bytes,
-// i.e. +2 in the >>4-encoded field) and the commit that frees the stage, issued by one
-// elected lane in a single asm block.  (Four separately elected MMAs cost about 120
-// cycles of issue each on sm_103a; batched, a 128 x 128 x 16 MMA issues every 64
-// cycles, the tensor core's rate.)  `accumulate` applies to the first MMA; the other
-// three always accumulate.  For CTA_GROUP == 2 the commit is multicast to both CTAs.
-template <int CTA_GROUP>
+// One 128-byte-deep stage (64 fp16/bf16 or 128 FP8 values of K): four MMAs of 32 bytes
+// of K each (K=16 for kind::f16, K=32 for kind::f8f6f4; descriptor start addresses
+// advance by 32 bytes, i.e. +2 in the >>4-encoded field) and the commit that frees the
+// stage, issued by one elected lane in a single asm block.  (Four separately elected
+// MMAs cost about 120 cycles of issue each on sm_103a; batched, a 128 x 128 x 16 MMA
+// issues every 64 cycles, the tensor core's rate.)  `accumulate` applies to the first
+// MMA; the other three always accumulate.  For CTA_GROUP == 2 the commit is multicast
+// to both CTAs.  KIND 0: kind::f16; KIND 1: kind::f8f6f4.
+#define GB300_STAGE_MMA(CG, KINDSTR)                                                     \
+  asm volatile(GB300_ELECT                                                               \
+               ".reg .pred p_;\n\t.reg .b64 a1_, a2_, a3_, b1_, b2_, b3_;\n\t"           \
+               "setp.ne.b32 p_, %4, 0;\n\t"                                              \
+               "add.s64 a1_, %1, 2;\n\tadd.s64 a2_, %1, 4;\n\tadd.s64 a3_, %1, 6;\n\t"    \
+               "add.s64 b1_, %2, 2;\n\tadd.s64 b2_, %2, 4;\n\tadd.s64 b3_, %2, 6;\n\t"    \
+               "@e_ tcgen05.mma.cta_group::" #CG ".kind::" KINDSTR " [%0], %1, %2, %3, p_;\n\t" \
+               "@e_ tcgen05.mma.cta_group::" #CG ".kind::" KINDSTR " [%0], a1_, b1_, %3, 1;\n\t" \
+               "@e_ tcgen05.mma.cta_group::" #CG ".kind::" KINDSTR " [%0], a2_, b2_, %3, 1;\n\t" \
+               "@e_ tcgen05.mma.cta_group::" #CG ".kind::" KINDSTR " [%0], a3_, b3_, %3, 1;\n\t" \
+               GB300_STAGE_COMMIT_##CG "\n\t}"                                               \
+               ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate),         \
+               "r"(empty_bar), "h"((uint16_t)0x3)                                          \
+               : "memory")
+#define GB300_STAGE_COMMIT_1 \
+  "@e_ tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];"
+#define GB300_STAGE_COMMIT_2                                                            \
+  "@e_ tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64" \
+  " [%5], %6;"
+
+template <int CTA_GROUP, int KIND = 0>
 __device__ __forceinline__ void umma_stage_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                  uint32_t idesc, uint32_t accumulate,
                                                  uint32_t empty_bar) {
-  if constexpr (CTA_GROUP == 1)
-    asm volatile(GB300_ELECT
-                 ".reg .pred p_;\n\t.reg .b64 a1_, a2_, a3_, b1_, b2_, b3_;\n\t"
-                 "setp.ne.b32 p_, %4, 0;\n\t"
-                 "add.s64 a1_, %1, 2;\n\tadd.s64 a2_, %1, 4;\n\tadd.s64 a3_, %1, 6;\n\t"
-                 "add.s64 b1_, %2, 2;\n\tadd.s64 b2_, %2, 4;\n\tadd.s64 b3_, %2, 6;\n\t"
-                 "@e_ tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p_;\n\t"
-                 "@e_ tcgen05.mma.cta_group::1.kind::f16 [%0], a1_, b1_, %3, 1;\n\t"
-                 "@e_ tcgen05.mma.cta_group::1.kind::f16 [%0], a2_, b2_, %3, 1;\n\t"
-                 "@e_ tcgen05.mma.cta_group::1.kind::f16 [%0], a3_, b3_, %3, 1;\n\t"
-                 "@e_ tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}"
-                 ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(empty_bar)
-                 : "memory");
-  else
-    asm volatile(GB300_ELECT
-                 ".reg .pred p_;\n\t.reg .b64 a1_, a2_, a3_, b1_, b2_, b3_;\n\t"
-                 "setp.ne.b32 p_, %4, 0;\n\t"
-                 "add.s64 a1_, %1, 2;\n\tadd.s64 a2_, %1, 4;\n\tadd.s64 a3_, %1, 6;\n\t"
-                 "add.s64 b1_, %2, 2;\n\tadd.s64 b2_, %2, 4;\n\tadd.s64 b3_, %2, 6;\n\t"
-                 "@e_ tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p_;\n\t"
-                 "@e_ tcgen05.mma.cta_group::2.kind::f16 [%0], a1_, b1_, %3, 1;\n\t"
-                 "@e_ tcgen05.mma.cta_group::2.kind::f16 [%0], a2_, b2_, %3, 1;\n\t"
-                 "@e_ tcgen05.mma.cta_group::2.kind::f16 [%0], a3_, b3_, %3, 1;\n\t"
-                 "@e_ tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-                 " [%5], %6;\n\t}"
-                 ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(empty_bar),
-                 "h"((uint16_t)0x3)
-                 : "memory");
+  if constexpr (CTA_GROUP == 1 && KIND == 0) GB300_STAGE_MMA(1, "f16");
+  else if constexpr (CTA_GROUP == 2 && KIND == 0) GB300_STAGE_MMA(2, "f16");
+  else if constexpr (CTA_GROUP == 1) GB300_STAGE_MMA(1, "f8f6f4");
+  else GB300_STAGE_MMA(2, "f8f6f4");
 }
 
 template <int CTA_GROUP>

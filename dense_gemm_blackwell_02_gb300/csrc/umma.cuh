@@ -41,4 +41,13 @@ __host__ __device__ constexpr uint32_t idesc_f16_kmajor(uint32_t m, uint32_t n, 
          ((m >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4 with FP8 operands, fp32 accumulator, both
+// operands K-major: the kind::f16 layout above with the A/B format fields holding
+// 0 = E4M3 or 1 = E5M2 (NVIDIA's public PTX ISA instruction-descriptor table; an
+// E5M2 run on non-integer inputs checks the code, as for bf16).
+__host__ __device__ constexpr uint32_t idesc_f8_kmajor(uint32_t m, uint32_t n, bool e5m2) {
+  return (1u << 4) | ((e5m2 ? 1u : 0u) << 7) | ((e5m2 ? 1u : 0u) << 10) | ((n >> 3) << 17) |
+         ((m >> 4) << 24);
+}
+
 }  // namespace gb300

@@ -41,13 +41,23 @@ typedef struct CUstream_st* gemm_stream_t;
 
 typedef struct gemm_ctx* gemm_handle_t;
 
-typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_F32 = 2 } gemm_dtype_t;
+/* Element types.  GEMM_F32 is an output type only; GEMM_E4M3 and GEMM_E5M2 (OCP 8-bit
+ * floating point, one byte per element: E4M3 with bias 7, no infinities, largest
+ * finite 448; E5M2 IEEE-style with bias 15) are input types only ("CUTLASS Deep
+ * Dive: From CuTe Layouts to Blackwell tcgen05", Part 6: FP8 and Blockwise Scaling). */
+typedef enum {
+  GEMM_F16 = 0,
+  GEMM_BF16 = 1,
+  GEMM_F32 = 2,
+  GEMM_E4M3 = 3,
+  GEMM_E5M2 = 4
+} gemm_dtype_t;
 
 typedef enum {
   GEMM_OK = 0,
   GEMM_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad handle, bad config */
-  GEMM_ERR_UNSUPPORTED = 2, /* dtype combination, K % 8 != 0, pointer not 16-byte aligned,
-                               no sm_103 device */
+  GEMM_ERR_UNSUPPORTED = 2, /* dtype combination, K not a multiple of 16 bytes, pointer
+                               not 16-byte aligned, no sm_103 device */
   GEMM_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
   GEMM_ERR_OOM = 4,         /* device or host allocation failed */
   GEMM_ERR_TIMEOUT = 5      /* a kernel wait exceeded its limit (see gemm_device_status) */
@@ -67,10 +77,11 @@ typedef enum {
  *   stages    depth of the shared-memory operand ring
  *   group_m   grouped rasterisation: M tiles per group
  *   max_ctas  cap on the persistent grid (0 = one CTA per SM)
- *   chain_kblocks  64-deep K blocks accumulated in one Tensor-Memory accumulator
- *             before the epilogue adds it into its fp32 registers (0 = 64, i.e.
- *             K 4096: the tensor core's fp32 accumulation error grows with the
- *             length of one accumulation chain)
+ *   chain_kblocks  K blocks (128 bytes of K: 64 fp16/bf16 or 128 FP8 elements)
+ *             accumulated in one Tensor-Memory accumulator before the epilogue adds
+ *             it into its fp32 registers (0 = K 4096: 64 blocks, or 32 for FP8; the
+ *             tensor core's fp32 accumulation error grows with the length of one
+ *             accumulation chain)
  *   dp_tiles  reported by gemm_last_config only (must be 0 on input): how many
  *             tiles ran whole.  The rest ran as `splits` K slices each, or, when
  *             `splits` is 1, as two half-width (block_n / 2 column) units each.  A
@@ -110,8 +121,14 @@ gemm_status_t gemm_destroy(gemm_handle_t h);
  * Queue C = A . B^T on `stream`.
  *   A, B, C     device pointers, 16-byte aligned, layouts as above.
  *   M, N, K     sizes >= 0.  M == 0 or N == 0 is a no-op; K == 0 writes C = 0.
- *               K must be a multiple of 8 (TMA rows must be 16-byte multiples).
- *   dtype_in    GEMM_F16 or GEMM_BF16 (A and B share it).
+ *               A row of K elements must be a multiple of 16 bytes (TMA row
+ *               pitch): K % 8 == 0 for fp16/bf16, K % 16 == 0 for FP8.
+ *   dtype_in    GEMM_F16, GEMM_BF16, GEMM_E4M3 or GEMM_E5M2 (A and B share it).
+ *               FP8 runs tcgen05.mma kind::f8f6f4 with K blocks of 128 elements
+ *               ("A Blackwell GEMM by Hand in CuTe DSL", section 6: the 128-byte
+ *               swizzle atom holds 128 FP8 values of K); a per-tensor scale pair
+ *               (scale_a, scale_b) is applied as gemm_run_epilogue's
+ *               alpha = scale_a * scale_b.
  *   dtype_out   GEMM_F16, GEMM_BF16 or GEMM_F32.
  * Neither allocates on the steady path nor synchronises: the split-K workspace
  * grows on the first call that needs more of it (an allocation, outside any
@@ -215,7 +232,8 @@ const char* gemm_status_string(gemm_status_t s);
  * array: each call clears the parts it relies on, on `stream`, and calls whose
  * work overlaps on the GPU race on it -- order them on one stream.
  *
- * Arguments, layouts and argument errors are those of gemm_run (no handle).
+ * Arguments, layouts and argument errors are those of gemm_run (no handle), except
+ * that FP8 inputs are refused with GEMM_ERR_UNSUPPORTED.
  * The kernel is gemm_run's one-CTA split-K kernel with 256-column tiles; when
  * fewer tiles than half the SMs exist, K is sliced.  A product whose slices
  * would need more than GEMM_NOALLOC_WORKSPACE_BYTES of partial tiles is

@@ -55,6 +55,8 @@ WORKLOADS = {
     "decode_small_m": Workload("decode_small_m", tuple(
         Shape(m, n, k) for m in (1, 8, 32, 64, 128)
         for n, k in ((8192, 8192), (28672, 8192), (8192, 28672))), F16, F16, "uniform", 5),
+    "fp8": Workload("fp8", (Shape(4096, 4096, 4096), Shape(8192, 8192, 8192)),
+                    E4M3, BF16, "uniform", 6),
     "sweep_bf16_f32": Workload("sweep_bf16_f32", (
         Shape(1024, 1024, 1024), Shape(2048, 2048, 2048), Shape(8192, 8192, 8192),
         Shape(16384, 16384, 16384), Shape(4095, 4097, 4096), Shape(1000, 3000, 2000)),

@@ -61,9 +61,17 @@ def ulp_of(x: np.ndarray, dtype_out: int) -> np.ndarray:
     return np.exp2(np.floor(np.log2(mag)) - frac)
 
 
+def take_rows(t: torch.Tensor, idx) -> torch.Tensor:
+    """t[idx] for a list of row indices; FP8 tensors are gathered through their bytes
+    (torch has no CPU index kernel for them)."""
+    if t.element_size() == 1 and t.is_floating_point():
+        return t.view(torch.uint8)[list(idx)].view(t.dtype)
+    return t[list(idx)]
+
+
 def sigma_of(A, B, rows=None) -> np.ndarray:
     """sqrt(sum_k (a_ik b_jk)^2) for the selected rows (float64 on the host)."""
-    a = A if rows is None else A[rows]
+    a = A if rows is None else take_rows(A, rows)
     a2 = a.to(torch.float64).square()
     out = torch.empty(a.shape[0], B.shape[0], dtype=torch.float64)
     for j0 in range(0, B.shape[0], 8192):
@@ -144,7 +152,7 @@ def oracle_check(got_bits, A, B, dtype_in, dtype_out, rows=None, cols=None, what
     want, c64 = oracle.gemm_select(A, B, rows, cols, dtype_in, dtype_out, want_f64=True)
     if exact:
         return check(got_bits, want, dtype_out, exact=True, what=what)
-    Bs = B if cols is None else B[list(cols)]
+    Bs = B if cols is None else take_rows(B, cols)
     sig = sigma_of(A, Bs, rows)
     return check(got_bits, want, dtype_out, what=what, c64=c64, sigma=sig, K=A.shape[1])
 
