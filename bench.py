@@ -269,9 +269,11 @@ def fp8_peak(peaks):
 
 
 def measure_fp8(g, dev, stream, peaks, iters=20):
-    """Secondary figures: the FP8 (E4M3 -> bf16) square shapes, tensor-bound.  Each is
-    timed like the main workload, one launch per event pair after an L2 flush.  Their
-    parity is covered by the full-size tests; here only time is taken."""
+    """Secondary figures: the FP8 (E4M3 -> bf16) square shapes, tensor-bound, with a
+    per-tensor scale pair and with blockwise scales (per row of A and 128 of K; per
+    128 x 128 of B).  Each is timed like the main workload, one launch per event pair
+    after an L2 flush.  Their parity is covered by the full-size tests; here only time
+    is taken."""
     wl = si.WORKLOADS["fp8"]
     peak = fp8_peak(peaks)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -287,21 +289,32 @@ def measure_fp8(g, dev, stream, peaks, iters=20):
         def run(a, b, c):
             g.run(a, b, c, stream=stream)
 
-        for _ in range(3):
-            flush.fill_(0.5)
-            run(A, B, C)
-        torch.cuda.synchronize()
-        total, each = time_steps(run, [(A, B, C)], stream, iters, flush, per_step=True)
-        ms = total / iters
-        tf = rl.gemm_flops(s.M, s.N, s.K) / (ms * 1e-3) / 1e12
-        out[f"{s.M}x{s.N}x{s.K}"] = {"us": round(ms * 1e3, 2),
-                                     "median_us": round(1e3 * statistics.median(each), 2),
-                                     "TFLOP/s": round(tf, 1), "frac_of_peak": round(tf / peak, 4),
-                                     "peak": round(peak, 1),
-                                     "dtype_in": si.DTYPE_NAME[wl.dtype_in],
-                                     "dtype_out": si.DTYPE_NAME[wl.dtype_out],
-                                     "kernel": g.last_config()}
-        del A, B, C
+        # blockwise scales: one per row of A and 128 of K, one per 128 x 128 of B
+        nkb = -(-s.K // 128)
+        # (stored K-block-major, as the library takes them)
+        sfa = torch.exp2(torch.rand(nkb, s.M, generator=gen, device=dev) * 6 - 3)
+        sfb = torch.exp2(torch.rand(nkb, -(-s.N // 128), generator=gen, device=dev) * 6 - 3)
+
+        def run_bw(a, b, c):
+            g.run_blockwise(a, b, c, sfa, sfb, 1, stream=stream)
+
+        for name, fn in (("per_tensor", run), ("blockwise_1x128_128x128", run_bw)):
+            for _ in range(3):
+                flush.fill_(0.5)
+                fn(A, B, C)
+            torch.cuda.synchronize()
+            total, each = time_steps(fn, [(A, B, C)], stream, iters, flush, per_step=True)
+            ms = total / iters
+            tf = rl.gemm_flops(s.M, s.N, s.K) / (ms * 1e-3) / 1e12
+            key = f"{s.M}x{s.N}x{s.K}" + ("" if name == "per_tensor" else f" {name}")
+            out[key] = {"us": round(ms * 1e3, 2),
+                        "median_us": round(1e3 * statistics.median(each), 2),
+                        "TFLOP/s": round(tf, 1), "frac_of_peak": round(tf / peak, 4),
+                        "peak": round(peak, 1), "scales": name,
+                        "dtype_in": si.DTYPE_NAME[wl.dtype_in],
+                        "dtype_out": si.DTYPE_NAME[wl.dtype_out],
+                        "kernel": g.last_config()}
+        del A, B, C, sfa, sfb
     return out
 
 

@@ -15,7 +15,8 @@ STATUS_NAMES = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTE
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgemm.so")
 
 # Every function include/gemm.h declares (checked against the header by the tests).
-EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_epilogue", "gemm_run_host",
+EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_epilogue", "gemm_run_blockwise",
+           "gemm_run_host",
            "gemm_set_config",
            "gemm_last_config", "gemm_device_status", "gemm_set_wait_limit",
            "gemm_set_test_stall", "gemm_sm_count", "gemm_status_string", "gemm_run_noalloc")
@@ -37,6 +38,13 @@ class GemmEpilogue(ctypes.Structure):
     """gemm_epilogue_t: C = act(alpha * A . B^T + beta * C_prev + bias)."""
     _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
                 ("activation", ctypes.c_int32)]
+
+
+class GemmBlockScales(ctypes.Structure):
+    """gemm_block_scales_t: FP8 block scales, sfa per (block_m rows, 128 of K) of A and
+    sfb per (128 rows, 128 of K) of B."""
+    _fields_ = [("sfa", ctypes.c_void_p), ("sfb", ctypes.c_void_p), ("block_m", ctypes.c_int32),
+                ("block_n", ctypes.c_int32)]
 
 
 class GemmError(RuntimeError):
@@ -73,6 +81,8 @@ def lib():
     L.gemm_run_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i32, i32, vp]
     L.gemm_run_epilogue.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32,
                                     ctypes.POINTER(GemmEpilogue), vp]
+    L.gemm_run_blockwise.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32,
+                                     ctypes.POINTER(GemmBlockScales), vp]
     L.gemm_status_string.argtypes = [i32]
     L.gemm_status_string.restype = ctypes.c_char_p
     for name in EXPORTS:
@@ -185,6 +195,29 @@ class Gemm:
                                        torch_dtype_code(A.dtype), torch_dtype_code(C.dtype),
                                        ctypes.byref(epi), _stream_ptr(stream, A.device))
         _check(code, f"gemm_run_epilogue M={M} N={N} K={K}")
+        return C
+
+    def run_blockwise(self, A, B, C, sfa, sfb, block_m, block_n=128, stream=None):
+        """C = sum_kb sfa[kb, i // block_m] * sfb[kb, j // block_n] * (A @ B.T over the kb-th
+        128 columns of K), A and B FP8 CUDA tensors; sfa and sfb contiguous float32 CUDA
+        tensors stored K-block-major, ceil(K / 128) x ceil(M / block_m) and
+        ceil(K / 128) x ceil(N / block_n)."""
+        M, K = A.shape
+        N = B.shape[0]
+        nkb = -(-K // 128)
+        for t, rows, name in ((sfa, -(-M // max(block_m, 1)), "sfa"), (sfb, -(-N // max(block_n, 1)), "sfb")):
+            if not (t.is_cuda and t.dtype == torch_float32() and t.is_contiguous()
+                    and tuple(t.shape) == (nkb, rows)):
+                raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of {nkb} x {rows}")
+        if not (A.is_cuda and B.is_cuda and C.is_cuda and A.is_contiguous() and B.is_contiguous()
+                and C.is_contiguous() and B.shape[1] == K and tuple(C.shape) == (M, N)
+                and A.dtype == B.dtype):
+            raise ValueError("A (M,K), B (N,K), C (M,N): contiguous CUDA tensors, A and B of one dtype")
+        sc = GemmBlockScales(sfa.data_ptr(), sfb.data_ptr(), int(block_m), int(block_n))
+        code = lib().gemm_run_blockwise(self._h, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                                        torch_dtype_code(A.dtype), torch_dtype_code(C.dtype),
+                                        ctypes.byref(sc), _stream_ptr(stream, A.device))
+        _check(code, f"gemm_run_blockwise M={M} N={N} K={K}")
         return C
 
     def run_host(self, A, B, C, dtype_in, dtype_out, stream=None):

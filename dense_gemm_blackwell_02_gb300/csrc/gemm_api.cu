@@ -141,11 +141,14 @@ int resident_units(gemm_ctx* h, int cg, int bn, int stages, int out) {
 }
 
 // kb_elems: K elements per 128-byte K block (64 fp16/bf16, 128 FP8).
+// blockwise: one accumulation chain per K block (scaled in the general epilogue).
 gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int kb_elems,
-                     Choice* c) {
+                     bool blockwise, Choice* c) {
   const gemm_config_t& f = h->forced;
   // A CTA pair (256-row tiles, each CTA loading half of B) whenever M fills one.
-  c->variant = f.variant ? f.variant : (M > kBlockM ? 2 : 1);
+  // Blockwise scales hand every K block's accumulator to the epilogue: a CTA pair's
+  // cross-CTA hand-over made that 1.6x slower than one CTA per tile (measured, 4096^3).
+  c->variant = f.variant ? f.variant : (M > kBlockM && !blockwise ? 2 : 1);
   const int cg = c->variant;
   c->bn = f.block_n ? f.block_n : (N <= 128 ? 128 : 256);
   c->stages = f.stages ? f.stages : default_stages(cg, c->bn);
@@ -239,6 +242,10 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   c->group_m = f.group_m ? f.group_m : 16;
   // a chain of K 4096 elements: 64 blocks of fp16/bf16, 32 of FP8
   c->chain_kb = f.chain_kblocks ? f.chain_kblocks : kChainKBlocks * kBlockK / kb_elems;
+  if (blockwise) {
+    if (f.chain_kblocks > 1 || f.epilogue == 2) return GEMM_ERR_UNSUPPORTED;
+    c->chain_kb = 1;
+  }
   // Prefetching B into L2 ahead of the ring: off unless asked for (measured on the
   // M = 256 decode shapes and the square ones it did not help).
   c->prefetch_kb = f.prefetch_kblocks > 0 ? f.prefetch_kblocks : 0;
@@ -252,7 +259,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
     longest = c->kb_per_split;
   const bool one_ok = longest <= c->chain_kb;
   if (f.epilogue == 2 && !one_ok) return GEMM_ERR_UNSUPPORTED;
-  c->one_chain = f.epilogue == 1 ? false : one_ok;
+  c->one_chain = (f.epilogue == 1 || blockwise) ? false : one_ok;
   if (c->units > INT32_MAX || c->tiles * cg * 8 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   return GEMM_OK;
 }
@@ -376,8 +383,15 @@ namespace {
 
 gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M,
                        int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
-                       const gemm_epilogue_t* epi, gemm_stream_t stream_) {
+                       const gemm_epilogue_t* epi, const gemm_block_scales_t* bs,
+                       gemm_stream_t stream_) {
   if (!h) return GEMM_ERR_INVALID_ARG;
+  if (bs) {
+    if (!bs->sfa || !bs->sfb || bs->block_m < 1) return GEMM_ERR_INVALID_ARG;
+    if (!is_fp8(dtype_in) || bs->block_n != 128 ||
+        reinterpret_cast<uintptr_t>(bs->sfa) % 4 || reinterpret_cast<uintptr_t>(bs->sfb) % 4)
+      return GEMM_ERR_UNSUPPORTED;
+  }
   const bool fused = epi && (epi->alpha != 1.0f || epi->beta != 0.0f || epi->bias ||
                              epi->activation != GEMM_ACT_NONE);
   if (epi && epi->activation != GEMM_ACT_NONE && epi->activation != GEMM_ACT_RELU)
@@ -406,7 +420,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   const int out = out_kind(dtype_out);
   Choice ch;
   const bool fp8 = is_fp8(dtype_in);
-  gemm_status_t st = choose(h, M, N, K, out, fp8 ? 2 * kBlockK : kBlockK, &ch);
+  gemm_status_t st = choose(h, M, N, K, out, fp8 ? 2 * kBlockK : kBlockK, bs != nullptr, &ch);
   if (st != GEMM_OK) return st;
 
   LaunchSpec s;
@@ -418,8 +432,8 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   s.grid = ch.grid;
   s.one_chain = ch.one_chain;
   // FP8 kernels always carry the epilogue: the per-tensor scales arrive as alpha
-  s.fused = fused || fp8;
-  s.kind = fp8 ? 1 : 0;
+  s.fused = (fused || fp8) && !bs;
+  s.kind = bs ? 2 : fp8 ? 1 : 0;
   s.stream = stream;
   const bool c_tma = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0;
   // A single one-CTA row tile of M < 128 rows loads A as an M-row box: the stage's
@@ -468,6 +482,13 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
     p.idesc = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn, dtype_in == GEMM_BF16);
     p.idesc_half = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn / 2, dtype_in == GEMM_BF16);
   }
+  if (bs) {
+    p.sfa = bs->sfa;
+    p.sfb = bs->sfb;
+    p.sf_bm = bs->block_m;
+    p.sf_lda = (int32_t)ceil_div(M, (int64_t)bs->block_m);
+    p.sf_ldb = (int32_t)ceil_div(N, (int64_t)128);
+  }
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
   p.test_stall = h->test_stall;
@@ -492,14 +513,22 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
 gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M,
                        int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
                        gemm_stream_t stream) {
-  return run_impl(h, A, B, C, M, N, K, dtype_in, dtype_out, nullptr, stream);
+  return run_impl(h, A, B, C, M, N, K, dtype_in, dtype_out, nullptr, nullptr, stream);
+}
+
+gemm_status_t gemm_run_blockwise(gemm_handle_t h, const void* A, const void* B, void* C,
+                                 int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in,
+                                 gemm_dtype_t dtype_out, const gemm_block_scales_t* scales,
+                                 gemm_stream_t stream) {
+  if (!scales) return GEMM_ERR_INVALID_ARG;
+  return run_impl(h, A, B, C, M, N, K, dtype_in, dtype_out, nullptr, scales, stream);
 }
 
 gemm_status_t gemm_run_epilogue(gemm_handle_t h, const void* A, const void* B, void* C,
                                 int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in,
                                 gemm_dtype_t dtype_out, const gemm_epilogue_t* epilogue,
                                 gemm_stream_t stream) {
-  return run_impl(h, A, B, C, M, N, K, dtype_in, dtype_out, epilogue, stream);
+  return run_impl(h, A, B, C, M, N, K, dtype_in, dtype_out, epilogue, nullptr, stream);
 }
 
 gemm_status_t gemm_device_status(gemm_handle_t h, gemm_stream_t stream_, uint32_t* detail) {

@@ -436,7 +436,8 @@ struct Layout {
 // registers this frees go to loads in flight in the split-K hand-over.
 // FUSED: the fused epilogue (alpha, beta * C, bias, ReLU) is compiled in; kept out of
 // the plain kernels, whose general epilogue it would push into more register spills.
-// KIND 0: fp16/bf16 operands (tcgen05.mma kind::f16); KIND 1: FP8 operands (kind::f8f6f4).
+// KIND 0: fp16/bf16 operands (tcgen05.mma kind::f16); KIND 1: FP8 operands (kind::f8f6f4);
+// KIND 2: FP8 operands with blockwise scales (one chain per K block, general epilogue).
 // Either way a K block is one 128-byte row of the swizzle atom: 64 or 128 elements.
 template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN, bool FUSED, int KIND = 0>
 __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
@@ -446,6 +447,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
   using L = Layout<CTA_GROUP, BN, STAGES>;
   static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
   static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "CTA_GROUP must be 1 or 2");
+  static_assert(KIND != 2 || !ONE_CHAIN, "blockwise scales need the general epilogue");
   constexpr uint32_t kTmemCols = 2 * BN;       // two accumulator slots
   constexpr int kHalf = BN / 2;                // columns per epilogue warp
   constexpr int kPieces = kHalf / 32;          // tcgen05.ld x32 pieces per warp
@@ -761,6 +763,31 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       const bool active = w.half < 0 || h == 0;
       float acc[kHalf];
       const int32_t nchains = chains_of(w, p.chain_kb);
+      // Blockwise FP8 scales (KIND 2; "CUTLASS Deep Dive: From CuTe Layouts to Blackwell
+      // tcgen05", Part 6, FP8 and Blockwise Scaling): every chain is one 128-element K
+      // block kb; its TMEM value is scaled by sfa(row block, kb) * sfb(column block, kb)
+      // before it is added.  This thread's row and this warp's columns (one 128-column
+      // block: a warp's columns never cross one) fix the two scale columns; the scales
+      // are stored K-block-major, so a warp's 32 rows read one line per K block.  The
+      // scales of chains ch + 1 and ch + 2 are in flight while chain ch is consumed.
+      const float* sfa_col = nullptr;
+      const float* sfb_col = nullptr;
+      float s0a = 0.0f, s0b = 0.0f, s1a = 0.0f, s1b = 0.0f;  // next two chains, by parity
+      if constexpr (KIND == 2) {
+        const int32_t m = min(w.m_blk * kRowsTile + (int32_t)(rank * kBlockM + q * 32u + lane),
+                              p.M - 1);
+        const int32_t n = min(w.n_blk * BN + (w.half >= 0 ? w.half : (int32_t)h) * kHalf, p.N - 1);
+        sfa_col = p.sfa + m / p.sf_bm;
+        sfb_col = p.sfb + (n >> 7);
+        if (active) {
+          s0a = sfa_col[(size_t)w.kb0 * p.sf_lda];
+          s0b = sfb_col[(size_t)w.kb0 * p.sf_ldb];
+          if (nchains > 1) {
+            s1a = sfa_col[(size_t)(w.kb0 + 1) * p.sf_lda];
+            s1b = sfb_col[(size_t)(w.kb0 + 1) * p.sf_ldb];
+          }
+        }
+      }
       for (int32_t ch = 0; ch < nchains; ++ch) {
         const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
         // One lane polls; the warp follows its verdict, so tcgen05.ld below is always
@@ -776,17 +803,47 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * BN + h * kHalf;
         if (active) {
+          if constexpr (KIND == 2) {
+            const bool odd = (ch & 1) != 0;
+            const float sc = odd ? s1a * s1b : s0a * s0b;
+            if (ch + 2 < nchains) {
+              const size_t kb = (size_t)(w.kb0 + ch + 2);
+              const float na = sfa_col[kb * p.sf_lda], nb = sfb_col[kb * p.sf_ldb];
+              if (odd) {
+                s1a = na;
+                s1b = nb;
+              } else {
+                s0a = na;
+                s0b = nb;
+              }
+            }
 #pragma unroll
-          for (int pc = 0; pc < kPieces; ++pc) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + 32u * pc, r);
-            tmem_ld_wait(r);
-            if (ch == 0) {
+            for (int pc = 0; pc < kPieces; ++pc) {
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(taddr + 32u * pc, r);
+              tmem_ld_wait(r);
+              if (ch == 0) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) acc[32 * pc + j] = __uint_as_float(r[j]);
-            } else {
+                for (int j = 0; j < 32; ++j) acc[32 * pc + j] = __uint_as_float(r[j]) * sc;
+              } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) acc[32 * pc + j] += __uint_as_float(r[j]);
+                for (int j = 0; j < 32; ++j)
+                  acc[32 * pc + j] = fmaf(__uint_as_float(r[j]), sc, acc[32 * pc + j]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int pc = 0; pc < kPieces; ++pc) {
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(taddr + 32u * pc, r);
+              tmem_ld_wait(r);
+              if (ch == 0) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[32 * pc + j] = __uint_as_float(r[j]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[32 * pc + j] += __uint_as_float(r[j]);
+              }
             }
           }
         }

@@ -61,6 +61,11 @@ struct GemmParams {
   int32_t relu;            // act: ReLU when 1, the identity when 0
   float alpha, beta;
   const float* bias;       // N values (16-byte aligned), or nullptr
+  // blockwise FP8 scales (KIND 2), K-block-major: sfa[kb * sf_lda + m / sf_bm],
+  // sfb[kb * sf_ldb + n / 128]
+  const float* sfa;
+  const float* sfb;
+  int32_t sf_bm, sf_lda, sf_ldb;
   uint64_t wait_limit_ns;  // bound on every mbarrier wait
   int32_t test_stall;      // 1: the MMA issuer waits on a barrier that never completes
 };

@@ -172,6 +172,41 @@ gemm_status_t gemm_run_epilogue(gemm_handle_t h, const void* A, const void* B, v
                                 gemm_stream_t stream);
 
 /*
+ * Blockwise-scaled FP8 product ("CUTLASS Deep Dive: From CuTe Layouts to Blackwell
+ * tcgen05", Part 6: FP8 and Blockwise Scaling: one scale per (block_m, block_k) tile
+ * of A and one per (block_n, block_k) tile of B, applied during accumulation):
+ *     C[i][j] = sum_kb sfa[i / block_m][kb] * sfb[j / 128][kb]
+ *                      * sum_{k = 128 kb}^{min(K, 128 kb + 128) - 1} A[i][k] B[j][k]
+ *   sfa       the ceil(M / block_m) x ceil(K / 128) binary32 scales of A, stored
+ *             K-block-major: scale (r, kb) at sfa[kb * ceil(M / block_m) + r]; device
+ *             memory, 4-byte aligned; the caller owns it
+ *   sfb       the ceil(N / 128) x ceil(K / 128) scales of B, likewise: scale (c, kb) at
+ *             sfb[kb * ceil(N / 128) + c]
+ *   block_m   rows of A per scale, >= 1 (1: one scale per row and K block; 128: per
+ *             128 x 128 tile)
+ *   block_n   rows of B per scale: 128
+ * Each 128-element K block is accumulated in its own Tensor-Memory chain, then scaled
+ * and added in fp32 registers (fma(P_kb, sfa * sfb, acc)).  Automatically the
+ * one-CTA kernel (variant 1) is used.
+ */
+typedef struct {
+  const float* sfa;
+  const float* sfb;
+  int32_t block_m;
+  int32_t block_n;
+} gemm_block_scales_t;
+
+/* gemm_run with FP8 operands and block scales.  Errors as gemm_run, and:
+ *   GEMM_ERR_INVALID_ARG   scales NULL, block_m < 1;
+ *   GEMM_ERR_UNSUPPORTED   dtype_in not FP8, block_n != 128, a scale pointer not
+ *                          4-byte aligned, or a forced configuration with
+ *                          chain_kblocks > 1 or the single-chain epilogue. */
+gemm_status_t gemm_run_blockwise(gemm_handle_t h, const void* A, const void* B, void* C,
+                                 int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in,
+                                 gemm_dtype_t dtype_out, const gemm_block_scales_t* scales,
+                                 gemm_stream_t stream);
+
+/*
  * The same product with HOST buffers: copies A and B to device staging buffers
  * owned by the handle, runs the GEMM and copies C back, all on `stream`, then
  * synchronises `stream` and reports kernel timeouts like gemm_device_status.
