@@ -136,6 +136,15 @@ def gemm(A, B, dtype_in: int, dtype_out: int, nthreads: int = 0, lib=None) -> np
     return C
 
 
+def gemm_grouped(problems, dtype_in: int, dtype_out: int, nthreads: int = 0, lib=None) -> list:
+    """A group of independent products ("CUTLASS Deep Dive: From CuTe Layouts to
+    Blackwell tcgen05", Part 6, Grouped GEMM: many GEMMs of different shapes, as the
+    experts of a Mixture-of-Experts layer need): for each (A_g, B_g) in `problems`,
+    C_g = A_g . B_g^T by the definition above (its own M_g, N_g, K_g; K_g = 0 gives
+    zeros).  Returns the list of C_g bit patterns, in order."""
+    return [gemm(A, B, dtype_in, dtype_out, nthreads=nthreads, lib=lib) for A, B in problems]
+
+
 def gemm_select(A, B, rows, cols, dtype_in: int, dtype_out: int, nthreads: int = 0,
                 want_f64: bool = False):
     """Outputs C[rows][:, cols] (len(rows) x len(cols)); rows/cols None = all.
