@@ -318,6 +318,49 @@ def measure_fp8(g, dev, stream, peaks, iters=20):
     return out
 
 
+def measure_grouped(g, dev, stream, peaks, iters=10):
+    """Secondary figures: the MoE projections as grouped GEMMs (one launch per layer),
+    timed like the main workload (one launch per event pair after an L2 flush).  The
+    roofline is the larger of the tensor time (2 sum M_e N K FLOPs at the measured peak)
+    and the HBM time (every A_e, B_e and C_e moved once, at the measured copy
+    bandwidth).  Parity is covered by the full-size tests."""
+    tpeak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for name, wl in si.MOE_WORKLOADS.items():
+        counts = si.moe_counts(wl.experts, wl.rows, wl.seed)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(wl.seed)
+        td_in, td_out = si.TORCH_DTYPE[wl.dtype_in], si.TORCH_DTYPE[wl.dtype_out]
+        probs = [((torch.rand(m, wl.K, generator=gen, device=dev) * 2 - 1).to(td_in),
+                  (torch.rand(wl.N, wl.K, generator=gen, device=dev) * 2 - 1).to(td_in),
+                  torch.empty(m, wl.N, dtype=td_out, device=dev)) for m in counts]
+
+        def run(*_):
+            g.run_grouped(probs, stream=stream)
+
+        for _ in range(3):
+            flush.fill_(0.5)
+            run()
+        torch.cuda.synchronize()
+        total, each = time_steps(run, [()], stream, iters, flush, per_step=True)
+        us = 1e3 * total / iters
+        flops = sum(2.0 * m * wl.N * wl.K for m in counts)
+        nbytes = sum(2.0 * (m * wl.K + wl.N * wl.K + m * wl.N) for m in counts)
+        tf, gbs = flops / us / 1e6, nbytes / us / 1e3
+        t_tensor, t_hbm = flops / (tpeak * 1e6), nbytes / (hbm * 1e3)
+        bound = "tensor" if t_tensor >= t_hbm else "hbm"
+        out[name] = {"experts": wl.experts, "rows": wl.rows, "N": wl.N, "K": wl.K,
+                     "rows_per_expert_min_max": [min(counts), max(counts)],
+                     "us": round(us, 2), "median_us": round(1e3 * statistics.median(each), 2),
+                     "TFLOP/s": round(tf, 1), "GB/s": round(gbs, 1), "bound": bound,
+                     "frac_of_roofline": round(max(t_tensor, t_hbm) / us, 4),
+                     "kernel": g.last_config()}
+        del probs
+    return out
+
+
 def run_reference(args):
     """The oracle as it stands, timed on the host cores on bounded samples."""
     ws, rank, _ = dist_env()
@@ -441,6 +484,7 @@ def run_ours(args):
     decode_small = (measure_decode(g, dev, stream, peaks, name="decode_small_m")
                     if args.decode > 1 else None)
     fp8 = measure_fp8(g, dev, stream, peaks) if args.fp8 else None
+    grouped = measure_grouped(g, dev, stream, peaks) if args.grouped else None
     flops = rl.gemm_flops(M, N, K)
     ms_per_step = total_ms / args.steps
     value = replica_throughput(ws, flops, args.steps, total_ms)
@@ -521,6 +565,8 @@ def run_ours(args):
             line["decode_small_m"] = decode_small
         if fp8 is not None:
             line["fp8"] = fp8
+        if grouped is not None:
+            line["grouped"] = grouped
         print(json.dumps(line))
     g.close()
     if ws > 1:
@@ -542,6 +588,8 @@ def main():
                          "2 adds the M=1..128 decode shapes")
     ap.add_argument("--fp8", type=int, default=1,
                     help="also time the FP8 (E4M3 -> bf16) square shapes into the line")
+    ap.add_argument("--grouped", type=int, default=1,
+                    help="also time the MoE projections as grouped GEMMs into the line")
     ap.add_argument("--l2", default="flush", choices=["rotate", "flush"],
                     help="main workload: flush L2 before each separately timed step (default), "
                          "or cycle operand copies larger than L2 with launches back to back")

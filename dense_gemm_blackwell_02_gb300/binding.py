@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgemm.so"
 
 # Every function include/gemm.h declares (checked against the header by the tests).
 EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_epilogue", "gemm_run_blockwise",
-           "gemm_run_host",
+           "gemm_run_grouped", "gemm_run_host",
            "gemm_set_config",
            "gemm_last_config", "gemm_device_status", "gemm_set_wait_limit",
            "gemm_set_test_stall", "gemm_sm_count", "gemm_status_string", "gemm_run_noalloc")
@@ -45,6 +45,12 @@ class GemmBlockScales(ctypes.Structure):
     sfb per (128 rows, 128 of K) of B."""
     _fields_ = [("sfa", ctypes.c_void_p), ("sfb", ctypes.c_void_p), ("block_m", ctypes.c_int32),
                 ("block_n", ctypes.c_int32)]
+
+
+class GemmProblem(ctypes.Structure):
+    """gemm_problem_t: one problem of a grouped launch, C = A . B^T."""
+    _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("C", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
 class GemmError(RuntimeError):
@@ -83,6 +89,7 @@ def lib():
                                     ctypes.POINTER(GemmEpilogue), vp]
     L.gemm_run_blockwise.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32,
                                      ctypes.POINTER(GemmBlockScales), vp]
+    L.gemm_run_grouped.argtypes = [vp, ctypes.POINTER(GemmProblem), i32, i32, i32, vp]
     L.gemm_status_string.argtypes = [i32]
     L.gemm_status_string.restype = ctypes.c_char_p
     for name in EXPORTS:
@@ -219,6 +226,28 @@ class Gemm:
                                         ctypes.byref(sc), _stream_ptr(stream, A.device))
         _check(code, f"gemm_run_blockwise M={M} N={N} K={K}")
         return C
+
+    def run_grouped(self, problems, stream=None):
+        """C_g = A_g @ B_g.T for every (A_g, B_g, C_g) in `problems`, in one launch: CUDA
+        tensors, contiguous, one input dtype and one output dtype for all."""
+        if not problems:
+            return
+        din, dout = problems[0][0].dtype, problems[0][2].dtype
+        arr = (GemmProblem * len(problems))()
+        for i, (A, B, C) in enumerate(problems):
+            M, K = A.shape
+            N = B.shape[0]
+            if not (A.is_cuda and B.is_cuda and C.is_cuda and A.is_contiguous()
+                    and B.is_contiguous() and C.is_contiguous() and B.shape[1] == K
+                    and tuple(C.shape) == (M, N) and A.dtype == din and B.dtype == din
+                    and C.dtype == dout):
+                raise ValueError(f"problem {i}: A (M,K), B (N,K), C (M,N) contiguous CUDA tensors "
+                                 "with the group's dtypes")
+            arr[i] = GemmProblem(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K)
+        code = lib().gemm_run_grouped(self._h, arr, len(problems), torch_dtype_code(din),
+                                      torch_dtype_code(dout),
+                                      _stream_ptr(stream, problems[0][0].device))
+        _check(code, f"gemm_run_grouped count={len(problems)}")
 
     def run_host(self, A, B, C, dtype_in, dtype_out, stream=None):
         """gemm_run_host on CPU tensors (pinned for asynchronous copies)."""

@@ -10,6 +10,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "gemm.h"
 #include "launch.h"
@@ -56,6 +57,16 @@ struct gemm_ctx {
   TmapEntry cache[kTmapCacheSize] = {};
   int cache_next = 0;
   int resident[2][2][3] = {};  // [cta_group-1][bn==256][out]: co-resident units (0: unknown)
+  // grouped launches: a ring of problem tables (pinned host copy, device copy and the
+  // event that marks the host copy reusable)
+  static constexpr int kGroupRing = 4;
+  GroupDesc* h_groups[kGroupRing] = {};
+  GroupDesc* d_groups[kGroupRing] = {};
+  int32_t* h_gstart[kGroupRing] = {};
+  int32_t* d_gstart[kGroupRing] = {};
+  cudaEvent_t group_done[kGroupRing] = {};
+  size_t group_cap[kGroupRing] = {};
+  int group_next = 0;
 };
 
 namespace {
@@ -334,6 +345,13 @@ gemm_status_t gemm_destroy(gemm_handle_t h) {
   if (h->d_ctr) cudaFree(h->d_ctr);
   for (auto* p : h->d_stage)
     if (p) cudaFree(p);
+  for (int i = 0; i < gemm_ctx::kGroupRing; ++i) {
+    if (h->h_groups[i]) cudaFreeHost(h->h_groups[i]);
+    if (h->h_gstart[i]) cudaFreeHost(h->h_gstart[i]);
+    if (h->d_groups[i]) cudaFree(h->d_groups[i]);
+    if (h->d_gstart[i]) cudaFree(h->d_gstart[i]);
+    if (h->group_done[i]) cudaEventDestroy(h->group_done[i]);
+  }
   delete h;
   return GEMM_OK;
 }
@@ -529,6 +547,158 @@ gemm_status_t gemm_run_epilogue(gemm_handle_t h, const void* A, const void* B, v
                                 gemm_dtype_t dtype_out, const gemm_epilogue_t* epilogue,
                                 gemm_stream_t stream) {
   return run_impl(h, A, B, C, M, N, K, dtype_in, dtype_out, epilogue, nullptr, stream);
+}
+
+gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, int32_t count,
+                               gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                               gemm_stream_t stream_) {
+  if (!h || count < 0 || (count > 0 && !problems)) return GEMM_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype_in) || !valid_dtype(dtype_out)) return GEMM_ERR_INVALID_ARG;
+  if (dtype_in != GEMM_F16 && dtype_in != GEMM_BF16) return GEMM_ERR_UNSUPPORTED;
+  if (is_fp8(dtype_out)) return GEMM_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const size_t osz = out_size(dtype_out);
+  // Validate everything before queueing anything.
+  for (int32_t g = 0; g < count; ++g) {
+    const gemm_problem_t& q = problems[g];
+    if (q.M < 0 || q.N < 0 || q.K < 0) return GEMM_ERR_INVALID_ARG;
+    if (q.M == 0 || q.N == 0) continue;
+    if (!q.C || (q.K > 0 && (!q.A || !q.B))) return GEMM_ERR_INVALID_ARG;
+    if (q.M > INT32_MAX || q.N > INT32_MAX || q.K > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(q.C) % osz) return GEMM_ERR_UNSUPPORTED;
+    if (q.K > 0 && (q.K % 8 || reinterpret_cast<uintptr_t>(q.A) % 16 ||
+                    reinterpret_cast<uintptr_t>(q.B) % 16))
+      return GEMM_ERR_UNSUPPORTED;
+  }
+  const gemm_config_t& f = h->forced;
+  if ((f.splits != 0 && f.splits != 1) || f.epilogue == 2) return GEMM_ERR_UNSUPPORTED;
+  // Problems with K = 0 are the empty sum; the rest go into one launch.
+  std::vector<int32_t> live;
+  int64_t padded[3] = {0, 0, 0};  // MACs with M padded to 128 and to 256 rows
+  bool narrow = true;
+  for (int32_t g = 0; g < count; ++g) {
+    const gemm_problem_t& q = problems[g];
+    if (q.M == 0 || q.N == 0) continue;
+    if (q.K == 0) {
+      if (cudaMemsetAsync(q.C, 0, (size_t)q.M * (size_t)q.N * osz, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+      continue;
+    }
+    live.push_back(g);
+    for (int v = 1; v <= 2; ++v)
+      padded[v] += ceil_div(q.M, (int64_t)kBlockM * v) * kBlockM * v * q.N / 64 * q.K;
+    narrow = narrow && q.N <= 128;
+  }
+  if (live.empty()) return GEMM_OK;
+  const int G = (int)live.size();
+  // A CTA pair when padding every problem's M to 256 rows costs at most 10% more work
+  // than padding to 128; 128-column tiles when every N fits one.
+  const int cg = f.variant ? f.variant : (padded[2] * 10 <= padded[1] * 11 ? 2 : 1);
+  const int bn = f.block_n ? f.block_n : (narrow ? 128 : 256);
+  const int stages = f.stages ? f.stages : default_stages(cg, bn);
+  if (!kernel_supported(cg, bn, stages)) return GEMM_ERR_INVALID_ARG;
+
+  // The next table of the ring: its host copy is free once its last upload is done.
+  const int slot = h->group_next;
+  h->group_next = (slot + 1) % gemm_ctx::kGroupRing;
+  if (h->group_done[slot]) {
+    if (cudaEventSynchronize(h->group_done[slot]) != cudaSuccess) return GEMM_ERR_CUDA;
+  } else if (cudaEventCreateWithFlags(&h->group_done[slot], cudaEventDisableTiming) != cudaSuccess) {
+    return GEMM_ERR_CUDA;
+  }
+  if ((size_t)G > h->group_cap[slot]) {
+    if (h->h_groups[slot]) cudaFreeHost(h->h_groups[slot]);
+    if (h->h_gstart[slot]) cudaFreeHost(h->h_gstart[slot]);
+    if (h->d_groups[slot]) cudaFree(h->d_groups[slot]);
+    if (h->d_gstart[slot]) cudaFree(h->d_gstart[slot]);
+    h->h_groups[slot] = nullptr;
+    h->h_gstart[slot] = nullptr;
+    h->d_groups[slot] = nullptr;
+    h->d_gstart[slot] = nullptr;
+    h->group_cap[slot] = 0;
+    const size_t cap = std::max<size_t>(G, 16);
+    if (cudaMallocHost(&h->h_groups[slot], cap * sizeof(GroupDesc)) != cudaSuccess ||
+        cudaMallocHost(&h->h_gstart[slot], (cap + 1) * sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc(&h->d_groups[slot], cap * sizeof(GroupDesc)) != cudaSuccess ||
+        cudaMalloc(&h->d_gstart[slot], (cap + 1) * sizeof(int32_t)) != cudaSuccess)
+      return GEMM_ERR_OOM;
+    h->group_cap[slot] = cap;
+  }
+  GroupDesc* desc = h->h_groups[slot];
+  int32_t* start = h->h_gstart[slot];
+  int64_t units = 0;
+  for (int i = 0; i < G; ++i) {
+    const gemm_problem_t& q = problems[live[i]];
+    GroupDesc& d = desc[i];
+    std::memset(&d, 0, sizeof(d));
+    const int a_box = (cg == 1 && q.M < kBlockM) ? (int)q.M : kBlockM;
+    const bool c_tma =
+        reinterpret_cast<uintptr_t>(q.C) % 16 == 0 && ((size_t)q.N * osz) % 16 == 0;
+    if (!make_map(h, q.A, q.M, q.K, dtype_in, a_box, &d.tmA) ||
+        !make_map(h, q.B, q.N, q.K, dtype_in, bn / cg, &d.tmB) ||
+        (c_tma && !make_map(h, q.C, q.M, q.N, dtype_out, 32, &d.tmC)))
+      return GEMM_ERR_CUDA;
+    d.C = q.C;
+    d.M = (int32_t)q.M;
+    d.N = (int32_t)q.N;
+    d.K = (int32_t)q.K;
+    d.k_blocks = (int32_t)ceil_div(q.K, (int64_t)kBlockK);
+    d.num_m = (int32_t)ceil_div(q.M, (int64_t)kBlockM * cg);
+    d.num_n = (int32_t)ceil_div(q.N, (int64_t)bn);
+    d.a_tx_short = (uint32_t)(kBlockM - a_box) * 128u;
+    d.vec_store = c_tma ? 1 : 0;
+    d.tma_store = c_tma ? 1 : 0;
+    start[i] = (int32_t)units;
+    units += (int64_t)d.num_m * d.num_n;
+    if (units > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  }
+  start[G] = (int32_t)units;
+  if (cudaMemcpyAsync(h->d_groups[slot], desc, G * sizeof(GroupDesc), cudaMemcpyHostToDevice,
+                      stream) != cudaSuccess ||
+      cudaMemcpyAsync(h->d_gstart[slot], start, (G + 1) * sizeof(int32_t),
+                      cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaEventRecord(h->group_done[slot], stream) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+
+  int64_t slots = resident_units(h, cg, bn, stages, out_kind(dtype_out));
+  if (f.max_ctas) slots = std::min<int64_t>(slots, std::max<int64_t>(f.max_ctas / cg, 1));
+  LaunchSpec s;
+  std::memset(&s, 0, sizeof(s));
+  s.cta_group = cg;
+  s.bn = bn;
+  s.stages = stages;
+  s.out = out_kind(dtype_out);
+  s.grid = (int)(std::min<int64_t>(units, slots) * cg);
+  s.grouped = true;
+  s.stream = stream;
+  // the parameter maps are not read by a grouped kernel; they hold the first problem's
+  s.tmA = desc[0].tmA;
+  s.tmB = desc[0].tmB;
+  s.tmB2 = desc[0].tmB;
+  s.tmC = desc[0].tmC;
+  GemmParams& p = s.p;
+  p.C = desc[0].C;
+  p.M = desc[0].M;
+  p.N = desc[0].N;
+  p.K = desc[0].K;
+  p.tiles = (int32_t)units;
+  p.units = (int32_t)units;
+  p.dp_tiles = (int32_t)units;
+  p.splits = 1;
+  p.kb_per_split = 0;
+  p.group_m = f.group_m ? f.group_m : 16;
+  p.chain_kb = f.chain_kblocks ? f.chain_kblocks : kChainKBlocks;
+  p.idesc = idesc_f16_kmajor(kBlockM * cg, bn, dtype_in == GEMM_BF16);
+  p.idesc_half = p.idesc;
+  p.groups = h->d_groups[slot];
+  p.group_start = h->d_gstart[slot];
+  p.num_groups = G;
+  p.status = h->d_status;
+  p.wait_limit_ns = h->wait_limit_ns;
+  p.test_stall = h->test_stall;
+  if (launch_gemm(s) != cudaSuccess) return GEMM_ERR_CUDA;
+  h->last = gemm_config_t{cg, bn, 1, stages, p.group_m, s.grid, p.chain_kb, (int32_t)units, -1, 1};
+  return GEMM_OK;
 }
 
 gemm_status_t gemm_device_status(gemm_handle_t h, gemm_stream_t stream_, uint32_t* detail) {

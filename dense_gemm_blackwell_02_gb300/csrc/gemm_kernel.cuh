@@ -120,6 +120,7 @@ __device__ __forceinline__ void pause_ns(uint64_t ns) {
 struct Unit {
   int32_t tile, split, nsplit, m_blk, n_blk, kb0, kb1;
   int32_t half;  // -1: the whole BN columns; 0 / 1: that BN/2-column half of the tile
+  int32_t g;     // grouped launches: the problem this unit belongs to
 };
 
 // Work unit -> (tile, K slice or column half) -> (m block, n block).
@@ -219,15 +220,48 @@ static __device__ __noinline__ bool sk_next(Walker& k, int32_t first, const Gemm
   return true;
 }
 
+// Grouped launch ("CUTLASS Deep Dive: From CuTe Layouts to Blackwell tcgen05", Part 6,
+// Grouped GEMM: each tile pulls its problem index from the scheduler): unit u is tile
+// u - group_start[g] of the problem g whose range holds it (binary search over the
+// problems' first units), a whole tile with the problem's whole K, rasterised inside
+// the problem as tile_coords does.  Kept out of line like sk_next.
+static __device__ __noinline__ void decode_grouped(int32_t u, const GemmParams& p, Unit& w) {
+  int32_t lo = 0, hi = p.num_groups - 1;
+  while (lo < hi) {
+    const int32_t mid = (lo + hi + 1) >> 1;
+    if (p.group_start[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  const GroupDesc& gd = p.groups[lo];
+  w.g = lo;
+  w.tile = u;
+  w.half = -1;
+  w.split = 0;
+  w.nsplit = 1;
+  w.kb0 = 0;
+  w.kb1 = gd.k_blocks;
+  const int32_t t = u - p.group_start[lo];
+  const int32_t group = p.group_m * gd.num_n;
+  const int32_t gi = t / group;
+  const int32_t first_m = gi * p.group_m;
+  const int32_t gm = min(gd.num_m - first_m, p.group_m);
+  const int32_t r = t - gi * group;
+  w.m_blk = first_m + r % gm;
+  w.n_blk = r / gm;
+}
+
 // Only two 32-bit counters live across a unit; the stream-K range is recomputed from
 // the worker's index on each call.
+template <bool GROUPED>
 __device__ __forceinline__ bool walker_next(Walker& k, int32_t first, int32_t stride,
                                             const GemmParams& p, Unit& w) {
   if (k.u < p.units) {
-    w = decode_unit(k.u, p);
+    if constexpr (GROUPED) decode_grouped(k.u, p, w);
+    else w = decode_unit(k.u, p);
     k.u += stride;
     return true;
   }
+  if constexpr (GROUPED) return false;
   if (first >= p.sk_workers) return false;
   return sk_next(k, first, p, w);
 }
@@ -321,10 +355,15 @@ __device__ __forceinline__ void fuse_piece(const GemmParams& p, int32_t m, int32
   }
 }
 
-// Direct stores of 32 consecutive values of one row (used when C cannot take TMA).
+// Direct stores of 32 consecutive values of one row (used when C cannot take TMA) into
+// the M x N row-major C; vec_store: C's rows are 16-byte aligned.
 template <int OUT>
-__device__ __forceinline__ void store_row_direct(const GemmParams& p, int32_t m, int32_t n0,
-                                                 const float* v) {
+__device__ __forceinline__ void store_row_to(void* C, int32_t M, int32_t N, int32_t vec_store,
+                                             int32_t m, int32_t n0, const float* v) {
+  struct {
+    void* C;
+    int32_t M, N, vec_store;
+  } p{C, M, N, vec_store};
   if (m >= p.M) return;
   if constexpr (OUT == kOutF32) {
     float* dst = reinterpret_cast<float*>(p.C) + (size_t)m * p.N + n0;
@@ -353,6 +392,12 @@ __device__ __forceinline__ void store_row_direct(const GemmParams& p, int32_t m,
         if (n0 + j < p.N) dst[j] = (uint16_t)(packed[j >> 1] >> ((j & 1) * 16));
     }
   }
+}
+
+template <int OUT>
+__device__ __forceinline__ void store_row_direct(const GemmParams& p, int32_t m, int32_t n0,
+                                                 const float* v) {
+  store_row_to<OUT>(p.C, p.M, p.N, p.vec_store, m, n0, v);
 }
 
 // One 32-column piece of a single-chain unit's output, for the warp's rows: the TMEM
@@ -439,7 +484,10 @@ struct Layout {
 // KIND 0: fp16/bf16 operands (tcgen05.mma kind::f16); KIND 1: FP8 operands (kind::f8f6f4);
 // KIND 2: FP8 operands with blockwise scales (one chain per K block, general epilogue).
 // Either way a K block is one 128-byte row of the swizzle atom: 64 or 128 elements.
-template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN, bool FUSED, int KIND = 0>
+// GROUPED: a grouped launch (p.groups): per-problem tensor maps, shapes and C; whole
+// tiles only, general epilogue.
+template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN, bool FUSED, int KIND = 0,
+          bool GROUPED = false>
 __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
@@ -448,6 +496,8 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
   static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
   static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "CTA_GROUP must be 1 or 2");
   static_assert(KIND != 2 || !ONE_CHAIN, "blockwise scales need the general epilogue");
+  static_assert(!GROUPED || (!ONE_CHAIN && !FUSED && KIND == 0),
+                "grouped launches use the plain general epilogue");
   constexpr uint32_t kTmemCols = 2 * BN;       // two accumulator slots
   constexpr int kHalf = BN / 2;                // columns per epilogue warp
   constexpr int kPieces = kHalf / 32;          // tcgen05.ld x32 pieces per warp
@@ -495,10 +545,12 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    if (p.half_tail) tma_prefetch_desc(&tmB2);
-    if (p.tma_store) tma_prefetch_desc(&tmC);
+    if constexpr (!GROUPED) {  // a grouped launch's maps live in global memory
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      if (p.half_tail) tma_prefetch_desc(&tmB2);
+      if (p.tma_store) tma_prefetch_desc(&tmC);
+    }
   }
   if (warp == 1) {
     tmem_alloc<CTA_GROUP>(smem_addr(tmem_slot), kTmemCols);
@@ -525,7 +577,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     bool ok = true;
     Walker walk{first_unit, 0};
     Unit w;
-    while (ok && walker_next(walk, first_unit, unit_stride, p, w)) {
+    while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
       const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
       // a half-tile unit loads half the B rows (through the half-height map tmB2)
       const bool half = w.half >= 0;
@@ -533,7 +585,17 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
                             (half ? w.half * (BN / 2) + (int32_t)rank * (L::kRowsB / 2)
                                   : (int32_t)rank * L::kRowsB);
       const CUtensorMap* mapB = half ? &tmB2 : &tmB;
-      const uint32_t tx = (half ? L::kTxBytesHalf : L::kTxBytes) - p.a_tx_short;
+      const CUtensorMap* mapA = &tmA;
+      uint32_t tx = (half ? L::kTxBytesHalf : L::kTxBytes) - p.a_tx_short;
+      if constexpr (GROUPED) {
+        // the problem's own maps, written by the host before the launch
+        const GroupDesc* gd = p.groups + w.g;
+        mapA = &gd->tmA;
+        mapB = &gd->tmB;
+        tx = L::kTxBytes - gd->a_tx_short;
+        fence_tensormap_acquire(mapA);
+        fence_tensormap_acquire(mapB);
+      }
       // Streaming B from DRAM (decode shapes): keep more requests in flight than the
       // shared-memory ring holds by prefetching B into L2 prefetch_kb k-blocks ahead
       // ("A Blackwell GEMM by Hand in CuTe DSL", section 8: TMA prefetch).
@@ -550,14 +612,14 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         if constexpr (CTA_GROUP == 1) {
           mbar_arrive_expect_tx_elect(full_bar(stage), tx);
           tma_load_2d_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row, full_bar(stage));
-          tma_load_2d_elect(sA + stage * L::kABytes, &tmA, kb * kKbElems, a_row, full_bar(stage));
+          tma_load_2d_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row, full_bar(stage));
         } else {
           // Both CTAs' copies complete on the leader's full barrier; the leader arms it
           // with the bytes of the pair.
           const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
           if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), tx);
           tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row, leader_full);
-          tma_load_2d_pair_elect(sA + stage * L::kABytes, &tmA, kb * kKbElems, a_row, leader_full);
+          tma_load_2d_pair_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row, leader_full);
         }
         armed |= 1u << stage;
         armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -593,7 +655,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       if (p.test_stall) ok = warp_wait(drain_bar, 0, ctl, kSiteTestStall);
       Walker walk{first_unit, 0};
       Unit w;
-      while (ok && walker_next(walk, first_unit, unit_stride, p, w)) {
+      while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
         const uint32_t idesc = w.half >= 0 ? p.idesc_half : p.idesc;
         for (int32_t c0 = w.kb0; c0 < w.kb1 && ok; c0 += p.chain_kb) {
           const int32_t c1 = min(c0 + p.chain_kb, w.kb1);
@@ -649,7 +711,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       constexpr size_t kBlocksPerSlice = (size_t)CTA_GROUP * 8;  // (rank, quarter, half)
       constexpr size_t kSliceStride = kBlocksPerSlice * kBlockFloats;
       const size_t my_block = ((size_t)rank * 4 + q) * 2 + h;
-      while (ok && walker_next(walk, first_unit, unit_stride, p, w)) {
+      while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
         // in a half-tile unit the h = 1 warps only take part in the slot hand-over, and
         // so do warps whose 32 rows all lie at or past M (no partial, no store)
         const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
@@ -757,7 +819,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         ++iter;
       }
     } else {
-    while (ok && walker_next(walk, first_unit, unit_stride, p, w)) {
+    while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
       // In a half-tile unit the accumulator holds BN/2 columns: the h = 0 warps own
       // them, the h = 1 warps only take part in the slot hand-over.
       const bool active = w.half < 0 || h == 0;
@@ -937,7 +999,13 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
 #pragma unroll
         for (int pc = 0; pc < kPieces; ++pc) fuse_piece<OUT>(p, m, n_half + 32 * pc, acc + 32 * pc);
       }
-      if (p.tma_store) {
+      // this unit's output: the launch's C, or in a grouped launch its problem's
+      const GroupDesc* gd = nullptr;
+      if constexpr (GROUPED) gd = p.groups + w.g;
+      const bool out_tma = GROUPED ? gd->tma_store != 0 : p.tma_store != 0;
+      const int32_t out_m = GROUPED ? gd->M : p.M, out_n = GROUPED ? gd->N : p.N;
+      const CUtensorMap* out_map = GROUPED ? &gd->tmC : &tmC;
+      if (out_tma) {
         // Each 128-byte row of a staging box is written in the 128-byte swizzled order
         // (16-byte chunk j of row r at chunk j ^ (r % 8)) that the C tensor map's
         // CU_TENSOR_MAP_SWIZZLE_128B expects ("A Blackwell GEMM by Hand in CuTe DSL",
@@ -967,21 +1035,26 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
           __syncwarp();
           const int32_t box_n = n_half + bx * kBoxCols, box_m = m0 + (int32_t)(q * 32u);
           // a box wholly outside C (ragged last tiles) is not stored at all
-          if (lane == 0 && box_n < p.N && box_m < p.M) {
-            tma_store_2d(&tmC, staging, box_n, box_m);
+          if (lane == 0 && box_n < out_n && box_m < out_m) {
+            if constexpr (GROUPED) fence_tensormap_acquire(out_map);
+            tma_store_2d(out_map, staging, box_n, box_m);
             bulk_commit_group();
           }
         }
       } else {
         const int32_t m = m0 + (int32_t)row;
 #pragma unroll
-        for (int pc = 0; pc < kPieces; ++pc)
-          store_row_direct<OUT>(p, m, n_half + 32 * pc, acc + 32 * pc);
+        for (int pc = 0; pc < kPieces; ++pc) {
+          if constexpr (GROUPED)
+            store_row_to<OUT>(gd->C, gd->M, gd->N, gd->vec_store, m, n_half + 32 * pc, acc + 32 * pc);
+          else
+            store_row_direct<OUT>(p, m, n_half + 32 * pc, acc + 32 * pc);
+        }
       }
     }
     }  // general epilogue
     // Every TMA store of this warp must be complete before the CTA exits.
-    if (p.tma_store && lane == 0) bulk_wait_group<0>();
+    if ((GROUPED || p.tma_store) && lane == 0) bulk_wait_group<0>();
     __syncwarp();
   }
 

@@ -26,6 +26,12 @@ int max_resident_units(int cg, int bn, int stages, int out) {
 }
 
 cudaError_t launch_gemm(const LaunchSpec& s) {
+  if (s.grouped) {
+    if (s.kind != 0 || s.fused || s.one_chain) return cudaErrorInvalidValue;
+    if (s.cta_group == 1) return launch_cg1_grouped(s);
+    if (s.cta_group == 2) return launch_cg2_grouped(s);
+    return cudaErrorInvalidValue;
+  }
   if (s.kind == 2) {
     if (s.fused || s.one_chain) return cudaErrorInvalidValue;
     if (s.cta_group == 1) return launch_cg1_fp8bw(s);

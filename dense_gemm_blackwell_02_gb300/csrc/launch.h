@@ -18,6 +18,7 @@ struct LaunchSpec {
   bool fused;      // the fused epilogue (p.fused) is compiled in
   int kind;        // 0: fp16/bf16 operands (kind::f16); 1: FP8 (kind::f8f6f4, always fused);
                    // 2: FP8 with blockwise scales (general epilogue, not fused)
+  bool grouped;    // a grouped launch: p.groups holds the problems (kind 0, general epilogue)
   CUtensorMap tmA; // A: box {128 bytes of K, 128 (or M < 128) rows}
   CUtensorMap tmB; // B: box {128 bytes of K, bn / cta_group}
   CUtensorMap tmB2; // B: box {128 bytes of K, bn / cta_group / 2} (half-tile units; else tmB)
@@ -54,6 +55,9 @@ cudaError_t launch_cg2_one_fp8(const LaunchSpec& s);
 // ... and FP8 with blockwise scales (kernels_cg*_fp8bw.cu)
 cudaError_t launch_cg1_fp8bw(const LaunchSpec& s);
 cudaError_t launch_cg2_fp8bw(const LaunchSpec& s);
+// ... and grouped launches (kernels_cg*_grouped.cu)
+cudaError_t launch_cg1_grouped(const LaunchSpec& s);
+cudaError_t launch_cg2_grouped(const LaunchSpec& s);
 int resident_cg1(int bn, int stages, int out);
 int resident_cg2(int bn, int stages, int out);
 

@@ -1,6 +1,8 @@
 // Kernel parameter block and device status codes shared by the kernels and the
 // host dispatcher (internal; the public interface is include/gemm.h).
 #pragma once
+#include <cuda.h>
+
 #include <cstdint>
 
 namespace gb300 {
@@ -28,6 +30,22 @@ enum WaitSite : uint32_t {
   kSiteAccFull = 4,   // epilogue waiting for a finished accumulator
   kSiteTestStall = 5, // deliberate wait on a barrier nothing arrives on (test only)
   kSiteDrain = 6,     // teardown: outstanding copies / MMAs
+};
+
+// One problem of a grouped launch ("CUTLASS Deep Dive: From CuTe Layouts to Blackwell
+// tcgen05", Part 6, Grouped GEMM: each tile fetches its problem's pointers and tensor
+// maps).  Written by the host into device memory; 64-byte aligned for the maps.
+struct alignas(64) GroupDesc {
+  CUtensorMap tmA;        // A_g: box {128 bytes of K, 128 (or M_g < 128) rows}
+  CUtensorMap tmB;        // B_g: box {128 bytes of K, BN / CTA_GROUP rows}
+  CUtensorMap tmC;        // C_g: box {128 bytes of columns, 32 rows} (when tma_store)
+  void* C;
+  int32_t M, N, K;
+  int32_t k_blocks;       // ceil(K_g / K block)
+  int32_t num_m, num_n;   // tiles of this problem along M and N
+  uint32_t a_tx_short;    // as GemmParams::a_tx_short, for this problem
+  int32_t vec_store;      // 16-byte vector stores of C_g are aligned
+  int32_t tma_store;      // C_g is written through tmC
 };
 
 struct GemmParams {
@@ -66,6 +84,11 @@ struct GemmParams {
   const float* sfa;
   const float* sfb;
   int32_t sf_bm, sf_lda, sf_ldb;
+  // grouped launches (GROUPED kernels): problem g owns units [group_start[g],
+  // group_start[g + 1]); units = group_start[num_groups]
+  const GroupDesc* groups;
+  const int32_t* group_start;
+  int32_t num_groups;
   uint64_t wait_limit_ns;  // bound on every mbarrier wait
   int32_t test_stall;      // 1: the MMA issuer waits on a barrier that never completes
 };

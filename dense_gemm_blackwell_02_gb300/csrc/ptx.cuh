@@ -148,6 +148,15 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// A tensor map in global memory written before the launch (a grouped launch's problem
+// table): order this thread's later uses of it through the tensor-map proxy after that
+// write (PTX ISA, fence.proxy.tensormap::generic, acquire at system scope for a host
+// write).
+__device__ __forceinline__ void fence_tensormap_acquire(const void* tmap) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.sys [%0], 128;"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // 2-D tiled load global -> this CTA's shared memory, completing on `bar` (this CTA).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
                                             uint32_t bar) {

@@ -207,6 +207,37 @@ gemm_status_t gemm_run_blockwise(gemm_handle_t h, const void* A, const void* B, 
                                  gemm_stream_t stream);
 
 /*
+ * Grouped GEMM ("CUTLASS Deep Dive: From CuTe Layouts to Blackwell tcgen05", Part 6,
+ * Grouped GEMM: the many differently shaped GEMMs of a Mixture-of-Experts layer in one
+ * launch, each tile fetching its problem's pointers and tensor maps).  For every
+ * problem g: C_g = A_g . B_g^T, with A_g (M_g x K_g), B_g (N_g x K_g) and C_g
+ * (M_g x N_g) laid out, aligned and owned as for gemm_run.
+ *   problems   `count` descriptions in HOST memory, read before the call returns
+ *   dtype_in   GEMM_F16 or GEMM_BF16 (shared by every problem; FP8 is refused)
+ *   dtype_out  GEMM_F16, GEMM_BF16 or GEMM_F32
+ * Problems with M_g == 0 or N_g == 0 are skipped; K_g == 0 writes C_g = 0.  One
+ * kernel computes the rest: whole tiles of every problem, 128 x block_n (one CTA) or
+ * 256 x block_n (a CTA pair; chosen when padding every M_g to 256 rows costs at most
+ * 10% more work), handed to the persistent CTAs in problem order.  gemm_set_config's
+ * variant, block_n, stages, group_m, max_ctas and chain_kblocks apply; a forced
+ * splits other than 1, or the single-chain epilogue, gives GEMM_ERR_UNSUPPORTED.
+ * The problem table goes to the device with cudaMemcpyAsync on `stream` from a ring
+ * of four pinned buffers owned by the handle; a fifth call waits for the first's copy.
+ * Calls on one handle share its buffers: order them on one stream.
+ * Errors as gemm_run, checked for every problem before anything is queued.
+ */
+typedef struct {
+  const void* A;
+  const void* B;
+  void* C;
+  int64_t M, N, K;
+} gemm_problem_t;
+
+gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, int32_t count,
+                               gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                               gemm_stream_t stream);
+
+/*
  * The same product with HOST buffers: copies A and B to device staging buffers
  * owned by the handle, runs the GEMM and copies C back, all on `stream`, then
  * synchronises `stream` and reports kernel timeouts like gemm_device_status.

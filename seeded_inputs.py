@@ -93,6 +93,42 @@ def make_small_int_operands(M: int, N: int, K: int, dtype_in: int, seed: int = 0
     return A, B
 
 
+@dataclass(frozen=True)
+class MoeWorkload:
+    """A Mixture-of-Experts projection as a grouped GEMM: `rows` routed token rows
+    spread over `experts` experts, each expert a K x N weight (B_e, N x K) applied to
+    its rows (A_e, M_e x K)."""
+    name: str
+    experts: int
+    rows: int
+    N: int
+    K: int
+    dtype_in: int
+    dtype_out: int
+    seed: int
+
+
+# Expert counts and widths of two MoE layer families (8 large experts, 64 small ones),
+# sizes only; the token-to-expert assignment is drawn by moe_counts.
+MOE_WORKLOADS = {
+    "moe_8x14336x4096": MoeWorkload("moe_8x14336x4096", 8, 8192, 14336, 4096, BF16, BF16, 20),
+    "moe_64x2048x7168": MoeWorkload("moe_64x2048x7168", 64, 8192, 2048, 7168, BF16, BF16, 21),
+    "moe_64x7168x2048": MoeWorkload("moe_64x7168x2048", 64, 8192, 7168, 2048, BF16, BF16, 22),
+}
+
+
+def moe_counts(experts: int, rows: int, seed: int) -> list:
+    """Rows per expert: expert loads drawn from a flat Dirichlet (normalised iid
+    exponentials), then `rows` tokens assigned by a multinomial draw -- an imbalanced
+    routing, some experts possibly empty."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    w = -torch.log(torch.rand(experts, generator=g).clamp_min(1e-12))
+    w = w / w.sum()
+    return torch.multinomial(w, rows, replacement=True, generator=g).bincount(
+        minlength=experts).tolist()
+
+
 def make_block_scales(rows: int, cols: int, seed: int = 0, lo: float = -3.0, hi: float = 3.0):
     """A rows x cols float32 array of positive scales 2**u, u iid uniform in [lo, hi)
     (one per (row block, k block), as blockwise-scaled operands carry)."""

@@ -64,3 +64,38 @@ def test_freivalds_catches_a_skipped_tile(g):
     Cc[256:384, 512:768] = 0
     with pytest.raises(AssertionError):
         parity.freivalds(A, B, Cc, si.F16)
+
+
+MOE = sorted(si.MOE_WORKLOADS)
+
+
+@pytest.mark.parametrize("name", MOE)
+def test_grouped_moe_full_size(g, name):
+    """The grouped MoE workloads the bench times, in the configuration the library
+    chooses: per expert, seeded rows (first and last included) and two columns against
+    the oracle."""
+    wl = si.MOE_WORKLOADS[name]
+    counts = si.moe_counts(wl.experts, wl.rows, wl.seed)
+    probs = []
+    for e, m in enumerate(counts):
+        A, B = si.make_operands(m, wl.N, wl.K, wl.dtype_in, "uniform", wl.seed * 1000 + e)
+        probs.append((A, B))
+    dev = [(A.cuda(), B.cuda(), torch.empty(A.shape[0], wl.N, dtype=si.TORCH_DTYPE[wl.dtype_out],
+                                            device="cuda")) for A, B in probs]
+    g.reset_config()
+    g.run_grouped(dev)
+    code, word = g.device_status()
+    assert code == 0, f"device status {code} ({word:#x})"
+    cfg = g.last_config()
+    for e, ((A, B), (_, _, C)) in enumerate(zip(probs, dev)):
+        M = A.shape[0]
+        if M == 0:
+            continue
+        Cc = C.cpu()
+        rows = si.sample_indices(M, 3, seed=e, must=(0, -1))
+        cols = si.sample_indices(wl.N, 2, seed=e + 7, must=(-1,))
+        what = f"{name} expert {e} ({M} rows) {cfg}"
+        parity.oracle_check(parity.bits_of(Cc[rows]), A, B, wl.dtype_in, wl.dtype_out, rows=rows,
+                            what=what + " rows")
+        parity.oracle_check(parity.bits_of(Cc[:, cols].contiguous()), A, B, wl.dtype_in,
+                            wl.dtype_out, cols=cols, what=what + " cols")
