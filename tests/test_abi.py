@@ -51,6 +51,11 @@ def test_null_handle_is_rejected_without_touching_the_gpu(lib):
     assert lib.gemm_sm_count(None) == 0
     assert lib.gemm_destroy(None) == 0
     assert lib.gemm_create(None) == 1
+    # the wider entry points reject a NULL handle (or table) before any device work
+    assert lib.gemm_run_epilogue(None, None, None, None, 1, 1, 8, 0, 0, None, None) == 1
+    assert lib.gemm_run_blockwise(None, None, None, None, 1, 1, 16, 3, 0, None, None) == 1
+    assert lib.gemm_run_grouped(None, None, 0, 0, 0, None) == 1
+    assert lib.gemm_run_host(None, None, None, None, 1, 1, 8, 0, 0, None) == 1
 
 
 def test_library_is_built_for_sm_103a_only():
