@@ -133,6 +133,7 @@ size_t in_size(gemm_dtype_t d) { return is_fp8(d) ? 1 : 2; }
 struct Choice {
   int variant, bn, stages, splits, kb_per_split, group_m, grid, chain_kb, half_tail, prefetch_kb;
   bool one_chain;
+  bool kx2;  // the two K slices of a tile reduced inside a cluster (single chain)
   int64_t tiles, dp_tiles, units, k_blocks, num_m, num_n;
   int64_t sk_workers, ws_slots;
 };
@@ -153,8 +154,9 @@ int resident_units(gemm_ctx* h, int cg, int bn, int stages, int out) {
 
 // kb_elems: K elements per 128-byte K block (64 fp16/bf16, 128 FP8).
 // blockwise: one accumulation chain per K block (scaled in the general epilogue).
+// allow_kx: the cluster K split has kernels for this call (fp16/bf16, plain epilogue).
 gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int kb_elems,
-                     bool blockwise, Choice* c) {
+                     bool blockwise, bool allow_kx, Choice* c) {
   const gemm_config_t& f = h->forced;
   // A CTA pair (256-row tiles, each CTA loading half of B) whenever M fills one.
   // Blockwise scales hand every K block's accumulator to the epilogue: a CTA pair's
@@ -198,6 +200,36 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
       c->num_n = ceil_div(N, (int64_t)128);
       c->tiles = tiles128;
       slots = slots128;
+    }
+  }
+  // The cluster K split: when one of the two tile widths gives exactly two K slices of
+  // single chains for a wave, those slices meet in distributed shared memory rather than
+  // in the global workspace (measured, back to back: 256 x 4096 x 4096 16.7 us against
+  // 22.2 for four slices of 256-column tiles; 256 x 8192 x 8192 34.9 us against 36.5 for
+  // unsplit 128-column tiles; M <= 128, 8192 x 8192: 28-30 us against 30-32 for two
+  // slices through the workspace).  Unsplit 128-column tiles stay when K is short
+  // (256 x 8192 x 4096: 21.9 us against 23.2).
+  bool auto_kx = false;
+  if (allow_kx && !f.block_n && !f.splits && !f.stages && !f.epilogue && !f.chain_kblocks &&
+      c->k_blocks >= 8) {
+    const int chain = kChainKBlocks * kBlockK / kb_elems;
+    for (int bn : {128, 256}) {
+      const int st = default_stages(cg, bn);
+      int64_t sl = resident_units(h, cg, bn, st, out);
+      if (f.max_ctas) sl = std::min<int64_t>(sl, std::max<int64_t>(f.max_ctas / cg, 1));
+      const int64_t tl = c->num_m * ceil_div(N, (int64_t)bn);
+      if (tl * 2 > sl || std::min<int64_t>({sl / tl, c->k_blocks / 4, 32}) != 2) continue;
+      if (ceil_div(c->k_blocks, (int64_t)2) > chain) continue;
+      if (bn == 256 && c->bn == 128 && c->k_blocks < 128) continue;  // keep unsplit narrow tiles
+      const int clusters = max_resident_kx_clusters(cg, bn, st, out);
+      if (clusters <= 0 || tl > clusters) continue;
+      c->bn = bn;
+      c->stages = st;
+      c->num_n = ceil_div(N, (int64_t)bn);
+      c->tiles = tl;
+      slots = sl;
+      auto_kx = true;
+      break;
     }
   }
   int64_t s = 1, dp = c->tiles;
@@ -254,7 +286,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   // a chain of K 4096 elements: 64 blocks of fp16/bf16, 32 of FP8
   c->chain_kb = f.chain_kblocks ? f.chain_kblocks : kChainKBlocks * kBlockK / kb_elems;
   if (blockwise) {
-    if (f.chain_kblocks > 1 || f.epilogue == 2) return GEMM_ERR_UNSUPPORTED;
+    if (f.chain_kblocks > 1 || f.epilogue >= 2) return GEMM_ERR_UNSUPPORTED;
     c->chain_kb = 1;
   }
   // Prefetching B into L2 ahead of the ring: off unless asked for (measured on the
@@ -269,8 +301,25 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   else if (!c->half_tail && s > 1 && dp == 0)
     longest = c->kb_per_split;
   const bool one_ok = longest <= c->chain_kb;
-  if (f.epilogue == 2 && !one_ok) return GEMM_ERR_UNSUPPORTED;
+  if (f.epilogue >= 2 && !one_ok) return GEMM_ERR_UNSUPPORTED;
   c->one_chain = (f.epilogue == 1 || blockwise) ? false : one_ok;
+  // The cluster K split: every tile's two K slices run on the two CTA groups of one
+  // cluster of 2 * cg CTAs, each group one unit, and meet in distributed shared memory.
+  c->kx2 = false;
+  if (f.epilogue == 3 || auto_kx) {
+    bool valid = !blockwise && one_ok && !c->sk_workers && !c->half_tail && dp == 0 && s == 2 &&
+                 c->units <= slots;
+    if (valid) {
+      const int clusters = max_resident_kx_clusters(cg, c->bn, c->stages, out);
+      valid = clusters > 0 && c->tiles <= clusters;
+    }
+    if (valid) {
+      c->kx2 = true;
+      c->grid = (int)(c->units * cg);
+    } else if (f.epilogue == 3) {
+      return GEMM_ERR_UNSUPPORTED;
+    }
+  }
   if (c->units > INT32_MAX || c->tiles * cg * 8 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   return GEMM_OK;
 }
@@ -366,7 +415,7 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
   if (c.variant < 0 || c.variant > 2) return GEMM_ERR_INVALID_ARG;
   if (c.block_n != 0 && c.block_n != 128 && c.block_n != 256) return GEMM_ERR_INVALID_ARG;
   if (c.splits < -1 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
-      c.dp_tiles != 0 || c.prefetch_kblocks < -1 || c.epilogue < 0 || c.epilogue > 2)
+      c.dp_tiles != 0 || c.prefetch_kblocks < -1 || c.epilogue < 0 || c.epilogue > 3)
     return GEMM_ERR_INVALID_ARG;
   if (c.stages) {
     const int bn = c.block_n ? c.block_n : 256;
@@ -438,7 +487,8 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   const int out = out_kind(dtype_out);
   Choice ch;
   const bool fp8 = is_fp8(dtype_in);
-  gemm_status_t st = choose(h, M, N, K, out, fp8 ? 2 * kBlockK : kBlockK, bs != nullptr, &ch);
+  gemm_status_t st = choose(h, M, N, K, out, fp8 ? 2 * kBlockK : kBlockK, bs != nullptr,
+                            !fp8 && !fused && !bs, &ch);
   if (st != GEMM_OK) return st;
 
   LaunchSpec s;
@@ -449,6 +499,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   s.out = out;
   s.grid = ch.grid;
   s.one_chain = ch.one_chain;
+  s.kx2 = ch.kx2;
   // FP8 kernels always carry the epilogue: the per-tensor scales arrive as alpha
   s.fused = (fused || fp8) && !bs;
   s.kind = bs ? 2 : fp8 ? 1 : 0;
@@ -510,7 +561,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
   p.test_stall = h->test_stall;
-  if ((ch.splits > 1 && !ch.half_tail) || ch.sk_workers) {
+  if (!ch.kx2 && ((ch.splits > 1 && !ch.half_tail) || ch.sk_workers)) {
     const size_t sliced = (size_t)(ch.tiles - ch.dp_tiles);
     const size_t ws = sliced * ch.ws_slots * kBlockM * ch.variant * ch.bn * sizeof(float);
     st = ensure_workspace(h, ws, sliced * ch.variant * 8);
@@ -522,7 +573,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   h->last = gemm_config_t{ch.variant,  ch.bn,   ch.sk_workers ? -(int32_t)ch.sk_workers : ch.splits,
                           ch.stages,
                           ch.group_m,  ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles,
-                          ch.prefetch_kb ? ch.prefetch_kb : -1, ch.one_chain ? 2 : 1};
+                          ch.prefetch_kb ? ch.prefetch_kb : -1, ch.kx2 ? 3 : ch.one_chain ? 2 : 1};
   return GEMM_OK;
 }
 
@@ -571,7 +622,7 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
       return GEMM_ERR_UNSUPPORTED;
   }
   const gemm_config_t& f = h->forced;
-  if ((f.splits != 0 && f.splits != 1) || f.epilogue == 2) return GEMM_ERR_UNSUPPORTED;
+  if ((f.splits != 0 && f.splits != 1) || f.epilogue >= 2) return GEMM_ERR_UNSUPPORTED;
   // Problems with K = 0 are the empty sum; the rest go into one launch.
   std::vector<int32_t> live;
   int64_t padded[3] = {0, 0, 0};  // MACs with M padded to 128 and to 256 rows

@@ -404,12 +404,27 @@ __device__ __forceinline__ void store_row_direct(const GemmParams& p, int32_t m,
 // accumulator at `taddr`, or for a split tile the slices summed in slice order (the
 // own slice's partial is the TMEM value itself; two slices add in either order to the
 // same bits).  `ws_lane` is this lane's start of the tile's workspace block, `col` the
-// piece's first column within the warp's block.
+// piece's first column within the warp's block.  KX: the other K slice of a cluster
+// split was received into shared memory at kx_lane (this lane's 16 bytes of the warp's
+// block, 512 bytes per 4 columns); 0 for the slice that sent it.
+template <bool KX = false>
 __device__ __forceinline__ void one_chain_piece(uint32_t taddr, const Unit& w, const float* ws_lane,
-                                                size_t slice_stride, int col, float (&v)[32]) {
+                                                size_t slice_stride, int col, float (&v)[32],
+                                                uint32_t kx_lane = 0) {
   uint32_t r[32];
   tmem_ld_32x32b_x32(taddr, r);
   tmem_ld_wait(r);
+  if constexpr (KX) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const uint4 x = ld_shared_v4(kx_lane + (uint32_t)((col + j) / 4) * 512u);
+      v[j] = __uint_as_float(r[j]) + __uint_as_float(x.x);
+      v[j + 1] = __uint_as_float(r[j + 1]) + __uint_as_float(x.y);
+      v[j + 2] = __uint_as_float(r[j + 2]) + __uint_as_float(x.z);
+      v[j + 3] = __uint_as_float(r[j + 3]) + __uint_as_float(x.w);
+    }
+    return;
+  }
   if (w.nsplit <= 1) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
@@ -463,8 +478,8 @@ struct Layout {
   static constexpr uint32_t kBOff = STAGES * kABytes;
   static constexpr uint32_t kCOff = kBOff + STAGES * kBBytes;
   static constexpr uint32_t kBarOff = kCOff + kEpiWarps * kStagingBytes;
-  // full[S], empty[S], acc_full[2], acc_empty[2], drain
-  static constexpr uint32_t kNumBars = 2 * STAGES + 5;
+  // full[S], empty[S], acc_full[2], acc_empty[2], drain, kx_ready[8], kx_go[8]
+  static constexpr uint32_t kNumBars = 2 * STAGES + 5 + 2 * kEpiWarps;
   static constexpr uint32_t kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
   static constexpr uint32_t kEnd = kAbortOff + 4;
@@ -486,8 +501,12 @@ struct Layout {
 // Either way a K block is one 128-byte row of the swizzle atom: 64 or 128 elements.
 // GROUPED: a grouped launch (p.groups): per-problem tensor maps, shapes and C; whole
 // tiles only, general epilogue.
+// KX2: every tile is two K slices computed by the two CTA groups (CTAs or pairs) of one
+// cluster of 2 * CTA_GROUP CTAs; the second slice hands its accumulator to the first
+// through distributed shared memory instead of the global workspace.  One unit per CTA
+// group, single-chain epilogue.
 template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN, bool FUSED, int KIND = 0,
-          bool GROUPED = false>
+          bool GROUPED = false, bool KX2 = false>
 __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
@@ -498,6 +517,8 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
   static_assert(KIND != 2 || !ONE_CHAIN, "blockwise scales need the general epilogue");
   static_assert(!GROUPED || (!ONE_CHAIN && !FUSED && KIND == 0),
                 "grouped launches use the plain general epilogue");
+  static_assert(!KX2 || (ONE_CHAIN && !FUSED && KIND == 0 && !GROUPED),
+                "the cluster K split uses the plain single-chain epilogue");
   constexpr uint32_t kTmemCols = 2 * BN;       // two accumulator slots
   constexpr int kHalf = BN / 2;                // columns per epilogue warp
   constexpr int kPieces = kHalf / 32;          // tcgen05.ld x32 pieces per warp
@@ -521,13 +542,21 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
   auto acc_full_bar = [&](uint32_t i) { return bar0 + 8u * (2 * STAGES + i); };
   auto acc_empty_bar = [&](uint32_t i) { return bar0 + 8u * (2 * STAGES + 2 + i); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto kx_ready_bar = [&](uint32_t w) { return bar0 + 8u * (2 * STAGES + 5 + w); };
+  auto kx_go_bar = [&](uint32_t w) { return bar0 + 8u * (2 * STAGES + 5 + L::kEpiWarps + w); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlotOff);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kAbortOff);
 
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
   const WaitCtl ctl{p.wait_limit_ns, p.status, abort_flag};
-  const uint32_t rank = CTA_GROUP == 2 ? cluster_ctarank() : 0u;
+  // Cluster rank; with KX2 the cluster holds two CTA groups (K slices 0 and 1), the
+  // group of slice s starting at rank s * CTA_GROUP.
+  const uint32_t crank = (CTA_GROUP == 2 || KX2) ? cluster_ctarank() : 0u;
+  const uint32_t rank = CTA_GROUP == 2 ? (KX2 ? (crank & 1u) : crank) : 0u;  // place in the pair
+  const uint32_t group_base = KX2 ? crank - rank : 0u;        // cluster rank of the group's leader
+  const uint32_t slice_k = KX2 ? crank / CTA_GROUP : 0u;
+  const uint16_t pair_mask = (uint16_t)(KX2 ? (0x3u << group_base) : 0x3u);
   const bool leader = rank == 0;
   const int32_t first_unit = (int32_t)(blockIdx.x / CTA_GROUP);
   const int32_t unit_stride = (int32_t)(gridDim.x / CTA_GROUP);
@@ -541,6 +570,12 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     for (uint32_t i = 0; i < 2; ++i) {
       mbar_init(acc_full_bar(i), 1);
       mbar_init(acc_empty_bar(i), L::kEpiWarps * CTA_GROUP);  // every epilogue warp of the pair
+    }
+    if constexpr (KX2) {
+      for (uint32_t w = 0; w < L::kEpiWarps; ++w) {
+        mbar_init(kx_ready_bar(w), 1);  // the receiving warp arms it; the sender's bytes complete it
+        mbar_init(kx_go_bar(w), 1);     // the receiving warp: its ring is free
+      }
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -557,7 +592,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     tmem_relinquish<CTA_GROUP>();
   }
   tc_fence_before();
-  if constexpr (CTA_GROUP == 2) cluster_sync();
+  if constexpr (CTA_GROUP == 2 || KX2) cluster_sync();
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
@@ -616,7 +651,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         } else {
           // Both CTAs' copies complete on the leader's full barrier; the leader arms it
           // with the bytes of the pair.
-          const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
+          const uint32_t leader_full = mapa_shared(full_bar(stage), group_base);
           if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), tx);
           tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row, leader_full);
           tma_load_2d_pair_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row, leader_full);
@@ -678,7 +713,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
             // CTAs) once they are done
             static_assert(kBlockK * 2 == 128, "umma_stage_elect covers 128 bytes of K");
             umma_stage_elect<CTA_GROUP, KIND>(d_tmem, da, db, idesc, kb > c0 ? 1u : 0u,
-                                              empty_bar(stage));
+                                              empty_bar(stage), pair_mask);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -686,7 +721,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
           }
           if (!ok) break;
           if constexpr (CTA_GROUP == 1) umma_commit_elect<1>(acc_full_bar(slot));
-          else umma_commit_pair_elect(acc_full_bar(slot), 0x3);
+          else umma_commit_pair_elect(acc_full_bar(slot), pair_mask);
           ++iter;
         }
       }
@@ -730,7 +765,46 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         const int32_t n_half = w.n_blk * BN + (w.half >= 0 ? w.half : (int32_t)h) * kHalf;
         bool emit = active;
         const float* ws_lane = nullptr;
-        if (active && w.nsplit > 1) {
+        uint32_t kx_lane = 0;
+        if constexpr (KX2) {
+          // The two K slices of the tile are the two CTA groups of this cluster.  Slice
+          // 0's ring is idle once its MMAs completed: it takes slice 1's partial there,
+          // warp by warp (this warp's 32 rows x BN/2 columns, 16 bytes per lane and 4
+          // columns), then adds it to its own and emits C.
+          constexpr uint32_t kKxWarpBytes = 32u * kHalf * 4u;
+          static_assert(L::kEpiWarps * kKxWarpBytes <= STAGES * L::kStageBytes,
+                        "the received partials must fit in the operand ring");
+          const uint32_t wbuf = base + L::kAOff + ew * kKxWarpBytes;
+          if (active && slice_k == 0) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx_cluster(kx_ready_bar(ew), kKxWarpBytes);
+              mbar_arrive_cluster(mapa_shared(kx_go_bar(ew), crank + CTA_GROUP));
+            }
+            if (!warp_wait(kx_ready_bar(ew), 0, ctl, kSiteKx)) {
+              ok = false;
+              break;
+            }
+            kx_lane = wbuf + lane * 16u;
+          } else if (active) {
+            if (!warp_wait(kx_go_bar(ew), 0, ctl, kSiteKx)) {
+              ok = false;
+              break;
+            }
+            const uint32_t dst = mapa_shared(wbuf + lane * 16u, crank - CTA_GROUP);
+            const uint32_t rbar = mapa_shared(kx_ready_bar(ew), crank - CTA_GROUP);
+#pragma unroll
+            for (int pc = 0; pc < kPieces; ++pc) {
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(taddr + 32u * pc, r);
+              tmem_ld_wait(r);
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                st_async_v4(dst + (uint32_t)((32 * pc + j) / 4) * 512u, rbar, r[j], r[j + 1],
+                            r[j + 2], r[j + 3]);
+            }
+            emit = false;
+          }
+        } else if (active && w.nsplit > 1) {
           // Split-K: this slice's partial goes to the workspace straight from TMEM
           // (the same block layout as the general epilogue); the last slice to arrive
           // emits C, summing the slices in slice order.
@@ -772,7 +846,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
               for (int pp = 0; pp < kPiecesPerBox; ++pp) {
                 float v[32];
                 const int pc = bx * kPiecesPerBox + pp;
-                one_chain_piece(taddr + 32u * pc, w, ws_lane, kSliceStride, 32 * pc, v);
+                one_chain_piece<KX2>(taddr + 32u * pc, w, ws_lane, kSliceStride, 32 * pc, v, kx_lane);
                 if constexpr (FUSED) fuse_piece<OUT>(p, m0 + (int32_t)row, n_half + 32 * pc, v);
                 // 16-byte chunks of the 128-byte row, in the 128-byte swizzled order
                 constexpr int kChunks = 8 / kPiecesPerBox;
@@ -803,7 +877,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
 #pragma unroll
             for (int pc = 0; pc < kPieces; ++pc) {
               float v[32];
-              one_chain_piece(taddr + 32u * pc, w, ws_lane, kSliceStride, 32 * pc, v);
+              one_chain_piece<KX2>(taddr + 32u * pc, w, ws_lane, kSliceStride, 32 * pc, v, kx_lane);
                 if constexpr (FUSED) fuse_piece<OUT>(p, m0 + (int32_t)row, n_half + 32 * pc, v);
               store_row_direct<OUT>(p, m, n_half + 32 * pc, v);
             }
@@ -814,7 +888,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         __syncwarp();
         if (lane == 0) {
           if constexpr (CTA_GROUP == 1) mbar_arrive(acc_empty_bar(slot));
-          else mbar_arrive_cluster(mapa_shared(acc_empty_bar(slot), 0));
+          else mbar_arrive_cluster(mapa_shared(acc_empty_bar(slot), group_base));
         }
         ++iter;
       }
@@ -915,7 +989,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         if (lane == 0) {
           // the leader's acc_empty, in shared::cluster space (its own, for rank 0)
           if constexpr (CTA_GROUP == 1) mbar_arrive(acc_empty_bar(slot));
-          else mbar_arrive_cluster(mapa_shared(acc_empty_bar(slot), 0));
+          else mbar_arrive_cluster(mapa_shared(acc_empty_bar(slot), group_base));
         }
         ++iter;
       }
@@ -1060,7 +1134,8 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
 
   // --------------------------------------------------------------- teardown --
   tc_fence_before();
-  if constexpr (CTA_GROUP == 2) cluster_sync();  // no CTA leaves while its pair may still signal it
+  // no CTA leaves while its pair (or the other K slice) may still signal it
+  if constexpr (CTA_GROUP == 2 || KX2) cluster_sync();
   else __syncthreads();
   if (warp == 1) {
     tc_fence_after();

@@ -25,7 +25,17 @@ int max_resident_units(int cg, int bn, int stages, int out) {
   return cg == 1 ? resident_cg1(bn, stages, out) : resident_cg2(bn, stages, out);
 }
 
+int max_resident_kx_clusters(int cg, int bn, int stages, int out) {
+  return cg == 1 ? resident_cg1_kx(bn, stages, out) : resident_cg2_kx(bn, stages, out);
+}
+
 cudaError_t launch_gemm(const LaunchSpec& s) {
+  if (s.kx2) {
+    if (s.kind != 0 || s.fused || !s.one_chain || s.grouped) return cudaErrorInvalidValue;
+    if (s.cta_group == 1) return launch_cg1_kx(s);
+    if (s.cta_group == 2) return launch_cg2_kx(s);
+    return cudaErrorInvalidValue;
+  }
   if (s.grouped) {
     if (s.kind != 0 || s.fused || s.one_chain) return cudaErrorInvalidValue;
     if (s.cta_group == 1) return launch_cg1_grouped(s);

@@ -6,14 +6,15 @@
 namespace gb300 {
 
 template <int CG, int BN, int STAGES, int OUT, bool ONE, bool FUSED, int KIND = 0,
-          bool GROUPED = false>
+          bool GROUPED = false, bool KX2 = false>
 cudaError_t launch_one(const LaunchSpec& s) {
-  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED, KIND, GROUPED>;
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED, KIND, GROUPED, KX2>;
+  constexpr unsigned kCluster = CG * (KX2 ? 2 : 1);
   using L = Layout<CG, BN, STAGES>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes);
   if (e != cudaSuccess) return e;
-  if (CG == 2) {
+  if (kCluster > 1) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
     if (e != cudaSuccess) return e;
   }
@@ -30,9 +31,9 @@ cudaError_t launch_one(const LaunchSpec& s) {
   attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[n].val.programmaticStreamSerializationAllowed = 1;
   ++n;
-  if (CG == 2) {
+  if (kCluster > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.x = kCluster;
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -42,20 +43,21 @@ cudaError_t launch_one(const LaunchSpec& s) {
   return cudaLaunchKernelEx(&cfg, kernel, s.tmA, s.tmB, s.tmB2, s.tmC, s.p);
 }
 
-template <int CG, int BN, int STAGES, int OUT>
+template <int CG, int BN, int STAGES, int OUT, bool KX2 = false>
 int resident_one() {
-  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, false, false>;
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, !KX2 ? false : true, false, 0, false, KX2>;
+  constexpr unsigned kCluster = CG * (KX2 ? 2 : 1);
   using L = Layout<CG, BN, STAGES>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            L::kDynamicBytes) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * CG, 1, 1);
+  cfg.gridDim = dim3(2 * kCluster, 1, 1);
   cfg.blockDim = dim3(L::kThreads, 1, 1);
   cfg.dynamicSmemBytes = L::kDynamicBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.x = kCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -68,22 +70,23 @@ int resident_one() {
   return n;
 }
 
-template <int CG, int BN, int STAGES, bool ONE, bool FUSED, int KIND = 0, bool GROUPED = false>
+template <int CG, int BN, int STAGES, bool ONE, bool FUSED, int KIND = 0, bool GROUPED = false,
+          bool KX2 = false>
 cudaError_t by_out(const LaunchSpec& s) {
   switch (s.out) {
-    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED, KIND, GROUPED>(s);
-    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED, KIND, GROUPED>(s);
-    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED, KIND, GROUPED>(s);
+    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED, KIND, GROUPED, KX2>(s);
+    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED, KIND, GROUPED, KX2>(s);
+    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED, KIND, GROUPED, KX2>(s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <int CG, int BN, int STAGES>
+template <int CG, int BN, int STAGES, bool KX2 = false>
 int resident_by_out(int out) {
   switch (out) {
-    case kOutF16: return resident_one<CG, BN, STAGES, kOutF16>();
-    case kOutBF16: return resident_one<CG, BN, STAGES, kOutBF16>();
-    case kOutF32: return resident_one<CG, BN, STAGES, kOutF32>();
+    case kOutF16: return resident_one<CG, BN, STAGES, kOutF16, KX2>();
+    case kOutBF16: return resident_one<CG, BN, STAGES, kOutBF16, KX2>();
+    case kOutF32: return resident_one<CG, BN, STAGES, kOutF32, KX2>();
     default: return 0;
   }
 }

@@ -30,6 +30,7 @@ enum WaitSite : uint32_t {
   kSiteAccFull = 4,   // epilogue waiting for a finished accumulator
   kSiteTestStall = 5, // deliberate wait on a barrier nothing arrives on (test only)
   kSiteDrain = 6,     // teardown: outstanding copies / MMAs
+  kSiteKx = 7,        // two-slice exchange through distributed shared memory
 };
 
 // One problem of a grouped launch ("CUTLASS Deep Dive: From CuTe Layouts to Blackwell

@@ -136,6 +136,26 @@ __device__ __forceinline__ void cluster_sync() {
                ::: "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory (both addresses
+// shared::cluster); the bytes complete_tx on `remote_bar`, an mbarrier of the CTA that
+// owns `remote_addr`, which its waiter arms with the expected count.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t remote_bar, uint32_t a,
+                                            uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(remote_addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+      : "memory");
+}
+
 // shared::cta address -> the same offset in CTA `rank` of the cluster (shared::cluster).
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -325,7 +345,7 @@ __device__ __forceinline__ void umma_f16_elect(uint32_t d_tmem, uint64_t a_desc,
                "@e_ tcgen05.mma.cta_group::" #CG ".kind::" KINDSTR " [%0], a3_, b3_, %3, 1;\n\t" \
                GB300_STAGE_COMMIT_##CG "\n\t}"                                               \
                ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate),         \
-               "r"(empty_bar), "h"((uint16_t)0x3)                                          \
+               "r"(empty_bar), "h"(cta_mask)                                               \
                : "memory")
 #define GB300_STAGE_COMMIT_1 \
   "@e_ tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];"
@@ -333,10 +353,12 @@ __device__ __forceinline__ void umma_f16_elect(uint32_t d_tmem, uint64_t a_desc,
   "@e_ tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64" \
   " [%5], %6;"
 
+// cta_mask: the pair's two CTAs in the cluster (0b11, or 0b1100 for the second pair of
+// a four-CTA cluster).
 template <int CTA_GROUP, int KIND = 0>
 __device__ __forceinline__ void umma_stage_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                  uint32_t idesc, uint32_t accumulate,
-                                                 uint32_t empty_bar) {
+                                                 uint32_t empty_bar, uint16_t cta_mask = 0x3) {
   if constexpr (CTA_GROUP == 1 && KIND == 0) GB300_STAGE_MMA(1, "f16");
   else if constexpr (CTA_GROUP == 2 && KIND == 0) GB300_STAGE_MMA(2, "f16");
   else if constexpr (CTA_GROUP == 1) GB300_STAGE_MMA(1, "f8f6f4");

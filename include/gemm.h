@@ -93,7 +93,12 @@ typedef enum {
  *   epilogue  1 = general (the accumulator is copied to registers, chains summed
  *             there); 2 = single-chain (streamed out of Tensor Memory in 32-column
  *             pieces), valid only when every work unit spans at most chain_kblocks K
- *             blocks (else gemm_run returns GEMM_ERR_UNSUPPORTED); 0 = 2 when valid.
+ *             blocks (else gemm_run returns GEMM_ERR_UNSUPPORTED); 0 = 2 when valid;
+ *             3 = single-chain with a tile's two K slices run by the two CTA groups of
+ *             one cluster (2 CTAs, or 4 for pairs) and summed through distributed
+ *             shared memory instead of the global workspace: valid only when the
+ *             shape is cut into exactly 2 K slices of single chains, with every tile
+ *             and every unit resident at once (else GEMM_ERR_UNSUPPORTED).
  *             gemm_last_config reports the one used.
  */
 typedef struct {

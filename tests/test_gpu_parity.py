@@ -349,3 +349,64 @@ def test_small_m_decode_takes_narrow_tiles(g, M):
     cfg = g.last_config()
     assert cfg["variant"] == 1 and cfg["block_n"] == 128, cfg
     assert cfg["splits"] == min(g.sm_count // 64, 1024 // 64 // 4), cfg
+
+
+@pytest.mark.parametrize("variant,block_n", [(1, 128), (1, 256), (2, 128), (2, 256)])
+@pytest.mark.parametrize("M,N,K,dtype_out", [(256, 1024, 4096, F16), (200, 1000, 2048, F32),
+                                             (96, 520, 1024, BF16), (256, 777, 4096, F16)])
+def test_cluster_k_split_matches_the_workspace_split(g, variant, block_n, M, N, K, dtype_out):
+    # the two K slices summed through distributed shared memory (epilogue 3) give the same
+    # bits as the same slices summed through the global workspace (epilogue 2)
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=97)
+    Ad, Bd = A.cuda(), B.cuda()
+    outs = {}
+    for epi in (2, 3):
+        C = torch.empty(M, N, dtype=TD[dtype_out], device="cuda")
+        g.set_config(variant=variant, block_n=block_n, splits=2, epilogue=epi)
+        try:
+            g.run(Ad, Bd, C)
+            torch.cuda.synchronize()
+            assert g.device_status()[0] == 0
+            used = g.last_config()
+        finally:
+            g.reset_config()
+        assert used["epilogue"] == epi and used["splits"] == 2, used
+        outs[epi] = C
+    assert torch.equal(outs[2], outs[3])
+    parity.oracle_check(parity.bits_of(outs[3]), A, B, F16, dtype_out, what=f"cluster split {used}")
+    Ai, Bi = si.make_small_int_operands(M, N, K, F16, seed=98)
+    C = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    g.set_config(variant=variant, block_n=block_n, splits=2, epilogue=3)
+    try:
+        g.run(Ai.cuda(), Bi.cuda(), C)
+        torch.cuda.synchronize()
+    finally:
+        g.reset_config()
+    parity.oracle_check(parity.bits_of(C), Ai, Bi, F16, F32, exact=True, what="cluster split ints")
+
+
+def test_cluster_k_split_rejections(g):
+    from dense_gemm_blackwell_02_gb300.binding import GemmError
+    A = torch.zeros(256, 4096, dtype=torch.float16, device="cuda")
+    C = torch.zeros(256, 1024, dtype=torch.float16, device="cuda")
+    B = torch.zeros(1024, 4096, dtype=torch.float16, device="cuda")
+    for cfg in ({"splits": 3, "epilogue": 3},                    # not two slices
+                {"splits": 2, "epilogue": 3, "chain_kblocks": 16}):   # slices of several chains
+        g.set_config(**cfg)
+        try:
+            with pytest.raises(GemmError) as e:
+                g.run(A, B, C)
+            assert e.value.code == 2
+        finally:
+            g.reset_config()
+    # more tiles than fit at once in clusters
+    A = torch.zeros(4096, 4096, dtype=torch.float16, device="cuda")
+    C = torch.zeros(4096, 4096, dtype=torch.float16, device="cuda")
+    B = torch.zeros(4096, 4096, dtype=torch.float16, device="cuda")
+    g.set_config(variant=2, splits=2, epilogue=3)
+    try:
+        with pytest.raises(GemmError) as e:
+            g.run(A, B, C)
+        assert e.value.code == 2
+    finally:
+        g.reset_config()
