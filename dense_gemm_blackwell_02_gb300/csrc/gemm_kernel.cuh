@@ -770,7 +770,9 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
           // The two K slices of the tile are the two CTA groups of this cluster.  Slice
           // 0's ring is idle once its MMAs completed: it takes slice 1's partial there,
           // warp by warp (this warp's 32 rows x BN/2 columns, 16 bytes per lane and 4
-          // columns), then adds it to its own and emits C.
+          // columns), then adds it to its own and emits C.  The sender's own ring holds
+          // the partial until the copy has read it: the teardown's cluster barrier waits
+          // for slice 0, which waits for the copy.
           constexpr uint32_t kKxWarpBytes = 32u * kHalf * 4u;
           static_assert(L::kEpiWarps * kKxWarpBytes <= STAGES * L::kStageBytes,
                         "the received partials must fit in the operand ring");
@@ -786,12 +788,8 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
             }
             kx_lane = wbuf + lane * 16u;
           } else if (active) {
-            if (!warp_wait(kx_go_bar(ew), 0, ctl, kSiteKx)) {
-              ok = false;
-              break;
-            }
-            const uint32_t dst = mapa_shared(wbuf + lane * 16u, crank - CTA_GROUP);
-            const uint32_t rbar = mapa_shared(kx_ready_bar(ew), crank - CTA_GROUP);
+            // Slice 1: stage the partial in this CTA's own ring (idle too), then, once
+            // slice 0 is ready for it, one bulk copy per warp into slice 0's ring.
 #pragma unroll
             for (int pc = 0; pc < kPieces; ++pc) {
               uint32_t r[32];
@@ -799,9 +797,19 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
               tmem_ld_wait(r);
 #pragma unroll
               for (int j = 0; j < 32; j += 4)
-                st_async_v4(dst + (uint32_t)((32 * pc + j) / 4) * 512u, rbar, r[j], r[j + 1],
-                            r[j + 2], r[j + 3]);
+                st_shared_v4(wbuf + lane * 16u + (uint32_t)((32 * pc + j) / 4) * 512u, r[j],
+                             r[j + 1], r[j + 2], r[j + 3]);
             }
+            fence_proxy_async_smem();  // the copy engine reads what the threads wrote
+            __syncwarp();
+            if (!warp_wait(kx_go_bar(ew), 0, ctl, kSiteKx)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0)
+              bulk_copy_s2cluster(mapa_shared(wbuf, crank - CTA_GROUP), wbuf, kKxWarpBytes,
+                                  mapa_shared(kx_ready_bar(ew), crank - CTA_GROUP));
+            __syncwarp();
             emit = false;
           }
         } else if (active && w.nsplit > 1) {

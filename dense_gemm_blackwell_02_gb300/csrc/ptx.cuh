@@ -145,14 +145,15 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
-// Asynchronous 16-byte store into another CTA's shared memory (both addresses
-// shared::cluster); the bytes complete_tx on `remote_bar`, an mbarrier of the CTA that
-// owns `remote_addr`, which its waiter arms with the expected count.
-__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t remote_bar, uint32_t a,
-                                            uint32_t b, uint32_t c, uint32_t d) {
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to another
+// CTA's (distributed shared memory); the bytes complete_tx on `remote_bar`, an mbarrier
+// of the destination CTA.  Both shared addresses 16-byte aligned; dst and remote_bar in
+// the shared::cluster window.
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                    uint32_t remote_bar) {
   asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
-      ::"r"(remote_addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "r"(src), "r"(bytes), "r"(remote_bar)
       : "memory");
 }
 
