@@ -67,6 +67,10 @@ struct gemm_ctx {
   cudaEvent_t group_done[kGroupRing] = {};
   size_t group_cap[kGroupRing] = {};
   int group_next = 0;
+  // gemm_run_host: copy streams and the events that order the chunks of the pipeline
+  static constexpr int kHostChunks = 8;
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  cudaEvent_t host_ev[2 + 3 * kHostChunks] = {};
 };
 
 namespace {
@@ -394,6 +398,10 @@ gemm_status_t gemm_destroy(gemm_handle_t h) {
   if (h->d_ctr) cudaFree(h->d_ctr);
   for (auto* p : h->d_stage)
     if (p) cudaFree(p);
+  if (h->copy_in) cudaStreamDestroy(h->copy_in);
+  if (h->copy_out) cudaStreamDestroy(h->copy_out);
+  for (auto e : h->host_ev)
+    if (e) cudaEventDestroy(e);
   for (int i = 0; i < gemm_ctx::kGroupRing; ++i) {
     if (h->h_groups[i]) cudaFreeHost(h->h_groups[i]);
     if (h->h_gstart[i]) cudaFreeHost(h->h_gstart[i]);
@@ -790,18 +798,76 @@ gemm_status_t gemm_run_host(gemm_handle_t h, const void* A_host, const void* B_h
       h->stage_bytes[i] = bytes[i];
     }
   }
-  if (K > 0) {
-    if (cudaMemcpyAsync(h->d_stage[0], A_host, bytes[0], cudaMemcpyHostToDevice, stream) !=
-            cudaSuccess ||
-        cudaMemcpyAsync(h->d_stage[1], B_host, bytes[1], cudaMemcpyHostToDevice, stream) !=
-            cudaSuccess)
+  // A pipeline over row chunks of A and C: B goes over first, then every chunk's A rows
+  // go over on one copy stream while the GEMM of the chunk before runs on `stream` and
+  // the C rows of the chunk before that come back on another copy stream.  One chunk
+  // below 2048 rows.
+  // about 1024 rows per chunk, two to eight chunks (measured: 4096^3 478 us in four
+  // chunks against 489 in eight; 8192^3 1675 us in eight against 1760 in four)
+  const int64_t want_chunks =
+      std::min<int64_t>(gemm_ctx::kHostChunks, std::max<int64_t>(2, M / 1024));
+  const int64_t chunk_rows = M >= 2048 ? ceil_div(ceil_div(M, want_chunks), (int64_t)256) * 256 : M;
+  const int nc = (int)ceil_div(M, chunk_rows);
+  if (K == 0 || nc == 1) {
+    if (K > 0 &&
+        (cudaMemcpyAsync(h->d_stage[0], A_host, bytes[0], cudaMemcpyHostToDevice, stream) !=
+             cudaSuccess ||
+         cudaMemcpyAsync(h->d_stage[1], B_host, bytes[1], cudaMemcpyHostToDevice, stream) !=
+             cudaSuccess))
+      return GEMM_ERR_CUDA;
+    gemm_status_t st = gemm_run(h, h->d_stage[0], h->d_stage[1], h->d_stage[2], M, N, K,
+                                dtype_in, dtype_out, stream_);
+    if (st != GEMM_OK) return st;
+    if (cudaMemcpyAsync(C_host, h->d_stage[2], bytes[2], cudaMemcpyDeviceToHost, stream) !=
+        cudaSuccess)
+      return GEMM_ERR_CUDA;
+    return gemm_device_status(h, stream_, nullptr);
+  }
+  if (!h->copy_in) {
+    if (cudaStreamCreateWithFlags(&h->copy_in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&h->copy_out, cudaStreamNonBlocking) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    for (auto& e : h->host_ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return GEMM_ERR_CUDA;
+  }
+  cudaEvent_t* ev = h->host_ev;  // [0] start, [1] done, then per chunk: A in, GEMM, C out
+  const size_t osz = out_size(dtype_out);
+  const char* Ah = static_cast<const char*>(A_host);
+  char* Ch = static_cast<char*>(C_host);
+  char* Ad = static_cast<char*>(h->d_stage[0]);
+  char* Cd = static_cast<char*>(h->d_stage[2]);
+  // the staging buffers are free once the work already queued on `stream` is done
+  if (cudaEventRecord(ev[0], stream) != cudaSuccess ||
+      cudaStreamWaitEvent(h->copy_in, ev[0], 0) != cudaSuccess ||
+      cudaStreamWaitEvent(h->copy_out, ev[0], 0) != cudaSuccess ||
+      cudaMemcpyAsync(h->d_stage[1], B_host, bytes[1], cudaMemcpyHostToDevice, h->copy_in) !=
+          cudaSuccess)
+    return GEMM_ERR_CUDA;
+  for (int c = 0; c < nc; ++c) {
+    const int64_t r0 = c * chunk_rows, rows = std::min(chunk_rows, M - r0);
+    cudaEvent_t e_in = ev[2 + 3 * c], e_gemm = ev[3 + 3 * c], e_out = ev[4 + 3 * c];
+    if (cudaMemcpyAsync(Ad + r0 * K * isz, Ah + r0 * K * isz, rows * K * isz,
+                        cudaMemcpyHostToDevice, h->copy_in) != cudaSuccess ||
+        cudaEventRecord(e_in, h->copy_in) != cudaSuccess ||
+        cudaStreamWaitEvent(stream, e_in, 0) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    gemm_status_t st = gemm_run(h, Ad + r0 * K * isz, h->d_stage[1], Cd + r0 * N * osz, rows, N,
+                                K, dtype_in, dtype_out, stream_);
+    if (st != GEMM_OK) {
+      cudaStreamSynchronize(h->copy_in);
+      cudaStreamSynchronize(h->copy_out);
+      return st;
+    }
+    if (cudaEventRecord(e_gemm, stream) != cudaSuccess ||
+        cudaStreamWaitEvent(h->copy_out, e_gemm, 0) != cudaSuccess ||
+        cudaMemcpyAsync(Ch + r0 * N * osz, Cd + r0 * N * osz, rows * N * osz,
+                        cudaMemcpyDeviceToHost, h->copy_out) != cudaSuccess ||
+        cudaEventRecord(e_out, h->copy_out) != cudaSuccess)
       return GEMM_ERR_CUDA;
   }
-  gemm_status_t st = gemm_run(h, h->d_stage[0], h->d_stage[1], h->d_stage[2], M, N, K, dtype_in,
-                              dtype_out, stream_);
-  if (st != GEMM_OK) return st;
-  if (cudaMemcpyAsync(C_host, h->d_stage[2], bytes[2], cudaMemcpyDeviceToHost, stream) !=
-      cudaSuccess)
+  // the caller's stream resumes once the last rows of C are back
+  if (cudaEventRecord(ev[1], h->copy_out) != cudaSuccess ||
+      cudaStreamWaitEvent(stream, ev[1], 0) != cudaSuccess)
     return GEMM_ERR_CUDA;
   return gemm_device_status(h, stream_, nullptr);
 }

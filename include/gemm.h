@@ -244,8 +244,12 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
 
 /*
  * The same product with HOST buffers: copies A and B to device staging buffers
- * owned by the handle, runs the GEMM and copies C back, all on `stream`, then
- * synchronises `stream` and reports kernel timeouts like gemm_device_status.
+ * owned by the handle, runs the GEMM and copies C back, then synchronises `stream`
+ * and reports kernel timeouts like gemm_device_status.  From M = 2048 rows on, the
+ * work is a pipeline of two to eight row chunks of about 1024 rows (a multiple of 256):
+ * B goes over first, then chunk c's rows of A
+ * go over on a copy stream owned by the handle while the GEMM of chunk c - 1 runs on
+ * `stream` and the C rows of chunk c - 2 come back on a second copy stream.
  * Page-locked host memory makes the copies asynchronous DMA; pageable memory
  * works but is slower.
  */
