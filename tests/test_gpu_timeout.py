@@ -45,3 +45,51 @@ def test_stalled_wait_times_out_and_the_context_survives(variant, splits):
         assert g.device_status()[0] == 0
         parity.oracle_check(parity.bits_of(C2), A, B, si.F16, si.F32, what="after timeout")
         torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("case", ["cluster_split_pair", "cluster_split_one", "grouped", "fp8",
+                                  "blockwise"])
+def test_stalled_wait_times_out_in_every_kernel_family(case):
+    # the same stall in the other kernel families: the cluster K split (whose slices also
+    # wait on each other), a grouped launch, FP8 and blockwise FP8; each run must return
+    # a timeout and leave the handle and context usable
+    from dense_gemm_blackwell_02_gb300.binding import Gemm
+    M, N, K = 256, 1024, 4096
+    din = si.E4M3 if case in ("fp8", "blockwise") else si.F16
+    A, B = si.make_operands(M, N, K, din, "uniform", seed=62)
+    Ad, Bd = A.cuda(), B.cuda()
+    sfa = torch.ones(K // 128, M, device="cuda")
+    sfb = torch.ones(K // 128, N // 128, device="cuda")
+    C = torch.zeros(M, N, dtype=torch.float32, device="cuda")
+
+    def run(g):
+        if case == "grouped":
+            g.run_grouped([(Ad, Bd, C), (Ad[:100], Bd[:300], C[:100, :300].contiguous())])
+        elif case == "blockwise":
+            g.run_blockwise(Ad, Bd, C, sfa, sfb, 1)
+        else:
+            g.run(Ad, Bd, C)
+
+    with Gemm() as g:
+        if case == "cluster_split_pair":
+            g.set_config(variant=2, block_n=256, splits=2, epilogue=3)
+        elif case == "cluster_split_one":
+            g.set_config(variant=1, block_n=128, splits=2, epilogue=3)
+        g.set_wait_limit(50_000_000)
+        g.set_test_stall(True)
+        run(g)
+        code, word = g.device_status()
+        assert code == TIMEOUT, (code, hex(word))
+        assert word >> 24 == 1
+        g.set_test_stall(False)
+        g.set_wait_limit(2_000_000_000)
+        C.zero_()
+        run(g)
+        assert g.device_status()[0] == 0
+        if case in ("cluster_split_pair", "cluster_split_one"):
+            assert g.last_config()["epilogue"] == 3
+        if case == "grouped":
+            return
+        # unit block scales: the blockwise product is the plain one, up to the order of
+        # the fp32 additions, so the plain oracle and tolerance apply
+        parity.oracle_check(parity.bits_of(C), A, B, din, si.F32, what=f"after timeout ({case})")
