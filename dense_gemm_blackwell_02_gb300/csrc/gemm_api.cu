@@ -311,7 +311,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   // cluster of 2 * cg CTAs, each group one unit, and meet in distributed shared memory.
   c->kx2 = false;
   if (f.epilogue == 3 || auto_kx) {
-    bool valid = !blockwise && one_ok && !c->sk_workers && !c->half_tail && dp == 0 && s == 2 &&
+    bool valid = allow_kx && one_ok && !c->sk_workers && !c->half_tail && dp == 0 && s == 2 &&
                  c->units <= slots;
     if (valid) {
       const int clusters = max_resident_kx_clusters(cg, c->bn, c->stages, out);

@@ -407,6 +407,18 @@ def test_cluster_k_split_rejections(g):
     A = torch.zeros(256, 4096, dtype=torch.float16, device="cuda")
     C = torch.zeros(256, 1024, dtype=torch.float16, device="cuda")
     B = torch.zeros(1024, 4096, dtype=torch.float16, device="cuda")
+    g.set_config(variant=2, splits=2, epilogue=3)
+    try:
+        with pytest.raises(GemmError) as e:                     # with a fused epilogue
+            g.run_epilogue(A, B, C, alpha=2.0)
+        assert e.value.code == 2
+        A8 = torch.zeros(256, 4096, dtype=torch.float8_e4m3fn, device="cuda")
+        B8 = torch.zeros(1024, 4096, dtype=torch.float8_e4m3fn, device="cuda")
+        with pytest.raises(GemmError) as e:                     # FP8 operands
+            g.run(A8, B8, C)
+        assert e.value.code == 2
+    finally:
+        g.reset_config()
     for cfg in ({"splits": 3, "epilogue": 3},                    # not two slices
                 {"splits": 2, "epilogue": 3, "chain_kblocks": 16}):   # slices of several chains
         g.set_config(**cfg)
