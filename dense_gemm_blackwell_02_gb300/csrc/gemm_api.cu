@@ -21,6 +21,12 @@ using namespace gb300;
 namespace {
 
 constexpr int kTmapCacheSize = 16;
+// A single row of A takes the matrix-vector path without being asked when K is at most
+// this (measured back to back, M = 1: 8192 x 8192 27.5 us against 28.9 on the tensor
+// cores, 28672 x 8192 74.5 against 81.4, 4096 x 4096 9.0 against 13.9, 14336 x 4096
+// 22.1 against 25.7; but 8192 x 28672 85.0 against 83.9, and with two or more rows of
+// A the tensor cores win: 2 x 8192 x 8192 30.4 against 28.7).
+constexpr int64_t kGemvAutoMaxK = 16384;
 
 struct TmapKey {
   const void* ptr;
@@ -420,7 +426,7 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
     return GEMM_OK;
   }
   const gemm_config_t& c = *cfg;
-  if (c.variant < 0 || c.variant > 2) return GEMM_ERR_INVALID_ARG;
+  if (c.variant < 0 || c.variant > 3) return GEMM_ERR_INVALID_ARG;
   if (c.block_n != 0 && c.block_n != 128 && c.block_n != 256) return GEMM_ERR_INVALID_ARG;
   if (c.splits < -1 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
       c.dp_tiles != 0 || c.prefetch_kblocks < -1 || c.epilogue < 0 || c.epilogue > 3)
@@ -493,6 +499,30 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
     return GEMM_ERR_UNSUPPORTED;
 
   const int out = out_kind(dtype_out);
+  const bool fp8_in = is_fp8(dtype_in);
+  // A few rows of A: the CUDA-core matrix-vector path (variant 3), forced or automatic.
+  const gemm_config_t& fc = h->forced;
+  if (fc.variant == 3 || (!fc.variant && !fc.block_n && !fc.splits && !fc.stages && !fc.epilogue &&
+                          !fc.chain_kblocks && M == 1 && K <= kGemvAutoMaxK && !fused && !fp8_in &&
+                          !bs)) {
+    if (M > kGemvMaxRows || fused || fp8_in || bs) return GEMM_ERR_UNSUPPORTED;
+    GemvSpec g;
+    g.A = A;
+    g.B = B;
+    g.C = C;
+    g.M = (int32_t)M;
+    g.N = (int32_t)N;
+    g.chunks = (int32_t)(K / 8);
+    g.bf16 = dtype_in == GEMM_BF16;
+    g.out = out;
+    // 4 x 256 threads per SM, one warp per row of B at a time
+    const int64_t cap = fc.max_ctas ? fc.max_ctas : (int64_t)h->sms * 4;
+    g.grid = (int)std::min<int64_t>(ceil_div(N, (int64_t)8), cap);
+    g.stream = stream;
+    if (launch_gemv(g) != cudaSuccess) return GEMM_ERR_CUDA;
+    h->last = gemm_config_t{3, 0, 1, 0, 0, g.grid, 0, (int32_t)N, -1, 1};
+    return GEMM_OK;
+  }
   Choice ch;
   const bool fp8 = is_fp8(dtype_in);
   gemm_status_t st = choose(h, M, N, K, out, fp8 ? 2 * kBlockK : kBlockK, bs != nullptr,

@@ -29,6 +29,21 @@ struct LaunchSpec {
   cudaStream_t stream;
 };
 
+// The CUDA-core matrix-vector path (gemv_kernel.cu) for M <= kGemvMaxRows rows of A.
+constexpr int kGemvMaxRows = 4;
+struct GemvSpec {
+  const void* A;   // M x K, fp16 or bf16, 16-byte aligned rows
+  const void* B;   // N x K
+  void* C;         // M x N in `out`
+  int32_t M, N;
+  int32_t chunks;  // K / 8: 16-byte chunks per row
+  bool bf16;       // input type (else fp16)
+  int out;         // OutKind
+  int grid;        // CTAs (each takes rows blockIdx.x + j * grid of B)
+  cudaStream_t stream;
+};
+cudaError_t launch_gemv(const GemvSpec& s);
+
 // The instantiated (cta_group, bn, stages) menu.
 bool kernel_supported(int cta_group, int bn, int stages);
 int default_stages(int cta_group, int bn);

@@ -67,6 +67,9 @@ typedef enum {
  * Kernel selection.  Zero in any field means "choose automatically".
  *   variant   1 = one CTA per 128-row tile (cta_group::1)
  *             2 = a CTA pair per 256-row tile (cta_group::2, cluster of 2)
+ *             3 = the CUDA-core matrix-vector path for M <= 4 (fp16/bf16 inputs, no
+ *                 fused epilogue; other fields ignored except max_ctas); chosen
+ *                 automatically for M == 1 with K <= 16384
  *   block_n   128 or 256 columns of C per tile
  *   splits    K slices per tile (1 = no split; >1 = split-K with a deterministic
  *             in-kernel reduction in slice order; -1 = stream-K: every resident unit

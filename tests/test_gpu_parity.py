@@ -353,12 +353,13 @@ def test_one_row_tile_of_few_rows(g, M, cfg, N, K):
     try:
         _case(g, M, N, K, F16, F16, seed=90 + M)
         _case(g, M, N, K, BF16, F32, seed=91 + M, exact=True, ints=True)
-        assert g.last_config()["variant"] == 1
+        # one row of A without a forced configuration takes the matrix-vector path
+        assert g.last_config()["variant"] == (3 if (M == 1 and not cfg) else 1)
     finally:
         g.reset_config()
 
 
-@pytest.mark.parametrize("M", [1, 8, 64, 128])
+@pytest.mark.parametrize("M", [2, 8, 64, 128])
 def test_small_m_decode_takes_narrow_tiles(g, M):
     # M <= 128, N = 8192: 64 tiles of 128 columns in two K slices beat 32 tiles of 256
     # columns in four (fewer slices to reduce)
@@ -436,6 +437,51 @@ def test_cluster_k_split_rejections(g):
     try:
         with pytest.raises(GemmError) as e:
             g.run(A, B, C)
+        assert e.value.code == 2
+    finally:
+        g.reset_config()
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("N,K", [(1, 8), (7, 1000), (1000, 2048), (4097, 520), (300, 8192)])
+def test_matrix_vector_path(g, M, N, K):
+    # variant 3: the CUDA-core path for up to four rows of A
+    g.set_config(variant=3)
+    try:
+        _case(g, M, N, K, F16, F32, seed=110 + M)
+        _case(g, M, N, K, BF16, BF16, seed=111 + M)
+        _case(g, M, N, K, F16, F16, seed=112 + M, exact=True, ints=True)
+        assert g.last_config()["variant"] == 3
+    finally:
+        g.reset_config()
+
+
+def test_one_row_takes_the_matrix_vector_path(g):
+    _case(g, 1, 8192, 8192, F16, F16, seed=113)
+    assert g.last_config()["variant"] == 3
+    _case(g, 1, 8192, 28672, F16, F16, seed=114)      # long rows stay on the tensor cores
+    assert g.last_config()["variant"] == 1
+    _case(g, 2, 8192, 8192, F16, F16, seed=115)
+    assert g.last_config()["variant"] == 1
+
+
+def test_matrix_vector_path_rejections(g):
+    from dense_gemm_blackwell_02_gb300.binding import GemmError
+    g.set_config(variant=3)
+    try:
+        A = torch.zeros(5, 64, dtype=torch.float16, device="cuda")       # five rows
+        B = torch.zeros(32, 64, dtype=torch.float16, device="cuda")
+        C = torch.zeros(5, 32, dtype=torch.float32, device="cuda")
+        with pytest.raises(GemmError) as e:
+            g.run(A, B, C)
+        assert e.value.code == 2
+        with pytest.raises(GemmError) as e:                              # fused epilogue
+            g.run_epilogue(A[:2], B, C[:2], alpha=2.0)
+        assert e.value.code == 2
+        A8 = torch.zeros(2, 64, dtype=torch.float8_e4m3fn, device="cuda")
+        B8 = torch.zeros(32, 64, dtype=torch.float8_e4m3fn, device="cuda")
+        with pytest.raises(GemmError) as e:                              # FP8 operands
+            g.run(A8, B8, C[:2])
         assert e.value.code == 2
     finally:
         g.reset_config()
