@@ -217,19 +217,18 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   // in the global workspace (measured, back to back: 256 x 4096 x 4096 16.7 us against
   // 22.2 for four slices of 256-column tiles; 256 x 8192 x 8192 34.9 us against 36.5 for
   // unsplit 128-column tiles; M <= 128, 8192 x 8192: 28-30 us against 30-32 for two
-  // slices through the workspace).  Unsplit 128-column tiles stay when K is short
-  // (256 x 8192 x 4096: 21.9 us against 23.2).
+  // slices through the workspace; slices of several chains too: 256 x 8192 x 28672
+  // 93.7 us against 96.2, M <= 128 x 8192 x 28672 82-84 against 84-86).  Unsplit
+  // 128-column tiles stay when K is short (256 x 8192 x 4096: 21.9 us against 23.2).
   bool auto_kx = false;
   if (allow_kx && !f.block_n && !f.splits && !f.stages && !f.epilogue && !f.chain_kblocks &&
       c->k_blocks >= 8) {
-    const int chain = kChainKBlocks * kBlockK / kb_elems;
     for (int bn : {128, 256}) {
       const int st = default_stages(cg, bn);
       int64_t sl = resident_units(h, cg, bn, st, out);
       if (f.max_ctas) sl = std::min<int64_t>(sl, std::max<int64_t>(f.max_ctas / cg, 1));
       const int64_t tl = c->num_m * ceil_div(N, (int64_t)bn);
       if (tl * 2 > sl || std::min<int64_t>({sl / tl, c->k_blocks / 4, 32}) != 2) continue;
-      if (ceil_div(c->k_blocks, (int64_t)2) > chain) continue;
       if (bn == 256 && c->bn == 128 && c->k_blocks < 128) continue;  // keep unsplit narrow tiles
       const int clusters = max_resident_kx_clusters(cg, bn, st, out);
       if (clusters <= 0 || tl > clusters) continue;
@@ -311,13 +310,13 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   else if (!c->half_tail && s > 1 && dp == 0)
     longest = c->kb_per_split;
   const bool one_ok = longest <= c->chain_kb;
-  if (f.epilogue >= 2 && !one_ok) return GEMM_ERR_UNSUPPORTED;
-  c->one_chain = (f.epilogue == 1 || blockwise) ? false : one_ok;
+  if (f.epilogue == 2 && !one_ok) return GEMM_ERR_UNSUPPORTED;
+  c->one_chain = (f.epilogue == 1 || blockwise) ? false : one_ok;  // epilogue 3: either form
   // The cluster K split: every tile's two K slices run on the two CTA groups of one
   // cluster of 2 * cg CTAs, each group one unit, and meet in distributed shared memory.
   c->kx2 = false;
   if (f.epilogue == 3 || auto_kx) {
-    bool valid = allow_kx && one_ok && !c->sk_workers && !c->half_tail && dp == 0 && s == 2 &&
+    bool valid = allow_kx && !c->sk_workers && !c->half_tail && dp == 0 && s == 2 &&
                  c->units <= slots;
     if (valid) {
       const int clusters = max_resident_kx_clusters(cg, c->bn, c->stages, out);

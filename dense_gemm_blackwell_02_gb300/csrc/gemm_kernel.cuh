@@ -415,15 +415,17 @@ __device__ __forceinline__ void one_chain_piece(uint32_t taddr, const Unit& w, c
   tmem_ld_32x32b_x32(taddr, r);
   tmem_ld_wait(r);
   if constexpr (KX) {
+    if (kx_lane != 0) {
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      const uint4 x = ld_shared_v4(kx_lane + (uint32_t)((col + j) / 4) * 512u);
-      v[j] = __uint_as_float(r[j]) + __uint_as_float(x.x);
-      v[j + 1] = __uint_as_float(r[j + 1]) + __uint_as_float(x.y);
-      v[j + 2] = __uint_as_float(r[j + 2]) + __uint_as_float(x.z);
-      v[j + 3] = __uint_as_float(r[j + 3]) + __uint_as_float(x.w);
+      for (int j = 0; j < 32; j += 4) {
+        const uint4 x = ld_shared_v4(kx_lane + (uint32_t)((col + j) / 4) * 512u);
+        v[j] = __uint_as_float(r[j]) + __uint_as_float(x.x);
+        v[j + 1] = __uint_as_float(r[j + 1]) + __uint_as_float(x.y);
+        v[j + 2] = __uint_as_float(r[j + 2]) + __uint_as_float(x.z);
+        v[j + 3] = __uint_as_float(r[j + 3]) + __uint_as_float(x.w);
+      }
+      return;
     }
-    return;
   }
   if (w.nsplit <= 1) {
 #pragma unroll
@@ -517,8 +519,8 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
   static_assert(KIND != 2 || !ONE_CHAIN, "blockwise scales need the general epilogue");
   static_assert(!GROUPED || (!ONE_CHAIN && !FUSED && KIND == 0),
                 "grouped launches use the plain general epilogue");
-  static_assert(!KX2 || (ONE_CHAIN && !FUSED && KIND == 0 && !GROUPED),
-                "the cluster K split uses the plain single-chain epilogue");
+  static_assert(!KX2 || (!FUSED && KIND == 0 && !GROUPED),
+                "the cluster K split uses the plain epilogues");
   constexpr uint32_t kTmemCols = 2 * BN;       // two accumulator slots
   constexpr int kHalf = BN / 2;                // columns per epilogue warp
   constexpr int kPieces = kHalf / 32;          // tcgen05.ld x32 pieces per warp
@@ -777,7 +779,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
           static_assert(L::kEpiWarps * kKxWarpBytes <= STAGES * L::kStageBytes,
                         "the received partials must fit in the operand ring");
           const uint32_t wbuf = base + L::kAOff + ew * kKxWarpBytes;
-          if (active && slice_k == 0) {
+          if (active && w.nsplit > 1 && slice_k == 0) {
             if (lane == 0) {
               mbar_arrive_expect_tx_cluster(kx_ready_bar(ew), kKxWarpBytes);
               mbar_arrive_cluster(mapa_shared(kx_go_bar(ew), crank + CTA_GROUP));
@@ -787,7 +789,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
               break;
             }
             kx_lane = wbuf + lane * 16u;
-          } else if (active) {
+          } else if (active && w.nsplit > 1) {
             // Slice 1: stage the partial in this CTA's own ring (idle too), then, once
             // slice 0 is ready for it, one bulk copy per warp into slice 0's ring.
 #pragma unroll
@@ -1007,7 +1009,58 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;  // first row of this CTA
       // first column written by this warp
       const int32_t n_half = w.n_blk * BN + (w.half >= 0 ? w.half : (int32_t)h) * kHalf;
-      if (w.nsplit > 1) {
+      bool exchanged = false;
+      if constexpr (KX2) {
+        if (w.nsplit > 1) {
+          // Cluster K split (see the single-chain epilogue): slice 1 stages its summed
+          // chains in its own idle ring and copies them into slice 0's ring once slice 0
+          // has finished with it; slice 0 adds them to its own (p0 + p1, the same bits as
+          // the workspace path) and stores C.
+          constexpr uint32_t kKxWarpBytes = 32u * kHalf * 4u;
+          static_assert(L::kEpiWarps * kKxWarpBytes <= STAGES * L::kStageBytes,
+                        "the received partials must fit in the operand ring");
+          const uint32_t wlane = base + L::kAOff + ew * kKxWarpBytes + lane * 16u;
+          if (slice_k == 0) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx_cluster(kx_ready_bar(ew), kKxWarpBytes);
+              mbar_arrive_cluster(mapa_shared(kx_go_bar(ew), crank + CTA_GROUP));
+            }
+            if (!warp_wait(kx_ready_bar(ew), 0, ctl, kSiteKx)) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int j = 0; j < kHalf; j += 4) {
+              const uint4 x = ld_shared_v4(wlane + (uint32_t)(j / 4) * 512u);
+              acc[j] += __uint_as_float(x.x);
+              acc[j + 1] += __uint_as_float(x.y);
+              acc[j + 2] += __uint_as_float(x.z);
+              acc[j + 3] += __uint_as_float(x.w);
+            }
+            exchanged = true;
+          } else {
+#pragma unroll
+            for (int j = 0; j < kHalf; j += 4)
+              st_shared_v4(wlane + (uint32_t)(j / 4) * 512u, __float_as_uint(acc[j]),
+                           __float_as_uint(acc[j + 1]), __float_as_uint(acc[j + 2]),
+                           __float_as_uint(acc[j + 3]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (!warp_wait(kx_go_bar(ew), 0, ctl, kSiteKx)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0) {
+              const uint32_t wbuf = base + L::kAOff + ew * kKxWarpBytes;
+              bulk_copy_s2cluster(mapa_shared(wbuf, crank - CTA_GROUP), wbuf, kKxWarpBytes,
+                                  mapa_shared(kx_ready_bar(ew), crank - CTA_GROUP));
+            }
+            __syncwarp();
+            continue;
+          }
+        }
+      }
+      if (w.nsplit > 1 && !exchanged) {
         // Split-K: this slice's fp32 block (the warp's 32 rows x BN/2 columns) goes to
         // the workspace; the last slice of the block to arrive sums all slices in slice
         // order.  Within a block, each group of 4 columns holds the warp's 32 rows

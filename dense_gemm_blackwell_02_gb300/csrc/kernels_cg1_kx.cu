@@ -1,6 +1,6 @@
 // Instantiations of the one-CTA kernel for the cluster K split: two K slices of one
 // tile in one cluster of 2 CTAs, reduced through distributed shared memory,
-// single-chain epilogue.
+// single-chain and general epilogues.
 #include "launch_impl.cuh"
 
 namespace gb300 {

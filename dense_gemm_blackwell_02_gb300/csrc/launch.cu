@@ -31,9 +31,9 @@ int max_resident_kx_clusters(int cg, int bn, int stages, int out) {
 
 cudaError_t launch_gemm(const LaunchSpec& s) {
   if (s.kx2) {
-    if (s.kind != 0 || s.fused || !s.one_chain || s.grouped) return cudaErrorInvalidValue;
-    if (s.cta_group == 1) return launch_cg1_kx(s);
-    if (s.cta_group == 2) return launch_cg2_kx(s);
+    if (s.kind != 0 || s.fused || s.grouped) return cudaErrorInvalidValue;
+    if (s.cta_group == 1) return s.one_chain ? launch_cg1_kx(s) : launch_cg1_kxg(s);
+    if (s.cta_group == 2) return s.one_chain ? launch_cg2_kx(s) : launch_cg2_kxg(s);
     return cudaErrorInvalidValue;
   }
   if (s.grouped) {

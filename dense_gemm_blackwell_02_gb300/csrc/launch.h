@@ -20,7 +20,7 @@ struct LaunchSpec {
                    // 2: FP8 with blockwise scales (general epilogue, not fused)
   bool grouped;    // a grouped launch: p.groups holds the problems (kind 0, general epilogue)
   bool kx2;        // two K slices per tile, one per CTA group of a cluster of 2 * cta_group
-                   // (single-chain epilogue, one unit per CTA group)
+                   // (one unit per CTA group)
   CUtensorMap tmA; // A: box {128 bytes of K, 128 (or M < 128) rows}
   CUtensorMap tmB; // B: box {128 bytes of K, bn / cta_group}
   CUtensorMap tmB2; // B: box {128 bytes of K, bn / cta_group / 2} (half-tile units; else tmB)
@@ -78,6 +78,8 @@ cudaError_t launch_cg2_grouped(const LaunchSpec& s);
 // ... and the cluster K split (kernels_cg*_kx.cu)
 cudaError_t launch_cg1_kx(const LaunchSpec& s);
 cudaError_t launch_cg2_kx(const LaunchSpec& s);
+cudaError_t launch_cg1_kxg(const LaunchSpec& s);  // general epilogue
+cudaError_t launch_cg2_kxg(const LaunchSpec& s);
 int resident_cg1_kx(int bn, int stages, int out);
 int resident_cg2_kx(int bn, int stages, int out);
 // Clusters of 2 * cta_group CTAs of the cluster-K-split kernel that fit at once (0 if the

@@ -99,11 +99,12 @@ typedef enum {
  *             blocks (else gemm_run returns GEMM_ERR_UNSUPPORTED); 0 = 2 when valid;
  *             3 = single-chain with a tile's two K slices run by the two CTA groups of
  *             one cluster (2 CTAs, or 4 for pairs) and summed through distributed
- *             shared memory instead of the global workspace: valid only for
- *             fp16/bf16 inputs without a fused epilogue, when the shape is cut into
- *             exactly 2 K slices of single chains, with every tile and every unit
- *             resident at once (else GEMM_ERR_UNSUPPORTED).  Chosen automatically
- *             when one of the two tile widths gives exactly that.
+ *             shared memory instead of the global workspace (each slice summed in
+ *             the single-chain or the general epilogue, whichever its length allows):
+ *             valid only for fp16/bf16 inputs without a fused epilogue, when the shape
+ *             is cut into exactly 2 K slices, with every tile and every unit resident
+ *             at once (else GEMM_ERR_UNSUPPORTED).  Chosen automatically when one of
+ *             the two tile widths gives exactly that.
  *             gemm_last_config reports the one used.
  */
 typedef struct {

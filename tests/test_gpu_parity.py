@@ -403,6 +403,33 @@ def test_cluster_k_split_matches_the_workspace_split(g, variant, block_n, M, N, 
     parity.oracle_check(parity.bits_of(C), Ai, Bi, F16, F32, exact=True, what="cluster split ints")
 
 
+@pytest.mark.parametrize("variant,block_n", [(1, 128), (2, 256)])
+@pytest.mark.parametrize("M,N,K,chain,dtype_out", [(256, 1024, 16384, 0, F16),
+                                                   (200, 1000, 2048, 3, F32),
+                                                   (96, 520, 4096, 5, BF16)])
+def test_cluster_k_split_of_several_chains(g, variant, block_n, M, N, K, chain, dtype_out):
+    # slices of several accumulation chains: the general epilogue sums each slice's chains
+    # in registers, then the two slices meet in distributed shared memory (epilogue 3) or
+    # in the workspace (epilogue 1); the bits agree
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=99)
+    Ad, Bd = A.cuda(), B.cuda()
+    outs = {}
+    for epi in (1, 3):
+        C = torch.empty(M, N, dtype=TD[dtype_out], device="cuda")
+        g.set_config(variant=variant, block_n=block_n, splits=2, epilogue=epi, chain_kblocks=chain)
+        try:
+            g.run(Ad, Bd, C)
+            torch.cuda.synchronize()
+            assert g.device_status()[0] == 0
+            used = g.last_config()
+        finally:
+            g.reset_config()
+        assert used["epilogue"] == epi and used["splits"] == 2, used
+        outs[epi] = C
+    assert torch.equal(outs[1], outs[3])
+    parity.oracle_check(parity.bits_of(outs[3]), A, B, F16, dtype_out, what=f"cluster split {used}")
+
+
 def test_cluster_k_split_rejections(g):
     from dense_gemm_blackwell_02_gb300.binding import GemmError
     A = torch.zeros(256, 4096, dtype=torch.float16, device="cuda")
@@ -420,8 +447,7 @@ def test_cluster_k_split_rejections(g):
         assert e.value.code == 2
     finally:
         g.reset_config()
-    for cfg in ({"splits": 3, "epilogue": 3},                    # not two slices
-                {"splits": 2, "epilogue": 3, "chain_kblocks": 16}):   # slices of several chains
+    for cfg in ({"splits": 3, "epilogue": 3},):                   # not two slices
         g.set_config(**cfg)
         try:
             with pytest.raises(GemmError) as e:
