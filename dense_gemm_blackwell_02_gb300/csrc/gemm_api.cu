@@ -142,6 +142,7 @@ size_t in_size(gemm_dtype_t d) { return is_fp8(d) ? 1 : 2; }
 
 struct Choice {
   int variant, bn, stages, splits, kb_per_split, group_m, grid, chain_kb, half_tail, prefetch_kb;
+  int l2_hint;
   bool one_chain;
   bool kx2;  // the two K slices of a tile reduced inside a cluster (single chain)
   int64_t tiles, dp_tiles, units, k_blocks, num_m, num_n;
@@ -301,6 +302,9 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   // Prefetching B into L2 ahead of the ring: off unless asked for (measured on the
   // M = 256 decode shapes and the square ones it did not help).
   c->prefetch_kb = f.prefetch_kblocks > 0 ? f.prefetch_kblocks : 0;
+  // One row of tiles reads every B element once while every tile re-reads A: B's lines
+  // go first out of L2, A's last.
+  c->l2_hint = f.l2_hint ? f.l2_hint : (c->num_m == 1 ? 2 : 1);
   c->grid = (int)(std::min<int64_t>(std::max(c->units, c->sk_workers), slots) * cg);
   // The single-chain epilogue needs every unit to be one accumulation chain.
   int64_t longest = c->k_blocks;  // whole tiles and half-tile units
@@ -428,7 +432,8 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
   if (c.variant < 0 || c.variant > 3) return GEMM_ERR_INVALID_ARG;
   if (c.block_n != 0 && c.block_n != 128 && c.block_n != 256) return GEMM_ERR_INVALID_ARG;
   if (c.splits < -1 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
-      c.dp_tiles != 0 || c.prefetch_kblocks < -1 || c.epilogue < 0 || c.epilogue > 3)
+      c.dp_tiles != 0 || c.prefetch_kblocks < -1 || c.epilogue < 0 || c.epilogue > 3 ||
+      c.l2_hint < 0 || c.l2_hint > 2)
     return GEMM_ERR_INVALID_ARG;
   if (c.stages) {
     const int bn = c.block_n ? c.block_n : 256;
@@ -519,7 +524,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
     g.grid = (int)std::min<int64_t>(ceil_div(N, (int64_t)8), cap);
     g.stream = stream;
     if (launch_gemv(g) != cudaSuccess) return GEMM_ERR_CUDA;
-    h->last = gemm_config_t{3, 0, 1, 0, 0, g.grid, 0, (int32_t)N, -1, 1};
+    h->last = gemm_config_t{3, 0, 1, 0, 0, g.grid, 0, (int32_t)N, -1, 1, 1};
     return GEMM_OK;
   }
   Choice ch;
@@ -578,6 +583,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.group_m = ch.group_m;
   p.chain_kb = ch.chain_kb;
   p.prefetch_kb = ch.prefetch_kb;
+  p.l2_hint = ch.l2_hint;
   p.a_tx_short = (uint32_t)(kBlockM - a_box) * 128u;
   p.vec_store = c_tma ? 1 : 0;
   p.tma_store = c_tma ? 1 : 0;
@@ -610,7 +616,8 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   h->last = gemm_config_t{ch.variant,  ch.bn,   ch.sk_workers ? -(int32_t)ch.sk_workers : ch.splits,
                           ch.stages,
                           ch.group_m,  ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles,
-                          ch.prefetch_kb ? ch.prefetch_kb : -1, ch.kx2 ? 3 : ch.one_chain ? 2 : 1};
+                          ch.prefetch_kb ? ch.prefetch_kb : -1, ch.kx2 ? 3 : ch.one_chain ? 2 : 1,
+                          ch.l2_hint};
   return GEMM_OK;
 }
 
@@ -715,6 +722,7 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
   GroupDesc* desc = h->h_groups[slot];
   int32_t* start = h->h_gstart[slot];
   int64_t units = 0;
+  int32_t max_num_m = 0;
   for (int i = 0; i < G; ++i) {
     const gemm_problem_t& q = problems[live[i]];
     GroupDesc& d = desc[i];
@@ -733,6 +741,7 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
     d.k_blocks = (int32_t)ceil_div(q.K, (int64_t)kBlockK);
     d.num_m = (int32_t)ceil_div(q.M, (int64_t)kBlockM * cg);
     d.num_n = (int32_t)ceil_div(q.N, (int64_t)bn);
+    max_num_m = std::max(max_num_m, d.num_m);
     d.a_tx_short = (uint32_t)(kBlockM - a_box) * 128u;
     d.vec_store = c_tma ? 1 : 0;
     d.tma_store = c_tma ? 1 : 0;
@@ -781,11 +790,14 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
   p.groups = h->d_groups[slot];
   p.group_start = h->d_gstart[slot];
   p.num_groups = G;
+  // every problem one row of tiles: its B (an expert's weights) is read once
+  p.l2_hint = f.l2_hint ? f.l2_hint : (max_num_m <= 1 ? 2 : 1);
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
   p.test_stall = h->test_stall;
   if (launch_gemm(s) != cudaSuccess) return GEMM_ERR_CUDA;
-  h->last = gemm_config_t{cg, bn, 1, stages, p.group_m, s.grid, p.chain_kb, (int32_t)units, -1, 1};
+  h->last = gemm_config_t{cg, bn, 1, stages, p.group_m, s.grid, p.chain_kb, (int32_t)units, -1, 1,
+                          p.l2_hint};
   return GEMM_OK;
 }
 

@@ -558,6 +558,8 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
   const uint32_t rank = CTA_GROUP == 2 ? (KX2 ? (crank & 1u) : crank) : 0u;  // place in the pair
   const uint32_t group_base = KX2 ? crank - rank : 0u;        // cluster rank of the group's leader
   const uint32_t slice_k = KX2 ? crank / CTA_GROUP : 0u;
+  // the same rank of the other K slice's CTA group
+  const uint32_t kx_peer = slice_k == 0 ? crank + (uint32_t)CTA_GROUP : crank - (uint32_t)CTA_GROUP;
   const uint16_t pair_mask = (uint16_t)(KX2 ? (0x3u << group_base) : 0x3u);
   const bool leader = rank == 0;
   const int32_t first_unit = (int32_t)(blockIdx.x / CTA_GROUP);
@@ -612,6 +614,12 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     // (1-3% faster there, neutral on square shapes; measured).
     uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
     bool ok = true;
+    // When every B element is read by one tile only (one row of tiles), B's lines are
+    // marked first to be evicted and A's last: A, re-read by every tile from L2, then
+    // stays there however far apart in K the tiles running at once are (stream-K).
+    const bool hint = p.l2_hint == 2;
+    const uint64_t pol_a = hint ? l2_policy_evict_last() : 0ull;
+    const uint64_t pol_b = hint ? l2_policy_evict_first() : 0ull;
     Walker walk{first_unit, 0};
     Unit w;
     while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
@@ -648,15 +656,29 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         }
         if constexpr (CTA_GROUP == 1) {
           mbar_arrive_expect_tx_elect(full_bar(stage), tx);
-          tma_load_2d_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row, full_bar(stage));
-          tma_load_2d_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row, full_bar(stage));
+          if (hint) {
+            tma_load_2d_hint_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
+                                   full_bar(stage), pol_b);
+            tma_load_2d_hint_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
+                                   full_bar(stage), pol_a);
+          } else {
+            tma_load_2d_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row, full_bar(stage));
+            tma_load_2d_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row, full_bar(stage));
+          }
         } else {
           // Both CTAs' copies complete on the leader's full barrier; the leader arms it
           // with the bytes of the pair.
           const uint32_t leader_full = mapa_shared(full_bar(stage), group_base);
           if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), tx);
-          tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row, leader_full);
-          tma_load_2d_pair_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row, leader_full);
+          if (hint) {
+            tma_load_2d_pair_hint_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
+                                        leader_full, pol_b);
+            tma_load_2d_pair_hint_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
+                                        leader_full, pol_a);
+          } else {
+            tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row, leader_full);
+            tma_load_2d_pair_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row, leader_full);
+          }
         }
         armed |= 1u << stage;
         armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -769,20 +791,22 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         const float* ws_lane = nullptr;
         uint32_t kx_lane = 0;
         if constexpr (KX2) {
-          // The two K slices of the tile are the two CTA groups of this cluster.  Slice
-          // 0's ring is idle once its MMAs completed: it takes slice 1's partial there,
-          // warp by warp (this warp's 32 rows x BN/2 columns, 16 bytes per lane and 4
-          // columns), then adds it to its own and emits C.  The sender's own ring holds
-          // the partial until the copy has read it: the teardown's cluster barrier waits
-          // for slice 0, which waits for the copy.
+          // The two K slices of the tile are the two CTA groups of this cluster, and
+          // each finishes one column half of it: slice k the warps of half h = k.  A
+          // ring is idle once its MMAs completed; the finishing warp takes the other
+          // slice's partial there (its 32 rows x BN/2 columns, 16 bytes per lane and 4
+          // columns), adds it to its own and emits C; the warp of the other half sends
+          // its partial the other way.  A sender's own ring holds the partial until the
+          // copy has read it: the teardown's cluster barrier waits for the receiver,
+          // which waits for the copy.
           constexpr uint32_t kKxWarpBytes = 32u * kHalf * 4u;
           static_assert(L::kEpiWarps * kKxWarpBytes <= STAGES * L::kStageBytes,
                         "the received partials must fit in the operand ring");
           const uint32_t wbuf = base + L::kAOff + ew * kKxWarpBytes;
-          if (active && w.nsplit > 1 && slice_k == 0) {
+          if (active && w.nsplit > 1 && h == slice_k) {
             if (lane == 0) {
               mbar_arrive_expect_tx_cluster(kx_ready_bar(ew), kKxWarpBytes);
-              mbar_arrive_cluster(mapa_shared(kx_go_bar(ew), crank + CTA_GROUP));
+              mbar_arrive_cluster(mapa_shared(kx_go_bar(ew), kx_peer));
             }
             if (!warp_wait(kx_ready_bar(ew), 0, ctl, kSiteKx)) {
               ok = false;
@@ -790,8 +814,8 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
             }
             kx_lane = wbuf + lane * 16u;
           } else if (active && w.nsplit > 1) {
-            // Slice 1: stage the partial in this CTA's own ring (idle too), then, once
-            // slice 0 is ready for it, one bulk copy per warp into slice 0's ring.
+            // The other half: stage the partial in this CTA's own ring (idle too), then,
+            // once the other slice's warp is ready for it, one bulk copy into its ring.
 #pragma unroll
             for (int pc = 0; pc < kPieces; ++pc) {
               uint32_t r[32];
@@ -809,8 +833,8 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
               break;
             }
             if (lane == 0)
-              bulk_copy_s2cluster(mapa_shared(wbuf, crank - CTA_GROUP), wbuf, kKxWarpBytes,
-                                  mapa_shared(kx_ready_bar(ew), crank - CTA_GROUP));
+              bulk_copy_s2cluster(mapa_shared(wbuf, kx_peer), wbuf, kKxWarpBytes,
+                                  mapa_shared(kx_ready_bar(ew), kx_peer));
             __syncwarp();
             emit = false;
           }
@@ -1012,18 +1036,19 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       bool exchanged = false;
       if constexpr (KX2) {
         if (w.nsplit > 1) {
-          // Cluster K split (see the single-chain epilogue): slice 1 stages its summed
-          // chains in its own idle ring and copies them into slice 0's ring once slice 0
-          // has finished with it; slice 0 adds them to its own (p0 + p1, the same bits as
+          // Cluster K split (see the single-chain epilogue): the warp of the column half
+          // the other slice finishes stages its summed chains in its own idle ring and
+          // copies them into the other slice's ring once that one has finished with it;
+          // the receiving warp adds them to its own (p0 + p1 = p1 + p0, the same bits as
           // the workspace path) and stores C.
           constexpr uint32_t kKxWarpBytes = 32u * kHalf * 4u;
           static_assert(L::kEpiWarps * kKxWarpBytes <= STAGES * L::kStageBytes,
                         "the received partials must fit in the operand ring");
           const uint32_t wlane = base + L::kAOff + ew * kKxWarpBytes + lane * 16u;
-          if (slice_k == 0) {
+          if (h == slice_k) {
             if (lane == 0) {
               mbar_arrive_expect_tx_cluster(kx_ready_bar(ew), kKxWarpBytes);
-              mbar_arrive_cluster(mapa_shared(kx_go_bar(ew), crank + CTA_GROUP));
+              mbar_arrive_cluster(mapa_shared(kx_go_bar(ew), kx_peer));
             }
             if (!warp_wait(kx_ready_bar(ew), 0, ctl, kSiteKx)) {
               ok = false;
@@ -1052,8 +1077,8 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
             }
             if (lane == 0) {
               const uint32_t wbuf = base + L::kAOff + ew * kKxWarpBytes;
-              bulk_copy_s2cluster(mapa_shared(wbuf, crank - CTA_GROUP), wbuf, kKxWarpBytes,
-                                  mapa_shared(kx_ready_bar(ew), crank - CTA_GROUP));
+              bulk_copy_s2cluster(mapa_shared(wbuf, kx_peer), wbuf, kKxWarpBytes,
+                                  mapa_shared(kx_ready_bar(ew), kx_peer));
             }
             __syncwarp();
             continue;

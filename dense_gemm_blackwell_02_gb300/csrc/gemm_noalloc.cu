@@ -219,6 +219,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   p.group_m = 16;
   p.chain_kb = kChainKBlocks;
   p.prefetch_kb = 0;
+  p.l2_hint = 1;
   p.a_tx_short = (uint32_t)(kBlockM - a_box) * 128u;
   p.vec_store = c_tma ? 1 : 0;
   p.tma_store = c_tma ? 1 : 0;

@@ -66,6 +66,7 @@ struct GemmParams {
   int32_t group_m;         // grouped rasterisation: M-tiles per group
   int32_t chain_kb;        // k-blocks per TMEM accumulation chain
   int32_t prefetch_kb;     // L2 prefetch of B this many k-blocks ahead of the ring (0: off)
+  int32_t l2_hint;         // 2: B's loads evict-first and A's evict-last in L2; else none
   uint32_t a_tx_short;     // bytes of A's 128-row box that A's tensor map does not load:
                            // (128 - M) * 128 when a one-CTA tile's A box is M < 128 rows
   int32_t vec_store;       // 1 when 16-byte vector stores of C are aligned

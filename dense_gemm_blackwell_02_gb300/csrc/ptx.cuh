@@ -225,6 +225,41 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// L2 cache policies for the hinted loads: the whole access range marked first to be
+// evicted (an operand read once), or last (an operand re-read from L2 by many tiles).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_2d_hint_elect(uint32_t dst, const void* tmap, int32_t c0,
+                                                       int32_t c1, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      GB300_ELECT
+      "@e_ cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint_elect(uint32_t dst, const void* tmap,
+                                                            int32_t c0, int32_t c1,
+                                                            uint32_t cluster_bar, uint64_t policy) {
+  asm volatile(
+      GB300_ELECT
+      "@e_ cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(cluster_bar), "l"(policy)
+      : "memory");
+}
+
 // 2-D tiled load for a CTA pair: the data lands in this CTA's shared memory, the
 // completion is signalled on `cluster_bar`, which may live in the peer CTA.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t c0,

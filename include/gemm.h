@@ -106,6 +106,11 @@ typedef enum {
  *             at once (else GEMM_ERR_UNSUPPORTED).  Chosen automatically when one of
  *             the two tile widths gives exactly that.
  *             gemm_last_config reports the one used.
+ *   l2_hint   L2 cache policy of the operand loads: 1 = none; 2 = B's loads marked
+ *             evict-first and A's evict-last (for one row of tiles, where every B
+ *             element is read once and A is re-read by every tile); 0 = 2 when the
+ *             tiles form one row (M <= 256 for CTA pairs, M <= 128 for one CTA per
+ *             tile), else 1.  gemm_last_config reports the one used.
  */
 typedef struct {
   int32_t variant;
@@ -118,6 +123,7 @@ typedef struct {
   int32_t dp_tiles;
   int32_t prefetch_kblocks;
   int32_t epilogue;
+  int32_t l2_hint;
 } gemm_config_t;
 
 /* Create a handle on the current CUDA device.  Fails with GEMM_ERR_UNSUPPORTED

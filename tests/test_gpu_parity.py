@@ -430,6 +430,36 @@ def test_cluster_k_split_of_several_chains(g, variant, block_n, M, N, K, chain, 
     parity.oracle_check(parity.bits_of(outs[3]), A, B, F16, dtype_out, what=f"cluster split {used}")
 
 
+@pytest.mark.parametrize("M,N,K,cfg", [(256, 2048, 4096, {}), (200, 1000, 2048, {"splits": -1}),
+                                       (64, 4096, 1024, {}), (1000, 600, 512, {"variant": 2}),
+                                       (96, 520, 1024, {"variant": 1, "splits": 3})])
+def test_l2_policy_changes_no_bits(g, M, N, K, cfg):
+    # the evict-first / evict-last hints on the operand loads only steer L2: every
+    # policy gives the same bits, and the automatic choice takes the hints exactly
+    # when the tiles form one row
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=101)
+    Ad, Bd = A.cuda(), B.cuda()
+    outs = {}
+    for hint in (0, 1, 2):
+        C = torch.empty(M, N, dtype=torch.float16, device="cuda")
+        g.set_config(l2_hint=hint, **cfg)
+        try:
+            g.run(Ad, Bd, C)
+            torch.cuda.synchronize()
+            assert g.device_status()[0] == 0
+            used = g.last_config()
+        finally:
+            g.reset_config()
+        if hint:
+            assert used["l2_hint"] == hint, used
+        else:
+            rows = 128 * used["variant"]
+            assert used["l2_hint"] == (2 if M <= rows else 1), used
+        outs[hint] = C
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    parity.oracle_check(parity.bits_of(outs[2]), A, B, F16, F16, what=f"l2 hints {used}")
+
+
 def test_cluster_k_split_rejections(g):
     from dense_gemm_blackwell_02_gb300.binding import GemmError
     A = torch.zeros(256, 4096, dtype=torch.float16, device="cuda")
