@@ -19,7 +19,8 @@ EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_epilogue", "gemm
            "gemm_run_grouped", "gemm_run_host",
            "gemm_set_config",
            "gemm_last_config", "gemm_device_status", "gemm_set_wait_limit",
-           "gemm_set_test_stall", "gemm_sm_count", "gemm_status_string", "gemm_run_noalloc")
+           "gemm_set_test_stall", "gemm_sm_count", "gemm_status_string", "gemm_run_noalloc",
+           "gemm_last_cuda_error")
 
 
 class GemmConfig(ctypes.Structure):
@@ -93,15 +94,21 @@ def lib():
     L.gemm_run_grouped.argtypes = [vp, ctypes.POINTER(GemmProblem), i32, i32, i32, vp]
     L.gemm_status_string.argtypes = [i32]
     L.gemm_status_string.restype = ctypes.c_char_p
+    L.gemm_last_cuda_error.argtypes = [vp]
+    L.gemm_last_cuda_error.restype = ctypes.c_char_p
     for name in EXPORTS:
-        if name not in ("gemm_sm_count", "gemm_status_string"):
+        if name not in ("gemm_sm_count", "gemm_status_string", "gemm_last_cuda_error"):
             getattr(L, name).restype = i32
     _lib = L
     return L
 
 
-def _check(code: int, what: str = ""):
+def _check(code: int, what: str = "", h=None):
     if code != 0:
+        if code == 3 and h is not None:  # GEMM_ERR_CUDA: name the CUDA error behind it
+            detail = lib().gemm_last_cuda_error(h).decode()
+            if detail:
+                what = f"{what} ({detail})" if what else detail
         raise GemmError(code, what)
 
 
@@ -181,7 +188,7 @@ class Gemm:
         code = self.run_ptr(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
                             torch_dtype_code(A.dtype), torch_dtype_code(C.dtype),
                             _stream_ptr(stream, A.device))
-        _check(code, f"gemm_run M={M} N={N} K={K}")
+        _check(code, f"gemm_run M={M} N={N} K={K}", self._h)
         return C
 
     def run_epilogue(self, A, B, C, alpha=1.0, beta=0.0, bias=None, relu=False, stream=None):
@@ -202,7 +209,7 @@ class Gemm:
         code = lib().gemm_run_epilogue(self._h, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
                                        torch_dtype_code(A.dtype), torch_dtype_code(C.dtype),
                                        ctypes.byref(epi), _stream_ptr(stream, A.device))
-        _check(code, f"gemm_run_epilogue M={M} N={N} K={K}")
+        _check(code, f"gemm_run_epilogue M={M} N={N} K={K}", self._h)
         return C
 
     def run_blockwise(self, A, B, C, sfa, sfb, block_m, block_n=128, stream=None):
@@ -225,7 +232,7 @@ class Gemm:
         code = lib().gemm_run_blockwise(self._h, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
                                         torch_dtype_code(A.dtype), torch_dtype_code(C.dtype),
                                         ctypes.byref(sc), _stream_ptr(stream, A.device))
-        _check(code, f"gemm_run_blockwise M={M} N={N} K={K}")
+        _check(code, f"gemm_run_blockwise M={M} N={N} K={K}", self._h)
         return C
 
     def run_grouped(self, problems, stream=None):
@@ -248,7 +255,7 @@ class Gemm:
         code = lib().gemm_run_grouped(self._h, arr, len(problems), torch_dtype_code(din),
                                       torch_dtype_code(dout),
                                       _stream_ptr(stream, problems[0][0].device))
-        _check(code, f"gemm_run_grouped count={len(problems)}")
+        _check(code, f"gemm_run_grouped count={len(problems)}", self._h)
 
     def run_host(self, A, B, C, dtype_in, dtype_out, stream=None):
         """gemm_run_host on CPU tensors (pinned for asynchronous copies)."""
@@ -257,7 +264,7 @@ class Gemm:
         sp = 0 if stream is None else _stream_ptr(stream, None)
         code = lib().gemm_run_host(self._h, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
                                    dtype_in, dtype_out, sp)
-        _check(code, "gemm_run_host")
+        _check(code, "gemm_run_host", self._h)
         return C
 
     # ----------------------------------------------------------------- control --

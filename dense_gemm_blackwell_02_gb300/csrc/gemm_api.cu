@@ -48,6 +48,7 @@ struct TmapEntry {
 
 struct gemm_ctx {
   int device = 0;
+  cudaError_t last_cuda = cudaSuccess;  // the CUDA error behind the last GEMM_ERR_CUDA launch
   int sms = 0;
   uint32_t* d_status = nullptr;
   float* d_ws = nullptr;
@@ -163,9 +164,13 @@ int resident_units(gemm_ctx* h, int cg, int bn, int stages, int out) {
   return slot;
 }
 
+// The default accumulation chain: K 4096 elements, 64 blocks of fp16/bf16, 32 of FP8.
+int64_t chain_kb_of(int kb_elems) { return kChainKBlocks * kBlockK / kb_elems; }
+
 // kb_elems: K elements per 128-byte K block (64 fp16/bf16, 128 FP8).
 // blockwise: one accumulation chain per K block (scaled in the general epilogue).
-// allow_kx: the cluster K split has kernels for this call (fp16/bf16, plain epilogue).
+// allow_kx: the cluster K split and the staged stream-K fix-up have kernels for this call
+// (fp16/bf16, plain epilogue).
 gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int kb_elems,
                      bool blockwise, bool allow_kx, Choice* c) {
   const gemm_config_t& f = h->forced;
@@ -264,6 +269,16 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
     // decided by waves).
     s = std::min<int64_t>({slots / c->tiles, c->k_blocks / 4, 32});
     dp = 0;
+  } else if (allow_kx && !f.max_ctas && !f.block_n && !f.stages && !f.epilogue &&
+             !f.chain_kblocks && c->tiles > slots && c->tiles < 2 * slots && c->k_blocks > chain_kb_of(kb_elems) &&
+             c->tiles * c->k_blocks * slots < (int64_t(1) << 32)) {
+    // Between one and two waves of tiles of several accumulation chains: stream-K over
+    // every resident unit instead of a second, mostly idle wave (measured, back to back:
+    // 256 x 28672 x 8192 88.9 us against 97.6 for whole tiles and half tiles; 512 x 10240 x
+    // 8192 66.4 against 87.2).  Below one wave the segments' fix-up costs more than the
+    // balance gains (512 x 8192 x 8192: 58.7 against 48.4 us).
+    dp = 0;
+    c->sk_workers = slots;
   } else if (c->tiles > slots && c->tiles % slots != 0) {
     // Whole waves run whole tiles; the tiles of the partial last wave are spread over
     // more units so that the last wave keeps (nearly) every unit busy: as two
@@ -293,8 +308,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
     c->ws_slots = ceil_div(c->k_blocks, std::max<int64_t>(share, 1)) + 1;
   }
   c->group_m = f.group_m ? f.group_m : 16;
-  // a chain of K 4096 elements: 64 blocks of fp16/bf16, 32 of FP8
-  c->chain_kb = f.chain_kblocks ? f.chain_kblocks : kChainKBlocks * kBlockK / kb_elems;
+  c->chain_kb = f.chain_kblocks ? f.chain_kblocks : chain_kb_of(kb_elems);
   if (blockwise) {
     if (f.chain_kblocks > 1 || f.epilogue >= 2) return GEMM_ERR_UNSUPPORTED;
     c->chain_kb = 1;
@@ -359,6 +373,11 @@ gemm_status_t ensure_workspace(gemm_ctx* h, size_t ws_bytes, size_t ctr_count) {
 }  // namespace
 
 extern "C" {
+
+const char* gemm_last_cuda_error(gemm_handle_t h) {
+  if (!h) return "";
+  return h->last_cuda == cudaSuccess ? "" : cudaGetErrorName(h->last_cuda);
+}
 
 const char* gemm_status_string(gemm_status_t s) {
   switch (s) {
@@ -523,7 +542,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
     const int64_t cap = fc.max_ctas ? fc.max_ctas : (int64_t)h->sms * 4;
     g.grid = (int)std::min<int64_t>(ceil_div(N, (int64_t)8), cap);
     g.stream = stream;
-    if (launch_gemv(g) != cudaSuccess) return GEMM_ERR_CUDA;
+    if ((h->last_cuda = launch_gemv(g)) != cudaSuccess) return GEMM_ERR_CUDA;
     h->last = gemm_config_t{3, 0, 1, 0, 0, g.grid, 0, (int32_t)N, -1, 1, 1};
     return GEMM_OK;
   }
@@ -545,6 +564,8 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   // FP8 kernels always carry the epilogue: the per-tensor scales arrive as alpha
   s.fused = (fused || fp8) && !bs;
   s.kind = bs ? 2 : fp8 ? 1 : 0;
+  s.staged = !ch.kx2 && !s.fused && s.kind == 0 && !ch.one_chain &&
+             ((ch.splits > 1 && !ch.half_tail) || ch.sk_workers);
   s.stream = stream;
   const bool c_tma = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0;
   // A single one-CTA row tile of M < 128 rows loads A as an M-row box: the stage's
@@ -612,7 +633,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
     p.workspace = h->d_ws;
     p.counters = h->d_ctr;
   }
-  if (launch_gemm(s) != cudaSuccess) return GEMM_ERR_CUDA;
+  if ((h->last_cuda = launch_gemm(s)) != cudaSuccess) return GEMM_ERR_CUDA;
   h->last = gemm_config_t{ch.variant,  ch.bn,   ch.sk_workers ? -(int32_t)ch.sk_workers : ch.splits,
                           ch.stages,
                           ch.group_m,  ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles,
@@ -795,7 +816,7 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
   p.test_stall = h->test_stall;
-  if (launch_gemm(s) != cudaSuccess) return GEMM_ERR_CUDA;
+  if ((h->last_cuda = launch_gemm(s)) != cudaSuccess) return GEMM_ERR_CUDA;
   h->last = gemm_config_t{cg, bn, 1, stages, p.group_m, s.grid, p.chain_kb, (int32_t)units, -1, 1,
                           p.l2_hint};
   return GEMM_OK;

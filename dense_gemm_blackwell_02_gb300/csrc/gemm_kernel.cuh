@@ -250,6 +250,17 @@ static __device__ __noinline__ void decode_grouped(int32_t u, const GemmParams& 
   w.n_blk = r / gm;
 }
 
+// Whether walker_next will return another unit (the walker is not advanced).  Kept out
+// of line like sk_next.
+static __device__ __noinline__ bool walker_has_next(const Walker& k, int32_t first,
+                                                    const GemmParams& p) {
+  if (k.u < p.units) return true;
+  if (first >= p.sk_workers) return false;
+  const uint32_t W = (uint32_t)p.sk_workers;
+  const uint32_t T = (uint32_t)(p.tiles - p.dp_tiles) * (uint32_t)p.k_blocks;
+  return (uint32_t)first * T / W + (uint32_t)k.sk_done < ((uint32_t)first + 1u) * T / W;
+}
+
 // Only two 32-bit counters live across a unit; the stream-K range is recomputed from
 // the worker's index on each call.
 template <bool GROUPED>
@@ -507,8 +518,14 @@ struct Layout {
 // cluster of 2 * CTA_GROUP CTAs; the second slice hands its accumulator to the first
 // through distributed shared memory instead of the global workspace.  One unit per CTA
 // group, single-chain epilogue.
+// STAGED: in the general epilogue, the last K slice of a tile to finish on a CTA's last
+// unit brings the other slices' partials into the idle operand ring with asynchronous
+// copies instead of reading them into registers, and skips publishing its own when the
+// others are all in (the stream-K fix-up).  Built for the plain kernels' split launches;
+// the kernel for whole tiles keeps the direct form (its register allocation, and its
+// time at 8192^3, measured better with that form than with the staged one or with none).
 template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN, bool FUSED, int KIND = 0,
-          bool GROUPED = false, bool KX2 = false>
+          bool GROUPED = false, bool KX2 = false, bool STAGED = false>
 __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
@@ -931,6 +948,9 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       // In a half-tile unit the accumulator holds BN/2 columns: the h = 0 warps own
       // them, the h = 1 warps only take part in the slot hand-over.
       const bool active = w.half < 0 || h == 0;
+      // (asked before the accumulator is live: a call with it live would spill it)
+      bool final_unit = false;
+      if constexpr (STAGED) final_unit = w.nsplit > 1 && !walker_has_next(walk, first_unit, p);
       float acc[kHalf];
       const int32_t nchains = chains_of(w, p.chain_kb);
       // Blockwise FP8 scales (KIND 2; "CUTLASS Deep Dive: From CuTe Layouts to Blackwell
@@ -1085,75 +1105,220 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
           }
         }
       }
-      if (w.nsplit > 1 && !exchanged) {
-        // Split-K: this slice's fp32 block (the warp's 32 rows x BN/2 columns) goes to
-        // the workspace; the last slice of the block to arrive sums all slices in slice
-        // order.  Within a block, each group of 4 columns holds the warp's 32 rows
-        // contiguously (float index (col / 4) * 128 + lane * 4 + col % 4), so every
-        // warp-wide 16-byte access covers 512 contiguous bytes.
-        constexpr size_t kBlockFloats = 32 * kHalf;
-        constexpr size_t kBlocksPerSlice = (size_t)CTA_GROUP * 8;  // (rank, quarter, half)
-        const size_t sliced = (size_t)(w.tile - p.dp_tiles);      // index among sliced tiles
-        const size_t my_block = ((size_t)rank * 4 + q) * 2 + h;
-        float* ws_tile = p.workspace + sliced * p.ws_slots * kBlocksPerSlice * kBlockFloats;
-        float* mine = ws_tile + ((size_t)w.split * kBlocksPerSlice + my_block) * kBlockFloats +
-                      lane * 4;
-#pragma unroll
-        for (int j = 0; j < kHalf; j += 4)
-          st_global_cg_v4(mine + j * 32, __float_as_uint(acc[j]), __float_as_uint(acc[j + 1]),
-                          __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
-        // The warp's partial is published by lane 0's release-increment of the block's
-        // counter (after the warp barrier); the slice that sees the count reach the
-        // number of slices acquires every other slice's partial the same way.
-        __syncwarp();
-        uint32_t last = 0;
-        if (lane == 0) {
+      if constexpr (STAGED) {
+        if (w.nsplit > 1 && !exchanged) {
+          // Split-K: this slice's fp32 block (the warp's 32 rows x BN/2 columns) goes to
+          // the workspace; the last slice of the block to arrive sums all slices in slice
+          // order.  Within a block, each group of 4 columns holds the warp's 32 rows
+          // contiguously (float index (col / 4) * 128 + lane * 4 + col % 4), so every
+          // warp-wide 16-byte access covers 512 contiguous bytes.
+          constexpr size_t kBlockFloats = 32 * kHalf;
+          constexpr size_t kBlocksPerSlice = (size_t)CTA_GROUP * 8;  // (rank, quarter, half)
+          const size_t sliced = (size_t)(w.tile - p.dp_tiles);      // index among sliced tiles
+          const size_t my_block = ((size_t)rank * 4 + q) * 2 + h;
+          float* ws_tile = p.workspace + sliced * p.ws_slots * kBlocksPerSlice * kBlockFloats;
           uint32_t* ctr = p.counters + sliced * kBlocksPerSlice + my_block;
-          const uint32_t before = atom_add_acq_rel_gpu(ctr, 1u);
-          last = (before == (uint32_t)w.nsplit - 1u) ? 1u : 0u;
-          if (last) st_relaxed_gpu_u32(ctr, 0u);  // ready for the next launch
-        }
-        last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        __syncwarp();
-        if (!last) continue;
-        // Sum the slices in slice order: the result is the same whichever slice arrived
-        // last.  With two slices the sum is p0 + p1 = p1 + p0 exactly, so the last one
-        // adds the other's partial to its own registers; with more, every partial is
-        // read back and added in order.
-        const float* ws_lane = ws_tile + (size_t)my_block * kBlockFloats + lane * 4;
-        const size_t slice_stride = kBlocksPerSlice * kBlockFloats;
-        if (w.nsplit == 2) {
-          const float* other = ws_lane + (size_t)(1 - w.split) * slice_stride;
-#pragma unroll
-          for (int j = 0; j < kHalf; j += 4) {
-            const uint4 x = ld_global_cg_v4(other + j * 32);
-            acc[j] += __uint_as_float(x.x);
-            acc[j + 1] += __uint_as_float(x.y);
-            acc[j + 2] += __uint_as_float(x.z);
-            acc[j + 3] += __uint_as_float(x.w);
+          const float* ws_lane = ws_tile + (size_t)my_block * kBlockFloats + lane * 4;
+          const size_t slice_stride = kBlocksPerSlice * kBlockFloats;
+          // The last unit of this CTA: its operand ring is idle (every MMA has completed
+          // and nothing more is loaded), so the other slices' blocks can be staged there.
+          // With at most two of them, a slice that finds them all published does not
+          // publish its own (the common case for the last segment of a stream-K worker,
+          // whose partners ran at the starts of their ranges).
+          const bool fast = w.nsplit <= 3 && final_unit;
+          uint32_t last = 0;
+          if (fast && lane == 0) last = ld_acquire_gpu_u32(ctr) == (uint32_t)w.nsplit - 1u ? 1u : 0u;
+          last = __shfl_sync(0xFFFFFFFFu, last, 0);
+          if (!last) {
+            float* mine = ws_tile + ((size_t)w.split * kBlocksPerSlice + my_block) * kBlockFloats +
+                          lane * 4;
+  #pragma unroll
+            for (int j = 0; j < kHalf; j += 4)
+              st_global_cg_v4(mine + j * 32, __float_as_uint(acc[j]), __float_as_uint(acc[j + 1]),
+                              __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
+            // The warp's partial is published by lane 0's release-increment of the block's
+            // counter (after the warp barrier); the slice that sees the count reach the
+            // number of slices acquires every other slice's partial the same way.
+            __syncwarp();
+            if (lane == 0) {
+              const uint32_t before = atom_add_acq_rel_gpu(ctr, 1u);
+              last = (before == (uint32_t)w.nsplit - 1u) ? 1u : 0u;
+            }
+            last = __shfl_sync(0xFFFFFFFFu, last, 0);
+            __syncwarp();
+            if (!last) continue;
           }
-        } else {
-          for (int32_t s = 0; s < w.nsplit; ++s) {
-            const float* src = ws_lane + (size_t)s * slice_stride;
-#pragma unroll
-            for (int j = 0; j < kHalf; j += 4) {
-              const uint4 x = ld_global_cg_v4(src + j * 32);
-              if (s == 0) {
-                acc[j] = __uint_as_float(x.x);
-                acc[j + 1] = __uint_as_float(x.y);
-                acc[j + 2] = __uint_as_float(x.z);
-                acc[j + 3] = __uint_as_float(x.w);
-              } else {
+          if (lane == 0) st_relaxed_gpu_u32(ctr, 0u);  // ready for the next launch
+          // Sum the slices in slice order: the result is the same whichever slice arrived
+          // last.  With two slices the sum is p0 + p1 = p1 + p0 exactly, so the last one
+          // adds the other's partial to its own registers; with three, (p0 + p1) + p2 is
+          // formed with its own partial taken from the registers.
+          if (fast) {
+            // The other blocks come into this warp's share of the idle ring through
+            // asynchronous copies (all in flight at once, no registers held), in the
+            // block layout above: one block, or the two others' halves of the columns.
+            constexpr uint32_t kRegion = 32u * kHalf * 4u;
+            static_assert(L::kEpiWarps * kRegion <= STAGES * L::kStageBytes,
+                          "the staged partials must fit in the operand ring");
+            const uint32_t wreg = base + L::kAOff + ew * kRegion + lane * 16u;
+            if (w.nsplit == 2) {
+              const float* other = ws_lane + (size_t)(1 - w.split) * slice_stride;
+  #pragma unroll
+              for (int j = 0; j < kHalf; j += 4) cp_async_cg_16(wreg + (uint32_t)(j / 4) * 512u, other + j * 32);
+              cp_async_wait_all();
+              __syncwarp();
+  #pragma unroll
+              for (int j = 0; j < kHalf; j += 4) {
+                const uint4 x = ld_shared_v4(wreg + (uint32_t)(j / 4) * 512u);
                 acc[j] += __uint_as_float(x.x);
                 acc[j + 1] += __uint_as_float(x.y);
                 acc[j + 2] += __uint_as_float(x.z);
                 acc[j + 3] += __uint_as_float(x.w);
               }
+            } else {
+              // the two other slices, in slice order
+              const int32_t sa = w.split == 0 ? 1 : 0, sb = w.split == 2 ? 1 : 2;
+              const float* pa = ws_lane + (size_t)sa * slice_stride;
+              const float* pb = ws_lane + (size_t)sb * slice_stride;
+              constexpr int kCols = kHalf / 2;
+              constexpr uint32_t kSecond = kRegion / 2;
+              // one column half at a time (its index a compile-time constant, so that the
+              // accumulator stays in registers)
+              auto column_half = [&](auto half) {
+                constexpr int c0 = decltype(half)::value * kCols;
+  #pragma unroll
+                for (int j = 0; j < kCols; j += 4) {
+                  cp_async_cg_16(wreg + (uint32_t)(j / 4) * 512u, pa + (c0 + j) * 32);
+                  cp_async_cg_16(wreg + kSecond + (uint32_t)(j / 4) * 512u, pb + (c0 + j) * 32);
+                }
+                cp_async_wait_all();
+                __syncwarp();
+  #pragma unroll
+                for (int j = 0; j < kCols; j += 4) {
+                  const uint4 xa = ld_shared_v4(wreg + (uint32_t)(j / 4) * 512u);
+                  const uint4 xb = ld_shared_v4(wreg + kSecond + (uint32_t)(j / 4) * 512u);
+                  // (p0 + p1) + p2 with this slice's own partial in acc
+                  if (w.split == 2) {
+                    acc[c0 + j] += __uint_as_float(xa.x) + __uint_as_float(xb.x);
+                    acc[c0 + j + 1] += __uint_as_float(xa.y) + __uint_as_float(xb.y);
+                    acc[c0 + j + 2] += __uint_as_float(xa.z) + __uint_as_float(xb.z);
+                    acc[c0 + j + 3] += __uint_as_float(xa.w) + __uint_as_float(xb.w);
+                  } else {
+                    acc[c0 + j] = (acc[c0 + j] + __uint_as_float(xa.x)) + __uint_as_float(xb.x);
+                    acc[c0 + j + 1] = (acc[c0 + j + 1] + __uint_as_float(xa.y)) + __uint_as_float(xb.y);
+                    acc[c0 + j + 2] = (acc[c0 + j + 2] + __uint_as_float(xa.z)) + __uint_as_float(xb.z);
+                    acc[c0 + j + 3] = (acc[c0 + j + 3] + __uint_as_float(xa.w)) + __uint_as_float(xb.w);
+                  }
+                }
+                __syncwarp();  // the region is refilled for the next half
+              };
+              column_half(std::integral_constant<int, 0>{});
+              column_half(std::integral_constant<int, 1>{});
+            }
+          } else if (w.nsplit == 2) {
+            const float* other = ws_lane + (size_t)(1 - w.split) * slice_stride;
+  #pragma unroll
+            for (int j = 0; j < kHalf; j += 4) {
+              const uint4 x = ld_global_cg_v4(other + j * 32);
+              acc[j] += __uint_as_float(x.x);
+              acc[j + 1] += __uint_as_float(x.y);
+              acc[j + 2] += __uint_as_float(x.z);
+              acc[j + 3] += __uint_as_float(x.w);
+            }
+          } else {
+            // every slice's partial (this one's published too) read back in order
+            for (int32_t s = 0; s < w.nsplit; ++s) {
+              const float* src = ws_lane + (size_t)s * slice_stride;
+  #pragma unroll
+              for (int j = 0; j < kHalf; j += 4) {
+                const uint4 x = ld_global_cg_v4(src + j * 32);
+                if (s == 0) {
+                  acc[j] = __uint_as_float(x.x);
+                  acc[j + 1] = __uint_as_float(x.y);
+                  acc[j + 2] = __uint_as_float(x.z);
+                  acc[j + 3] = __uint_as_float(x.w);
+                } else {
+                  acc[j] += __uint_as_float(x.x);
+                  acc[j + 1] += __uint_as_float(x.y);
+                  acc[j + 2] += __uint_as_float(x.z);
+                  acc[j + 3] += __uint_as_float(x.w);
+                }
+              }
             }
           }
         }
-      }
 
+      } else {
+        if (w.nsplit > 1 && !exchanged) {
+          // Split-K: this slice's fp32 block (the warp's 32 rows x BN/2 columns) goes to
+          // the workspace; the last slice of the block to arrive sums all slices in slice
+          // order.  Within a block, each group of 4 columns holds the warp's 32 rows
+          // contiguously (float index (col / 4) * 128 + lane * 4 + col % 4), so every
+          // warp-wide 16-byte access covers 512 contiguous bytes.
+          constexpr size_t kBlockFloats = 32 * kHalf;
+          constexpr size_t kBlocksPerSlice = (size_t)CTA_GROUP * 8;  // (rank, quarter, half)
+          const size_t sliced = (size_t)(w.tile - p.dp_tiles);      // index among sliced tiles
+          const size_t my_block = ((size_t)rank * 4 + q) * 2 + h;
+          float* ws_tile = p.workspace + sliced * p.ws_slots * kBlocksPerSlice * kBlockFloats;
+          float* mine = ws_tile + ((size_t)w.split * kBlocksPerSlice + my_block) * kBlockFloats +
+                        lane * 4;
+  #pragma unroll
+          for (int j = 0; j < kHalf; j += 4)
+            st_global_cg_v4(mine + j * 32, __float_as_uint(acc[j]), __float_as_uint(acc[j + 1]),
+                            __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
+          // The warp's partial is published by lane 0's release-increment of the block's
+          // counter (after the warp barrier); the slice that sees the count reach the
+          // number of slices acquires every other slice's partial the same way.
+          __syncwarp();
+          uint32_t last = 0;
+          if (lane == 0) {
+            uint32_t* ctr = p.counters + sliced * kBlocksPerSlice + my_block;
+            const uint32_t before = atom_add_acq_rel_gpu(ctr, 1u);
+            last = (before == (uint32_t)w.nsplit - 1u) ? 1u : 0u;
+            if (last) st_relaxed_gpu_u32(ctr, 0u);  // ready for the next launch
+          }
+          last = __shfl_sync(0xFFFFFFFFu, last, 0);
+          __syncwarp();
+          if (!last) continue;
+          // Sum the slices in slice order: the result is the same whichever slice arrived
+          // last.  With two slices the sum is p0 + p1 = p1 + p0 exactly, so the last one
+          // adds the other's partial to its own registers; with more, every partial is
+          // read back and added in order.
+          const float* ws_lane = ws_tile + (size_t)my_block * kBlockFloats + lane * 4;
+          const size_t slice_stride = kBlocksPerSlice * kBlockFloats;
+          if (w.nsplit == 2) {
+            const float* other = ws_lane + (size_t)(1 - w.split) * slice_stride;
+  #pragma unroll
+            for (int j = 0; j < kHalf; j += 4) {
+              const uint4 x = ld_global_cg_v4(other + j * 32);
+              acc[j] += __uint_as_float(x.x);
+              acc[j + 1] += __uint_as_float(x.y);
+              acc[j + 2] += __uint_as_float(x.z);
+              acc[j + 3] += __uint_as_float(x.w);
+            }
+          } else {
+            for (int32_t s = 0; s < w.nsplit; ++s) {
+              const float* src = ws_lane + (size_t)s * slice_stride;
+  #pragma unroll
+              for (int j = 0; j < kHalf; j += 4) {
+                const uint4 x = ld_global_cg_v4(src + j * 32);
+                if (s == 0) {
+                  acc[j] = __uint_as_float(x.x);
+                  acc[j + 1] = __uint_as_float(x.y);
+                  acc[j + 2] = __uint_as_float(x.z);
+                  acc[j + 3] = __uint_as_float(x.w);
+                } else {
+                  acc[j] += __uint_as_float(x.x);
+                  acc[j + 1] += __uint_as_float(x.y);
+                  acc[j + 2] += __uint_as_float(x.z);
+                  acc[j + 3] += __uint_as_float(x.w);
+                }
+              }
+            }
+          }
+        }
+
+      }
       if constexpr (FUSED) {
         const int32_t m = m0 + (int32_t)row;
 #pragma unroll

@@ -56,11 +56,13 @@ cudaError_t launch_gemm(const LaunchSpec& s) {
   }
   if (s.cta_group == 1) {
     if (s.fused) return s.one_chain ? launch_cg1_one_fused(s) : launch_cg1_fused(s);
-    return s.one_chain ? launch_cg1_one(s) : launch_cg1(s);
+    if (s.one_chain) return launch_cg1_one(s);
+    return s.staged ? launch_cg1_staged(s) : launch_cg1(s);
   }
   if (s.cta_group == 2) {
     if (s.fused) return s.one_chain ? launch_cg2_one_fused(s) : launch_cg2_fused(s);
-    return s.one_chain ? launch_cg2_one(s) : launch_cg2(s);
+    if (s.one_chain) return launch_cg2_one(s);
+    return s.staged ? launch_cg2_staged(s) : launch_cg2(s);
   }
   return cudaErrorInvalidValue;
 }

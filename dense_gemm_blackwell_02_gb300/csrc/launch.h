@@ -21,6 +21,8 @@ struct LaunchSpec {
   bool grouped;    // a grouped launch: p.groups holds the problems (kind 0, general epilogue)
   bool kx2;        // two K slices per tile, one per CTA group of a cluster of 2 * cta_group
                    // (one unit per CTA group)
+  bool staged;     // plain general epilogue, K slices or stream-K segments meeting in the
+                   // workspace: the kernel with the staged fix-up
   CUtensorMap tmA; // A: box {128 bytes of K, 128 (or M < 128) rows}
   CUtensorMap tmB; // B: box {128 bytes of K, bn / cta_group}
   CUtensorMap tmB2; // B: box {128 bytes of K, bn / cta_group / 2} (half-tile units; else tmB)
@@ -79,6 +81,8 @@ cudaError_t launch_cg2_grouped(const LaunchSpec& s);
 cudaError_t launch_cg1_kx(const LaunchSpec& s);
 cudaError_t launch_cg2_kx(const LaunchSpec& s);
 cudaError_t launch_cg1_kxg(const LaunchSpec& s);  // general epilogue
+cudaError_t launch_cg1_staged(const LaunchSpec& s);  // general epilogue, staged fix-up
+cudaError_t launch_cg2_staged(const LaunchSpec& s);
 cudaError_t launch_cg2_kxg(const LaunchSpec& s);
 int resident_cg1_kx(int bn, int stages, int out);
 int resident_cg2_kx(int bn, int stages, int out);

@@ -6,9 +6,9 @@
 namespace gb300 {
 
 template <int CG, int BN, int STAGES, int OUT, bool ONE, bool FUSED, int KIND = 0,
-          bool GROUPED = false, bool KX2 = false>
+          bool GROUPED = false, bool KX2 = false, bool STAGED = false>
 cudaError_t launch_one(const LaunchSpec& s) {
-  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED, KIND, GROUPED, KX2>;
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED, KIND, GROUPED, KX2, STAGED>;
   constexpr unsigned kCluster = CG * (KX2 ? 2 : 1);
   using L = Layout<CG, BN, STAGES>;
   cudaError_t e =
@@ -71,12 +71,12 @@ int resident_one() {
 }
 
 template <int CG, int BN, int STAGES, bool ONE, bool FUSED, int KIND = 0, bool GROUPED = false,
-          bool KX2 = false>
+          bool KX2 = false, bool STAGED = false>
 cudaError_t by_out(const LaunchSpec& s) {
   switch (s.out) {
-    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED, KIND, GROUPED, KX2>(s);
-    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED, KIND, GROUPED, KX2>(s);
-    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED, KIND, GROUPED, KX2>(s);
+    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED>(s);
+    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED>(s);
+    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED, KIND, GROUPED, KX2, STAGED>(s);
     default: return cudaErrorInvalidValue;
   }
 }

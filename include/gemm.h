@@ -298,6 +298,11 @@ int32_t gemm_sm_count(gemm_handle_t h);
 /* Static description of a status code; never NULL. */
 const char* gemm_status_string(gemm_status_t s);
 
+/* The name of the CUDA error (e.g. "cudaErrorLaunchOutOfResources") that made the
+ * last kernel launch on this handle fail with GEMM_ERR_CUDA; "" if none did, or for
+ * a NULL handle.  Static storage; never NULL. */
+const char* gemm_last_cuda_error(gemm_handle_t h);
+
 /*
  * gemm_run_noalloc -- the same product for callers that cannot allocate device
  * memory.  The pages have no counterpart of this call; it exists for users of

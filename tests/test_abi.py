@@ -41,6 +41,7 @@ def test_status_strings(lib):
     for code in range(6):
         assert lib.gemm_status_string(code)
     assert lib.gemm_status_string(99) == b"unknown status"
+    assert lib.gemm_last_cuda_error(None) == b""
 
 
 def test_null_handle_is_rejected_without_touching_the_gpu(lib):

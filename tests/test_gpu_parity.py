@@ -155,6 +155,52 @@ def test_stream_k(g, variant, block_n, max_ctas, M, N, K):
         g.reset_config()
 
 
+@pytest.mark.parametrize("variant,block_n", [(1, 128), (1, 256), (2, 128), (2, 256)])
+@pytest.mark.parametrize("max_ctas,M,N,K", [(38, 256, 2560, 8192), (24, 256, 1024, 2048),
+                                             (40, 200, 1800, 1504), (30, 256, 4096, 1024)])
+def test_stream_k_staged_fix_up_matches_the_direct_one(g, variant, block_n, max_ctas, M, N, K):
+    # segments of two and three per tile: the plain kernel's last segment stages the
+    # others' partials in its idle operand ring (and may skip publishing its own), the
+    # fused kernel with the identity epilogue reads them straight into registers; both sum
+    # in K order, so the bits agree
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=43)
+    Ad, Bd = A.cuda(), B.cuda()
+    C1 = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    C2 = torch.empty_like(C1)
+    # chains of 4 K blocks: the launch takes the general epilogue
+    g.set_config(variant=variant, block_n=block_n, max_ctas=max_ctas, splits=-1, chain_kblocks=4)
+    try:
+        g.run(Ad, Bd, C1)
+        g.run_epilogue(Ad, Bd, C2, alpha=1.0, beta=0.0)
+        torch.cuda.synchronize()
+        assert g.device_status()[0] == 0
+        cfg = g.last_config()
+    finally:
+        g.reset_config()
+    assert cfg["splits"] < 0 and cfg["epilogue"] == 1, cfg
+    assert torch.equal(C1, C2)
+    parity.oracle_check(parity.bits_of(C1), A, B, F16, F32, what=f"staged stream-K {cfg}")
+
+
+@pytest.mark.parametrize("dtype_out", [F16, F32])
+def test_between_one_and_two_waves_takes_stream_k(g, dtype_out):
+    # more tiles than resident pairs but fewer than twice as many, each of several
+    # accumulation chains: the library spreads them over every pair by stream-K
+    pairs = g.sm_count // 2
+    M, N, K = 256, 256 * (pairs + pairs // 4), 4160
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=44)
+    C = torch.empty(M, N, dtype=TD[dtype_out], device="cuda")
+    g.reset_config()
+    g.run(A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    assert g.device_status()[0] == 0
+    cfg = g.last_config()
+    assert cfg["splits"] == -pairs and cfg["dp_tiles"] == 0 and cfg["epilogue"] == 1, cfg
+    rows = si.sample_indices(M, 12, seed=45, must=(0, 127, 128, 255))
+    parity.oracle_check(parity.bits_of(C.cpu()[rows]), A, B, F16, dtype_out, rows=rows,
+                        what=f"auto stream-K {cfg}")
+
+
 @pytest.mark.parametrize("variant", [1, 2])
 @pytest.mark.parametrize("chain", [1, 3, 5, 64])
 @pytest.mark.parametrize("splits", [1, 3])
