@@ -41,6 +41,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "params.h"
 #include "ptx.cuh"
 #include "umma.cuh"
@@ -633,78 +635,87 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     bool ok = true;
     // When every B element is read by one tile only (one row of tiles), B's lines are
     // marked first to be evicted and A's last: A, re-read by every tile from L2, then
-    // stays there however far apart in K the tiles running at once are (stream-K).
-    const bool hint = p.l2_hint == 2;
-    const uint64_t pol_a = hint ? l2_policy_evict_last() : 0ull;
-    const uint64_t pol_b = hint ? l2_policy_evict_first() : 0ull;
-    Walker walk{first_unit, 0};
-    Unit w;
-    while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
-      const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
-      // a half-tile unit loads half the B rows (through the half-height map tmB2)
-      const bool half = w.half >= 0;
-      const int32_t b_row = w.n_blk * BN +
-                            (half ? w.half * (BN / 2) + (int32_t)rank * (L::kRowsB / 2)
-                                  : (int32_t)rank * L::kRowsB);
-      const CUtensorMap* mapB = half ? &tmB2 : &tmB;
-      const CUtensorMap* mapA = &tmA;
-      uint32_t tx = (half ? L::kTxBytesHalf : L::kTxBytes) - p.a_tx_short;
-      if constexpr (GROUPED) {
-        // the problem's own maps, written by the host before the launch
-        const GroupDesc* gd = p.groups + w.g;
-        mapA = &gd->tmA;
-        mapB = &gd->tmB;
-        tx = L::kTxBytes - gd->a_tx_short;
-        fence_tensormap_acquire(mapA);
-        fence_tensormap_acquire(mapB);
-      }
-      // Streaming B from DRAM (decode shapes): keep more requests in flight than the
-      // shared-memory ring holds by prefetching B into L2 prefetch_kb k-blocks ahead
-      // ("A Blackwell GEMM by Hand in CuTe DSL", section 8: TMA prefetch).
-      if (p.prefetch_kb > 0)
-        for (int32_t kb = w.kb0; kb < min(w.kb0 + p.prefetch_kb, w.kb1); ++kb)
-          tma_prefetch_l2_2d_elect(mapB, kb * kKbElems, b_row);
-      for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-        if (p.prefetch_kb > 0 && kb + p.prefetch_kb < w.kb1)
-          tma_prefetch_l2_2d_elect(mapB, (kb + p.prefetch_kb) * kKbElems, b_row);
-        if (!warp_wait(empty_bar(stage), phase ^ 1u, ctl, kSiteEmpty)) {
-          ok = false;
-          break;
+    // stays there however far apart in K the tiles running at once are (stream-K).  The
+    // loop is built twice, with and without the hint: the hinted copy, even with the
+    // default policy, or a branch between the two forms in the loop, cost 3-4% at
+    // 4096^3 (measured).
+    auto produce = [&](auto hinted) {
+      constexpr bool kHint = decltype(hinted)::value;
+      const uint64_t pol_a = kHint ? l2_policy_evict_last() : 0ull;
+      const uint64_t pol_b = kHint ? l2_policy_evict_first() : 0ull;
+      Walker walk{first_unit, 0};
+      Unit w;
+      while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
+        const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
+        // a half-tile unit loads half the B rows (through the half-height map tmB2)
+        const bool half = w.half >= 0;
+        const int32_t b_row = w.n_blk * BN +
+                              (half ? w.half * (BN / 2) + (int32_t)rank * (L::kRowsB / 2)
+                                    : (int32_t)rank * L::kRowsB);
+        const CUtensorMap* mapB = half ? &tmB2 : &tmB;
+        const CUtensorMap* mapA = &tmA;
+        uint32_t tx = (half ? L::kTxBytesHalf : L::kTxBytes) - p.a_tx_short;
+        if constexpr (GROUPED) {
+          // the problem's own maps, written by the host before the launch
+          const GroupDesc* gd = p.groups + w.g;
+          mapA = &gd->tmA;
+          mapB = &gd->tmB;
+          tx = L::kTxBytes - gd->a_tx_short;
+          fence_tensormap_acquire(mapA);
+          fence_tensormap_acquire(mapB);
         }
-        if constexpr (CTA_GROUP == 1) {
-          mbar_arrive_expect_tx_elect(full_bar(stage), tx);
-          if (hint) {
-            tma_load_2d_hint_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
-                                   full_bar(stage), pol_b);
-            tma_load_2d_hint_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
-                                   full_bar(stage), pol_a);
-          } else {
-            tma_load_2d_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row, full_bar(stage));
-            tma_load_2d_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row, full_bar(stage));
+        // Streaming B from DRAM (decode shapes): keep more requests in flight than the
+        // shared-memory ring holds by prefetching B into L2 prefetch_kb k-blocks ahead
+        // ("A Blackwell GEMM by Hand in CuTe DSL", section 8: TMA prefetch).
+        if (p.prefetch_kb > 0)
+          for (int32_t kb = w.kb0; kb < min(w.kb0 + p.prefetch_kb, w.kb1); ++kb)
+            tma_prefetch_l2_2d_elect(mapB, kb * kKbElems, b_row);
+        for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+          if (p.prefetch_kb > 0 && kb + p.prefetch_kb < w.kb1)
+            tma_prefetch_l2_2d_elect(mapB, (kb + p.prefetch_kb) * kKbElems, b_row);
+          if (!warp_wait(empty_bar(stage), phase ^ 1u, ctl, kSiteEmpty)) {
+            ok = false;
+            break;
           }
-        } else {
-          // Both CTAs' copies complete on the leader's full barrier; the leader arms it
-          // with the bytes of the pair.
-          const uint32_t leader_full = mapa_shared(full_bar(stage), group_base);
-          if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), tx);
-          if (hint) {
-            tma_load_2d_pair_hint_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
-                                        leader_full, pol_b);
-            tma_load_2d_pair_hint_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
-                                        leader_full, pol_a);
+          if constexpr (CTA_GROUP == 1) {
+            mbar_arrive_expect_tx_elect(full_bar(stage), tx);
+            if constexpr (kHint) {
+              tma_load_2d_hint_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
+                                     full_bar(stage), pol_b);
+              tma_load_2d_hint_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
+                                     full_bar(stage), pol_a);
+            } else {
+              tma_load_2d_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row, full_bar(stage));
+              tma_load_2d_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row, full_bar(stage));
+            }
           } else {
-            tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row, leader_full);
-            tma_load_2d_pair_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row, leader_full);
+            // Both CTAs' copies complete on the leader's full barrier; the leader arms it
+            // with the bytes of the pair.
+            const uint32_t leader_full = mapa_shared(full_bar(stage), group_base);
+            if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), tx);
+            if constexpr (kHint) {
+              tma_load_2d_pair_hint_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
+                                          leader_full, pol_b);
+              tma_load_2d_pair_hint_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
+                                          leader_full, pol_a);
+            } else {
+              tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
+                                     leader_full);
+              tma_load_2d_pair_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
+                                     leader_full);
+            }
+          }
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
-        armed |= 1u << stage;
-        armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
       }
-    }
+    };
+    if (p.l2_hint == 2) produce(std::true_type{});
+    else produce(std::false_type{});
     // No copy may still be landing in shared memory when the CTA exits.
     if (lane == 0) {
       if (leader) {
