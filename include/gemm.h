@@ -111,6 +111,13 @@ typedef enum {
  *             element is read once and A is re-read by every tile); 0 = 2 when the
  *             tiles form one row (M <= 256 for CTA pairs, M <= 128 for one CTA per
  *             tile), else 1.  gemm_last_config reports the one used.
+ *   multicast 2 = a cluster of two CTA pairs computes two tiles of the same 256 rows
+ *             side by side, each pair loading half of A's rows and multicasting them
+ *             to both (TMA .multicast::cluster): A is read from L2 once for the two
+ *             tiles.  Valid for fp16/bf16 inputs without a fused epilogue, CTA pairs
+ *             (variant 2), every tile whole (no split, no half tiles); else
+ *             GEMM_ERR_UNSUPPORTED.  gemm_last_config then reports dp_tiles as the
+ *             pairs of tiles.  0 or 1 = off (the default).
  */
 typedef struct {
   int32_t variant;
@@ -124,6 +131,7 @@ typedef struct {
   int32_t prefetch_kblocks;
   int32_t epilogue;
   int32_t l2_hint;
+  int32_t multicast;
 } gemm_config_t;
 
 /* Create a handle on the current CUDA device.  Fails with GEMM_ERR_UNSUPPORTED
