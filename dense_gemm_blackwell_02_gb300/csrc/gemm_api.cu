@@ -63,7 +63,7 @@ struct gemm_ctx {
   int32_t test_stall = 0;
   TmapEntry cache[kTmapCacheSize] = {};
   int cache_next = 0;
-  int resident[2][2][3] = {};  // [cta_group-1][bn==256][out]: co-resident units (0: unknown)
+  int resident[2][2][2][3] = {};  // [cta_group-1][bn==256][small A][out]: co-resident units (0: unknown)
   // grouped launches: a ring of problem tables (pinned host copy, device copy and the
   // event that marks the host copy reusable)
   static constexpr int kGroupRing = 4;
@@ -156,7 +156,7 @@ int out_kind(gemm_dtype_t d) { return d == GEMM_F16 ? kOutF16 : d == GEMM_BF16 ?
 // Units of this configuration that can run at once: CTAs (variant 1) or CTA pairs
 // (variant 2), from the occupancy query, at most one CTA per SM.
 int resident_units(gemm_ctx* h, int cg, int bn, int stages, int out) {
-  int& slot = h->resident[cg - 1][bn == 256 ? 1 : 0][out];
+  int& slot = h->resident[cg - 1][bn == 256 ? 1 : 0][a_rows(cg, bn, stages) < kBlockM ? 1 : 0][out];
   if (slot == 0) {
     int n = max_resident_units(cg, bn, stages, out);
     const int cap = h->sms / cg;
@@ -181,7 +181,10 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   c->variant = f.variant ? f.variant : (M > kBlockM && !blockwise ? 2 : 1);
   const int cg = c->variant;
   c->bn = f.block_n ? f.block_n : (N <= 128 ? 128 : 256);
-  c->stages = f.stages ? f.stages : default_stages(cg, c->bn);
+  // A row tile of at most 16 rows holds 16 rows of A per stage and a deeper ring (the
+  // plain fp16/bf16 kernels)
+  const bool small_a = cg == 1 && M <= 16 && allow_kx;
+  c->stages = f.stages ? f.stages : default_stages(cg, c->bn, small_a);
   if (!kernel_supported(cg, c->bn, c->stages)) return GEMM_ERR_INVALID_ARG;
   c->k_blocks = ceil_div(K, (int64_t)kb_elems);
   c->num_m = ceil_div(M, (int64_t)kBlockM * cg);
@@ -202,7 +205,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
       (c->k_blocks <= 128 || cg == 1)) {
     const int64_t tiles128 = c->num_m * ceil_div(N, (int64_t)128);
     const int64_t slots128 = [&] {
-      int64_t n = resident_units(h, cg, 128, default_stages(cg, 128), out);
+      int64_t n = resident_units(h, cg, 128, default_stages(cg, 128, small_a), out);
       if (f.max_ctas) n = std::min<int64_t>(n, std::max<int64_t>(f.max_ctas / cg, 1));
       return n;
     }();
@@ -213,7 +216,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
                                : tiles128 * 2 > slots128;
     if (tiles128 <= slots128 && fewer) {
       c->bn = 128;
-      c->stages = default_stages(cg, 128);
+      c->stages = default_stages(cg, 128, small_a);
       c->num_n = ceil_div(N, (int64_t)128);
       c->tiles = tiles128;
       slots = slots128;
@@ -232,7 +235,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
       !f.chain_kblocks &&
       c->k_blocks >= 8) {
     for (int bn : {128, 256}) {
-      const int st = default_stages(cg, bn);
+      const int st = default_stages(cg, bn, small_a);
       int64_t sl = resident_units(h, cg, bn, st, out);
       if (f.max_ctas) sl = std::min<int64_t>(sl, std::max<int64_t>(f.max_ctas / cg, 1));
       const int64_t tl = c->num_m * ceil_div(N, (int64_t)bn);
@@ -371,6 +374,9 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
     c->grid = (int)(std::min<int64_t>(c->units, clusters) * 4);
     c->l2_hint = 1;  // the multicast producer issues plain copies
   }
+  // the deeper rings of 16-row A stages: plain fp16/bf16 kernels, row tiles of <= 16 rows
+  if (a_rows(cg, c->bn, c->stages) < kBlockM && (M > a_rows(cg, c->bn, c->stages) || !allow_kx))
+    return GEMM_ERR_UNSUPPORTED;
   if (c->units > INT32_MAX || c->tiles * cg * 8 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   return GEMM_OK;
 }
@@ -635,7 +641,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.chain_kb = ch.chain_kb;
   p.prefetch_kb = ch.prefetch_kb;
   p.l2_hint = ch.l2_hint;
-  p.a_tx_short = (uint32_t)(kBlockM - a_box) * 128u;
+  p.a_tx_short = (uint32_t)(a_rows(ch.variant, ch.bn, ch.stages) - a_box) * 128u;
   p.vec_store = c_tma ? 1 : 0;
   p.tma_store = c_tma ? 1 : 0;
   if (fp8) {
@@ -743,6 +749,7 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
   const int bn = f.block_n ? f.block_n : (narrow ? 128 : 256);
   const int stages = f.stages ? f.stages : default_stages(cg, bn);
   if (!kernel_supported(cg, bn, stages)) return GEMM_ERR_INVALID_ARG;
+  if (a_rows(cg, bn, stages) < kBlockM) return GEMM_ERR_UNSUPPORTED;  // no grouped kernel
 
   // The next table of the ring: its host copy is free once its last upload is done.
   const int slot = h->group_next;

@@ -481,12 +481,21 @@ __device__ __forceinline__ void one_chain_piece(uint32_t taddr, const Unit& w, c
 }
 
 // ------------------------------------------------------------- shared memory map --
+// One-CTA rings deeper than a 128-row A tile allows (10 stages of 128 columns, 5 of 256)
+// hold 16 rows of A per stage, for row tiles of M <= 16 rows: A's stage stride is then
+// 2 KiB, and the MMA's 128-row A operand runs on over the following stages' bytes.  The
+// rows past 16 are whatever those bytes hold; each feeds only its own accumulator row,
+// which is never stored, and the span stays inside the ring.  The ring keeps more of B
+// in flight (160 KiB against 96 or 128).
 template <int CTA_GROUP, int BN, int STAGES>
 struct Layout {
   static constexpr int kEpiWarps = 8;
   static constexpr uint32_t kThreads = 32 * (2 + kEpiWarps);
   static constexpr int kRowsB = BN / CTA_GROUP;                // B rows loaded per CTA
-  static constexpr uint32_t kABytes = kBlockM * kBlockK * 2;   // 16 KiB
+  static constexpr bool kSmallA =
+      CTA_GROUP == 1 && ((BN == 128 && STAGES > 6) || (BN == 256 && STAGES > 4));
+  static constexpr int kARows = kSmallA ? 16 : kBlockM;        // A rows held per stage
+  static constexpr uint32_t kABytes = kARows * kBlockK * 2;    // 16 KiB, or 2 KiB
   static constexpr uint32_t kBBytes = kRowsB * kBlockK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;   // per CTA
   static constexpr uint32_t kTxBytes = kStageBytes * CTA_GROUP;  // expected on the leader
@@ -506,6 +515,9 @@ struct Layout {
                     kCOff % 1024 == 0,
                 "every operand stage and staging box must start on a 1024-byte boundary");
   static_assert(kDynamicBytes <= 227 * 1024, "shared memory over the per-block limit");
+  // the MMA reads 128 rows of A from every stage's A start: inside the ring
+  static_assert((STAGES - 1) * kABytes + kBlockM * kBlockK * 2 <= kCOff,
+                "the A operand's 128-row span must stay inside the operand ring");
 };
 
 // ONE_CHAIN: every work unit is a single accumulation chain (at most p.chain_kb

@@ -8,12 +8,16 @@ namespace gb300 {
 cudaError_t launch_cg1(const LaunchSpec& s) {
   if (s.bn == 256 && s.stages == 4) return by_out<1, 256, 4, false, false>(s);
   if (s.bn == 128 && s.stages == 6) return by_out<1, 128, 6, false, false>(s);
+  if (s.bn == 256 && s.stages == 5) return by_out<1, 256, 5, false, false>(s);
+  if (s.bn == 128 && s.stages == 10) return by_out<1, 128, 10, false, false>(s);
   return cudaErrorInvalidValue;
 }
 
 int resident_cg1(int bn, int stages, int out) {
   if (bn == 256 && stages == 4) return resident_by_out<1, 256, 4>(out);
   if (bn == 128 && stages == 6) return resident_by_out<1, 128, 6>(out);
+  if (bn == 256 && stages == 5) return resident_by_out<1, 256, 5>(out);
+  if (bn == 128 && stages == 10) return resident_by_out<1, 128, 10>(out);
   return 0;
 }
 

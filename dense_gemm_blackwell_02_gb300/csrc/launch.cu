@@ -5,20 +5,32 @@
 namespace gb300 {
 
 bool kernel_supported(int cg, int bn, int stages) {
-  if (cg == 1) return (bn == 256 && stages == 4) || (bn == 128 && stages == 6);
+  if (cg == 1)
+    return (bn == 256 && (stages == 4 || stages == 5)) || (bn == 128 && (stages == 6 || stages == 10));
   if (cg == 2) return (bn == 256 && stages == 6) || (bn == 128 && stages == 8);
   return false;
 }
 
-int default_stages(int cg, int bn) {
-  if (cg == 1) return bn == 256 ? 4 : 6;
+int default_stages(int cg, int bn, bool small_a) {
+  if (cg == 1) return bn == 256 ? (small_a ? 5 : 4) : (small_a ? 10 : 6);
   return bn == 256 ? 6 : 8;
 }
 
 size_t kernel_smem_bytes(int cg, int bn, int stages) {
   if (!kernel_supported(cg, bn, stages)) return 0;
-  if (cg == 1) return bn == 256 ? Layout<1, 256, 4>::kDynamicBytes : Layout<1, 128, 6>::kDynamicBytes;
+  if (cg == 1) {
+    if (bn == 256) return stages == 5 ? Layout<1, 256, 5>::kDynamicBytes : Layout<1, 256, 4>::kDynamicBytes;
+    return stages == 10 ? Layout<1, 128, 10>::kDynamicBytes : Layout<1, 128, 6>::kDynamicBytes;
+  }
   return bn == 256 ? Layout<2, 256, 6>::kDynamicBytes : Layout<2, 128, 8>::kDynamicBytes;
+}
+
+int a_rows(int cg, int bn, int stages) {
+  if (cg == 1) {
+    if (bn == 256) return stages == 5 ? Layout<1, 256, 5>::kARows : Layout<1, 256, 4>::kARows;
+    return stages == 10 ? Layout<1, 128, 10>::kARows : Layout<1, 128, 6>::kARows;
+  }
+  return kBlockM;
 }
 
 int max_resident_units(int cg, int bn, int stages, int out) {

@@ -50,7 +50,10 @@ cudaError_t launch_gemv(const GemvSpec& s);
 
 // The instantiated (cta_group, bn, stages) menu.
 bool kernel_supported(int cta_group, int bn, int stages);
-int default_stages(int cta_group, int bn);
+// small_a: a one-CTA row tile of at most 16 rows (the ring then holds 16 rows of A per
+// stage and is deeper)
+int default_stages(int cta_group, int bn, bool small_a = false);
+int a_rows(int cta_group, int bn, int stages);  // A rows a stage of that kernel holds
 size_t kernel_smem_bytes(int cta_group, int bn, int stages);
 // Clusters (CTAs for cta_group 1) of this configuration that can be resident at once
 // on the current device; 0 if the query fails.

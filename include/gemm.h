@@ -77,7 +77,10 @@ typedef enum {
  *             gemm_last_config reports -W for stream-K over W units.  Stream-K
  *             needs tiles * K blocks * W < 2^32; gemm_run returns
  *             GEMM_ERR_UNSUPPORTED beyond that.
- *   stages    depth of the shared-memory operand ring
+ *   stages    depth of the shared-memory operand ring: 6 (pairs, BN 256), 8 (pairs, BN
+ *             128), 4 (one CTA, BN 256), 6 (one CTA, BN 128); or, for one CTA and at most 16
+ *             rows of A with fp16/bf16 inputs and no fused epilogue, 5 (BN 256) or 10 (BN
+ *             128) stages that hold 16 rows of A each (chosen automatically for M <= 16)
  *   group_m   grouped rasterisation: M tiles per group
  *   max_ctas  cap on the persistent grid (0 = one CTA per SM)
  *   chain_kblocks  K blocks (128 bytes of K: 64 fp16/bf16 or 128 FP8 elements)

@@ -544,6 +544,40 @@ def test_a_multicast_across_two_pairs(g, block_n, M, N, K, dtype_out):
     assert used["dp_tiles"] == -(-M // 256) * -(-(-(-N // block_n)) // 2), used
 
 
+@pytest.mark.parametrize("M", [1, 3, 8, 16, 17])
+@pytest.mark.parametrize("N,K,dtype_out", [(8192, 1024, F16), (1000, 8192, F32), (4096, 2048, BF16),
+                                           (3000, 520, F16)])
+def test_rows_of_at_most_16_take_the_deeper_ring(g, M, N, K, dtype_out):
+    # one CTA per row tile of <= 16 rows: stages of 16 A rows (2 KiB), a deeper ring
+    # (10 stages of 128 columns, 5 of 256); the MMA's 128-row A operand runs on over the
+    # next stages' bytes, which feed only accumulator rows that are never stored
+    _case(g, M, N, K, F16, dtype_out, seed=48)
+    cfg = g.last_config()
+    if cfg["variant"] == 1:          # (one row of A may take the matrix-vector path)
+        deep = {128: 10, 256: 5}[cfg["block_n"]]
+        assert (cfg["stages"] == deep) == (M <= 16), cfg
+    _case(g, M, N, K, BF16, F32, seed=49, exact=True, ints=True)
+
+
+def test_deeper_ring_rejections(g):
+    from dense_gemm_blackwell_02_gb300.binding import GemmError
+    A = torch.zeros(20, 1024, dtype=torch.float16, device="cuda")
+    B = torch.zeros(512, 1024, dtype=torch.float16, device="cuda")
+    C = torch.zeros(20, 512, dtype=torch.float16, device="cuda")
+    g.set_config(variant=1, block_n=128, stages=10)
+    try:
+        with pytest.raises(GemmError) as e:                 # 20 rows do not fit 16-row stages
+            g.run(A, B, C)
+        assert e.value.code == 2
+        with pytest.raises(GemmError) as e:                 # no fused kernel with that ring
+            g.run_epilogue(A[:8], B, C[:8], alpha=2.0)
+        assert e.value.code == 2
+        g.run(A[:16], B, C[:16])                            # 16 rows: fine
+        torch.cuda.synchronize()
+    finally:
+        g.reset_config()
+
+
 def test_a_multicast_rejections(g):
     from dense_gemm_blackwell_02_gb300.binding import GemmError
     A = torch.zeros(256, 1024, dtype=torch.float16, device="cuda")
