@@ -234,9 +234,13 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   if (allow_kx && f.multicast != 2 && !f.block_n && !f.splits && !f.stages && !f.epilogue &&
       !f.chain_kblocks &&
       c->k_blocks >= 8) {
-    for (int bn : {128, 256}) {
+    // 320-column pair tiles (two MMAs per K step) have a cluster-K-split kernel for
+    // single-chain slices only
+    const bool try320 = cg == 2 && ceil_div(c->k_blocks, (int64_t)2) <= chain_kb_of(kb_elems);
+    for (int bn : {128, 256, 320}) {
+      if (bn == 320 && !try320) continue;
       const int st = default_stages(cg, bn, small_a);
-      int64_t sl = resident_units(h, cg, bn, st, out);
+      int64_t sl = bn == 320 ? h->sms / cg : resident_units(h, cg, bn, st, out);
       if (f.max_ctas) sl = std::min<int64_t>(sl, std::max<int64_t>(f.max_ctas / cg, 1));
       const int64_t tl = c->num_m * ceil_div(N, (int64_t)bn);
       if (tl * 2 > sl || std::min<int64_t>({sl / tl, c->k_blocks / 4, 32}) != 2) continue;
@@ -374,6 +378,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
     c->grid = (int)(std::min<int64_t>(c->units, clusters) * 4);
     c->l2_hint = 1;  // the multicast producer issues plain copies
   }
+  if (c->bn == 320 && !(c->kx2 && c->one_chain)) return GEMM_ERR_UNSUPPORTED;
   // the deeper rings of 16-row A stages: plain fp16/bf16 kernels, row tiles of <= 16 rows
   if (a_rows(cg, c->bn, c->stages) < kBlockM && (M > a_rows(cg, c->bn, c->stages) || !allow_kx))
     return GEMM_ERR_UNSUPPORTED;
@@ -479,7 +484,8 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
   }
   const gemm_config_t& c = *cfg;
   if (c.variant < 0 || c.variant > 3) return GEMM_ERR_INVALID_ARG;
-  if (c.block_n != 0 && c.block_n != 128 && c.block_n != 256) return GEMM_ERR_INVALID_ARG;
+  if (c.block_n != 0 && c.block_n != 128 && c.block_n != 256 && c.block_n != 320)
+    return GEMM_ERR_INVALID_ARG;
   if (c.splits < -1 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
       c.dp_tiles != 0 || c.prefetch_kblocks < -1 || c.epilogue < 0 || c.epilogue > 3 ||
       c.l2_hint < 0 || c.l2_hint > 2 || c.multicast < 0 || c.multicast > 2)
@@ -605,13 +611,16 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   // decode shapes than over 8 or more, measured.)
   const int a_box = (ch.variant == 1 && M < kBlockM) ? (int)M : kBlockM;
   if (!make_map(h, A, M, K, dtype_in, a_box, &s.tmA) ||
-      !make_map(h, B, N, K, dtype_in, ch.bn / ch.variant, &s.tmB) ||
+      !make_map(h, B, N, K, dtype_in, ch.bn == 320 ? 128 : ch.bn / ch.variant, &s.tmB) ||
       (ch.half_tail && !make_map(h, B, N, K, dtype_in, ch.bn / ch.variant / 2, &s.tmB2)) ||
       (c_tma && !make_map(h, C, M, N, dtype_out, 32, &s.tmC)))
     return GEMM_ERR_CUDA;
   if (ch.mca) {
     // A's 64-row half boxes, one per pair of the cluster
     if (!make_map(h, A, M, K, dtype_in, kBlockM / 2, &s.tmB2)) return GEMM_ERR_CUDA;
+  } else if (ch.bn == 320) {
+    // the last 32 of each CTA's 160 B rows
+    if (!make_map(h, B, N, K, dtype_in, 32, &s.tmB2)) return GEMM_ERR_CUDA;
   } else if (!ch.half_tail) {
     s.tmB2 = s.tmB;
   }
@@ -643,13 +652,14 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.l2_hint = ch.l2_hint;
   p.a_tx_short = (uint32_t)(a_rows(ch.variant, ch.bn, ch.stages) - a_box) * 128u;
   p.vec_store = c_tma ? 1 : 0;
-  p.tma_store = c_tma ? 1 : 0;
+  p.tma_store = c_tma && ch.bn != 320 ? 1 : 0;  // (320 columns: 160 per warp, direct stores)
   if (fp8) {
     p.idesc = idesc_f8_kmajor(kBlockM * ch.variant, ch.bn, dtype_in == GEMM_E5M2);
     p.idesc_half = idesc_f8_kmajor(kBlockM * ch.variant, ch.bn / 2, dtype_in == GEMM_E5M2);
   } else {
-    p.idesc = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn, dtype_in == GEMM_BF16);
-    p.idesc_half = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn / 2, dtype_in == GEMM_BF16);
+    p.idesc = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn == 320 ? 256 : ch.bn, dtype_in == GEMM_BF16);
+    p.idesc_half = idesc_f16_kmajor(kBlockM * ch.variant, ch.bn == 320 ? 64 : ch.bn / 2,
+                                    dtype_in == GEMM_BF16);
   }
   if (bs) {
     p.sfa = bs->sfa;
@@ -749,7 +759,7 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
   const int bn = f.block_n ? f.block_n : (narrow ? 128 : 256);
   const int stages = f.stages ? f.stages : default_stages(cg, bn);
   if (!kernel_supported(cg, bn, stages)) return GEMM_ERR_INVALID_ARG;
-  if (a_rows(cg, bn, stages) < kBlockM) return GEMM_ERR_UNSUPPORTED;  // no grouped kernel
+  if (a_rows(cg, bn, stages) < kBlockM || bn == 320) return GEMM_ERR_UNSUPPORTED;  // no grouped kernel
 
   // The next table of the ring: its host copy is free once its last upload is done.
   const int slot = h->group_next;

@@ -552,7 +552,11 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
                 const GemmParams p) {
   using L = Layout<CTA_GROUP, BN, STAGES>;
-  static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+  static_assert(BN == 128 || BN == 256 || BN == 320, "BN must be 128, 256 or 320");
+  // 320 columns: two MMAs per K step (N = 256 and N = 64) into one 320-column
+  // accumulator; built for the pair's cluster K split with single-chain slices only (one
+  // unit per CTA group, so one accumulator slot)
+  static_assert(BN != 320 || (CTA_GROUP == 2 && KX2 && ONE_CHAIN), "BN 320: pair, cluster K split");
   static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "CTA_GROUP must be 1 or 2");
   static_assert(KIND != 2 || !ONE_CHAIN, "blockwise scales need the general epilogue");
   static_assert(!GROUPED || (!ONE_CHAIN && !FUSED && KIND == 0),
@@ -561,12 +565,13 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
                 "the cluster K split uses the plain epilogues");
   static_assert(!MCA || (CTA_GROUP == 2 && !KX2 && !GROUPED && !FUSED && KIND == 0 && !STAGED),
                 "the multicast of A pairs plain CTA-pair kernels");
-  constexpr uint32_t kTmemCols = 2 * BN;       // two accumulator slots
+  constexpr uint32_t kTmemCols = BN == 320 ? 512 : 2 * BN;  // two accumulator slots (one for 320)
   constexpr int kHalf = BN / 2;                // columns per epilogue warp
   constexpr int kPieces = kHalf / 32;          // tcgen05.ld x32 pieces per warp
   constexpr int kOutBytes = OUT == kOutF32 ? 4 : 2;
   constexpr int kBoxCols = 128 / kOutBytes;    // columns of one 128-byte staging row
   constexpr int kBoxes = kHalf / kBoxCols;     // staging boxes per warp
+  constexpr bool kTmaStoreOk = kHalf % kBoxCols == 0;  // (BN 320 writes C with direct stores)
   constexpr int kRowsTile = kBlockM * CTA_GROUP;
   constexpr int kKbElems = KIND == 0 ? kBlockK : 2 * kBlockK;  // K elements per K block
 
@@ -631,7 +636,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     if constexpr (!GROUPED) {  // a grouped launch's maps live in global memory
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
-      if (p.half_tail || MCA) tma_prefetch_desc(&tmB2);
+      if (p.half_tail || MCA || BN == 320) tma_prefetch_desc(&tmB2);
       if (p.tma_store) tma_prefetch_desc(&tmC);
     }
   }
@@ -674,9 +679,12 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
         // a half-tile unit loads half the B rows (through the half-height map tmB2)
         const bool half = w.half >= 0;
+        // (BN 320: each CTA's first 128 B rows are columns 128 * rank.. of the tile, its
+        // last 32 columns 256 + 32 * rank.., so that the accumulator's columns are in order)
         const int32_t b_row = w.n_blk * BN +
                               (half ? w.half * (BN / 2) + (int32_t)rank * (L::kRowsB / 2)
-                                    : (int32_t)rank * L::kRowsB);
+                                    : (int32_t)rank * (BN == 320 ? 128 : L::kRowsB));
+        const int32_t b_row320 = w.n_blk * BN + 256 + (int32_t)rank * 32;
         const CUtensorMap* mapB = half ? &tmB2 : &tmB;
         const CUtensorMap* mapA = &tmA;
         uint32_t tx = (half ? L::kTxBytesHalf : L::kTxBytes) - p.a_tx_short;
@@ -730,11 +738,17 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
             } else if constexpr (kHint) {
               tma_load_2d_pair_hint_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
                                           leader_full, pol_b);
+              if constexpr (BN == 320)  // rows 256 + 32 * rank.. of the tile (32-row map)
+                tma_load_2d_pair_hint_elect(sB + stage * L::kBBytes + 128 * 128, &tmB2,
+                                            kb * kKbElems, b_row320, leader_full, pol_b);
               tma_load_2d_pair_hint_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
                                           leader_full, pol_a);
             } else {
               tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
                                      leader_full);
+              if constexpr (BN == 320)
+                tma_load_2d_pair_elect(sB + stage * L::kBBytes + 128 * 128, &tmB2, kb * kKbElems,
+                                       b_row320, leader_full);
               tma_load_2d_pair_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
                                      leader_full);
             }
@@ -798,8 +812,14 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
             // four MMAs of 32 bytes of K, then the commit that frees the stage (in both
             // CTAs) once they are done
             static_assert(kBlockK * 2 == 128, "umma_stage_elect covers 128 bytes of K");
-            umma_stage_elect<CTA_GROUP, KIND>(d_tmem, da, db, idesc, kb > c0 ? 1u : 0u,
-                                              empty_bar(stage), stage_mask);
+            if constexpr (BN == 320) {
+              // columns 0-255 from each CTA's first 128 B rows, 256-319 from the next 32
+              umma_stage320_elect(d_tmem, da, db, p.idesc, p.idesc_half, kb > c0 ? 1u : 0u,
+                                  empty_bar(stage), stage_mask);
+            } else {
+              umma_stage_elect<CTA_GROUP, KIND>(d_tmem, da, db, idesc, kb > c0 ? 1u : 0u,
+                                                empty_bar(stage), stage_mask);
+            }
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -930,7 +950,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
           __syncwarp();
         }
         if (emit) {
-          if (p.tma_store) {
+          if (kTmaStoreOk && p.tma_store) {
             constexpr int kPiecesPerBox = kBoxCols / 32;
             const uint32_t row_addr = staging + lane * 128u;
 #pragma unroll

@@ -7,13 +7,14 @@ namespace gb300 {
 bool kernel_supported(int cg, int bn, int stages) {
   if (cg == 1)
     return (bn == 256 && (stages == 4 || stages == 5)) || (bn == 128 && (stages == 6 || stages == 10));
-  if (cg == 2) return (bn == 256 && stages == 6) || (bn == 128 && stages == 8);
+  if (cg == 2) return (bn == 256 && stages == 6) || (bn == 128 && stages == 8) ||
+                     (bn == 320 && stages == 5);
   return false;
 }
 
 int default_stages(int cg, int bn, bool small_a) {
   if (cg == 1) return bn == 256 ? (small_a ? 5 : 4) : (small_a ? 10 : 6);
-  return bn == 256 ? 6 : 8;
+  return bn == 320 ? 5 : bn == 256 ? 6 : 8;
 }
 
 size_t kernel_smem_bytes(int cg, int bn, int stages) {
@@ -22,6 +23,7 @@ size_t kernel_smem_bytes(int cg, int bn, int stages) {
     if (bn == 256) return stages == 5 ? Layout<1, 256, 5>::kDynamicBytes : Layout<1, 256, 4>::kDynamicBytes;
     return stages == 10 ? Layout<1, 128, 10>::kDynamicBytes : Layout<1, 128, 6>::kDynamicBytes;
   }
+  if (bn == 320) return Layout<2, 320, 5>::kDynamicBytes;
   return bn == 256 ? Layout<2, 256, 6>::kDynamicBytes : Layout<2, 128, 8>::kDynamicBytes;
 }
 

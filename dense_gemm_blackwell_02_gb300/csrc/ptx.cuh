@@ -403,6 +403,36 @@ __device__ __forceinline__ void umma_f16_elect(uint32_t d_tmem, uint64_t a_desc,
   "@e_ tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64" \
   " [%5], %6;"
 
+// One 64-deep stage of a 320-column pair tile: per 16-deep K step an N = 256 MMA into
+// columns 0-255 (B from the stage start) and an N = 64 MMA into columns 256-319 (B from
+// 16 KiB on: the descriptor's address field counts 16-byte units), then the commit.
+__device__ __forceinline__ void umma_stage320_elect(uint32_t d_tmem, uint64_t a_desc,
+                                                    uint64_t b_desc, uint32_t idesc256,
+                                                    uint32_t idesc64, uint32_t accumulate,
+                                                    uint32_t empty_bar, uint16_t cta_mask) {
+  asm volatile(GB300_ELECT
+               ".reg .pred p_;\n\t.reg .b64 a1_, a2_, a3_, b1_, b2_, b3_, c0_, c1_, c2_, c3_;\n\t"
+               ".reg .b32 d2_;\n\t"
+               "setp.ne.b32 p_, %4, 0;\n\t"
+               "add.s64 a1_, %1, 2;\n\tadd.s64 a2_, %1, 4;\n\tadd.s64 a3_, %1, 6;\n\t"
+               "add.s64 b1_, %2, 2;\n\tadd.s64 b2_, %2, 4;\n\tadd.s64 b3_, %2, 6;\n\t"
+               "add.s64 c0_, %2, 1024;\n\tadd.s64 c1_, %2, 1026;\n\t"
+               "add.s64 c2_, %2, 1028;\n\tadd.s64 c3_, %2, 1030;\n\t"
+               "add.u32 d2_, %0, 256;\n\t"
+               "@e_ tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p_;\n\t"
+               "@e_ tcgen05.mma.cta_group::2.kind::f16 [d2_], %1, c0_, %7, p_;\n\t"
+               "@e_ tcgen05.mma.cta_group::2.kind::f16 [%0], a1_, b1_, %3, 1;\n\t"
+               "@e_ tcgen05.mma.cta_group::2.kind::f16 [d2_], a1_, c1_, %7, 1;\n\t"
+               "@e_ tcgen05.mma.cta_group::2.kind::f16 [%0], a2_, b2_, %3, 1;\n\t"
+               "@e_ tcgen05.mma.cta_group::2.kind::f16 [d2_], a2_, c2_, %7, 1;\n\t"
+               "@e_ tcgen05.mma.cta_group::2.kind::f16 [%0], a3_, b3_, %3, 1;\n\t"
+               "@e_ tcgen05.mma.cta_group::2.kind::f16 [d2_], a3_, c3_, %7, 1;\n\t"
+               GB300_STAGE_COMMIT_2 "\n\t}"
+               ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc256), "r"(accumulate),
+               "r"(empty_bar), "h"(cta_mask), "r"(idesc64)
+               : "memory");
+}
+
 // cta_mask: the pair's two CTAs in the cluster (0b11, or 0b1100 for the second pair of
 // a four-CTA cluster).
 template <int CTA_GROUP, int KIND = 0>

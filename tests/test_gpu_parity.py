@@ -601,6 +601,54 @@ def test_a_multicast_rejections(g):
         g.reset_config()
 
 
+@pytest.mark.parametrize("M,N,K,dtype_out", [(256, 1280, 4096, F16), (256, 1000, 2048, BF16),
+                                             (200, 700, 8192, F32), (256, 3200, 1024, F16)])
+def test_320_column_pair_tiles(g, M, N, K, dtype_out):
+    # two MMAs per K step (N = 256 and N = 64) into one 320-column accumulator, each CTA
+    # loading 128 + 32 B rows; two K slices in a 4-CTA cluster
+    g.set_config(variant=2, block_n=320, splits=2, epilogue=3)
+    try:
+        _case(g, M, N, K, F16, dtype_out, seed=50)
+        used = g.last_config()
+        _case(g, M, N, K, BF16, F32, seed=51, exact=True, ints=True)
+    finally:
+        g.reset_config()
+    assert used["block_n"] == 320 and used["epilogue"] == 3 and used["splits"] == 2, used
+
+
+def test_320_column_tiles_taken_when_256_do_not_fit_the_split(g):
+    # 40 tiles of 256 columns need 80 pairs for two K slices; 32 tiles of 320 need 64
+    M, N, K = 256, 10240, 2048
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=52)
+    C = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    g.reset_config()
+    g.run(A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    assert g.device_status()[0] == 0
+    cfg = g.last_config()
+    assert cfg["block_n"] == 320 and cfg["epilogue"] == 3, cfg
+    rows = si.sample_indices(M, 10, seed=53, must=(0, 127, 128, 255))
+    parity.oracle_check(parity.bits_of(C.cpu()[rows]), A, B, F16, F16, rows=rows,
+                        what=f"auto 320-column tiles {cfg}")
+
+
+def test_320_column_rejections(g):
+    from dense_gemm_blackwell_02_gb300.binding import GemmError
+    A = torch.zeros(256, 16384, dtype=torch.float16, device="cuda")
+    B = torch.zeros(640, 16384, dtype=torch.float16, device="cuda")
+    C = torch.zeros(256, 640, dtype=torch.float16, device="cuda")
+    for cfg in ({"variant": 2, "block_n": 320},                           # no K split
+                {"variant": 2, "block_n": 320, "splits": 2, "epilogue": 3},  # slices of 2 chains
+                {"variant": 1, "block_n": 320, "splits": 2, "epilogue": 3}):  # one CTA
+        g.set_config(**cfg)
+        try:
+            with pytest.raises(GemmError) as e:
+                g.run(A, B, C)
+            assert e.value.code in (1, 2), cfg
+        finally:
+            g.reset_config()
+
+
 def test_cluster_k_split_rejections(g):
     from dense_gemm_blackwell_02_gb300.binding import GemmError
     A = torch.zeros(256, 4096, dtype=torch.float16, device="cuda")
