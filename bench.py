@@ -166,7 +166,9 @@ def cpu_rows_sample(A, B, din, dout, M, target_s=10.0):
     enough rows for ~target_s seconds.  Returns (rows, bits, seconds, threads)."""
     import oracle
     N, K = B.shape[0], B.shape[1]
-    probe = si.sample_indices(M, 32, seed=99)
+    # a probe of 128 rows (fewer timed too short to scale from: the estimate then fell
+    # well below the target)
+    probe = si.sample_indices(M, min(M, 128), seed=99)
     oracle.gemm_select(A, B, probe[:2], None, din, dout)   # decode tables, threads
     t0 = time.perf_counter()
     oracle.gemm_select(A, B, probe, None, din, dout)
