@@ -166,18 +166,28 @@ def cpu_rows_sample(A, B, din, dout, M, target_s=10.0):
     enough rows for ~target_s seconds.  Returns (rows, bits, seconds, threads)."""
     import oracle
     N, K = B.shape[0], B.shape[1]
-    # a probe of 128 rows (fewer timed too short to scale from: the estimate then fell
-    # well below the target)
-    probe = si.sample_indices(M, min(M, 128), seed=99)
-    oracle.gemm_select(A, B, probe[:2], None, din, dout)   # decode tables, threads
-    t0 = time.perf_counter()
-    oracle.gemm_select(A, B, probe, None, din, dout)
-    t = max(time.perf_counter() - t0, 1e-3)
-    nrows = int(min(M, max(32, len(probe) * target_s / t)))
-    rows = si.sample_indices(M, nrows, seed=7, must=(0, 127, 128, 255, 256, -1))
-    t0 = time.perf_counter()
-    bits, c64 = oracle.gemm_select(A, B, rows, None, din, dout, want_f64=True)
-    dt = time.perf_counter() - t0
+    # Two probes (32 and 128 rows) separate each call's fixed cost (operand conversion)
+    # from the cost per row, so that the sample is sized to the target.
+    oracle.gemm_select(A, B, si.sample_indices(M, 2, seed=98), None, din, dout)  # tables, threads
+    times = []
+    for n in (min(M, 32), min(M, 128)):
+        probe = si.sample_indices(M, n, seed=99)
+        t0 = time.perf_counter()
+        oracle.gemm_select(A, B, probe, None, din, dout)
+        times.append((n, time.perf_counter() - t0))
+    (n1, t1), (n2, t2) = times
+    per_row = max((t2 - t1) / max(n2 - n1, 1), t2 / max(n2, 1) * 0.05, 1e-7)
+    fixed = max(t1 - per_row * n1, 0.0)
+    nrows = int(min(M, max(32, (target_s - fixed) / per_row)))
+    for attempt in range(2):
+        rows = si.sample_indices(M, nrows, seed=7, must=(0, 127, 128, 255, 256, -1))
+        t0 = time.perf_counter()
+        bits, c64 = oracle.gemm_select(A, B, rows, None, din, dout, want_f64=True)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * target_s or len(rows) >= M:
+            break
+        # the probes overestimated a row: size once more from this run
+        nrows = int(min(M, len(rows) * target_s / max(dt, 1e-3)))
     return rows, bits, c64, dt, os.cpu_count()
 
 
