@@ -180,7 +180,9 @@ def cpu_rows_sample(A, B, din, dout, M, target_s=10.0):
     fixed = max(t1 - per_row * n1, 0.0)
     nrows = int(min(M, max(32, (target_s - fixed) / per_row)))
     for attempt in range(2):
-        rows = si.sample_indices(M, nrows, seed=7, must=(0, 127, 128, 255, 256, -1))
+        # (draws with repeats: every row once the count reaches M)
+        rows = (list(range(M)) if nrows >= M else
+                si.sample_indices(M, nrows, seed=7, must=(0, 127, 128, 255, 256, -1)))
         t0 = time.perf_counter()
         bits, c64 = oracle.gemm_select(A, B, rows, None, din, dout, want_f64=True)
         dt = time.perf_counter() - t0
