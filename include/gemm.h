@@ -70,7 +70,11 @@ typedef enum {
  *             3 = the CUDA-core matrix-vector path for M <= 4 (fp16/bf16 inputs, no
  *                 fused epilogue; other fields ignored except max_ctas); chosen
  *                 automatically for M == 1 with K <= 16384
- *   block_n   128 or 256 columns of C per tile
+ *   block_n   128 or 256 columns of C per tile; or 320 (two MMAs per K step, N = 256
+ *             and N = 64) for CTA pairs under the cluster K split with single-chain
+ *             slices only (epilogue 3; else GEMM_ERR_UNSUPPORTED), chosen automatically
+ *             when 256-column tiles cannot be cut into two K slices within the resident
+ *             pairs and 320-column tiles can
  *   splits    K slices per tile (1 = no split; >1 = split-K with a deterministic
  *             in-kernel reduction in slice order; -1 = stream-K: every resident unit
  *             takes an equal share of the (tile, K block) iterations).
