@@ -33,11 +33,6 @@ __device__ __forceinline__ void fence_mbarrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -66,18 +61,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_try_wait_cluster_acq(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // ------------------------------------------------- warp-uniform single issue --
 // The producer and MMA warps run their loops with all 32 lanes in lock-step, so the
 // compiler keeps loop state and descriptors warp-uniform; each asynchronous
@@ -91,10 +74,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32
   asm volatile(GB300_ELECT "@e_ mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar),
                "r"(bytes)
                : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_elect(uint32_t bar) {
-  asm volatile(GB300_ELECT "@e_ mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar) : "memory");
 }
 
 // Programmatic dependent launch: wait until the grids this one depends on (the
@@ -118,10 +97,6 @@ __device__ __forceinline__ void tc_fence_before() {
 
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // ------------------------------------------------------------------- cluster --
@@ -178,16 +153,8 @@ __device__ __forceinline__ void fence_tensormap_acquire(const void* tmap) {
                ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// 2-D tiled load global -> this CTA's shared memory, completing on `bar` (this CTA).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-
+// 2-D tiled load global -> this CTA's shared memory, completing on `bar` (this CTA);
+// one elected lane issues it.
 __device__ __forceinline__ void tma_load_2d_elect(uint32_t dst, const void* tmap, int32_t c0,
                                                   int32_t c1, uint32_t bar) {
   asm volatile(GB300_ELECT
@@ -197,6 +164,8 @@ __device__ __forceinline__ void tma_load_2d_elect(uint32_t dst, const void* tmap
                : "memory");
 }
 
+// 2-D tiled load for a CTA pair: the data lands in this CTA's shared memory, the
+// completion is signalled on `cluster_bar`, which may live in the peer CTA.
 __device__ __forceinline__ void tma_load_2d_pair_elect(uint32_t dst, const void* tmap, int32_t c0,
                                                        int32_t c1, uint32_t cluster_bar) {
   asm volatile(
@@ -213,16 +182,6 @@ __device__ __forceinline__ void tma_prefetch_l2_2d_elect(const void* tmap, int32
                    reinterpret_cast<uint64_t>(tmap)),
                "r"(c0), "r"(c1)
                : "memory");
-}
-
-// Same, with an L2 cache-policy hint.
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap, int32_t c0,
-                                                 int32_t c1, uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-      : "memory");
 }
 
 // L2 cache policies for the hinted loads: the whole access range marked first to be
@@ -271,17 +230,6 @@ __device__ __forceinline__ void tma_load_2d_pair_mc_elect(uint32_t dst, const vo
       "@e_ cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".multicast::cluster.cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(cluster_bar), "h"(cta_mask)
-      : "memory");
-}
-
-// 2-D tiled load for a CTA pair: the data lands in this CTA's shared memory, the
-// completion is signalled on `cluster_bar`, which may live in the peer CTA.
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t c0,
-                                                 int32_t c1, uint32_t cluster_bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(cluster_bar)
       : "memory");
 }
 
@@ -341,39 +289,8 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }
 
 // ------------------------------------------------------------------- tcgen05.mma --
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (fp16 or bf16 inputs, fp32 D).
-template <int CTA_GROUP>
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  if constexpr (CTA_GROUP == 1)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  else
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Warp-uniform forms: every lane executes them, one elected lane issues.
-template <int CTA_GROUP>
-__device__ __forceinline__ void umma_f16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                               uint32_t idesc, uint32_t accumulate) {
-  if constexpr (CTA_GROUP == 1)
-    asm volatile(GB300_ELECT ".reg .pred p_;\n\tsetp.ne.b32 p_, %4, 0;\n\t"
-                 "@e_ tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p_;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-  else
-    asm volatile(GB300_ELECT ".reg .pred p_;\n\tsetp.ne.b32 p_, %4, 0;\n\t"
-                 "@e_ tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p_;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, fp32 D; issued by one elected lane of a
+// warp whose lanes all execute the call.
 
 // One 128-byte-deep stage (64 fp16/bf16 or 128 FP8 values of K): four MMAs of 32 bytes
 // of K each (K=16 for kind::f16, K=32 for kind::f8f6f4; descriptor start addresses
@@ -445,6 +362,8 @@ __device__ __forceinline__ void umma_stage_elect(uint32_t d_tmem, uint64_t a_des
   else GB300_STAGE_MMA(2, "f8f6f4");
 }
 
+// Make `bar` arrive once all MMAs this thread issued before have completed (the
+// cta_group must match the one every other tcgen05 instruction of the kernel uses).
 template <int CTA_GROUP>
 __device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
   if constexpr (CTA_GROUP == 1)
@@ -459,35 +378,13 @@ __device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
                  : "memory");
 }
 
+// Pair form: the arrive lands on the barrier at the same offset in every CTA of cta_mask.
 __device__ __forceinline__ void umma_commit_pair_elect(uint32_t bar, uint16_t cta_mask) {
   asm volatile(GB300_ELECT
                "@e_ tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
                " [%0], %1;\n\t}" ::"r"(bar),
                "h"(cta_mask)
                : "memory");
-}
-
-// Make `bar` (this CTA) arrive once all previously issued MMAs of this thread completed.
-// The cta_group must match the one every other tcgen05 instruction of the kernel uses.
-template <int CTA_GROUP>
-__device__ __forceinline__ void umma_commit_group(uint32_t bar) {
-  if constexpr (CTA_GROUP == 1)
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     bar)
-                 : "memory");
-  else
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     bar)
-                 : "memory");
-}
-
-// Pair form: the arrive lands on the barrier at the same offset in every CTA named in mask.
-__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
 }
 
 // 32 lanes x 32 bits, 32 consecutive columns: thread t of the warp receives lane
