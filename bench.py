@@ -1,16 +1,19 @@
 """Benchmark of the GB300 GEMM  C = A . B^T  (one JSON line on rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload square_4096|...]
+                    [--workload square_4096|...] [--seconds S]
 
-A step is one GEMM over the workload's synthetic seeded operands (inputs
-resident in HBM).  By default a 512 MiB buffer is overwritten before each step
-to flush the 129 MB L2, outside that step's pair of CUDA events on the launching
-stream.  `--l2 rotate` instead cycles through copies of A, B and C totalling at
-least four times the L2 with the K steps launched back to back between two
-events (cold operands in every step, no launch gap; the GPU then runs at its
-power cap throughout).  The decode shapes are always timed the second way.
-`value` is TFLOP/s (2MNK per step) over all ranks; `e2e` is the same metric through gemm_run_host with
+A step is a batch of R GEMMs over the workload's synthetic seeded operands
+(inputs resident in HBM), R chosen after the warm-up so that the K timed steps
+last about S seconds (default 12): long enough for clock samplers polling a few
+times a second to see the GPU under this load.  By default a 512 MiB buffer is
+overwritten before each GEMM to flush the 129 MB L2, outside that GEMM's pair of
+CUDA events on the launching stream; a step's time is the sum of its GEMMs'.
+`--l2 rotate` instead cycles through copies of A, B and C totalling at least
+four times the L2 with the step's R launches back to back between two events
+(cold operands in every launch, no launch gap; the GPU then runs at its power
+cap throughout).  The decode shapes are always timed the second way.
+`value` is TFLOP/s (2MNK per GEMM) over all ranks; `e2e` is the same metric through gemm_run_host with
 pinned host buffers (host->device copies of A and B and the device->host copy
 of C inside the timed region).  `cpu_baseline` times the CPU oracle on a
 bounded sample of the same product (whole rows of C) on the host cores, and
@@ -29,7 +32,9 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
+from datetime import datetime
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -47,6 +52,10 @@ L2_FLUSH_BYTES = 512 << 20
 L2_NOMINAL_BYTES = 129 * 1000 * 1000
 # Nominal GB300 figures, reported as context beside the measured peaks.
 NOMINAL_TFLOPS = 2250.0   # dense fp16/bf16
+# Dense fp16/bf16 tensor work of one SM per clock ("Optimizing GEMMs using tcgen05":
+# a 128 x 256 x 16 MMA in 128 cycles); times the SMs and the SM clock observed under
+# load, the peak at the clock the kernel actually ran at.
+TENSOR_FLOP_PER_SM_CLK = 8192
 NOMINAL_HBM_GBS = 7900.0
 NOMINAL_FP8_RATIO = 2.0  # dense FP8 / dense bf16 (4.5 / 2.25 PFLOP/s nominal)
 # The device code of the kernels (the host-side files -- the C ABI, the launch table --
@@ -100,8 +109,10 @@ def replica_throughput(world: int, flops_per_step: float, steps: int, slowest_ms
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+    """nvidia-smi clock / throttle-reason sampling; statistics are taken over the
+    samples inside the timed region (mark() brackets it), and among those over the ones
+    with the GPU busy (utilization >= 30%).  The samples go to a temporary file."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
               "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -109,19 +120,56 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = None
+        self.fh = None
+        self.window = None
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
-            self.fh = open(self.path, "w")
+            self.fh = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def mark(self, t0: datetime, t1: datetime):
+        """The timed region, in the host's local time (nvidia-smi's timestamps)."""
+        self.window = (t0, t1)
+
+    @staticmethod
+    def parse(lines, window=None):
+        rows = []
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 11:
+                continue
+            try:
+                ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append({"t": ts, "sm": float(parts[2]), "max": float(parts[3]),
+                             "power": float(parts[4]), "util": float(parts[5]),
+                             "hw": parts[7], "hw_thermal": parts[8], "sw_thermal": parts[9],
+                             "sw_power": parts[10]})
+            except ValueError:
+                continue
+        inside = [r for r in rows if window is None or window[0] <= r["t"] <= window[1]]
+        loaded = [r for r in inside if r["util"] >= 30]
+        use = loaded or inside
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "samples": 0, "samples_under_load": 0}
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in use):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in use),
+                "sm_max_mhz": max(r["max"] for r in use),
+                "sm_mhz_min": min(r["sm"] for r in use), "reasons": reasons,
+                "power_w_max": max(r["power"] for r in use),
+                "samples": len(inside), "samples_under_load": len(loaded),
+                "over": "samples inside the timed region with utilization >= 30%"
+                        if loaded else "samples inside the timed region (none busy)"}
 
     def stop(self):
         if self.proc is None:
@@ -131,29 +179,10 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        self.fh.seek(0)
+        out = self.parse(self.fh.readlines(), self.window)
         self.fh.close()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "util": float(parts[4]),
-                             "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
-                             "sw_power": parts[9]})
-            except ValueError:
-                continue
-        loaded = [r for r in rows if r["util"] >= 30] or rows
-        if not loaded:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        reasons = []
-        for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
-                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
-            if any(r[key].lower() == "active" for r in loaded):
-                reasons.append(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
-                "sm_max_mhz": max(r["max"] for r in loaded), "reasons": reasons,
-                "samples": len(loaded)}
+        return out
 
 
 def workload_shape(name: str):
@@ -454,26 +483,68 @@ def run_ours(args):
     if code != 0:
         raise RuntimeError(f"device status after warm-up: {code} ({word:#x})")
 
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.25)  # let the sampler take its first reading
-    for i in range(max(args.warmup, 3)):
+    # R GEMMs per step, so that the K timed steps last about args.seconds: calibrated on
+    # the wall time of a few warm-up steps of the same form.
+    t0 = time.perf_counter()
+    for i in range(16):
         if flush is not None:
             flush.fill_(1.0)
         run(*sets[i % len(sets)])
+    torch.cuda.synchronize()
+    per_launch_s = (time.perf_counter() - t0) / 16
+    reps = max(1, int(round(args.seconds / max(args.steps, 1) / max(per_launch_s, 1e-6))))
+    if args.reps:
+        reps = args.reps
+    if ws > 1:
+        # every rank runs the same R (rank 0's)
+        r = torch.tensor([reps], dtype=torch.int64, device=dev)
+        torch.distributed.broadcast(r, 0)
+        reps = int(r.item())
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps if flush is not None else 1)]
+
+    def step(i0):
+        """One step: R GEMMs; returns (ms of the step's GEMMs, per-launch ms list)."""
+        if flush is not None:
+            for j in range(reps):
+                flush.fill_(float(j & 7))
+                ev[j][0].record(stream)
+                run(*sets[0])
+                ev[j][1].record(stream)
+            torch.cuda.synchronize()
+            each = [a.elapsed_time(b) for a, b in ev]
+            return sum(each), each
+        # back to back between one event pair (events between the launches would stop
+        # each from starting early: programmatic dependent launch)
+        ev[0][0].record(stream)
+        for j in range(reps):
+            run(*sets[(i0 + j) % len(sets)])
+        ev[0][1].record(stream)
+        torch.cuda.synchronize()
+        t = ev[0][0].elapsed_time(ev[0][1])
+        return t, [t / reps]
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.25)  # let the sampler take its first reading
+    for i in range(args.warmup):
+        step(i * reps)
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    # Per-step events only in the flushed form: between back-to-back launches they would
-    # also stop each launch from starting early (programmatic dependent launch).
-    if flush is not None:
-        local_ms, each_ms = time_steps(run, sets, stream, args.steps, flush, per_step=True)
-    else:
-        local_ms = time_steps(run, sets, stream, args.steps)
-        each_ms = [local_ms / args.steps]
+    wall0 = datetime.now()
+    step_ms, each_ms = [], []
+    for i in range(args.steps):
+        t, each = step(i * reps)
+        step_ms.append(t)
+        each_ms += each
     if ws > 1:
         torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall1 = datetime.now()
+    local_ms = sum(step_ms)
     time.sleep(0.1)
+    sampler.mark(wall0, wall1)
     clocks = sampler.stop()
     total_ms = max_over_ranks(local_ms, dev)
     code, word = g.device_status(stream)
@@ -501,8 +572,9 @@ def run_ours(args):
     grouped = measure_grouped(g, dev, stream, peaks) if args.grouped else None
     flops = rl.gemm_flops(M, N, K)
     ms_per_step = total_ms / args.steps
-    value = replica_throughput(ws, flops, args.steps, total_ms)
-    kernel_tflops = flops / (ms_per_step * 1e-3) / 1e12
+    value = replica_throughput(ws, flops * reps, args.steps, total_ms)
+    ms_per_launch = total_ms / (args.steps * reps)
+    kernel_tflops = flops / (ms_per_launch * 1e-3) / 1e12
 
     # ---- end to end through the C ABI with pinned host buffers
     A_h = A_cpu.pin_memory()
@@ -534,11 +606,20 @@ def run_ours(args):
         cpu_value = 2.0 * len(rows) * N * K / cpu_s / 1e12
 
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         peak_note = f"{peak_src} bf16_tflops (burst; fp16 has the same dense rate)"
+        ratio = 1.0
         if in_b == 1:
+            ratio = NOMINAL_FP8_RATIO
             peak = fp8_peak(peaks)
+            peak_sus *= ratio
             peak_note = (f"{peak_src} bf16_tflops (burst) x {NOMINAL_FP8_RATIO:g}, the nominal "
                          f"FP8 / bf16 dense ratio")
+        # the tensor peak at the SM clock observed under load during the timed region
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        clock_peak = None
+        if clocks.get("sm_mhz"):
+            clock_peak = sms * TENSOR_FLOP_PER_SM_CLK * ratio * clocks["sm_mhz"] * 1e6 / 1e12
         traffic = None
         tf_path = os.path.join(ROOT, "profiles", "traffic.json")
         if os.path.exists(tf_path):
@@ -557,13 +638,23 @@ def run_ours(args):
                        "kernel": cfg, "parallelism": "replicas" if ws > 1 else "single-gpu"},
             "clocks": clocks,
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * reps,
             "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak,
                          "unit": "TFLOP/s", "frac": kernel_tflops / peak, "traffic": traffic,
                          "peak_source": peak_note,
+                         "frac_of_sustained": kernel_tflops / peak_sus,
+                         "sustained_peak": peak_sus,
+                         "clock_peak": clock_peak,
+                         "frac_of_clock_peak": (kernel_tflops / clock_peak) if clock_peak else None,
+                         "clock_peak_source": (f"{sms} SMs x {TENSOR_FLOP_PER_SM_CLK * ratio:g} "
+                                               f"FLOP/clk x the median SM clock under load"),
+                         "kernel_mcycles": (ms_per_launch * 1e-3 * clocks["sm_mhz"])
+                                           if clocks.get("sm_mhz") else None,
                          "algorithmic_flops_per_launch": flops},
-            "per_step_us": {"median": 1e3 * statistics.median(each_ms), "best": 1e3 * min(each_ms),
-                            "mean": 1e3 * ms_per_step},
+            "gemms_per_step": reps,
+            "per_launch_us": {"median": 1e3 * statistics.median(each_ms), "best": 1e3 * min(each_ms),
+                              "mean": 1e3 * ms_per_launch},
+            "timed_region_s": (wall1 - wall0).total_seconds(),
             "timed_other_way": {"how": other_how, "us": 1e3 * other_ms,
                                 "TFLOP/s": flops / (other_ms * 1e-3) / 1e12},
             "nominal_context": {"tensor_tflops": NOMINAL_TFLOPS, "hbm_gbs": NOMINAL_HBM_GBS,
@@ -597,6 +688,9 @@ def main():
     ap.add_argument("--workload", default="square_4096", choices=sorted(si.WORKLOADS))
     ap.add_argument("--config", default=None, help="JSON gemm_config_t override (sweeps)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--seconds", type=float, default=12.0,
+                    help="target length of the timed region (sets the GEMMs per step)")
+    ap.add_argument("--reps", type=int, default=0, help="GEMMs per step (0: from --seconds)")
     ap.add_argument("--decode", type=int, default=2,
                     help="also time the M=256 decode shapes (HBM GB/s) into the line; "
                          "2 adds the M=1..128 decode shapes")

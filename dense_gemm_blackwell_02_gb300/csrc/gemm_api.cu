@@ -146,7 +146,6 @@ struct Choice {
   int l2_hint;
   bool one_chain;
   bool kx2;  // the two K slices of a tile reduced inside a cluster (single chain)
-  bool mca;  // A multicast across two CTA pairs (units are pairs of tiles)
   int64_t tiles, dp_tiles, units, k_blocks, num_m, num_n;
   int64_t sk_workers, ws_slots;
 };
@@ -231,7 +230,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   // 93.7 us against 96.2, M <= 128 x 8192 x 28672 82-84 against 84-86).  Unsplit
   // 128-column tiles stay when K is short (256 x 8192 x 4096: 21.9 us against 23.2).
   bool auto_kx = false;
-  if (allow_kx && f.multicast != 2 && !f.block_n && !f.splits && !f.stages && !f.epilogue &&
+  if (allow_kx && !f.block_n && !f.splits && !f.stages && !f.epilogue &&
       !f.chain_kblocks &&
       c->k_blocks >= 8) {
     // 320-column pair tiles (two MMAs per K step) have a cluster-K-split kernel for
@@ -259,10 +258,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   int64_t s = 1, dp = c->tiles;
   c->half_tail = 0;
   c->sk_workers = 0;
-  if (f.multicast == 2) {
-    // every tile whole (the multicast pairs two whole tiles)
-    if (f.splits > 1 || f.splits < 0) return GEMM_ERR_UNSUPPORTED;
-  } else if (f.splits < 0) {
+  if (f.splits < 0) {
     // forced stream-K: every resident unit takes an equal share of the (tile, k-block)
     // iterations ("A Blackwell GEMM by Hand in CuTe DSL", section 9; "CUTLASS Deep
     // Dive", StreamK).  Measured on the M = 256 decode shapes it lost to split-K (the
@@ -345,7 +341,6 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   // The cluster K split: every tile's two K slices run on the two CTA groups of one
   // cluster of 2 * cg CTAs, each group one unit, and meet in distributed shared memory.
   c->kx2 = false;
-  c->mca = false;
   if (f.epilogue == 3 || auto_kx) {
     bool valid = allow_kx && !c->sk_workers && !c->half_tail && dp == 0 && s == 2 &&
                  c->units <= slots;
@@ -359,24 +354,6 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
     } else if (f.epilogue == 3) {
       return GEMM_ERR_UNSUPPORTED;
     }
-  }
-  // A multicast across the two CTA pairs of a 4-CTA cluster: a unit is then a pair of
-  // tiles of the same rows (columns 2j and 2j + 1; the second past N when the tile
-  // columns are odd: it loads zeros and stores nothing).
-  if (f.multicast == 2) {
-    if (!allow_kx || cg != 2 || c->sk_workers || c->half_tail || s != 1 || dp != c->tiles ||
-        f.epilogue == 3)
-      return GEMM_ERR_UNSUPPORTED;
-    int clusters = resident_cg2_mca(c->bn, c->stages, out);
-    if (f.max_ctas) clusters = std::min(clusters, std::max(f.max_ctas / 4, 1));
-    if (clusters <= 0) return GEMM_ERR_UNSUPPORTED;
-    c->mca = true;
-    c->num_n = ceil_div(c->num_n, (int64_t)2);
-    c->tiles = c->num_m * c->num_n;
-    c->dp_tiles = c->tiles;
-    c->units = c->tiles;
-    c->grid = (int)(std::min<int64_t>(c->units, clusters) * 4);
-    c->l2_hint = 1;  // the multicast producer issues plain copies
   }
   if (c->bn == 320 && !(c->kx2 && c->one_chain)) return GEMM_ERR_UNSUPPORTED;
   // the deeper rings of 16-row A stages: plain fp16/bf16 kernels, row tiles of <= 16 rows
@@ -488,7 +465,7 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
     return GEMM_ERR_INVALID_ARG;
   if (c.splits < -1 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
       c.dp_tiles != 0 || c.prefetch_kblocks < -1 || c.epilogue < 0 || c.epilogue > 3 ||
-      c.l2_hint < 0 || c.l2_hint > 2 || c.multicast < 0 || c.multicast > 2)
+      c.l2_hint < 0 || c.l2_hint > 2)
     return GEMM_ERR_INVALID_ARG;
   if (c.stages) {
     const int bn = c.block_n ? c.block_n : 256;
@@ -579,7 +556,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
     g.grid = (int)std::min<int64_t>(ceil_div(N, (int64_t)8), cap);
     g.stream = stream;
     if ((h->last_cuda = launch_gemv(g)) != cudaSuccess) return GEMM_ERR_CUDA;
-    h->last = gemm_config_t{3, 0, 1, 0, 0, g.grid, 0, (int32_t)N, -1, 1, 1, 1};
+    h->last = gemm_config_t{3, 0, 1, 0, 0, g.grid, 0, (int32_t)N, -1, 1, 1};
     return GEMM_OK;
   }
   Choice ch;
@@ -597,7 +574,6 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   s.grid = ch.grid;
   s.one_chain = ch.one_chain;
   s.kx2 = ch.kx2;
-  s.mca = ch.mca;
   // FP8 kernels always carry the epilogue: the per-tensor scales arrive as alpha
   s.fused = (fused || fp8) && !bs;
   s.kind = bs ? 2 : fp8 ? 1 : 0;
@@ -615,10 +591,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
       (ch.half_tail && !make_map(h, B, N, K, dtype_in, ch.bn / ch.variant / 2, &s.tmB2)) ||
       (c_tma && !make_map(h, C, M, N, dtype_out, 32, &s.tmC)))
     return GEMM_ERR_CUDA;
-  if (ch.mca) {
-    // A's 64-row half boxes, one per pair of the cluster
-    if (!make_map(h, A, M, K, dtype_in, kBlockM / 2, &s.tmB2)) return GEMM_ERR_CUDA;
-  } else if (ch.bn == 320) {
+  if (ch.bn == 320) {
     // the last 32 of each CTA's 160 B rows
     if (!make_map(h, B, N, K, dtype_in, 32, &s.tmB2)) return GEMM_ERR_CUDA;
   } else if (!ch.half_tail) {
@@ -684,7 +657,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
                           ch.stages,
                           ch.group_m,  ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles,
                           ch.prefetch_kb ? ch.prefetch_kb : -1, ch.kx2 ? 3 : ch.one_chain ? 2 : 1,
-                          ch.l2_hint, ch.mca ? 2 : 1};
+                          ch.l2_hint};
   return GEMM_OK;
 }
 
@@ -865,7 +838,7 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
   p.test_stall = h->test_stall;
   if ((h->last_cuda = launch_gemm(s)) != cudaSuccess) return GEMM_ERR_CUDA;
   h->last = gemm_config_t{cg, bn, 1, stages, p.group_m, s.grid, p.chain_kb, (int32_t)units, -1, 1,
-                          p.l2_hint, 1};
+                          p.l2_hint};
   return GEMM_OK;
 }
 

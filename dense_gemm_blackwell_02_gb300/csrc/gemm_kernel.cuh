@@ -265,15 +265,12 @@ static __device__ __noinline__ bool walker_has_next(const Walker& k, int32_t fir
 
 // Only two 32-bit counters live across a unit; the stream-K range is recomputed from
 // the worker's index on each call.
-// With MCA a unit is a pair of tiles: pair mc_pair of the cluster takes column 2j + mc_pair
-// of the tile-pair grid's column j.
-template <bool GROUPED, bool MCA = false>
+template <bool GROUPED>
 __device__ __forceinline__ bool walker_next(Walker& k, int32_t first, int32_t stride,
-                                            const GemmParams& p, Unit& w, uint32_t mc_pair = 0) {
+                                            const GemmParams& p, Unit& w) {
   if (k.u < p.units) {
     if constexpr (GROUPED) decode_grouped(k.u, p, w);
     else w = decode_unit(k.u, p);
-    if constexpr (MCA) w.n_blk = 2 * w.n_blk + (int32_t)mc_pair;
     k.u += stride;
     return true;
   }
@@ -541,12 +538,8 @@ struct Layout {
 // others are all in (the stream-K fix-up).  Built for the plain kernels' split launches;
 // the kernel for whole tiles keeps the direct form (its register allocation, and its
 // time at 8192^3, measured better with that form than with the staged one or with none).
-// MCA: a cluster of two CTA pairs computes two tiles of the same 256 rows side by side
-// (columns 2j and 2j + 1 of a grid of tile pairs), in lockstep over K; A, the same for
-// both, is loaded once: each pair loads 64 of a CTA's 128 rows and multicasts them to
-// the CTA of the same rank in both pairs.  Whole tiles only.
 template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN, bool FUSED, int KIND = 0,
-          bool GROUPED = false, bool KX2 = false, bool STAGED = false, bool MCA = false>
+          bool GROUPED = false, bool KX2 = false, bool STAGED = false>
 __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
@@ -563,8 +556,6 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
                 "grouped launches use the plain general epilogue");
   static_assert(!KX2 || (!FUSED && KIND == 0 && !GROUPED),
                 "the cluster K split uses the plain epilogues");
-  static_assert(!MCA || (CTA_GROUP == 2 && !KX2 && !GROUPED && !FUSED && KIND == 0 && !STAGED),
-                "the multicast of A pairs plain CTA-pair kernels");
   constexpr uint32_t kTmemCols = BN == 320 ? 512 : 2 * BN;  // two accumulator slots (one for 320)
   constexpr int kHalf = BN / 2;                // columns per epilogue warp
   constexpr int kPieces = kHalf / 32;          // tcgen05.ld x32 pieces per warp
@@ -599,26 +590,24 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
   const WaitCtl ctl{p.wait_limit_ns, p.status, abort_flag};
   // Cluster rank; with KX2 the cluster holds two CTA groups (K slices 0 and 1), the
   // group of slice s starting at rank s * CTA_GROUP.
-  // With MCA the cluster holds two pairs, the second at ranks 2-3.
   const uint32_t crank = (CTA_GROUP == 2 || KX2) ? cluster_ctarank() : 0u;
-  const uint32_t rank = CTA_GROUP == 2 ? ((KX2 || MCA) ? (crank & 1u) : crank) : 0u;  // place in the pair
-  const uint32_t group_base = (KX2 || MCA) ? crank - rank : 0u;  // cluster rank of the group's leader
-  const uint32_t mc_pair = MCA ? crank >> 1 : 0u;              // which pair of the cluster
+  const uint32_t rank = CTA_GROUP == 2 ? (KX2 ? (crank & 1u) : crank) : 0u;  // place in the pair
+  const uint32_t group_base = KX2 ? crank - rank : 0u;  // cluster rank of the group's leader
   const uint32_t slice_k = KX2 ? crank / CTA_GROUP : 0u;
   // the same rank of the other K slice's CTA group
   const uint32_t kx_peer = slice_k == 0 ? crank + (uint32_t)CTA_GROUP : crank - (uint32_t)CTA_GROUP;
-  const uint16_t pair_mask = (uint16_t)((KX2 || MCA) ? (0x3u << group_base) : 0x3u);
-  // a stage's commit frees it in every CTA whose copies land in it: with MCA both pairs
-  const uint16_t stage_mask = (uint16_t)(MCA ? 0xFu : pair_mask);
+  const uint16_t pair_mask = (uint16_t)(KX2 ? (0x3u << group_base) : 0x3u);
+  // a stage's commit frees it in both CTAs of the pair, whose copies land in it
+  const uint16_t stage_mask = pair_mask;
   const bool leader = rank == 0;
-  const int32_t first_unit = (int32_t)(blockIdx.x / (MCA ? 4 : CTA_GROUP));
-  const int32_t unit_stride = (int32_t)(gridDim.x / (MCA ? 4 : CTA_GROUP));
+  const int32_t first_unit = (int32_t)(blockIdx.x / CTA_GROUP);
+  const int32_t unit_stride = (int32_t)(gridDim.x / CTA_GROUP);
 
   // ---------------------------------------------------------------- setup --
   if (warp == 0 && lane == 0) {
     for (uint32_t s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);   // the leader's producer arms it; copies complete it
-      mbar_init(empty_bar(s), MCA ? 2 : 1);  // one (multicast) commit per pair per use
+      mbar_init(empty_bar(s), 1);  // one commit per use
     }
     for (uint32_t i = 0; i < 2; ++i) {
       mbar_init(acc_full_bar(i), 1);
@@ -636,7 +625,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     if constexpr (!GROUPED) {  // a grouped launch's maps live in global memory
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
-      if (p.half_tail || MCA || BN == 320) tma_prefetch_desc(&tmB2);
+      if (p.half_tail || BN == 320) tma_prefetch_desc(&tmB2);
       if (p.tma_store) tma_prefetch_desc(&tmC);
     }
   }
@@ -675,7 +664,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       const uint64_t pol_b = kHint ? l2_policy_evict_first() : 0ull;
       Walker walk{first_unit, 0};
       Unit w;
-      while (ok && walker_next<GROUPED, MCA>(walk, first_unit, unit_stride, p, w, mc_pair)) {
+      while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
         const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
         // a half-tile unit loads half the B rows (through the half-height map tmB2)
         const bool half = w.half >= 0;
@@ -726,16 +715,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
             // with the bytes of the pair.
             const uint32_t leader_full = mapa_shared(full_bar(stage), group_base);
             if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), tx);
-            if constexpr (MCA) {
-              // B as usual; A: this pair's 64-row half of the rank's rows (the 64-row map
-              // in tmB2's place), to both pairs' CTAs of this rank, each of whose leader
-              // barriers takes the bytes (the pair leader of every destination)
-              tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
-                                     leader_full);
-              tma_load_2d_pair_mc_elect(sA + stage * L::kABytes + mc_pair * (L::kABytes / 2), &tmB2,
-                                        kb * kKbElems, a_row + (int32_t)mc_pair * (kBlockM / 2),
-                                        leader_full, (uint16_t)(0x5u << rank));
-            } else if constexpr (kHint) {
+            if constexpr (kHint) {
               tma_load_2d_pair_hint_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
                                           leader_full, pol_b);
               if constexpr (BN == 320)  // rows 256 + 32 * rank.. of the tile (32-row map)
@@ -790,7 +770,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       if (p.test_stall) ok = warp_wait(drain_bar, 0, ctl, kSiteTestStall);
       Walker walk{first_unit, 0};
       Unit w;
-      while (ok && walker_next<GROUPED, MCA>(walk, first_unit, unit_stride, p, w, mc_pair)) {
+      while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
         const uint32_t idesc = w.half >= 0 ? p.idesc_half : p.idesc;
         for (int32_t c0 = w.kb0; c0 < w.kb1 && ok; c0 += p.chain_kb) {
           const int32_t c1 = min(c0 + p.chain_kb, w.kb1);
@@ -852,7 +832,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       constexpr size_t kBlocksPerSlice = (size_t)CTA_GROUP * 8;  // (rank, quarter, half)
       constexpr size_t kSliceStride = kBlocksPerSlice * kBlockFloats;
       const size_t my_block = ((size_t)rank * 4 + q) * 2 + h;
-      while (ok && walker_next<GROUPED, MCA>(walk, first_unit, unit_stride, p, w, mc_pair)) {
+      while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
         // in a half-tile unit the h = 1 warps only take part in the slot hand-over, and
         // so do warps whose 32 rows all lie at or past M (no partial, no store)
         const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
@@ -1009,7 +989,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         ++iter;
       }
     } else {
-    while (ok && walker_next<GROUPED, MCA>(walk, first_unit, unit_stride, p, w, mc_pair)) {
+    while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
       // In a half-tile unit the accumulator holds BN/2 columns: the h = 0 warps own
       // them, the h = 1 warps only take part in the slot hand-over.
       const bool active = w.half < 0 || h == 0;

@@ -17,8 +17,9 @@
 // array of fixed size (GEMM_NOALLOC_SCRATCH_BYTES in include/gemm.h).  The CUDA driver
 // places that array on every GPU that loads this library, where it stays until the
 // process exits.  On its first call on a device, with that device current, the entry
-// point looks up the array's device address once (cudaGetSymbolAddress); a first call
-// that has to do this should therefore come before any stream capture.  No call makes
+// point looks up the array's device address (cudaGetSymbolAddress) and keeps it once the
+// lookup has succeeded; a first call that has to do this should therefore come before any
+// stream capture.  No call makes
 // a device or host allocation: no cudaMalloc, no cudaFree, no allocating library call.
 //
 // Sharing.  Every call on a device uses the same array, which keeps the previous
@@ -60,29 +61,38 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 
 struct DeviceSetup {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
+  bool done = false;                 // set only once the lookup below has succeeded
   unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
   int sms = 0;
   bool supported = false;
 };
 
 DeviceSetup g_setup[kMaxDevices];
+std::mutex g_setup_mutex;
 
-// Once per device, with that device current: find the array's device address.
-void setup_device(int dev, DeviceSetup* s) {
-  int major = 0, minor = 0;
-  s->err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  if (s->err == cudaSuccess)
-    s->err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (s->err == cudaSuccess)
-    s->err = cudaDeviceGetAttribute(&s->sms, cudaDevAttrMultiProcessorCount, dev);
-  if (s->err != cudaSuccess) return;
-  s->supported = (major == 10 && minor == 3);
-  if (!s->supported) return;
+// Once per device, with that device current: find the array's device address.  Only a
+// successful set-up is remembered: a first call that fails (for instance one made by
+// mistake during a stream capture, where the lookup may be refused) leaves the device
+// unset, and a later call tries again.
+cudaError_t setup_device(int dev, DeviceSetup* s) {
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (s->done) return cudaSuccess;
+  int major = 0, minor = 0, sms = 0;
+  cudaError_t err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  const bool supported = (major == 10 && minor == 3);
   void* p = nullptr;
-  s->err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-  if (s->err == cudaSuccess) s->scratch = static_cast<unsigned char*>(p);
+  if (supported) {
+    err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (err != cudaSuccess) return err;
+  }
+  s->scratch = static_cast<unsigned char*>(p);
+  s->sms = sms;
+  s->supported = supported;
+  s->done = true;
+  return cudaSuccess;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -150,11 +160,12 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED;
   DeviceSetup& ds = g_setup[dev];
-  std::call_once(ds.once, setup_device, dev, &ds);
-  if (ds.err != cudaSuccess) return GEMM_ERR_CUDA;
+  if (setup_device(dev, &ds) != cudaSuccess) return GEMM_ERR_CUDA;
   if (!ds.supported) return GEMM_ERR_UNSUPPORTED;
 
-  // Fixed K-slice rule: slice K only when there are fewer tiles than half the SMs.
+  // Fixed K-slice rule: slice K only when there are fewer tiles than half the SMs, and
+  // into no more slices than the fixed scratch holds partial tiles for (one slice needs
+  // none, so every valid product runs).
   const int64_t k_blocks = cdiv(K, kBlockK);
   const int64_t num_m = cdiv(M, kBlockM), num_n = cdiv(N, kBN);
   const int64_t tiles = num_m * num_n;
@@ -163,6 +174,8 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
     splits = ds.sms / tiles;
     if (splits > k_blocks / 4) splits = k_blocks / 4;
     if (splits > 32) splits = 32;
+    const int64_t fit = (int64_t)(kWorkspaceBytes / ((size_t)tiles * kBlockM * kBN * sizeof(float)));
+    if (splits > fit) splits = fit;
     if (splits < 1) splits = 1;
   }
   const int64_t per = cdiv(k_blocks, splits);
@@ -171,7 +184,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   if (units > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   const size_t ws_need = splits > 1 ? (size_t)tiles * splits * kBlockM * kBN * sizeof(float) : 0;
   const size_t ctr_need = splits > 1 ? (size_t)tiles * 8 : 0;  // (tile, quarter, half)
-  // The scratch has a fixed size: a product that would need more is refused.
+  // (cannot happen with the rule above; kept as the guard of the fixed-size scratch)
   if (ws_need > kWorkspaceBytes || ctr_need > kCounterWords) return GEMM_ERR_UNSUPPORTED;
 
   LaunchSpec s;

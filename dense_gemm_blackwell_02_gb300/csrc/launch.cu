@@ -44,11 +44,6 @@ int max_resident_kx_clusters(int cg, int bn, int stages, int out) {
 }
 
 cudaError_t launch_gemm(const LaunchSpec& s) {
-  if (s.mca) {
-    if (s.kind != 0 || s.fused || s.grouped || s.kx2 || s.staged || s.cta_group != 2)
-      return cudaErrorInvalidValue;
-    return launch_cg2_mca(s);
-  }
   if (s.kx2) {
     if (s.kind != 0 || s.fused || s.grouped) return cudaErrorInvalidValue;
     if (s.cta_group == 1) return s.one_chain ? launch_cg1_kx(s) : launch_cg1_kxg(s);

@@ -21,13 +21,12 @@ struct LaunchSpec {
   bool grouped;    // a grouped launch: p.groups holds the problems (kind 0, general epilogue)
   bool kx2;        // two K slices per tile, one per CTA group of a cluster of 2 * cta_group
                    // (one unit per CTA group)
-  bool mca;        // A multicast across the two CTA pairs of a 4-CTA cluster (whole tiles)
   bool staged;     // plain general epilogue, K slices or stream-K segments meeting in the
                    // workspace: the kernel with the staged fix-up
   CUtensorMap tmA; // A: box {128 bytes of K, 128 (or M < 128) rows}
   CUtensorMap tmB; // B: box {128 bytes of K, bn / cta_group}
   CUtensorMap tmB2; // B: box {128 bytes of K, bn / cta_group / 2} (half-tile units; else tmB);
-                    // with mca, A's box {128 bytes of K, 64 rows}
+                    // with bn 320, {128 bytes of K, 32 rows}
   CUtensorMap tmC; // C: box {128 bytes of columns, 32 rows} (used when p.tma_store)
   GemmParams p;
   cudaStream_t stream;
@@ -94,8 +93,6 @@ int resident_cg2_kx(int bn, int stages, int out);
 // Clusters of 2 * cta_group CTAs of the cluster-K-split kernel that fit at once (0 if the
 // query fails).
 int max_resident_kx_clusters(int cta_group, int bn, int stages, int out);
-cudaError_t launch_cg2_mca(const LaunchSpec& s);
-int resident_cg2_mca(int bn, int stages, int out);  // clusters of two pairs
 int resident_cg1(int bn, int stages, int out);
 int resident_cg2(int bn, int stages, int out);
 

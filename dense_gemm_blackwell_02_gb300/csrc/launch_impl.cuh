@@ -6,10 +6,10 @@
 namespace gb300 {
 
 template <int CG, int BN, int STAGES, int OUT, bool ONE, bool FUSED, int KIND = 0,
-          bool GROUPED = false, bool KX2 = false, bool STAGED = false, bool MCA = false>
+          bool GROUPED = false, bool KX2 = false, bool STAGED = false>
 cudaError_t launch_one(const LaunchSpec& s) {
-  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED, KIND, GROUPED, KX2, STAGED, MCA>;
-  constexpr unsigned kCluster = CG * (KX2 ? 2 : 1) * (MCA ? 2 : 1);
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED, KIND, GROUPED, KX2, STAGED>;
+  constexpr unsigned kCluster = CG * (KX2 ? 2 : 1);
   using L = Layout<CG, BN, STAGES>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes);
@@ -43,10 +43,10 @@ cudaError_t launch_one(const LaunchSpec& s) {
   return cudaLaunchKernelEx(&cfg, kernel, s.tmA, s.tmB, s.tmB2, s.tmC, s.p);
 }
 
-template <int CG, int BN, int STAGES, int OUT, bool KX2 = false, bool MCA = false>
+template <int CG, int BN, int STAGES, int OUT, bool KX2 = false>
 int resident_one() {
-  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, KX2, false, 0, false, KX2, false, MCA>;
-  constexpr unsigned kCluster = CG * (KX2 ? 2 : 1) * (MCA ? 2 : 1);
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, KX2, false, 0, false, KX2, false>;
+  constexpr unsigned kCluster = CG * (KX2 ? 2 : 1);
   using L = Layout<CG, BN, STAGES>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            L::kDynamicBytes) != cudaSuccess)
@@ -71,22 +71,22 @@ int resident_one() {
 }
 
 template <int CG, int BN, int STAGES, bool ONE, bool FUSED, int KIND = 0, bool GROUPED = false,
-          bool KX2 = false, bool STAGED = false, bool MCA = false>
+          bool KX2 = false, bool STAGED = false>
 cudaError_t by_out(const LaunchSpec& s) {
   switch (s.out) {
-    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED, MCA>(s);
-    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED, MCA>(s);
-    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED, KIND, GROUPED, KX2, STAGED, MCA>(s);
+    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED>(s);
+    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED>(s);
+    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED, KIND, GROUPED, KX2, STAGED>(s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <int CG, int BN, int STAGES, bool KX2 = false, bool MCA = false>
+template <int CG, int BN, int STAGES, bool KX2 = false>
 int resident_by_out(int out) {
   switch (out) {
-    case kOutF16: return resident_one<CG, BN, STAGES, kOutF16, KX2, MCA>();
-    case kOutBF16: return resident_one<CG, BN, STAGES, kOutBF16, KX2, MCA>();
-    case kOutF32: return resident_one<CG, BN, STAGES, kOutF32, KX2, MCA>();
+    case kOutF16: return resident_one<CG, BN, STAGES, kOutF16, KX2>();
+    case kOutBF16: return resident_one<CG, BN, STAGES, kOutBF16, KX2>();
+    case kOutF32: return resident_one<CG, BN, STAGES, kOutF32, KX2>();
     default: return 0;
   }
 }

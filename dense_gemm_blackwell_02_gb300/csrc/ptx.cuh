@@ -219,20 +219,6 @@ __device__ __forceinline__ void tma_load_2d_pair_hint_elect(uint32_t dst, const 
       : "memory");
 }
 
-// 2-D tiled load of a CTA pair multicast to the CTAs of `cta_mask`: the box lands at the
-// same offset in each, and each destination's bytes complete on the barrier at
-// `cluster_bar`'s offset in that destination's pair leader (cluster_bar: a pair leader's).
-__device__ __forceinline__ void tma_load_2d_pair_mc_elect(uint32_t dst, const void* tmap,
-                                                          int32_t c0, int32_t c1,
-                                                          uint32_t cluster_bar, uint16_t cta_mask) {
-  asm volatile(
-      GB300_ELECT
-      "@e_ cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;\n\t}" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(cluster_bar), "h"(cta_mask)
-      : "memory");
-}
-
 // 2-D tiled store shared -> global (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t c0, int32_t c1) {
   asm volatile(

@@ -118,13 +118,6 @@ typedef enum {
  *             element is read once and A is re-read by every tile); 0 = 2 when the
  *             tiles form one row (M <= 256 for CTA pairs, M <= 128 for one CTA per
  *             tile), else 1.  gemm_last_config reports the one used.
- *   multicast 2 = a cluster of two CTA pairs computes two tiles of the same 256 rows
- *             side by side, each pair loading half of A's rows and multicasting them
- *             to both (TMA .multicast::cluster): A is read from L2 once for the two
- *             tiles.  Valid for fp16/bf16 inputs without a fused epilogue, CTA pairs
- *             (variant 2), every tile whole (no split, no half tiles); else
- *             GEMM_ERR_UNSUPPORTED.  gemm_last_config then reports dp_tiles as the
- *             pairs of tiles.  0 or 1 = off (the default).
  */
 typedef struct {
   int32_t variant;
@@ -138,7 +131,6 @@ typedef struct {
   int32_t prefetch_kblocks;
   int32_t epilogue;
   int32_t l2_hint;
-  int32_t multicast;
 } gemm_config_t;
 
 /* Create a handle on the current CUDA device.  Fails with GEMM_ERR_UNSUPPORTED
@@ -342,9 +334,11 @@ const char* gemm_last_cuda_error(gemm_handle_t h);
  * Arguments, layouts and argument errors are those of gemm_run (no handle), except
  * that FP8 inputs are refused with GEMM_ERR_UNSUPPORTED.
  * The kernel is gemm_run's one-CTA split-K kernel with 256-column tiles; when
- * fewer tiles than half the SMs exist, K is sliced.  A product whose slices
- * would need more than GEMM_NOALLOC_WORKSPACE_BYTES of partial tiles is
- * refused with GEMM_ERR_UNSUPPORTED before anything is queued.  The call is
+ * fewer tiles than half the SMs exist, K is sliced, into no more slices than
+ * GEMM_NOALLOC_WORKSPACE_BYTES holds partial tiles for (an unsliced product needs
+ * none), so every product gemm_run accepts with these dtypes runs.  The first
+ * call on a device that fails its address lookup returns GEMM_ERR_CUDA and is
+ * retried by the next call.  The call is
  * asynchronous; a kernel wait that runs out of time leaves C undefined and is
  * not reported (gemm_run with gemm_device_status reports it).
  */

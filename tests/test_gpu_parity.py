@@ -506,44 +506,6 @@ def test_l2_policy_changes_no_bits(g, M, N, K, cfg):
     parity.oracle_check(parity.bits_of(outs[2]), A, B, F16, F16, what=f"l2 hints {used}")
 
 
-@pytest.mark.parametrize("block_n", [128, 256])
-@pytest.mark.parametrize("M,N,K,dtype_out", [(256, 1536, 1024, F16), (256, 1280, 1024, BF16),
-                                             (512, 1000, 1504, F32), (300, 700, 2048, F16),
-                                             (256, 768, 8192, F32), (600, 2100, 520, BF16)])
-def test_a_multicast_across_two_pairs(g, block_n, M, N, K, dtype_out):
-    # two pairs of a 4-CTA cluster compute two tiles of the same rows, each loading half
-    # of A's rows and multicasting them to both; odd tile columns leave the second pair a
-    # tile past N (zeros in, nothing stored)
-    cfg = dict(variant=2, block_n=block_n, multicast=2)
-    g.set_config(**cfg)
-    try:
-        _case(g, M, N, K, F16, dtype_out, seed=46)
-    finally:
-        g.reset_config()
-    used = None
-    A, B = si.make_small_int_operands(M, N, K, BF16, seed=47)
-    Ad, Bd = A.cuda(), B.cuda()
-    want = None
-    g.set_config(**cfg)
-    try:
-        for rep in range(3):   # exact every time: no copy may be read before it has landed
-            C = torch.empty(M, N, dtype=torch.float32, device="cuda")
-            g.run(Ad, Bd, C)
-            torch.cuda.synchronize()
-            assert g.device_status()[0] == 0
-            used = g.last_config()
-            got = parity.bits_of(C)
-            if want is None:
-                parity.oracle_check(got, A, B, BF16, F32, exact=True, what=f"multicast ints {used}")
-                want = got
-            else:
-                assert np.array_equal(got, want), f"multicast run {rep} differs"
-    finally:
-        g.reset_config()
-    assert used["multicast"] == 2 and used["block_n"] == block_n, used
-    assert used["dp_tiles"] == -(-M // 256) * -(-(-(-N // block_n)) // 2), used
-
-
 @pytest.mark.parametrize("M", [1, 3, 8, 16, 17])
 @pytest.mark.parametrize("N,K,dtype_out", [(8192, 1024, F16), (1000, 8192, F32), (4096, 2048, BF16),
                                            (3000, 520, F16)])
@@ -574,29 +536,6 @@ def test_deeper_ring_rejections(g):
         assert e.value.code == 2
         g.run(A[:16], B, C[:16])                            # 16 rows: fine
         torch.cuda.synchronize()
-    finally:
-        g.reset_config()
-
-
-def test_a_multicast_rejections(g):
-    from dense_gemm_blackwell_02_gb300.binding import GemmError
-    A = torch.zeros(256, 1024, dtype=torch.float16, device="cuda")
-    B = torch.zeros(512, 1024, dtype=torch.float16, device="cuda")
-    C = torch.zeros(256, 512, dtype=torch.float16, device="cuda")
-    for cfg in ({"variant": 1, "multicast": 2}, {"variant": 2, "splits": 2, "multicast": 2},
-                {"variant": 2, "splits": -1, "multicast": 2}):
-        g.set_config(**cfg)
-        try:
-            with pytest.raises(GemmError) as e:
-                g.run(A, B, C)
-            assert e.value.code == 2
-        finally:
-            g.reset_config()
-    g.set_config(variant=2, multicast=2)
-    try:
-        with pytest.raises(GemmError) as e:                       # a fused epilogue
-            g.run_epilogue(A, B, C, alpha=2.0)
-        assert e.value.code == 2
     finally:
         g.reset_config()
 

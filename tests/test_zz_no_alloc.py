@@ -6,12 +6,14 @@ reserved its memory up front).  gemm_run_noalloc keeps its scratch in a fixed
 static device array instead.  These tests call it through the C ABI and check
 that it gives the same answer as gemm_run, within the tolerance the other
 parity tests use, on two calls in a row (the second reuses the array the first
-left behind), and that it refuses a product whose scratch would not fit.
+left behind), and that a product whose K slices would overflow the fixed scratch
+is cut into fewer slices rather than refused.
 
 This file is named so that pytest collects it last.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
@@ -69,11 +71,35 @@ def test_noalloc_matches_gemm_run_on_two_calls(M, N, K, din, dout):
         parity.oracle_check(got, A, B, din, dout, what=f"noalloc vs oracle, call {call}")
 
 
-def test_noalloc_refuses_products_beyond_its_scratch():
-    # 16 tiles, K sliced 9 ways: 16 x 9 x 128 x 256 x 4 B = 18.9 MB > 16 MiB
+def test_noalloc_caps_its_k_slices_at_the_scratch():
+    # 16 tiles with long K: 9 slices would need 16 x 9 x 128 x 256 x 4 B = 18.9 MB of
+    # partial tiles, more than the 16 MiB the fixed scratch holds, so the call takes 8
+    # slices instead (two calls in a row, against the oracle and gemm_run)
+    from dense_gemm_blackwell_02_gb300.binding import Gemm
     M, N, K = 256, 2048, 16384
-    A = torch.zeros(M, K, dtype=torch.float16, device="cuda")
-    B = torch.zeros(N, K, dtype=torch.float16, device="cuda")
-    C = torch.zeros(M, N, dtype=torch.float32, device="cuda")
-    assert _noalloc(A, B, C, F16, F32) == 2          # GEMM_ERR_UNSUPPORTED
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=78)
+    Ad, Bd = A.cuda(), B.cuda()
+    with Gemm() as g:
+        ref = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        g.run(Ad, Bd, ref)
+        assert g.device_status()[0] == 0
+    ref_bits = parity.bits_of(ref)
+    rows = si.sample_indices(M, 24, seed=5, must=(0, 127, 128, 255))
+    cols = si.sample_indices(N, 24, seed=6, must=(0, 255, 256, N - 1))
+    for call in range(2):
+        C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        assert _noalloc(Ad, Bd, C, F16, F32) == 0
+        torch.cuda.synchronize()
+        got = parity.bits_of(C)
+        parity.check(got, ref_bits, F32, what=f"long-K noalloc vs gemm_run, call {call}")
+        parity.oracle_check(got[np.ix_(rows, cols)], A, B, F16, F32, rows=rows, cols=cols,
+                            what=f"long-K noalloc vs oracle, call {call}")
+
+
+def test_noalloc_argument_errors():
+    A = torch.zeros(256, 1024, dtype=torch.float16, device="cuda")
+    B = torch.zeros(512, 1024, dtype=torch.float16, device="cuda")
+    C = torch.zeros(256, 512, dtype=torch.float32, device="cuda")
     assert _noalloc(A, B, C, F16, 7) == 1            # bad dtype: GEMM_ERR_INVALID_ARG
+    assert _noalloc(A, B, C, 3, F32) == 2            # FP8 inputs: GEMM_ERR_UNSUPPORTED
+    assert _noalloc(A[:, :1020], B[:, :1020], C, F16, F32) != 0  # K % 8 != 0 / misaligned
