@@ -146,6 +146,8 @@ struct Choice {
   int l2_hint;
   bool one_chain;
   bool kx2;  // the two K slices of a tile reduced inside a cluster (single chain)
+  bool swap;      // the swapped tiling: B the MMA's row operand, swap_rows rows per CTA
+  int swap_rows;
   int64_t tiles, dp_tiles, units, k_blocks, num_m, num_n;
   int64_t sk_workers, ws_slots;
 };
@@ -171,9 +173,66 @@ int64_t chain_kb_of(int kb_elems) { return kChainKBlocks * kBlockK / kb_elems; }
 // blockwise: one accumulation chain per K block (scaled in the general epilogue).
 // allow_kx: the cluster K split and the staged stream-K fix-up have kernels for this call
 // (fp16/bf16, plain epilogue).
+// The swapped tiling for a few rows of A ("A Blackwell GEMM by Hand in CuTe DSL", section
+// 9: decode shapes are decided by how many SMs the tiles occupy).  B's rows are the MMA's
+// 128-row operand (swap_rows of them loaded per CTA), A's rows its columns (block_n per
+// tile, half of them loaded by each CTA of the pair), so that a handful of token rows
+// times thousands of weight rows fill every SM in one wave without cutting K.
+gemm_status_t choose_swap(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int kb_elems,
+                          Choice* c) {
+  const gemm_config_t& f = h->forced;
+  if ((f.variant && f.variant != 2) || (f.splits && f.splits != 1) || f.epilogue > 1 ||
+      f.block_n == 320)
+    return GEMM_ERR_UNSUPPORTED;
+  c->variant = 2;
+  c->bn = f.block_n ? f.block_n : 128;
+  c->stages = f.stages ? f.stages : default_stages(2, c->bn);
+  if (!kernel_supported(2, c->bn, c->stages) || c->stages != default_stages(2, c->bn))
+    return GEMM_ERR_INVALID_ARG;
+  c->k_blocks = ceil_div(K, (int64_t)kb_elems);
+  int64_t pairs = resident_units(h, 2, c->bn, c->stages, out);
+  if (f.max_ctas) pairs = std::min<int64_t>(pairs, std::max<int64_t>(f.max_ctas / 2, 1));
+  c->num_n = ceil_div(M, (int64_t)c->bn);  // tiles along A's rows
+  int64_t w = f.swap_rows;
+  if (!w) {
+    // the fewest B rows per CTA that make one wave: as many blocks of B rows as pairs
+    // are left per tile of A rows
+    const int64_t blocks = std::max<int64_t>(1, pairs / c->num_n);
+    w = std::min<int64_t>(128, ceil_div(ceil_div(N, 2 * blocks), (int64_t)8) * 8);
+  }
+  c->swap = true;
+  c->swap_rows = (int)w;
+  c->num_m = ceil_div(N, 2 * w);           // tiles along B's rows
+  c->tiles = c->num_m * c->num_n;
+  c->dp_tiles = c->tiles;
+  c->units = c->tiles;
+  c->splits = 1;
+  c->kb_per_split = (int)c->k_blocks;
+  c->half_tail = 0;
+  c->sk_workers = 0;
+  c->ws_slots = 1;
+  c->group_m = f.group_m ? f.group_m : 16;
+  c->chain_kb = f.chain_kblocks ? f.chain_kblocks : chain_kb_of(kb_elems);
+  c->prefetch_kb = f.prefetch_kblocks > 0 ? f.prefetch_kblocks : 0;
+  // One tile of A rows: every B element is read once and A by every tile, so B's lines
+  // are marked first to be evicted and A's last (as for one row of tiles otherwise).
+  c->l2_hint = f.l2_hint ? f.l2_hint : (c->num_n == 1 ? 2 : 1);
+  c->one_chain = false;
+  c->kx2 = false;
+  c->grid = (int)(std::min<int64_t>(c->units, pairs) * 2);
+  if (c->units > INT32_MAX || c->tiles * 16 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  return GEMM_OK;
+}
+
 gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int kb_elems,
                      bool blockwise, bool allow_kx, Choice* c) {
   const gemm_config_t& f = h->forced;
+  c->swap = false;
+  c->swap_rows = 0;
+  if (f.swap_ab == 2) {
+    if (!allow_kx) return GEMM_ERR_UNSUPPORTED;
+    return choose_swap(h, M, N, K, out, kb_elems, c);
+  }
   // A CTA pair (256-row tiles, each CTA loading half of B) whenever M fills one.
   // Blockwise scales hand every K block's accumulator to the epilogue: a CTA pair's
   // cross-CTA hand-over made that 1.6x slower than one CTA per tile (measured, 4096^3).
@@ -238,8 +297,9 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
     const bool try320 = cg == 2 && ceil_div(c->k_blocks, (int64_t)2) <= chain_kb_of(kb_elems);
     for (int bn : {128, 256, 320}) {
       if (bn == 320 && !try320) continue;
-      const int st = default_stages(cg, bn, small_a);
-      int64_t sl = bn == 320 ? h->sms / cg : resident_units(h, cg, bn, st, out);
+      const int st = kx_stages(cg, bn, small_a);
+      int64_t sl = bn == 320 ? h->sms / cg
+                             : resident_units(h, cg, bn, default_stages(cg, bn, small_a), out);
       if (f.max_ctas) sl = std::min<int64_t>(sl, std::max<int64_t>(f.max_ctas / cg, 1));
       const int64_t tl = c->num_m * ceil_div(N, (int64_t)bn);
       if (tl * 2 > sl || std::min<int64_t>({sl / tl, c->k_blocks / 4, 32}) != 2) continue;
@@ -344,12 +404,16 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   if (f.epilogue == 3 || auto_kx) {
     bool valid = allow_kx && !c->sk_workers && !c->half_tail && dp == 0 && s == 2 &&
                  c->units <= slots;
+    // its own ring depth (the staging inside the ring); a forced depth must be that one
+    const int kst = kx_stages(cg, c->bn, a_rows(cg, c->bn, c->stages) < kBlockM);
+    if (f.stages && f.stages != kst) valid = false;
     if (valid) {
-      const int clusters = max_resident_kx_clusters(cg, c->bn, c->stages, out);
+      const int clusters = max_resident_kx_clusters(cg, c->bn, kst, out);
       valid = clusters > 0 && c->tiles <= clusters;
     }
     if (valid) {
       c->kx2 = true;
+      c->stages = kst;
       c->grid = (int)(c->units * cg);
     } else if (f.epilogue == 3) {
       return GEMM_ERR_UNSUPPORTED;
@@ -465,7 +529,8 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
     return GEMM_ERR_INVALID_ARG;
   if (c.splits < -1 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
       c.dp_tiles != 0 || c.prefetch_kblocks < -1 || c.epilogue < 0 || c.epilogue > 3 ||
-      c.l2_hint < 0 || c.l2_hint > 2)
+      c.l2_hint < 0 || c.l2_hint > 2 || c.swap_ab < 0 || c.swap_ab > 2 || c.swap_rows < 0 ||
+      c.swap_rows > 128)
     return GEMM_ERR_INVALID_ARG;
   if (c.stages) {
     const int bn = c.block_n ? c.block_n : 256;
@@ -539,8 +604,8 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   // A few rows of A: the CUDA-core matrix-vector path (variant 3), forced or automatic.
   const gemm_config_t& fc = h->forced;
   if (fc.variant == 3 || (!fc.variant && !fc.block_n && !fc.splits && !fc.stages && !fc.epilogue &&
-                          !fc.chain_kblocks && M == 1 && K <= kGemvAutoMaxK && !fused && !fp8_in &&
-                          !bs)) {
+                          !fc.chain_kblocks && fc.swap_ab != 2 && M == 1 && K <= kGemvAutoMaxK &&
+                          !fused && !fp8_in && !bs)) {
     if (M > kGemvMaxRows || fused || fp8_in || bs) return GEMM_ERR_UNSUPPORTED;
     GemvSpec g;
     g.A = A;
@@ -556,7 +621,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
     g.grid = (int)std::min<int64_t>(ceil_div(N, (int64_t)8), cap);
     g.stream = stream;
     if ((h->last_cuda = launch_gemv(g)) != cudaSuccess) return GEMM_ERR_CUDA;
-    h->last = gemm_config_t{3, 0, 1, 0, 0, g.grid, 0, (int32_t)N, -1, 1, 1};
+    h->last = gemm_config_t{3, 0, 1, 0, 0, g.grid, 0, (int32_t)N, -1, 1, 1, 1, 0};
     return GEMM_OK;
   }
   Choice ch;
@@ -574,10 +639,11 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   s.grid = ch.grid;
   s.one_chain = ch.one_chain;
   s.kx2 = ch.kx2;
+  s.swap = ch.swap;
   // FP8 kernels always carry the epilogue: the per-tensor scales arrive as alpha
   s.fused = (fused || fp8) && !bs;
   s.kind = bs ? 2 : fp8 ? 1 : 0;
-  s.staged = !ch.kx2 && !s.fused && s.kind == 0 && !ch.one_chain &&
+  s.staged = !ch.kx2 && !ch.swap && !s.fused && s.kind == 0 && !ch.one_chain &&
              ((ch.splits > 1 && !ch.half_tail) || ch.sk_workers);
   s.stream = stream;
   const bool c_tma = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ((size_t)N * osz) % 16 == 0;
@@ -586,12 +652,21 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   // stored.  (A 128-row box over fewer than 8 rows of A ran up to 1.5x slower on the
   // decode shapes than over 8 or more, measured.)
   const int a_box = (ch.variant == 1 && M < kBlockM) ? (int)M : kBlockM;
-  if (!make_map(h, A, M, K, dtype_in, a_box, &s.tmA) ||
+  if (ch.swap) {
+    // B is the MMA's row operand (swap_rows rows per CTA), A its columns (bn / 2 rows per
+    // CTA); C is written transposed with direct stores
+    if (!make_map(h, B, N, K, dtype_in, ch.swap_rows, &s.tmA) ||
+        !make_map(h, A, M, K, dtype_in, ch.bn / 2, &s.tmB))
+      return GEMM_ERR_CUDA;
+    s.tmB2 = s.tmB;
+    s.tmC = s.tmB;  // (not read: no TMA store)
+  } else if (!make_map(h, A, M, K, dtype_in, a_box, &s.tmA) ||
       !make_map(h, B, N, K, dtype_in, ch.bn == 320 ? 128 : ch.bn / ch.variant, &s.tmB) ||
       (ch.half_tail && !make_map(h, B, N, K, dtype_in, ch.bn / ch.variant / 2, &s.tmB2)) ||
       (c_tma && !make_map(h, C, M, N, dtype_out, 32, &s.tmC)))
     return GEMM_ERR_CUDA;
-  if (ch.bn == 320) {
+  if (ch.swap) {
+  } else if (ch.bn == 320) {
     // the last 32 of each CTA's 160 B rows
     if (!make_map(h, B, N, K, dtype_in, 32, &s.tmB2)) return GEMM_ERR_CUDA;
   } else if (!ch.half_tail) {
@@ -626,6 +701,12 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
   p.a_tx_short = (uint32_t)(a_rows(ch.variant, ch.bn, ch.stages) - a_box) * 128u;
   p.vec_store = c_tma ? 1 : 0;
   p.tma_store = c_tma && ch.bn != 320 ? 1 : 0;  // (320 columns: 160 per warp, direct stores)
+  p.swap_rows = ch.swap_rows;
+  if (ch.swap) {
+    p.a_tx_short = 2u * (uint32_t)(kBlockM - ch.swap_rows) * 128u;  // both CTAs' short boxes
+    p.vec_store = 0;
+    p.tma_store = 0;
+  }
   if (fp8) {
     p.idesc = idesc_f8_kmajor(kBlockM * ch.variant, ch.bn, dtype_in == GEMM_E5M2);
     p.idesc_half = idesc_f8_kmajor(kBlockM * ch.variant, ch.bn / 2, dtype_in == GEMM_E5M2);
@@ -657,7 +738,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
                           ch.stages,
                           ch.group_m,  ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles,
                           ch.prefetch_kb ? ch.prefetch_kb : -1, ch.kx2 ? 3 : ch.one_chain ? 2 : 1,
-                          ch.l2_hint};
+                          ch.l2_hint, ch.swap ? 2 : 1, ch.swap_rows};
   return GEMM_OK;
 }
 
@@ -706,7 +787,8 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
       return GEMM_ERR_UNSUPPORTED;
   }
   const gemm_config_t& f = h->forced;
-  if ((f.splits != 0 && f.splits != 1) || f.epilogue >= 2) return GEMM_ERR_UNSUPPORTED;
+  if ((f.splits != 0 && f.splits != 1) || f.epilogue >= 2 || f.swap_ab == 2)
+    return GEMM_ERR_UNSUPPORTED;
   // Problems with K = 0 are the empty sum; the rest go into one launch.
   std::vector<int32_t> live;
   int64_t padded[3] = {0, 0, 0};  // MACs with M padded to 128 and to 256 rows
@@ -838,7 +920,7 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
   p.test_stall = h->test_stall;
   if ((h->last_cuda = launch_gemm(s)) != cudaSuccess) return GEMM_ERR_CUDA;
   h->last = gemm_config_t{cg, bn, 1, stages, p.group_m, s.grid, p.chain_kb, (int32_t)units, -1, 1,
-                          p.l2_hint};
+                          p.l2_hint, 1, 0};
   return GEMM_OK;
 }
 

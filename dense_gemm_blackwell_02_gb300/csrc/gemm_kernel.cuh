@@ -413,6 +413,30 @@ __device__ __forceinline__ void store_row_direct(const GemmParams& p, int32_t m,
   store_row_to<OUT>(p.C, p.M, p.N, p.vec_store, m, n0, v);
 }
 
+// The swapped tiling's store: v[j] = C[m0 + j][n] for j < NV, n this thread's column of C
+// (in_tile: n is one of the CTA's rows of B).  The 32 lanes of a warp hold 32 consecutive
+// columns, so each store instruction writes 32 consecutive elements of one row of C.
+template <int OUT, int NV>
+__device__ __forceinline__ void store_col_direct(const GemmParams& p, int32_t n, bool in_tile,
+                                                 int32_t m0, const float* v) {
+  if (!in_tile || n >= p.N) return;
+  const int32_t rows = p.M - m0;
+  if constexpr (OUT == kOutF32) {
+    float* dst = reinterpret_cast<float*>(p.C) + (size_t)m0 * p.N + n;
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+      if (j < rows) dst[(size_t)j * p.N] = v[j];
+  } else {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(p.C) + (size_t)m0 * p.N + n;
+#pragma unroll
+    for (int j = 0; j < NV; j += 2) {
+      const uint32_t two = pack2<OUT>(v[j], v[j + 1]);
+      if (j < rows) dst[(size_t)j * p.N] = (uint16_t)(two & 0xFFFFu);
+      if (j + 1 < rows) dst[(size_t)(j + 1) * p.N] = (uint16_t)(two >> 16);
+    }
+  }
+}
+
 // One 32-column piece of a single-chain unit's output, for the warp's rows: the TMEM
 // accumulator at `taddr`, or for a split tile the slices summed in slice order (the
 // own slice's partial is the TMEM value itself; two slices add in either order to the
@@ -478,19 +502,23 @@ __device__ __forceinline__ void one_chain_piece(uint32_t taddr, const Unit& w, c
 }
 
 // ------------------------------------------------------------- shared memory map --
-// One-CTA rings deeper than a 128-row A tile allows (10 stages of 128 columns, 5 of 256)
-// hold 16 rows of A per stage, for row tiles of M <= 16 rows: A's stage stride is then
-// 2 KiB, and the MMA's 128-row A operand runs on over the following stages' bytes.  The
-// rows past 16 are whatever those bytes hold; each feeds only its own accumulator row,
-// which is never stored, and the span stays inside the ring.  The ring keeps more of B
-// in flight (160 KiB against 96 or 128).
-template <int CTA_GROUP, int BN, int STAGES>
+// One-CTA rings deeper than a 128-row A tile allows (10 stages of 128 columns, 5 of 256;
+// with the staging in the ring, 12 and 6) hold 16 rows of A per stage, for row tiles of
+// M <= 16 rows: A's stage stride is then 2 KiB, and the MMA's 128-row A operand runs on
+// over the following stages' bytes.  The rows past 16 are whatever those bytes hold; each
+// feeds only its own accumulator row, which is never stored, and the span stays inside
+// the ring.  The ring keeps more of B in flight (160 KiB against 96 or 128).
+// RING_STAGING (the cluster K split, one unit per CTA): the epilogue's staging boxes lie
+// inside the operand ring, after the blocks the K slices exchange, instead of after it:
+// the ring is idle once the unit's MMAs have completed, and the 32 KiB go to one more
+// stage (a CTA streams at about its bytes in flight over the round trip of a stage).
+template <int CTA_GROUP, int BN, int STAGES, bool RING_STAGING = false>
 struct Layout {
   static constexpr int kEpiWarps = 8;
   static constexpr uint32_t kThreads = 32 * (2 + kEpiWarps);
   static constexpr int kRowsB = BN / CTA_GROUP;                // B rows loaded per CTA
   static constexpr bool kSmallA =
-      CTA_GROUP == 1 && ((BN == 128 && STAGES > 6) || (BN == 256 && STAGES > 4));
+      CTA_GROUP == 1 && ((BN == 128 && STAGES > 7) || (BN == 256 && STAGES > 4));
   static constexpr int kARows = kSmallA ? 16 : kBlockM;        // A rows held per stage
   static constexpr uint32_t kABytes = kARows * kBlockK * 2;    // 16 KiB, or 2 KiB
   static constexpr uint32_t kBBytes = kRowsB * kBlockK * 2;
@@ -500,8 +528,12 @@ struct Layout {
   static constexpr uint32_t kStagingBytes = 32 * 128;           // one 32-row x 128 B box
   static constexpr uint32_t kAOff = 0;
   static constexpr uint32_t kBOff = STAGES * kABytes;
-  static constexpr uint32_t kCOff = kBOff + STAGES * kBBytes;
-  static constexpr uint32_t kBarOff = kCOff + kEpiWarps * kStagingBytes;
+  static constexpr uint32_t kRingEnd = kBOff + STAGES * kBBytes;
+  // the K slices' exchange blocks: 32 rows x BN/2 fp32 columns per epilogue warp
+  static constexpr uint32_t kKxBytes = kEpiWarps * 32u * (BN / 2) * 4u;
+  static constexpr uint32_t kCOff = RING_STAGING ? kKxBytes : kRingEnd;
+  static constexpr uint32_t kBarOff =
+      RING_STAGING ? kRingEnd : kCOff + kEpiWarps * kStagingBytes;
   // full[S], empty[S], acc_full[2], acc_empty[2], drain, kx_ready[8], kx_go[8]
   static constexpr uint32_t kNumBars = 2 * STAGES + 5 + 2 * kEpiWarps;
   static constexpr uint32_t kTmemSlotOff = kBarOff + kNumBars * 8;
@@ -512,8 +544,10 @@ struct Layout {
                     kCOff % 1024 == 0,
                 "every operand stage and staging box must start on a 1024-byte boundary");
   static_assert(kDynamicBytes <= 227 * 1024, "shared memory over the per-block limit");
+  static_assert(!RING_STAGING || kCOff + kEpiWarps * kStagingBytes <= kRingEnd,
+                "the staging boxes must fit in the ring after the exchange blocks");
   // the MMA reads 128 rows of A from every stage's A start: inside the ring
-  static_assert((STAGES - 1) * kABytes + kBlockM * kBlockK * 2 <= kCOff,
+  static_assert((STAGES - 1) * kABytes + kBlockM * kBlockK * 2 <= kRingEnd,
                 "the A operand's 128-row span must stay inside the operand ring");
 };
 
@@ -538,13 +572,19 @@ struct Layout {
 // others are all in (the stream-K fix-up).  Built for the plain kernels' split launches;
 // the kernel for whole tiles keeps the direct form (its register allocation, and its
 // time at 8192^3, measured better with that form than with the staged one or with none).
+// SWAP: the operands' roles are exchanged for a few rows of A (decode shapes): B is the
+// MMA's row operand, p.swap_rows (<= 128) of its rows per CTA loaded as a short box
+// whose rows past the box only feed accumulator lanes that are never stored, and A's
+// rows are the MMA's columns, BN of them per tile split over the pair like B's are
+// otherwise.  A thread's accumulator row is then a column of C, and the epilogue writes
+// it transposed.  CTA pairs, general epilogue, plain fp16/bf16, whole tiles.
 template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN, bool FUSED, int KIND = 0,
-          bool GROUPED = false, bool KX2 = false, bool STAGED = false>
-__global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
+          bool GROUPED = false, bool KX2 = false, bool STAGED = false, bool SWAP = false>
+__global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
                 const GemmParams p) {
-  using L = Layout<CTA_GROUP, BN, STAGES>;
+  using L = Layout<CTA_GROUP, BN, STAGES, KX2>;
   static_assert(BN == 128 || BN == 256 || BN == 320, "BN must be 128, 256 or 320");
   // 320 columns: two MMAs per K step (N = 256 and N = 64) into one 320-column
   // accumulator; built for the pair's cluster K split with single-chain slices only (one
@@ -556,6 +596,9 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
                 "grouped launches use the plain general epilogue");
   static_assert(!KX2 || (!FUSED && KIND == 0 && !GROUPED),
                 "the cluster K split uses the plain epilogues");
+  static_assert(!SWAP || (CTA_GROUP == 2 && BN != 320 && !ONE_CHAIN && !FUSED && KIND == 0 &&
+                          !GROUPED && !KX2 && !STAGED),
+                "the swapped tiling is a plain CTA-pair kernel with the general epilogue");
   constexpr uint32_t kTmemCols = BN == 320 ? 512 : 2 * BN;  // two accumulator slots (one for 320)
   constexpr int kHalf = BN / 2;                // columns per epilogue warp
   constexpr int kPieces = kHalf / 32;          // tcgen05.ld x32 pieces per warp
@@ -563,7 +606,10 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
   constexpr int kBoxCols = 128 / kOutBytes;    // columns of one 128-byte staging row
   constexpr int kBoxes = kHalf / kBoxCols;     // staging boxes per warp
   constexpr bool kTmaStoreOk = kHalf % kBoxCols == 0;  // (BN 320 writes C with direct stores)
-  constexpr int kRowsTile = kBlockM * CTA_GROUP;
+  // rows of the MMA's row operand per CTA and per tile: 128 (A), or with SWAP the
+  // p.swap_rows rows of B per CTA
+  const int32_t rows_cta = SWAP ? p.swap_rows : kBlockM;
+  const int32_t kRowsTile = rows_cta * CTA_GROUP;
   constexpr int kKbElems = KIND == 0 ? kBlockK : 2 * kBlockK;  // K elements per K block
 
   extern __shared__ uint8_t smem_raw[];
@@ -660,12 +706,13 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
     // 4096^3 (measured).
     auto produce = [&](auto hinted) {
       constexpr bool kHint = decltype(hinted)::value;
-      const uint64_t pol_a = kHint ? l2_policy_evict_last() : 0ull;
-      const uint64_t pol_b = kHint ? l2_policy_evict_first() : 0ull;
+      // (with SWAP the row operand, tmA, is B: B's lines go first, A's last either way)
+      const uint64_t pol_a = kHint ? (SWAP ? l2_policy_evict_first() : l2_policy_evict_last()) : 0ull;
+      const uint64_t pol_b = kHint ? (SWAP ? l2_policy_evict_last() : l2_policy_evict_first()) : 0ull;
       Walker walk{first_unit, 0};
       Unit w;
       while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
-        const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
+        const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * rows_cta;
         // a half-tile unit loads half the B rows (through the half-height map tmB2)
         const bool half = w.half >= 0;
         // (BN 320: each CTA's first 128 B rows are columns 128 * rank.. of the tile, its
@@ -835,7 +882,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
         // in a half-tile unit the h = 1 warps only take part in the slot hand-over, and
         // so do warps whose 32 rows all lie at or past M (no partial, no store)
-        const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;
+        const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * rows_cta;
         const bool active = (w.half < 0 || h == 0) && m0 + (int32_t)(q * 32u) < p.M;
         const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
         uint32_t good = 1;
@@ -1095,7 +1142,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
       if (!ok) break;
       if (!active) continue;
 
-      const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * kBlockM;  // first row of this CTA
+      const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * rows_cta;  // first row of this CTA
       // first column written by this warp
       const int32_t n_half = w.n_blk * BN + (w.half >= 0 ? w.half : (int32_t)h) * kHalf;
       bool exchanged = false;
@@ -1368,6 +1415,12 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES>::kThreads), 1)
         const int32_t m = m0 + (int32_t)row;
 #pragma unroll
         for (int pc = 0; pc < kPieces; ++pc) fuse_piece<OUT>(p, m, n_half + 32 * pc, acc + 32 * pc);
+      }
+      if constexpr (SWAP) {
+        // this thread holds column n = m0 + row of C (row n of B), for the kHalf rows of
+        // C (rows of A) from n_half on
+        store_col_direct<OUT, kHalf>(p, m0 + (int32_t)row, (int32_t)row < rows_cta, n_half, acc);
+        continue;
       }
       // this unit's output: the launch's C, or in a grouped launch its problem's
       const GroupDesc* gd = nullptr;

@@ -6,16 +6,16 @@
 namespace gb300 {
 
 cudaError_t launch_cg2_kx(const LaunchSpec& s) {
-  if (s.bn == 256 && s.stages == 6) return by_out<2, 256, 6, true, false, 0, false, true>(s);
-  if (s.bn == 128 && s.stages == 8) return by_out<2, 128, 8, true, false, 0, false, true>(s);
-  if (s.bn == 320 && s.stages == 5) return by_out<2, 320, 5, true, false, 0, false, true>(s);
+  if (s.bn == 256 && s.stages == 7) return by_out<2, 256, 7, true, false, 0, false, true>(s);
+  if (s.bn == 128 && s.stages == 9) return by_out<2, 128, 9, true, false, 0, false, true>(s);
+  if (s.bn == 320 && s.stages == 6) return by_out<2, 320, 6, true, false, 0, false, true>(s);
   return cudaErrorInvalidValue;
 }
 
 int resident_cg2_kx(int bn, int stages, int out) {
-  if (bn == 256 && stages == 6) return resident_by_out<2, 256, 6, true>(out);
-  if (bn == 128 && stages == 8) return resident_by_out<2, 128, 8, true>(out);
-  if (bn == 320 && stages == 5) return resident_by_out<2, 320, 5, true>(out);
+  if (bn == 256 && stages == 7) return resident_by_out<2, 256, 7, true>(out);
+  if (bn == 128 && stages == 9) return resident_by_out<2, 128, 9, true>(out);
+  if (bn == 320 && stages == 6) return resident_by_out<2, 320, 6, true>(out);
   return 0;
 }
 

@@ -4,34 +4,32 @@
 
 namespace gb300 {
 
+// The plain (unsplit or workspace-split) kernels' menu; the cluster K split has its own
+// ring depths (kx_stages).  BN 320 exists only for the cluster K split.
 bool kernel_supported(int cg, int bn, int stages) {
   if (cg == 1)
     return (bn == 256 && (stages == 4 || stages == 5)) || (bn == 128 && (stages == 6 || stages == 10));
   if (cg == 2) return (bn == 256 && stages == 6) || (bn == 128 && stages == 8) ||
-                     (bn == 320 && stages == 5);
+                     (bn == 320 && stages == 6);
   return false;
 }
 
 int default_stages(int cg, int bn, bool small_a) {
   if (cg == 1) return bn == 256 ? (small_a ? 5 : 4) : (small_a ? 10 : 6);
-  return bn == 320 ? 5 : bn == 256 ? 6 : 8;
+  return bn == 320 ? 6 : bn == 256 ? 6 : 8;
 }
 
-size_t kernel_smem_bytes(int cg, int bn, int stages) {
-  if (!kernel_supported(cg, bn, stages)) return 0;
-  if (cg == 1) {
-    if (bn == 256) return stages == 5 ? Layout<1, 256, 5>::kDynamicBytes : Layout<1, 256, 4>::kDynamicBytes;
-    return stages == 10 ? Layout<1, 128, 10>::kDynamicBytes : Layout<1, 128, 6>::kDynamicBytes;
-  }
-  if (bn == 320) return Layout<2, 320, 5>::kDynamicBytes;
-  return bn == 256 ? Layout<2, 256, 6>::kDynamicBytes : Layout<2, 128, 8>::kDynamicBytes;
+// The cluster K split keeps its epilogue staging inside the idle ring, which leaves room
+// for one more stage (two more of the 16-row A stages).
+int kx_stages(int cg, int bn, bool small_a) {
+  if (cg == 1) return bn == 256 ? (small_a ? 6 : 4) : (small_a ? 12 : 7);
+  return bn == 320 ? 6 : bn == 256 ? 7 : 9;
 }
 
+// One-CTA kernels deeper than 7 stages of 128 columns or 4 of 256 hold 16 rows of A per
+// stage (the Layout's rule).
 int a_rows(int cg, int bn, int stages) {
-  if (cg == 1) {
-    if (bn == 256) return stages == 5 ? Layout<1, 256, 5>::kARows : Layout<1, 256, 4>::kARows;
-    return stages == 10 ? Layout<1, 128, 10>::kARows : Layout<1, 128, 6>::kARows;
-  }
+  if (cg == 1 && ((bn == 128 && stages > 7) || (bn == 256 && stages > 4))) return 16;
   return kBlockM;
 }
 
@@ -44,6 +42,11 @@ int max_resident_kx_clusters(int cg, int bn, int stages, int out) {
 }
 
 cudaError_t launch_gemm(const LaunchSpec& s) {
+  if (s.swap) {
+    if (s.kind != 0 || s.fused || s.grouped || s.kx2 || s.staged || s.one_chain || s.cta_group != 2)
+      return cudaErrorInvalidValue;
+    return launch_cg2_swap(s);
+  }
   if (s.kx2) {
     if (s.kind != 0 || s.fused || s.grouped) return cudaErrorInvalidValue;
     if (s.cta_group == 1) return s.one_chain ? launch_cg1_kx(s) : launch_cg1_kxg(s);

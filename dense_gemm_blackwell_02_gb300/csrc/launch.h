@@ -23,6 +23,8 @@ struct LaunchSpec {
                    // (one unit per CTA group)
   bool staged;     // plain general epilogue, K slices or stream-K segments meeting in the
                    // workspace: the kernel with the staged fix-up
+  bool swap;       // the swapped tiling: tmA maps B (box p.swap_rows rows), tmB maps A
+                   // (box bn / 2 rows), C written transposed by direct stores
   CUtensorMap tmA; // A: box {128 bytes of K, 128 (or M < 128) rows}
   CUtensorMap tmB; // B: box {128 bytes of K, bn / cta_group}
   CUtensorMap tmB2; // B: box {128 bytes of K, bn / cta_group / 2} (half-tile units; else tmB);
@@ -52,8 +54,9 @@ bool kernel_supported(int cta_group, int bn, int stages);
 // small_a: a one-CTA row tile of at most 16 rows (the ring then holds 16 rows of A per
 // stage and is deeper)
 int default_stages(int cta_group, int bn, bool small_a = false);
+// the ring depth of the cluster-K-split kernels (their staging lies inside the ring)
+int kx_stages(int cta_group, int bn, bool small_a = false);
 int a_rows(int cta_group, int bn, int stages);  // A rows a stage of that kernel holds
-size_t kernel_smem_bytes(int cta_group, int bn, int stages);
 // Clusters (CTAs for cta_group 1) of this configuration that can be resident at once
 // on the current device; 0 if the query fails.
 int max_resident_units(int cta_group, int bn, int stages, int out);
@@ -87,6 +90,7 @@ cudaError_t launch_cg2_kx(const LaunchSpec& s);
 cudaError_t launch_cg1_kxg(const LaunchSpec& s);  // general epilogue
 cudaError_t launch_cg1_staged(const LaunchSpec& s);  // general epilogue, staged fix-up
 cudaError_t launch_cg2_staged(const LaunchSpec& s);
+cudaError_t launch_cg2_swap(const LaunchSpec& s);  // the swapped tiling (kernels_cg2_swap.cu)
 cudaError_t launch_cg2_kxg(const LaunchSpec& s);
 int resident_cg1_kx(int bn, int stages, int out);
 int resident_cg2_kx(int bn, int stages, int out);

@@ -6,11 +6,11 @@
 namespace gb300 {
 
 template <int CG, int BN, int STAGES, int OUT, bool ONE, bool FUSED, int KIND = 0,
-          bool GROUPED = false, bool KX2 = false, bool STAGED = false>
+          bool GROUPED = false, bool KX2 = false, bool STAGED = false, bool SWAP = false>
 cudaError_t launch_one(const LaunchSpec& s) {
-  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED, KIND, GROUPED, KX2, STAGED>;
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP>;
   constexpr unsigned kCluster = CG * (KX2 ? 2 : 1);
-  using L = Layout<CG, BN, STAGES>;
+  using L = Layout<CG, BN, STAGES, KX2>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes);
   if (e != cudaSuccess) return e;
@@ -47,7 +47,7 @@ template <int CG, int BN, int STAGES, int OUT, bool KX2 = false>
 int resident_one() {
   auto kernel = gemm_kernel<CG, BN, STAGES, OUT, KX2, false, 0, false, KX2, false>;
   constexpr unsigned kCluster = CG * (KX2 ? 2 : 1);
-  using L = Layout<CG, BN, STAGES>;
+  using L = Layout<CG, BN, STAGES, KX2>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            L::kDynamicBytes) != cudaSuccess)
     return 0;
@@ -71,12 +71,12 @@ int resident_one() {
 }
 
 template <int CG, int BN, int STAGES, bool ONE, bool FUSED, int KIND = 0, bool GROUPED = false,
-          bool KX2 = false, bool STAGED = false>
+          bool KX2 = false, bool STAGED = false, bool SWAP = false>
 cudaError_t by_out(const LaunchSpec& s) {
   switch (s.out) {
-    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED>(s);
-    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED>(s);
-    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED, KIND, GROUPED, KX2, STAGED>(s);
+    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP>(s);
+    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP>(s);
+    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP>(s);
     default: return cudaErrorInvalidValue;
   }
 }

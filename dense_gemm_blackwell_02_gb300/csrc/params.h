@@ -69,6 +69,8 @@ struct GemmParams {
   int32_t l2_hint;         // 2: B's loads evict-first and A's evict-last in L2; else none
   uint32_t a_tx_short;     // bytes of A's 128-row box that A's tensor map does not load:
                            // (128 - M) * 128 when a one-CTA tile's A box is M < 128 rows
+                           // (for the pair in the swapped tiling: 2 * (128 - swap_rows) * 128)
+  int32_t swap_rows;       // swapped tiling (B is the MMA's row operand): B rows per CTA
   int32_t vec_store;       // 1 when 16-byte vector stores of C are aligned
   int32_t tma_store;       // 1 when C is written through the C tensor map
   uint32_t idesc;          // tcgen05 instruction descriptor (N = BN)

@@ -84,7 +84,12 @@ typedef enum {
  *   stages    depth of the shared-memory operand ring: 6 (pairs, BN 256), 8 (pairs, BN
  *             128), 4 (one CTA, BN 256), 6 (one CTA, BN 128); or, for one CTA and at most 16
  *             rows of A with fp16/bf16 inputs and no fused epilogue, 5 (BN 256) or 10 (BN
- *             128) stages that hold 16 rows of A each (chosen automatically for M <= 16)
+ *             128) stages that hold 16 rows of A each (chosen automatically for M <= 16).
+ *             The cluster K split (epilogue 3) keeps its epilogue staging inside the idle
+ *             ring and runs one stage deeper: 7 (pairs, BN 256), 9 (pairs, BN 128), 6
+ *             (pairs, BN 320), 4 (one CTA, BN 256), 7 (one CTA, BN 128), 6 and 12 with
+ *             16-row A stages; a forced depth other than that one refuses it.
+ *             gemm_last_config reports the depth used.
  *   group_m   grouped rasterisation: M tiles per group
  *   max_ctas  cap on the persistent grid (0 = one CTA per SM)
  *   chain_kblocks  K blocks (128 bytes of K: 64 fp16/bf16 or 128 FP8 elements)
@@ -117,7 +122,19 @@ typedef enum {
  *             evict-first and A's evict-last (for one row of tiles, where every B
  *             element is read once and A is re-read by every tile); 0 = 2 when the
  *             tiles form one row (M <= 256 for CTA pairs, M <= 128 for one CTA per
- *             tile), else 1.  gemm_last_config reports the one used.
+ *             tile; with swap_ab, M <= block_n), else 1.  gemm_last_config reports the
+ *             one used.
+ *   swap_ab   2 = the swapped tiling for a few rows of A (decode shapes): B is the
+ *             MMA's row operand, swap_rows of its rows per CTA of a pair, and block_n
+ *             (128 or 256) rows of A are the MMA's columns, so a tile covers block_n
+ *             rows x 2 * swap_rows columns of C, written transposed from Tensor Memory
+ *             by direct stores.  Valid for fp16/bf16 inputs without a fused epilogue,
+ *             CTA pairs (variant 0 or 2), no K split (splits 0 or 1), the general
+ *             epilogue (epilogue 0 or 1); else GEMM_ERR_UNSUPPORTED.  1 = off;
+ *             0 = chosen automatically.  gemm_last_config reports 2 or 1.
+ *   swap_rows with swap_ab: rows of B per CTA, 1..128 (0 = the fewest that make one
+ *             wave of tiles, rounded up to a multiple of 8, at most 128).
+ *             gemm_last_config reports the one used (0 when not swapped).
  */
 typedef struct {
   int32_t variant;
@@ -131,6 +148,8 @@ typedef struct {
   int32_t prefetch_kblocks;
   int32_t epilogue;
   int32_t l2_hint;
+  int32_t swap_ab;
+  int32_t swap_rows;
 } gemm_config_t;
 
 /* Create a handle on the current CUDA device.  Fails with GEMM_ERR_UNSUPPORTED

@@ -511,12 +511,14 @@ def test_l2_policy_changes_no_bits(g, M, N, K, cfg):
                                            (3000, 520, F16)])
 def test_rows_of_at_most_16_take_the_deeper_ring(g, M, N, K, dtype_out):
     # one CTA per row tile of <= 16 rows: stages of 16 A rows (2 KiB), a deeper ring
-    # (10 stages of 128 columns, 5 of 256); the MMA's 128-row A operand runs on over the
-    # next stages' bytes, which feed only accumulator rows that are never stored
+    # (10 stages of 128 columns, 5 of 256; 12 and 6 under the cluster K split, whose
+    # staging lies in the ring); the MMA's 128-row A operand runs on over the next stages'
+    # bytes, which feed only accumulator rows that are never stored
     _case(g, M, N, K, F16, dtype_out, seed=48)
     cfg = g.last_config()
     if cfg["variant"] == 1:          # (one row of A may take the matrix-vector path)
-        deep = {128: 10, 256: 5}[cfg["block_n"]]
+        kx = cfg["epilogue"] == 3
+        deep = {128: 12 if kx else 10, 256: 6 if kx else 5}[cfg["block_n"]]
         assert (cfg["stages"] == deep) == (M <= 16), cfg
     _case(g, M, N, K, BF16, F32, seed=49, exact=True, ints=True)
 
@@ -669,3 +671,83 @@ def test_matrix_vector_path_rejections(g):
         assert e.value.code == 2
     finally:
         g.reset_config()
+
+
+# The swapped tiling: B's rows are the MMA's row operand (swap_rows per CTA, a short box
+# whose missing rows only feed accumulator lanes that are never stored), A's rows its
+# columns; C is written transposed.  Ragged rows of A and of B, K tails, two accumulation
+# chains, 256 rows of A per tile, a persistent loop of several tiles per pair.
+@pytest.mark.parametrize("M,N,K,din,dout,extra", [
+    (256, 8192, 1024, F16, F16, {}),                      # one wave, automatic rows
+    (200, 3000, 2048, BF16, F32, {}),                     # ragged rows of A and of B
+    (256, 1000, 520, F16, BF16, {"swap_rows": 40}),       # K tail, many tiles per pair
+    (100, 777, 4096, F16, F16, {"block_n": 256}),         # 256 rows of A per tile
+    (1, 4097, 512, BF16, F32, {}),                        # one row of A
+    (256, 2048, 8192, F16, F32, {"swap_rows": 128}),      # two accumulation chains
+    (129, 5000, 1024, F16, F16, {"swap_rows": 96, "max_ctas": 16}),  # persistent loop
+])
+def test_swapped_tiling(g, M, N, K, din, dout, extra):
+    cfg = dict(swap_ab=2, **extra)
+    g.set_config(**cfg)
+    try:
+        _case(g, M, N, K, din, dout, seed=61)
+        used = g.last_config()
+        _case(g, M, N, K, BF16, F32 if dout == F32 else dout, seed=62, exact=True, ints=True)
+    finally:
+        g.reset_config()
+    assert used["swap_ab"] == 2 and used["variant"] == 2 and used["splits"] == 1, used
+    w = used["swap_rows"]
+    assert 1 <= w <= 128 and (extra.get("swap_rows", w) == w), used
+    bn = extra.get("block_n", 128)
+    assert used["block_n"] == bn and used["dp_tiles"] == -(-N // (2 * w)) * -(-M // bn), used
+
+
+def test_swapped_tiling_matches_the_plain_tiling_on_integers(g):
+    # the same integer-valued product both ways: bit-identical (every partial sum exact)
+    M, N, K = 256, 4096, 2048
+    A, B = si.make_small_int_operands(M, N, K, F16, seed=63)
+    got = {}
+    for swap in (1, 2):
+        g.set_config(swap_ab=swap)
+        try:
+            C = parity.run_gpu(g, A, B, F32)
+            assert g.device_status()[0] == 0
+            assert g.last_config()["swap_ab"] == swap
+        finally:
+            g.reset_config()
+        got[swap] = parity.bits_of(C)
+    assert np.array_equal(got[1], got[2])
+
+
+def test_swapped_tiling_rejections(g):
+    from dense_gemm_blackwell_02_gb300.binding import GemmError
+    A = torch.zeros(256, 1024, dtype=torch.float16, device="cuda")
+    B = torch.zeros(512, 1024, dtype=torch.float16, device="cuda")
+    C = torch.zeros(256, 512, dtype=torch.float16, device="cuda")
+    for cfg in ({"swap_ab": 2, "variant": 1}, {"swap_ab": 2, "splits": 2},
+                {"swap_ab": 2, "splits": -1}, {"swap_ab": 2, "epilogue": 2},
+                {"swap_ab": 2, "block_n": 320}):
+        g.set_config(**cfg)
+        try:
+            with pytest.raises(GemmError) as e:
+                g.run(A, B, C)
+            assert e.value.code == 2, cfg
+        finally:
+            g.reset_config()
+    g.set_config(swap_ab=2)
+    try:
+        with pytest.raises(GemmError) as e:                       # a fused epilogue
+            g.run_epilogue(A, B, C, alpha=2.0)
+        assert e.value.code == 2
+        A8 = A.to(torch.float8_e4m3fn)
+        B8 = B.to(torch.float8_e4m3fn)
+        with pytest.raises(GemmError) as e:                       # FP8 operands
+            g.run(A8, B8, C)
+        assert e.value.code == 2
+    finally:
+        g.reset_config()
+    from dense_gemm_blackwell_02_gb300.binding import lib, GemmConfig
+    import ctypes
+    for bad in ({"swap_ab": 3}, {"swap_rows": 129}, {"swap_rows": -1}):
+        cfg = GemmConfig(**{**{n: 0 for n, _ in GemmConfig._fields_}, **bad})
+        assert lib().gemm_set_config(g._h, ctypes.byref(cfg)) == 1, bad
