@@ -27,7 +27,7 @@ class GemmConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("variant", "block_n", "splits", "stages",
                                                 "group_m", "max_ctas", "chain_kblocks",
                                                 "dp_tiles", "prefetch_kblocks", "epilogue",
-                                                "l2_hint", "swap_ab", "swap_rows")]
+                                                "l2_hint", "swap_ab", "swap_rows", "scheduler")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -270,9 +270,9 @@ class Gemm:
     # ----------------------------------------------------------------- control --
     def set_config(self, variant=0, block_n=0, splits=0, stages=0, group_m=0, max_ctas=0,
                    chain_kblocks=0, prefetch_kblocks=0, epilogue=0, l2_hint=0, swap_ab=0,
-                   swap_rows=0):
+                   swap_rows=0, scheduler=0):
         cfg = GemmConfig(variant, block_n, splits, stages, group_m, max_ctas, chain_kblocks, 0,
-                         prefetch_kblocks, epilogue, l2_hint, swap_ab, swap_rows)
+                         prefetch_kblocks, epilogue, l2_hint, swap_ab, swap_rows, scheduler)
         _check(lib().gemm_set_config(self._h, ctypes.byref(cfg)), "gemm_set_config")
 
     def reset_config(self):

@@ -530,7 +530,7 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
   if (c.splits < -1 || c.stages < 0 || c.group_m < 0 || c.max_ctas < 0 || c.chain_kblocks < 0 ||
       c.dp_tiles != 0 || c.prefetch_kblocks < -1 || c.epilogue < 0 || c.epilogue > 3 ||
       c.l2_hint < 0 || c.l2_hint > 2 || c.swap_ab < 0 || c.swap_ab > 2 || c.swap_rows < 0 ||
-      c.swap_rows > 128)
+      c.swap_rows > 128 || c.scheduler < 0 || c.scheduler > 2)
     return GEMM_ERR_INVALID_ARG;
   if (c.stages) {
     const int bn = c.block_n ? c.block_n : 256;
@@ -621,9 +621,10 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
     g.grid = (int)std::min<int64_t>(ceil_div(N, (int64_t)8), cap);
     g.stream = stream;
     if ((h->last_cuda = launch_gemv(g)) != cudaSuccess) return GEMM_ERR_CUDA;
-    h->last = gemm_config_t{3, 0, 1, 0, 0, g.grid, 0, (int32_t)N, -1, 1, 1, 1, 0};
+    h->last = gemm_config_t{3, 0, 1, 0, 0, g.grid, 0, (int32_t)N, -1, 1, 1, 1, 0, 1};
     return GEMM_OK;
   }
+  if (fc.scheduler == 2) return GEMM_ERR_UNSUPPORTED;  // (cluster launch control: grouped launches)
   Choice ch;
   const bool fp8 = is_fp8(dtype_in);
   gemm_status_t st = choose(h, M, N, K, out, fp8 ? 2 * kBlockK : kBlockK, bs != nullptr,
@@ -738,7 +739,7 @@ gemm_status_t run_impl(gemm_handle_t h, const void* A, const void* B, void* C, i
                           ch.stages,
                           ch.group_m,  ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles,
                           ch.prefetch_kb ? ch.prefetch_kb : -1, ch.kx2 ? 3 : ch.one_chain ? 2 : 1,
-                          ch.l2_hint, ch.swap ? 2 : 1, ch.swap_rows};
+                          ch.l2_hint, ch.swap ? 2 : 1, ch.swap_rows, 1};
   return GEMM_OK;
 }
 
@@ -808,6 +809,12 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
   }
   if (live.empty()) return GEMM_OK;
   const int G = (int)live.size();
+  // Problems with the longest K first (a stable sort): a tile's time grows with its K, so
+  // the long tiles are handed out first and the short ones fill in at the end of the
+  // launch, whichever scheduler hands them out (longest processing time first).  The
+  // result does not depend on the order.
+  std::stable_sort(live.begin(), live.end(),
+                   [&](int32_t a, int32_t b) { return problems[a].K > problems[b].K; });
   // A CTA pair when padding every problem's M to 256 rows costs at most 10% more work
   // than padding to 128; 128-column tiles when every N fits one.
   const int cg = f.variant ? f.variant : (padded[2] * 10 <= padded[1] * 11 ? 2 : 1);
@@ -888,7 +895,22 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
   s.bn = bn;
   s.stages = stages;
   s.out = out_kind(dtype_out);
-  s.grid = (int)(std::min<int64_t>(units, slots) * cg);
+  // Cluster launch control ("A Blackwell GEMM by Hand in CuTe DSL", section 8): a CTA
+  // (pair) per tile in the grid, each running one taking over the tiles of launches not
+  // yet started, instead of the resident ones taking the tiles round-robin.
+  // Chosen automatically when the tiles' costs differ, i.e. the problems' K do by 2x or
+  // more (measured, one GB300, problems longest K first: groups of 16, 24 and 48 problems
+  // with K from 256 to 16384, 1.22x / 1.08x / equal against round-robin); with one K for
+  // all (MoE layers) every tile costs the same, round-robin is already balanced and was
+  // 0.5-3.5% faster.
+  int64_t kmin = INT64_MAX, kmax = 0;
+  for (int i = 0; i < G; ++i) {
+    kmin = std::min<int64_t>(kmin, problems[live[i]].K);
+    kmax = std::max<int64_t>(kmax, problems[live[i]].K);
+  }
+  s.clc = f.scheduler == 2 || (f.scheduler == 0 && !f.max_ctas && kmax >= 2 * kmin);
+  if (s.clc && f.max_ctas) return GEMM_ERR_UNSUPPORTED;
+  s.grid = (int)((s.clc ? units : std::min<int64_t>(units, slots)) * cg);
   s.grouped = true;
   s.stream = stream;
   // the parameter maps are not read by a grouped kernel; they hold the first problem's
@@ -920,7 +942,7 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_problem_t* problems, 
   p.test_stall = h->test_stall;
   if ((h->last_cuda = launch_gemm(s)) != cudaSuccess) return GEMM_ERR_CUDA;
   h->last = gemm_config_t{cg, bn, 1, stages, p.group_m, s.grid, p.chain_kb, (int32_t)units, -1, 1,
-                          p.l2_hint, 1, 0};
+                          p.l2_hint, 1, 0, s.clc ? 2 : 1};
   return GEMM_OK;
 }
 

@@ -263,11 +263,65 @@ static __device__ __noinline__ bool walker_has_next(const Walker& k, int32_t fir
   return (uint32_t)first * T / W + (uint32_t)k.sk_done < ((uint32_t)first + 1u) * T / W;
 }
 
+// Cluster launch control (CLC): the units of a CTA (pair) are its own, u = blockIdx.x /
+// CTA_GROUP, then the one of each launch it cancels.  Answer q (the unit after the CTA's
+// q-th) lands in slot q % 4 of a ring in shared memory; the producer warp asks for it when
+// it starts its q-th unit, and every warp that walks the units (producer, MMA issuer,
+// epilogue warps; in both CTAs of a pair) reads it when it finishes that unit and frees
+// the slot on the group leader's clc_empty barrier.
+struct ClcLink {
+  uint32_t resp0;      // answer slot 0 (16 bytes each)
+  uint32_t full0;      // clc_full[0] (8 bytes each): armed by this CTA, completed by the answer
+  uint32_t empty0;     // clc_empty[0] of this CTA: the readers of both CTAs arrive on the leader's
+  uint32_t leader;     // cluster rank of the group leader
+};
+
+// (out of line, like sk_next, so that the epilogue's accumulator keeps its registers)
+template <int CTA_GROUP>
+static __device__ __noinline__ bool clc_next(const ClcLink& c, uint32_t q, const WaitCtl& ctl,
+                                             int32_t& unit) {
+  const uint32_t s = q & 3u;
+  if (!warp_wait(c.full0 + 8u * s, (q >> 2) & 1u, ctl, kSiteClc)) return false;
+  uint32_t x;
+  const uint32_t got = clc_query(c.resp0 + 16u * s, x);
+  __syncwarp();
+  if (lane_id() == 0) {
+    if constexpr (CTA_GROUP == 1) mbar_arrive(c.empty0 + 8u * s);
+    else mbar_arrive_cluster(mapa_shared(c.empty0 + 8u * s, c.leader));
+  }
+  unit = (int32_t)(x / (uint32_t)CTA_GROUP);
+  return got != 0;
+}
+
+// The producer warp asks for answer q (it starts its q-th unit): the leader waits until
+// every reader has taken answer q - 4 out of the slot, each CTA arms its own barrier for
+// the 16 bytes, and the leader's elected lane sends the request (to the whole cluster for
+// a pair).
+template <int CTA_GROUP>
+__device__ __forceinline__ bool clc_request(const ClcLink& c, uint32_t q, bool leader,
+                                            const WaitCtl& ctl) {
+  const uint32_t s = q & 3u;
+  if (leader && !warp_wait(c.empty0 + 8u * s, ((q >> 2) & 1u) ^ 1u, ctl, kSiteClc)) return false;
+  mbar_arrive_expect_tx_elect(c.full0 + 8u * s, 16u);
+  if (leader) clc_try_cancel_elect<CTA_GROUP == 2>(c.resp0 + 16u * s, c.full0 + 8u * s);
+  return true;
+}
+
 // Only two 32-bit counters live across a unit; the stream-K range is recomputed from
-// the worker's index on each call.
-template <bool GROUPED>
+// the worker's index on each call.  Under CLC, k.sk_done counts the units walked.
+template <bool GROUPED, bool CLC = false, int CTA_GROUP = 1>
 __device__ __forceinline__ bool walker_next(Walker& k, int32_t first, int32_t stride,
-                                            const GemmParams& p, Unit& w) {
+                                            const GemmParams& p, Unit& w,
+                                            const ClcLink* clc = nullptr,
+                                            const WaitCtl* ctl = nullptr) {
+  if constexpr (CLC) {
+    if (k.sk_done > 0 && !clc_next<CTA_GROUP>(*clc, (uint32_t)(k.sk_done - 1), *ctl, k.u))
+      return false;
+    ++k.sk_done;
+    if constexpr (GROUPED) decode_grouped(k.u, p, w);
+    else w = decode_unit(k.u, p);
+    return true;
+  }
   if (k.u < p.units) {
     if constexpr (GROUPED) decode_grouped(k.u, p, w);
     else w = decode_unit(k.u, p);
@@ -534,11 +588,15 @@ struct Layout {
   static constexpr uint32_t kCOff = RING_STAGING ? kKxBytes : kRingEnd;
   static constexpr uint32_t kBarOff =
       RING_STAGING ? kRingEnd : kCOff + kEpiWarps * kStagingBytes;
-  // full[S], empty[S], acc_full[2], acc_empty[2], drain, kx_ready[8], kx_go[8]
-  static constexpr uint32_t kNumBars = 2 * STAGES + 5 + 2 * kEpiWarps;
+  // cluster launch control: a ring of 16-byte answers
+  static constexpr uint32_t kClcSlots = 4;
+  // full[S], empty[S], acc_full[2], acc_empty[2], drain, kx_ready[8], kx_go[8],
+  // clc_full[4], clc_empty[4]
+  static constexpr uint32_t kNumBars = 2 * STAGES + 5 + 2 * kEpiWarps + 2 * kClcSlots;
   static constexpr uint32_t kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
-  static constexpr uint32_t kEnd = kAbortOff + 4;
+  static constexpr uint32_t kClcOff = (kAbortOff + 4 + 15) & ~15u;
+  static constexpr uint32_t kEnd = kClcOff + kClcSlots * 16;
   static constexpr uint32_t kDynamicBytes = kEnd + 1024;  // slack for 1024-byte alignment
   static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0 && kBOff % 1024 == 0 &&
                     kCOff % 1024 == 0,
@@ -578,8 +636,12 @@ struct Layout {
 // rows are the MMA's columns, BN of them per tile split over the pair like B's are
 // otherwise.  A thread's accumulator row is then a column of C, and the epilogue writes
 // it transposed.  CTA pairs, general epilogue, plain fp16/bf16, whole tiles.
+// CLC: the units are handed out by cluster launch control instead of round-robin: the grid
+// holds a CTA (pair) per unit and each running one takes over the work of launches that
+// have not started (ClcLink above).  Grouped launches (whole tiles).
 template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN, bool FUSED, int KIND = 0,
-          bool GROUPED = false, bool KX2 = false, bool STAGED = false, bool SWAP = false>
+          bool GROUPED = false, bool KX2 = false, bool STAGED = false, bool SWAP = false,
+          bool CLC = false>
 __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
@@ -599,6 +661,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
   static_assert(!SWAP || (CTA_GROUP == 2 && BN != 320 && !ONE_CHAIN && !FUSED && KIND == 0 &&
                           !GROUPED && !KX2 && !STAGED),
                 "the swapped tiling is a plain CTA-pair kernel with the general epilogue");
+  static_assert(!CLC || (GROUPED && !SWAP), "cluster launch control serves grouped launches");
   constexpr uint32_t kTmemCols = BN == 320 ? 512 : 2 * BN;  // two accumulator slots (one for 320)
   constexpr int kHalf = BN / 2;                // columns per epilogue warp
   constexpr int kPieces = kHalf / 32;          // tcgen05.ld x32 pieces per warp
@@ -628,6 +691,10 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
   auto kx_ready_bar = [&](uint32_t w) { return bar0 + 8u * (2 * STAGES + 5 + w); };
   auto kx_go_bar = [&](uint32_t w) { return bar0 + 8u * (2 * STAGES + 5 + L::kEpiWarps + w); };
+  auto clc_full_bar = [&](uint32_t s) { return bar0 + 8u * (2 * STAGES + 5 + 2 * L::kEpiWarps + s); };
+  auto clc_empty_bar = [&](uint32_t s) {
+    return bar0 + 8u * (2 * STAGES + 5 + 2 * L::kEpiWarps + L::kClcSlots + s);
+  };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlotOff);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kAbortOff);
 
@@ -648,6 +715,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
   const bool leader = rank == 0;
   const int32_t first_unit = (int32_t)(blockIdx.x / CTA_GROUP);
   const int32_t unit_stride = (int32_t)(gridDim.x / CTA_GROUP);
+  const ClcLink clc{base + L::kClcOff, clc_full_bar(0), clc_empty_bar(0), group_base};
 
   // ---------------------------------------------------------------- setup --
   if (warp == 0 && lane == 0) {
@@ -663,6 +731,13 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
       for (uint32_t w = 0; w < L::kEpiWarps; ++w) {
         mbar_init(kx_ready_bar(w), 1);  // the receiving warp arms it; the sender's bytes complete it
         mbar_init(kx_go_bar(w), 1);     // the receiving warp: its ring is free
+      }
+    }
+    if constexpr (CLC) {
+      for (uint32_t i = 0; i < L::kClcSlots; ++i) {
+        mbar_init(clc_full_bar(i), 1);  // this CTA's producer arms it; the answer completes it
+        // every reader: producer, MMA issuer (leader) and epilogue warps of the group
+        mbar_init(clc_empty_bar(i), CTA_GROUP == 2 ? 2 * (2 + L::kEpiWarps) - 1 : 2 + L::kEpiWarps);
       }
     }
     mbar_init(drain_bar, 1);
@@ -697,6 +772,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
     // out ahead of A's: on the decode shapes B streams from DRAM while A stays in L2
     // (1-3% faster there, neutral on square shapes; measured).
     uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
+    uint32_t clc_asked = 0;  // answers this warp has asked for (CLC)
     bool ok = true;
     // When every B element is read by one tile only (one row of tiles), B's lines are
     // marked first to be evicted and A's last: A, re-read by every tile from L2, then
@@ -711,7 +787,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
       const uint64_t pol_b = kHint ? (SWAP ? l2_policy_evict_last() : l2_policy_evict_first()) : 0ull;
       Walker walk{first_unit, 0};
       Unit w;
-      while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
+      while (ok && walker_next<GROUPED, CLC, CTA_GROUP>(walk, first_unit, unit_stride, p, w, &clc, &ctl)) {
         const int32_t a_row = w.m_blk * kRowsTile + (int32_t)rank * rows_cta;
         // a half-tile unit loads half the B rows (through the half-height map tmB2)
         const bool half = w.half >= 0;
@@ -787,6 +863,20 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
             phase ^= 1u;
           }
         }
+        if constexpr (CLC) {
+          // Ask for the unit after this one only now that this one's loads are all issued:
+          // a unit is claimed as late as the ring still hides the answer's latency (its
+          // stages are still being multiplied), so that a CTA holds no claimed unit it has
+          // not started while others run out of work.  Asking at the unit's start, or as
+          // soon as the previous answer was in, balanced worse (measured).
+          if (ok) {
+            if (!clc_request<CTA_GROUP>(clc, clc_asked, leader, ctl)) {
+              ok = false;
+              break;
+            }
+            ++clc_asked;
+          }
+        }
       }
     };
     if (p.l2_hint == 2) produce(std::true_type{});
@@ -796,6 +886,9 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
       if (leader) {
         for (uint32_t s = 0; s < STAGES; ++s)
           if (armed & (1u << s)) wait_parity_drain(full_bar(s), (armed_phase >> s) & 1u, ctl);
+        // nor an answer of cluster launch control (after an abort one may be under way)
+        if (CLC && clc_asked > 0)
+          wait_parity_drain(clc_full_bar((clc_asked - 1u) & 3u), ((clc_asked - 1u) >> 2) & 1u, ctl);
       } else if (*abort_flag) {
         // The follower's copies complete on the leader's barrier, which it cannot poll;
         // normally every one of them was consumed by an MMA before the teardown.  On an
@@ -817,7 +910,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
       if (p.test_stall) ok = warp_wait(drain_bar, 0, ctl, kSiteTestStall);
       Walker walk{first_unit, 0};
       Unit w;
-      while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
+      while (ok && walker_next<GROUPED, CLC, CTA_GROUP>(walk, first_unit, unit_stride, p, w, &clc, &ctl)) {
         const uint32_t idesc = w.half >= 0 ? p.idesc_half : p.idesc;
         for (int32_t c0 = w.kb0; c0 < w.kb1 && ok; c0 += p.chain_kb) {
           const int32_t c1 = min(c0 + p.chain_kb, w.kb1);
@@ -879,7 +972,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
       constexpr size_t kBlocksPerSlice = (size_t)CTA_GROUP * 8;  // (rank, quarter, half)
       constexpr size_t kSliceStride = kBlocksPerSlice * kBlockFloats;
       const size_t my_block = ((size_t)rank * 4 + q) * 2 + h;
-      while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
+      while (ok && walker_next<GROUPED, CLC, CTA_GROUP>(walk, first_unit, unit_stride, p, w, &clc, &ctl)) {
         // in a half-tile unit the h = 1 warps only take part in the slot hand-over, and
         // so do warps whose 32 rows all lie at or past M (no partial, no store)
         const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * rows_cta;
@@ -1036,7 +1129,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
         ++iter;
       }
     } else {
-    while (ok && walker_next<GROUPED>(walk, first_unit, unit_stride, p, w)) {
+    while (ok && walker_next<GROUPED, CLC, CTA_GROUP>(walk, first_unit, unit_stride, p, w, &clc, &ctl)) {
       // In a half-tile unit the accumulator holds BN/2 columns: the h = 0 warps own
       // them, the h = 1 warps only take part in the slot hand-over.
       const bool active = w.half < 0 || h == 0;

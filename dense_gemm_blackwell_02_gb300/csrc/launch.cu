@@ -42,6 +42,7 @@ int max_resident_kx_clusters(int cg, int bn, int stages, int out) {
 }
 
 cudaError_t launch_gemm(const LaunchSpec& s) {
+  if (s.clc && !s.grouped) return cudaErrorInvalidValue;
   if (s.swap) {
     if (s.kind != 0 || s.fused || s.grouped || s.kx2 || s.staged || s.one_chain || s.cta_group != 2)
       return cudaErrorInvalidValue;
@@ -55,8 +56,8 @@ cudaError_t launch_gemm(const LaunchSpec& s) {
   }
   if (s.grouped) {
     if (s.kind != 0 || s.fused || s.one_chain) return cudaErrorInvalidValue;
-    if (s.cta_group == 1) return launch_cg1_grouped(s);
-    if (s.cta_group == 2) return launch_cg2_grouped(s);
+    if (s.cta_group == 1) return s.clc ? launch_cg1_grouped_clc(s) : launch_cg1_grouped(s);
+    if (s.cta_group == 2) return s.clc ? launch_cg2_grouped_clc(s) : launch_cg2_grouped(s);
     return cudaErrorInvalidValue;
   }
   if (s.kind == 2) {

@@ -25,6 +25,8 @@ struct LaunchSpec {
                    // workspace: the kernel with the staged fix-up
   bool swap;       // the swapped tiling: tmA maps B (box p.swap_rows rows), tmB maps A
                    // (box bn / 2 rows), C written transposed by direct stores
+  bool clc;        // grouped launches: units handed out by cluster launch control (a CTA or
+                   // pair per unit in the grid) instead of round-robin over resident ones
   CUtensorMap tmA; // A: box {128 bytes of K, 128 (or M < 128) rows}
   CUtensorMap tmB; // B: box {128 bytes of K, bn / cta_group}
   CUtensorMap tmB2; // B: box {128 bytes of K, bn / cta_group / 2} (half-tile units; else tmB);
@@ -84,6 +86,8 @@ cudaError_t launch_cg2_fp8bw(const LaunchSpec& s);
 // ... and grouped launches (kernels_cg*_grouped.cu)
 cudaError_t launch_cg1_grouped(const LaunchSpec& s);
 cudaError_t launch_cg2_grouped(const LaunchSpec& s);
+cudaError_t launch_cg1_grouped_clc(const LaunchSpec& s);  // ... scheduled by cluster launch control
+cudaError_t launch_cg2_grouped_clc(const LaunchSpec& s);
 // ... and the cluster K split (kernels_cg*_kx.cu)
 cudaError_t launch_cg1_kx(const LaunchSpec& s);
 cudaError_t launch_cg2_kx(const LaunchSpec& s);

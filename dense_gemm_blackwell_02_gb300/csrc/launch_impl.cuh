@@ -6,9 +6,10 @@
 namespace gb300 {
 
 template <int CG, int BN, int STAGES, int OUT, bool ONE, bool FUSED, int KIND = 0,
-          bool GROUPED = false, bool KX2 = false, bool STAGED = false, bool SWAP = false>
+          bool GROUPED = false, bool KX2 = false, bool STAGED = false, bool SWAP = false,
+          bool CLC = false>
 cudaError_t launch_one(const LaunchSpec& s) {
-  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP>;
+  auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP, CLC>;
   constexpr unsigned kCluster = CG * (KX2 ? 2 : 1);
   using L = Layout<CG, BN, STAGES, KX2>;
   cudaError_t e =
@@ -71,12 +72,12 @@ int resident_one() {
 }
 
 template <int CG, int BN, int STAGES, bool ONE, bool FUSED, int KIND = 0, bool GROUPED = false,
-          bool KX2 = false, bool STAGED = false, bool SWAP = false>
+          bool KX2 = false, bool STAGED = false, bool SWAP = false, bool CLC = false>
 cudaError_t by_out(const LaunchSpec& s) {
   switch (s.out) {
-    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP>(s);
-    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP>(s);
-    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP>(s);
+    case kOutF16: return launch_one<CG, BN, STAGES, kOutF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP, CLC>(s);
+    case kOutBF16: return launch_one<CG, BN, STAGES, kOutBF16, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP, CLC>(s);
+    case kOutF32: return launch_one<CG, BN, STAGES, kOutF32, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP, CLC>(s);
     default: return cudaErrorInvalidValue;
   }
 }

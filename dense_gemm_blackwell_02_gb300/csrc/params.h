@@ -31,6 +31,7 @@ enum WaitSite : uint32_t {
   kSiteTestStall = 5, // deliberate wait on a barrier nothing arrives on (test only)
   kSiteDrain = 6,     // teardown: outstanding copies / MMAs
   kSiteKx = 7,        // two-slice exchange through distributed shared memory
+  kSiteClc = 8,       // cluster launch control: a free answer slot, or the next answer
 };
 
 // One problem of a grouped launch ("CUTLASS Deep Dive: From CuTe Layouts to Blackwell

@@ -466,4 +466,41 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// ---------------------------------------------------------- cluster launch control --
+// Dynamic scheduling ("A Blackwell GEMM by Hand in CuTe DSL", section 8: the tutorials'
+// cluster-launch-control scheduler): a running CTA asks to cancel the launch of a cluster
+// of the same grid that has not started yet, and takes over its work.  The 16-byte answer
+// lands in shared memory and completes 16 bytes on the mbarrier.  One elected lane issues
+// it; with MULTICAST the answer reaches the same offsets in every CTA of the cluster.
+template <bool MULTICAST>
+__device__ __forceinline__ void clc_try_cancel_elect(uint32_t resp, uint32_t bar) {
+  if constexpr (MULTICAST)
+    asm volatile(GB300_ELECT
+                 "@e_ clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+                 ".multicast::cluster::all.b128 [%0], [%1];\n\t}" ::"r"(resp), "r"(bar)
+                 : "memory");
+  else
+    asm volatile(GB300_ELECT
+                 "@e_ clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+                 ".b128 [%0], [%1];\n\t}" ::"r"(resp), "r"(bar)
+                 : "memory");
+}
+
+// Decode an answer: 1 and the cancelled cluster's first blockIdx.x if a launch was
+// cancelled; 0 if none was left to cancel (the grid's work is all taken).
+__device__ __forceinline__ uint32_t clc_query(uint32_t resp, uint32_t& first_ctaid_x) {
+  uint32_t ok, x = 0;
+  asm volatile(
+      "{\n\t.reg .b128 a_;\n\t.reg .pred c_;\n\t"
+      "ld.shared.b128 a_, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 c_, a_;\n\t"
+      "selp.u32 %0, 1, 0, c_;\n\t"
+      "@c_ clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, a_;\n\t}"
+      : "=r"(ok), "+r"(x)
+      : "r"(resp)
+      : "memory");
+  first_ctaid_x = x;
+  return ok;
+}
+
 }  // namespace gb300

@@ -135,6 +135,16 @@ typedef enum {
  *   swap_rows with swap_ab: rows of B per CTA, 1..128 (0 = the fewest that make one
  *             wave of tiles, rounded up to a multiple of 8, at most 128).
  *             gemm_last_config reports the one used (0 when not swapped).
+ *   scheduler how a grouped launch (gemm_run_grouped) hands its tiles to the CTAs:
+ *             1 = round-robin over the resident CTAs (pairs), a persistent grid;
+ *             2 = cluster launch control ("A Blackwell GEMM by Hand in CuTe DSL",
+ *             section 8): a CTA (pair) per tile in the grid, and every running one
+ *             takes over the tiles of launches that have not started yet, so CTAs that
+ *             finish early take more (not with max_ctas: GEMM_ERR_UNSUPPORTED);
+ *             0 = 2 when the problems' K differ by 2x or more (unequal tile costs),
+ *             else 1.  Either way the problems' tiles are handed out longest K first.
+ *             Other calls refuse 2 with GEMM_ERR_UNSUPPORTED.  gemm_last_config
+ *             reports 1 or 2.
  */
 typedef struct {
   int32_t variant;
@@ -150,6 +160,7 @@ typedef struct {
   int32_t l2_hint;
   int32_t swap_ab;
   int32_t swap_rows;
+  int32_t scheduler;
 } gemm_config_t;
 
 /* Create a handle on the current CUDA device.  Fails with GEMM_ERR_UNSUPPORTED

@@ -147,3 +147,72 @@ def test_grouped_rejections(g):
     assert lib().gemm_run_grouped(g._h, bad, 2, F16, F32, None) == 1      # negative M
     assert lib().gemm_run_grouped(g._h, None, 1, F16, F32, None) == 1     # no table
     assert lib().gemm_run_grouped(g._h, None, 0, F16, F32, None) == 0     # nothing to do
+
+
+# Cluster launch control ("A Blackwell GEMM by Hand in CuTe DSL", section 8): a CTA (pair)
+# per tile in the grid; running ones cancel the launches of the rest and take their tiles.
+MANY = [(1000, 2048, 512), (3, 2048, 512), (600, 2048, 512), (0, 2048, 512), (2100, 2048, 512),
+        (130, 2048, 512)]   # 3833 rows: more tiles than resident CTAs, so tiles are stolen
+
+
+@pytest.mark.parametrize("cfg", [{"variant": 1, "block_n": 128}, {"variant": 1, "block_n": 256},
+                                 {"variant": 2, "block_n": 128}, {"variant": 2, "block_n": 256}])
+def test_grouped_cluster_launch_control(g, cfg):
+    cfg = dict(cfg, scheduler=2)
+    used = _run_and_check(g, MOE + RAGGED, F16, F16, seed=620, cfg=cfg)
+    assert used["scheduler"] == 2 and used["variant"] == cfg["variant"], used
+    cg = cfg["variant"]
+    assert used["max_ctas"] == used["dp_tiles"] * cg, used   # a CTA (pair) per tile
+    _run_and_check(g, RAGGED, BF16, F32, seed=621, cfg=cfg, ints=True)
+    used = _run_and_check(g, MANY, BF16, BF16, seed=622, cfg=cfg)
+    assert used["dp_tiles"] > g.sm_count // cg, used
+
+
+def test_grouped_cluster_launch_control_matches_round_robin(g):
+    # integer operands: every schedule gives the same bits; repeated launches too
+    probs = _make(MANY, F16, 623, ints=True)
+    got = {}
+    for sched in (1, 2, 2):
+        dev = [(A.cuda(), B.cuda(), torch.empty(A.shape[0], B.shape[0], dtype=torch.float32,
+                                                device="cuda")) for A, B in probs]
+        g.set_config(scheduler=sched, variant=2)
+        try:
+            g.run_grouped(dev)
+            torch.cuda.synchronize()
+            assert g.device_status()[0] == 0
+            assert g.last_config()["scheduler"] == sched
+        finally:
+            g.reset_config()
+        bits = [parity.bits_of(C) for _, _, C in dev]
+        if sched in got:
+            assert all(np.array_equal(a, b) for a, b in zip(got[sched], bits)), "CLC rerun differs"
+        got[sched] = bits
+    assert all(np.array_equal(a, b) for a, b in zip(got[1], got[2]))
+
+
+def test_grouped_cluster_launch_control_rejections(g):
+    from dense_gemm_blackwell_02_gb300.binding import GemmError
+    A = torch.zeros(64, 64, dtype=torch.float16, device="cuda")
+    C = torch.zeros(64, 64, dtype=torch.float32, device="cuda")
+    for cfg, call in (({"scheduler": 2}, lambda: g.run(A, A, C)),                 # not grouped
+                      ({"scheduler": 2, "max_ctas": 8}, lambda: g.run_grouped([(A, A, C)]))):
+        g.set_config(**cfg)
+        try:
+            with pytest.raises(GemmError) as e:
+                call()
+            assert e.value.code == 2, cfg
+        finally:
+            g.reset_config()
+
+
+def test_grouped_unequal_k_takes_cluster_launch_control(g):
+    # problems whose K differ by 2x or more: tiles of unequal cost, scheduled by cluster
+    # launch control automatically, handed out longest K first (the result does not
+    # depend on the order); equal K: round-robin
+    mixed = [(300, 512, 256), (200, 512, 4096), (64, 300, 1024), (512, 512, 8192), (7, 100, 512)]
+    used = _run_and_check(g, mixed, F16, F32, seed=630)
+    assert used["scheduler"] == 2, used
+    used = _run_and_check(g, mixed, BF16, BF16, seed=631, ints=True)
+    assert used["scheduler"] == 2, used
+    used = _run_and_check(g, [(300, 512, 1024), (200, 512, 1024)], F16, F16, seed=632)
+    assert used["scheduler"] == 1, used

@@ -47,8 +47,8 @@ def test_stalled_wait_times_out_and_the_context_survives(variant, splits):
         torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("case", ["cluster_split_pair", "cluster_split_one", "grouped", "fp8",
-                                  "blockwise"])
+@pytest.mark.parametrize("case", ["cluster_split_pair", "cluster_split_one", "grouped",
+                                  "grouped_clc", "fp8", "blockwise"])
 def test_stalled_wait_times_out_in_every_kernel_family(case):
     # the same stall in the other kernel families: the cluster K split (whose slices also
     # wait on each other), a grouped launch, FP8 and blockwise FP8; each run must return
@@ -63,7 +63,7 @@ def test_stalled_wait_times_out_in_every_kernel_family(case):
     C = torch.zeros(M, N, dtype=torch.float32, device="cuda")
 
     def run(g):
-        if case == "grouped":
+        if case in ("grouped", "grouped_clc"):
             g.run_grouped([(Ad, Bd, C), (Ad[:100], Bd[:300], C[:100, :300].contiguous())])
         elif case == "blockwise":
             g.run_blockwise(Ad, Bd, C, sfa, sfb, 1)
@@ -75,6 +75,8 @@ def test_stalled_wait_times_out_in_every_kernel_family(case):
             g.set_config(variant=2, block_n=256, splits=2, epilogue=3)
         elif case == "cluster_split_one":
             g.set_config(variant=1, block_n=128, splits=2, epilogue=3)
+        elif case == "grouped_clc":
+            g.set_config(variant=2, scheduler=2)   # the answer ring's waits and drain
         g.set_wait_limit(50_000_000)
         g.set_test_stall(True)
         run(g)
@@ -88,7 +90,9 @@ def test_stalled_wait_times_out_in_every_kernel_family(case):
         assert g.device_status()[0] == 0
         if case in ("cluster_split_pair", "cluster_split_one"):
             assert g.last_config()["epilogue"] == 3
-        if case == "grouped":
+        if case == "grouped_clc":
+            assert g.last_config()["scheduler"] == 2
+        if case in ("grouped", "grouped_clc"):
             return
         # unit block scales: the blockwise product is the plain one, up to the order of
         # the fp32 additions, so the plain oracle and tolerance apply
