@@ -401,6 +401,38 @@ def measure_grouped(g, dev, stream, peaks, iters=10):
                      "frac_of_roofline": round(max(t_tensor, t_hbm) / us, 4),
                      "kernel": g.last_config()}
         del probs
+    # a group of unequal tile costs (K from 256 to 16384 across its problems), timed with
+    # the automatic scheduler (cluster launch control for such a group) and with
+    # round-robin over resident CTAs forced, for comparison
+    for name, wl in si.MIXED_K_WORKLOADS.items():
+        Ks = si.mixed_k_values(wl.problems, wl.seed)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(wl.seed)
+        td_in, td_out = si.TORCH_DTYPE[wl.dtype_in], si.TORCH_DTYPE[wl.dtype_out]
+        probs = [((torch.rand(wl.M, k, generator=gen, device=dev) * 2 - 1).to(td_in),
+                  (torch.rand(wl.N, k, generator=gen, device=dev) * 2 - 1).to(td_in),
+                  torch.empty(wl.M, wl.N, dtype=td_out, device=dev)) for k in Ks]
+        flops = sum(2.0 * wl.M * wl.N * k for k in Ks)
+        entry = {"problems": wl.problems, "M": wl.M, "N": wl.N, "K": Ks}
+        for key, sched in (("auto", 0), ("round_robin", 1)):
+            g.set_config(scheduler=sched)
+
+            def run(*_):
+                g.run_grouped(probs, stream=stream)
+
+            for _ in range(3):
+                flush.fill_(0.5)
+                run()
+            torch.cuda.synchronize()
+            total, each = time_steps(run, [()], stream, iters, flush, per_step=True)
+            us = 1e3 * total / iters
+            entry[key] = {"us": round(us, 2), "median_us": round(1e3 * statistics.median(each), 2),
+                          "TFLOP/s": round(flops / us / 1e6, 1),
+                          "frac_of_tensor_peak": round(flops / us / 1e6 / tpeak, 4),
+                          "kernel": g.last_config()}
+            g.reset_config()
+        out[name] = entry
+        del probs
     return out
 
 

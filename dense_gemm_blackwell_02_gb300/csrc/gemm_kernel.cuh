@@ -467,6 +467,43 @@ __device__ __forceinline__ void store_row_direct(const GemmParams& p, int32_t m,
   store_row_to<OUT>(p.C, p.M, p.N, p.vec_store, m, n0, v);
 }
 
+// Direct stores of a warp's 32 rows x 32 columns (rows m_first.., columns n0..; each lane
+// holds its own row's 32 values in v), used when C is not written by TMA (its rows are not
+// 16-byte aligned, or a tile's columns are not a whole number of staging boxes).  The
+// piece goes through the warp's staging box, transposed: each store instruction then
+// writes 32 consecutive elements of one row of C, instead of one element of 32 rows.  The
+// box's 16-byte chunks are XOR-swizzled by row so that neither side conflicts on banks.
+template <int OUT>
+__device__ __forceinline__ void store_piece_rows(void* C, int32_t M, int32_t N, int32_t m_first,
+                                                 int32_t n0, const float* v, uint32_t staging) {
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    st_shared_v4(staging + lane * 128u + (((uint32_t)c ^ (lane & 7u)) << 4), __float_as_uint(v[4 * c]),
+                 __float_as_uint(v[4 * c + 1]), __float_as_uint(v[4 * c + 2]),
+                 __float_as_uint(v[4 * c + 3]));
+  __syncwarp();
+  const int32_t n = n0 + (int32_t)lane;
+  const bool col_ok = n < N;
+#pragma unroll 4
+  for (int r = 0; r < 32; ++r) {
+    const int32_t m = m_first + r;
+    const float x = __uint_as_float(ld_shared_u32(
+        staging + (uint32_t)r * 128u + (((lane >> 2) ^ ((uint32_t)r & 7u)) << 4) + (lane & 3u) * 4u));
+    if (col_ok && m < M) {
+      if constexpr (OUT == kOutF32) {
+        reinterpret_cast<float*>(C)[(size_t)m * N + n] = x;
+      } else if constexpr (OUT == kOutF16) {
+        reinterpret_cast<uint16_t*>(C)[(size_t)m * N + n] = __half_as_ushort(__float2half_rn(x));
+      } else {
+        reinterpret_cast<uint16_t*>(C)[(size_t)m * N + n] =
+            __bfloat16_as_ushort(__float2bfloat16_rn(x));
+      }
+    }
+  }
+  __syncwarp();  // (the box is refilled by the next piece)
+}
+
 // The swapped tiling's store: v[j] = C[m0 + j][n] for j < NV, n this thread's column of C
 // (in_tile: n is one of the CTA's rows of B).  The 32 lanes of a warp hold 32 consecutive
 // columns, so each store instruction writes 32 consecutive elements of one row of C.
@@ -1109,13 +1146,13 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
               }
             }
           } else {
-            const int32_t m = m0 + (int32_t)row;
 #pragma unroll
             for (int pc = 0; pc < kPieces; ++pc) {
               float v[32];
               one_chain_piece<KX2>(taddr + 32u * pc, w, ws_lane, kSliceStride, 32 * pc, v, kx_lane);
-                if constexpr (FUSED) fuse_piece<OUT>(p, m0 + (int32_t)row, n_half + 32 * pc, v);
-              store_row_direct<OUT>(p, m, n_half + 32 * pc, v);
+              if constexpr (FUSED) fuse_piece<OUT>(p, m0 + (int32_t)row, n_half + 32 * pc, v);
+              store_piece_rows<OUT>(p.C, p.M, p.N, m0 + (int32_t)(q * 32u), n_half + 32 * pc, v,
+                                    staging);
             }
           }
         }
@@ -1558,6 +1595,8 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
           }
         }
       } else {
+        // (row stores: the transposed form of the single-chain epilogue raised this
+        // epilogue's register spills)
         const int32_t m = m0 + (int32_t)row;
 #pragma unroll
         for (int pc = 0; pc < kPieces; ++pc) {

@@ -117,6 +117,30 @@ MOE_WORKLOADS = {
 }
 
 
+# A group whose problems differ in K, so that its tiles differ in cost: `problems` GEMMs of
+# M x N with K drawn log-uniformly from {256, 512, ..., 16384} (seeded).
+@dataclass(frozen=True)
+class MixedKWorkload:
+    name: str
+    problems: int
+    M: int
+    N: int
+    dtype_in: int
+    dtype_out: int
+    seed: int
+
+
+MIXED_K_WORKLOADS = {
+    "mixed_k_24x512x2048": MixedKWorkload("mixed_k_24x512x2048", 24, 512, 2048, F16, F16, 23),
+}
+
+
+def mixed_k_values(problems: int, seed: int) -> list:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return [256 << int(e) for e in torch.randint(0, 7, (problems,), generator=g)]
+
+
 def moe_counts(experts: int, rows: int, seed: int) -> list:
     """Rows per expert: expert loads drawn from a flat Dirichlet (normalised iid
     exponentials), then `rows` tokens assigned by a multinomial draw -- an imbalanced
