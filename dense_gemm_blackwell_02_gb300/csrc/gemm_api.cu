@@ -234,11 +234,14 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
     return choose_swap(h, M, N, K, out, kb_elems, c);
   }
   // A CTA pair (256-row tiles, each CTA loading half of B) whenever M fills one.
-  // Blockwise scales hand every K block's accumulator to the epilogue: a CTA pair's
-  // cross-CTA hand-over made that 1.6x slower than one CTA per tile (measured, 4096^3).
+  // Blockwise scales hand every K block's accumulator to the epilogue and back: one CTA
+  // per 128 x 128 tile, whose kernel keeps four accumulator slots (so the MMAs run up to
+  // three K blocks ahead of the scaling) where 256 columns leave room for two (measured,
+  // E4M3 -> bf16, one GB300: 4096^3 106.0 us against 114.8 for 128 x 256 and 102.4 for a
+  // pair's 256 x 128; 8192^3 687.9 against 679.9 and 827.5).
   c->variant = f.variant ? f.variant : (M > kBlockM && !blockwise ? 2 : 1);
   const int cg = c->variant;
-  c->bn = f.block_n ? f.block_n : (N <= 128 ? 128 : 256);
+  c->bn = f.block_n ? f.block_n : (N <= 128 || blockwise ? 128 : 256);
   // A row tile of at most 16 rows holds 16 rows of A per stage and a deeper ring (the
   // plain fp16/bf16 kernels)
   const bool small_a = cg == 1 && M <= 16 && allow_kx;

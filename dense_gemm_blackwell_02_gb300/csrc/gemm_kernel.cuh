@@ -112,6 +112,20 @@ static __device__ __noinline__ bool warp_wait(uint32_t bar, uint32_t parity, con
   }
 }
 
+// Inline fast paths of the two waits: a phase that is already complete costs one test
+// here instead of a call (whose register saves cost about 200 cycles per wait, measured
+// with clock64 in the MMA warp); the bounded loops above run only when it is not.
+__device__ __forceinline__ bool warp_wait_inl(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                              uint32_t site) {
+  if (__any_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
+  return warp_wait(bar, parity, c, site);
+}
+__device__ __forceinline__ bool wait_parity_inl(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                                uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_parity(bar, parity, c, site);
+}
+
 // Bounded pause (used by a pair's follower while aborting, so copies it issued can land).
 __device__ __forceinline__ void pause_ns(uint64_t ns) {
   const uint64_t t0 = globaltimer_ns();
@@ -627,9 +641,9 @@ struct Layout {
       RING_STAGING ? kRingEnd : kCOff + kEpiWarps * kStagingBytes;
   // cluster launch control: a ring of 16-byte answers
   static constexpr uint32_t kClcSlots = 4;
-  // full[S], empty[S], acc_full[2], acc_empty[2], drain, kx_ready[8], kx_go[8],
+  // full[S], empty[S], acc_full[4], acc_empty[4], drain, kx_ready[8], kx_go[8],
   // clc_full[4], clc_empty[4]
-  static constexpr uint32_t kNumBars = 2 * STAGES + 5 + 2 * kEpiWarps + 2 * kClcSlots;
+  static constexpr uint32_t kNumBars = 2 * STAGES + 9 + 2 * kEpiWarps + 2 * kClcSlots;
   static constexpr uint32_t kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
   static constexpr uint32_t kClcOff = (kAbortOff + 4 + 15) & ~15u;
@@ -699,7 +713,13 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
                           !GROUPED && !KX2 && !STAGED),
                 "the swapped tiling is a plain CTA-pair kernel with the general epilogue");
   static_assert(!CLC || (GROUPED && !SWAP), "cluster launch control serves grouped launches");
-  constexpr uint32_t kTmemCols = BN == 320 ? 512 : 2 * BN;  // two accumulator slots (one for 320)
+  // Accumulator slots in Tensor Memory: two, so that a unit's epilogue overlaps the next
+  // chain's MMAs; four for blockwise scales with 128-column tiles, whose chains are one K
+  // block each (the MMA then runs up to three K blocks ahead of the epilogue that scales
+  // them; Tensor Memory holds 512 columns).  One for 320 columns.
+  constexpr uint32_t kSlots = (KIND == 2 && BN == 128) ? 4u : 2u;
+  constexpr uint32_t kSlotShift = kSlots == 4u ? 2u : 1u;
+  constexpr uint32_t kTmemCols = BN == 320 ? 512 : kSlots * BN;
   constexpr int kHalf = BN / 2;                // columns per epilogue warp
   constexpr int kPieces = kHalf / 32;          // tcgen05.ld x32 pieces per warp
   constexpr int kOutBytes = OUT == kOutF32 ? 4 : 2;
@@ -724,13 +744,13 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
   auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
   auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (STAGES + s); };
   auto acc_full_bar = [&](uint32_t i) { return bar0 + 8u * (2 * STAGES + i); };
-  auto acc_empty_bar = [&](uint32_t i) { return bar0 + 8u * (2 * STAGES + 2 + i); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  auto kx_ready_bar = [&](uint32_t w) { return bar0 + 8u * (2 * STAGES + 5 + w); };
-  auto kx_go_bar = [&](uint32_t w) { return bar0 + 8u * (2 * STAGES + 5 + L::kEpiWarps + w); };
-  auto clc_full_bar = [&](uint32_t s) { return bar0 + 8u * (2 * STAGES + 5 + 2 * L::kEpiWarps + s); };
+  auto acc_empty_bar = [&](uint32_t i) { return bar0 + 8u * (2 * STAGES + 4 + i); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 8);
+  auto kx_ready_bar = [&](uint32_t w) { return bar0 + 8u * (2 * STAGES + 9 + w); };
+  auto kx_go_bar = [&](uint32_t w) { return bar0 + 8u * (2 * STAGES + 9 + L::kEpiWarps + w); };
+  auto clc_full_bar = [&](uint32_t s) { return bar0 + 8u * (2 * STAGES + 9 + 2 * L::kEpiWarps + s); };
   auto clc_empty_bar = [&](uint32_t s) {
-    return bar0 + 8u * (2 * STAGES + 5 + 2 * L::kEpiWarps + L::kClcSlots + s);
+    return bar0 + 8u * (2 * STAGES + 9 + 2 * L::kEpiWarps + L::kClcSlots + s);
   };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlotOff);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kAbortOff);
@@ -760,7 +780,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
       mbar_init(full_bar(s), 1);   // the leader's producer arms it; copies complete it
       mbar_init(empty_bar(s), 1);  // one commit per use
     }
-    for (uint32_t i = 0; i < 2; ++i) {
+    for (uint32_t i = 0; i < kSlots; ++i) {
       mbar_init(acc_full_bar(i), 1);
       mbar_init(acc_empty_bar(i), L::kEpiWarps * CTA_GROUP);  // every epilogue warp of the pair
     }
@@ -855,7 +875,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
         for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
           if (p.prefetch_kb > 0 && kb + p.prefetch_kb < w.kb1)
             tma_prefetch_l2_2d_elect(mapB, (kb + p.prefetch_kb) * kKbElems, b_row);
-          if (!warp_wait(empty_bar(stage), phase ^ 1u, ctl, kSiteEmpty)) {
+          if (!warp_wait_inl(empty_bar(stage), phase ^ 1u, ctl, kSiteEmpty)) {
             ok = false;
             break;
           }
@@ -951,15 +971,15 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
         const uint32_t idesc = w.half >= 0 ? p.idesc_half : p.idesc;
         for (int32_t c0 = w.kb0; c0 < w.kb1 && ok; c0 += p.chain_kb) {
           const int32_t c1 = min(c0 + p.chain_kb, w.kb1);
-          const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
-          if (!warp_wait(acc_empty_bar(slot), acc_phase ^ 1u, ctl, kSiteAccEmpty)) {
+          const uint32_t slot = iter & (kSlots - 1u), acc_phase = (iter >> kSlotShift) & 1u;
+          if (!warp_wait_inl(acc_empty_bar(slot), acc_phase ^ 1u, ctl, kSiteAccEmpty)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + slot * BN;
           for (int32_t kb = c0; kb < c1; ++kb) {
-            if (!warp_wait(full_bar(stage), phase, ctl, kSiteFull)) {
+            if (!warp_wait_inl(full_bar(stage), phase, ctl, kSiteFull)) {
               ok = false;
               break;
             }
@@ -1014,10 +1034,10 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
         // so do warps whose 32 rows all lie at or past M (no partial, no store)
         const int32_t m0 = w.m_blk * kRowsTile + (int32_t)rank * rows_cta;
         const bool active = (w.half < 0 || h == 0) && m0 + (int32_t)(q * 32u) < p.M;
-        const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
+        const uint32_t slot = iter & (kSlots - 1u), acc_phase = (iter >> kSlotShift) & 1u;
         uint32_t good = 1;
         if (lane == 0)
-          good = wait_parity(acc_full_bar(slot), acc_phase, ctl, kSiteAccFull) ? 1u : 0u;
+          good = wait_parity_inl(acc_full_bar(slot), acc_phase, ctl, kSiteAccFull) ? 1u : 0u;
         good = __shfl_sync(0xFFFFFFFFu, good, 0);
         if (!good) {
           ok = false;
@@ -1161,7 +1181,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
         __syncwarp();
         if (lane == 0) {
           if constexpr (CTA_GROUP == 1) mbar_arrive(acc_empty_bar(slot));
-          else mbar_arrive_cluster(mapa_shared(acc_empty_bar(slot), group_base));
+          else mbar_arrive_cluster_relaxed(mapa_shared(acc_empty_bar(slot), group_base));
         }
         ++iter;
       }
@@ -1175,75 +1195,127 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
       if constexpr (STAGED) final_unit = w.nsplit > 1 && !walker_has_next(walk, first_unit, p);
       float acc[kHalf];
       const int32_t nchains = chains_of(w, p.chain_kb);
-      // Blockwise FP8 scales (KIND 2; "CUTLASS Deep Dive: From CuTe Layouts to Blackwell
-      // tcgen05", Part 6, FP8 and Blockwise Scaling): every chain is one 128-element K
-      // block kb; its TMEM value is scaled by sfa(row block, kb) * sfb(column block, kb)
-      // before it is added.  This thread's row and this warp's columns (one 128-column
-      // block: a warp's columns never cross one) fix the two scale columns; the scales
-      // are stored K-block-major, so a warp's 32 rows read one line per K block.  The
-      // scales of chains ch + 1 and ch + 2 are in flight while chain ch is consumed.
-      const float* sfa_col = nullptr;
-      const float* sfb_col = nullptr;
-      float s0a = 0.0f, s0b = 0.0f, s1a = 0.0f, s1b = 0.0f;  // next two chains, by parity
       if constexpr (KIND == 2) {
-        const int32_t m = min(w.m_blk * kRowsTile + (int32_t)(rank * kBlockM + q * 32u + lane),
-                              p.M - 1);
-        const int32_t n = min(w.n_blk * BN + (w.half >= 0 ? w.half : (int32_t)h) * kHalf, p.N - 1);
-        sfa_col = p.sfa + m / p.sf_bm;
-        sfb_col = p.sfb + (n >> 7);
-        if (active) {
-          s0a = sfa_col[(size_t)w.kb0 * p.sf_lda];
-          s0b = sfb_col[(size_t)w.kb0 * p.sf_ldb];
-          if (nchains > 1) {
-            s1a = sfa_col[(size_t)(w.kb0 + 1) * p.sf_lda];
-            s1b = sfb_col[(size_t)(w.kb0 + 1) * p.sf_ldb];
-          }
-        }
-      }
-      for (int32_t ch = 0; ch < nchains; ++ch) {
-        const uint32_t slot = iter & 1u, acc_phase = (iter >> 1) & 1u;
+      // One accumulation chain: wait for it, read it out of Tensor Memory into the fp32
+      // registers scaled by sc, hand the slot back.  False when the wait gave up.
+      auto consume_chain = [&](int32_t ch, float sc) -> bool {
+        const uint32_t slot = iter & (kSlots - 1u), acc_phase = (iter >> kSlotShift) & 1u;
         // One lane polls; the warp follows its verdict, so tcgen05.ld below is always
         // executed by the whole, converged warp.
         uint32_t good = 1;
         if (lane == 0)
-          good = wait_parity(acc_full_bar(slot), acc_phase, ctl, kSiteAccFull) ? 1u : 0u;
+          good = wait_parity_inl(acc_full_bar(slot), acc_phase, ctl, kSiteAccFull) ? 1u : 0u;
         good = __shfl_sync(0xFFFFFFFFu, good, 0);
-        if (!good) {
-          ok = false;
-          break;
-        }
+        if (!good) return false;
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * BN + h * kHalf;
         if (active) {
-          if constexpr (KIND == 2) {
-            const bool odd = (ch & 1) != 0;
-            const float sc = odd ? s1a * s1b : s0a * s0b;
-            if (ch + 2 < nchains) {
-              const size_t kb = (size_t)(w.kb0 + ch + 2);
-              const float na = sfa_col[kb * p.sf_lda], nb = sfb_col[kb * p.sf_ldb];
-              if (odd) {
-                s1a = na;
-                s1b = nb;
-              } else {
-                s0a = na;
-                s0b = nb;
-              }
+          if constexpr (KIND == 2 && kPieces == 2) {
+            // both pieces in flight behind one wait (64 columns: the registers allow it)
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(taddr, r0);
+            tmem_ld_32x32b_x32(taddr + 32u, r1);
+            tmem_ld_wait(r0);
+            tie_regs(r1);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              acc[j] = ch == 0 ? __uint_as_float(r0[j]) * sc : fmaf(__uint_as_float(r0[j]), sc, acc[j]);
+              acc[32 + j] =
+                  ch == 0 ? __uint_as_float(r1[j]) * sc : fmaf(__uint_as_float(r1[j]), sc, acc[32 + j]);
             }
+          } else {
 #pragma unroll
             for (int pc = 0; pc < kPieces; ++pc) {
               uint32_t r[32];
               tmem_ld_32x32b_x32(taddr + 32u * pc, r);
               tmem_ld_wait(r);
-              if (ch == 0) {
+              if constexpr (KIND == 2) {
+                if (ch == 0) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) acc[32 * pc + j] = __uint_as_float(r[j]) * sc;
+                  for (int j = 0; j < 32; ++j) acc[32 * pc + j] = __uint_as_float(r[j]) * sc;
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j)
+                    acc[32 * pc + j] = fmaf(__uint_as_float(r[j]), sc, acc[32 * pc + j]);
+                }
               } else {
+                if (ch == 0) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  acc[32 * pc + j] = fmaf(__uint_as_float(r[j]), sc, acc[32 * pc + j]);
+                  for (int j = 0; j < 32; ++j) acc[32 * pc + j] = __uint_as_float(r[j]);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) acc[32 * pc + j] += __uint_as_float(r[j]);
+                }
               }
             }
-          } else {
+          }
+        }
+        // The slot is free for the next chain as soon as the loads are done.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          // the leader's acc_empty, in shared::cluster space (its own, for rank 0)
+          if constexpr (CTA_GROUP == 1) mbar_arrive(acc_empty_bar(slot));
+          else mbar_arrive_cluster_relaxed(mapa_shared(acc_empty_bar(slot), group_base));
+        }
+        ++iter;
+        return true;
+      };
+        // Blockwise FP8 scales ("CUTLASS Deep Dive: From CuTe Layouts to Blackwell
+        // tcgen05", Part 6, FP8 and Blockwise Scaling): every chain is one 128-element K
+        // block kb; its TMEM value is scaled by sfa(row block, kb) * sfb(column block, kb)
+        // before it is added.  This thread's row and this warp's columns (one 128-column
+        // block: a warp's columns never cross one) fix the two scale columns; the scales
+        // are stored K-block-major, so a warp's 32 rows read one line per K block.  The
+        // chains go four at a time with the scales of the next four in flight, each in a
+        // register of its own: a scale is loaded into the register its chain of four
+        // earlier has just used, and first read four chains later (loading into one of
+        // two registers chosen at run time made every chain wait for its load).
+        const int32_t m = min(w.m_blk * kRowsTile + (int32_t)(rank * kBlockM + q * 32u + lane),
+                              p.M - 1);
+        const int32_t n = min(w.n_blk * BN + (w.half >= 0 ? w.half : (int32_t)h) * kHalf, p.N - 1);
+        const float* sfa_col = p.sfa + m / p.sf_bm;
+        const float* sfb_col = p.sfb + (n >> 7);
+        float sa[4], sb[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          sa[j] = 0.0f;
+          sb[j] = 0.0f;
+          if (active && j < nchains) {
+            sa[j] = sfa_col[(size_t)(w.kb0 + j) * p.sf_lda];
+            sb[j] = sfb_col[(size_t)(w.kb0 + j) * p.sf_ldb];
+          }
+        }
+        for (int32_t c0 = 0; c0 < nchains && ok; c0 += 4) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int32_t ch = c0 + j;
+            if (ch < nchains && ok) {
+              const float sc = sa[j] * sb[j];
+              if (!consume_chain(ch, sc)) ok = false;
+              if (active && ch + 4 < nchains) {
+                sa[j] = sfa_col[(size_t)(w.kb0 + ch + 4) * p.sf_lda];
+                sb[j] = sfb_col[(size_t)(w.kb0 + ch + 4) * p.sf_ldb];
+              }
+            }
+          }
+        }
+      } else {
+        for (int32_t ch = 0; ch < nchains; ++ch) {
+          const uint32_t slot = iter & (kSlots - 1u), acc_phase = (iter >> kSlotShift) & 1u;
+          // One lane polls; the warp follows its verdict, so tcgen05.ld below is always
+          // executed by the whole, converged warp.
+          uint32_t good = 1;
+          if (lane == 0)
+            good = wait_parity_inl(acc_full_bar(slot), acc_phase, ctl, kSiteAccFull) ? 1u : 0u;
+          good = __shfl_sync(0xFFFFFFFFu, good, 0);
+          if (!good) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * BN + h * kHalf;
+          if (active) {
 #pragma unroll
             for (int pc = 0; pc < kPieces; ++pc) {
               uint32_t r[32];
@@ -1258,16 +1330,16 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
               }
             }
           }
+          // The slot is free for the next chain as soon as the loads are done.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            // the leader's acc_empty, in shared::cluster space (its own, for rank 0)
+            if constexpr (CTA_GROUP == 1) mbar_arrive(acc_empty_bar(slot));
+            else mbar_arrive_cluster_relaxed(mapa_shared(acc_empty_bar(slot), group_base));
+          }
+          ++iter;
         }
-        // The slot is free for the next chain as soon as the loads are done.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          // the leader's acc_empty, in shared::cluster space (its own, for rank 0)
-          if constexpr (CTA_GROUP == 1) mbar_arrive(acc_empty_bar(slot));
-          else mbar_arrive_cluster(mapa_shared(acc_empty_bar(slot), group_base));
-        }
-        ++iter;
       }
       if (!ok) break;
       if (!active) continue;

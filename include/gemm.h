@@ -240,8 +240,8 @@ gemm_status_t gemm_run_epilogue(gemm_handle_t h, const void* A, const void* B, v
  *             128 x 128 tile)
  *   block_n   rows of B per scale: 128
  * Each 128-element K block is accumulated in its own Tensor-Memory chain, then scaled
- * and added in fp32 registers (fma(P_kb, sfa * sfb, acc)).  Automatically the
- * one-CTA kernel (variant 1) is used.
+ * and added in fp32 registers (fma(P_kb, sfa * sfb, acc)).  Automatically one CTA per
+ * 128 x 128 tile (variant 1, block_n 128), whose kernel keeps four accumulator slots.
  */
 typedef struct {
   const float* sfa;

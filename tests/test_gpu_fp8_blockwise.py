@@ -103,7 +103,8 @@ def _case(g, M, N, K, dt, dtype_out, bm, seed, cfg=None, ints=False):
 def test_blockwise_against_oracle(g, dt, dtype_out, bm):
     used = _case(g, 300, 700, 1040, dt, dtype_out, bm, seed=400)   # ragged M, N, K tails
     assert used["chain_kblocks"] == 1 and used["epilogue"] == 1, used
-    assert used["variant"] == 1, used                              # one CTA per tile
+    # one CTA per 128 x 128 tile (four accumulator slots)
+    assert used["variant"] == 1 and used["block_n"] == 128, used
 
 
 @pytest.mark.parametrize("cfg,M,N,K", [
