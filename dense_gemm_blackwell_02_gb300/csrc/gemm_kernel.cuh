@@ -1630,7 +1630,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
       const bool out_tma = GROUPED ? gd->tma_store != 0 : p.tma_store != 0;
       const int32_t out_m = GROUPED ? gd->M : p.M, out_n = GROUPED ? gd->N : p.N;
       const CUtensorMap* out_map = GROUPED ? &gd->tmC : &tmC;
-      if (out_tma) {
+      if (kTmaStoreOk && out_tma) {
         // Each 128-byte row of a staging box is written in the 128-byte swizzled order
         // (16-byte chunk j of row r at chunk j ^ (r % 8)) that the C tensor map's
         // CU_TENSOR_MAP_SWIZZLE_128B expects ("A Blackwell GEMM by Hand in CuTe DSL",
