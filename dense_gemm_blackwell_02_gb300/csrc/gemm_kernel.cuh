@@ -1003,8 +1003,11 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
             }
           }
           if (!ok) break;
-          if constexpr (CTA_GROUP == 1) umma_commit_elect<1>(acc_full_bar(slot));
-          else umma_commit_pair_elect(acc_full_bar(slot), pair_mask);
+          // (blockwise: a chain is one stage, whose own commit tells the epilogue too)
+          if constexpr (KIND != 2) {
+            if constexpr (CTA_GROUP == 1) umma_commit_elect<1>(acc_full_bar(slot));
+            else umma_commit_pair_elect(acc_full_bar(slot), pair_mask);
+          }
           ++iter;
         }
       }
@@ -1199,12 +1202,19 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
       // One accumulation chain: wait for it, read it out of Tensor Memory into the fp32
       // registers scaled by sc, hand the slot back.  False when the wait gave up.
       auto consume_chain = [&](int32_t ch, float sc) -> bool {
-        const uint32_t slot = iter & (kSlots - 1u), acc_phase = (iter >> kSlotShift) & 1u;
+        const uint32_t slot = iter & (kSlots - 1u);
+        // A chain is one K block, i.e. one operand stage (the iter-th of this CTA), and the
+        // MMA issuer's commit that frees that stage also tells that its accumulator is
+        // complete: wait on the stage's empty barrier (use iter / STAGES of it).  Its next
+        // phase cannot complete before this one is seen: the MMAs of stage use
+        // iter + STAGES need the slot of chain iter + STAGES - kSlots >= iter released.
+        static_assert(STAGES >= (int)kSlots, "a stage must not come round before its slot");
+        const uint32_t st_idx = iter % (uint32_t)STAGES, st_phase = (iter / (uint32_t)STAGES) & 1u;
         // One lane polls; the warp follows its verdict, so tcgen05.ld below is always
         // executed by the whole, converged warp.
         uint32_t good = 1;
         if (lane == 0)
-          good = wait_parity_inl(acc_full_bar(slot), acc_phase, ctl, kSiteAccFull) ? 1u : 0u;
+          good = wait_parity_inl(empty_bar(st_idx), st_phase, ctl, kSiteAccFull) ? 1u : 0u;
         good = __shfl_sync(0xFFFFFFFFu, good, 0);
         if (!good) return false;
         tc_fence_after();
