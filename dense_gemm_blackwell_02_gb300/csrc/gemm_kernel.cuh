@@ -1067,8 +1067,11 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
           const uint32_t wbuf = base + L::kAOff + ew * kKxWarpBytes;
           if (active && w.nsplit > 1 && h == slice_k) {
             if (lane == 0) {
-              mbar_arrive_expect_tx_cluster(kx_ready_bar(ew), kKxWarpBytes);
-              mbar_arrive_cluster(mapa_shared(kx_go_bar(ew), kx_peer));
+              // (its own barrier: a local arm; the go carries no data of this warp's, only
+              // that its ring is idle -- its MMAs are complete -- so a relaxed arrive: the
+              // cluster-scope release forms cost about a microsecond each, measured)
+              mbar_arrive_expect_tx(kx_ready_bar(ew), kKxWarpBytes);
+              mbar_arrive_cluster_relaxed(mapa_shared(kx_go_bar(ew), kx_peer));
             }
             if (!warp_wait(kx_ready_bar(ew), 0, ctl, kSiteKx)) {
               ok = false;
@@ -1371,8 +1374,11 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
           const uint32_t wlane = base + L::kAOff + ew * kKxWarpBytes + lane * 16u;
           if (h == slice_k) {
             if (lane == 0) {
-              mbar_arrive_expect_tx_cluster(kx_ready_bar(ew), kKxWarpBytes);
-              mbar_arrive_cluster(mapa_shared(kx_go_bar(ew), kx_peer));
+              // (its own barrier: a local arm; the go carries no data of this warp's, only
+              // that its ring is idle -- its MMAs are complete -- so a relaxed arrive: the
+              // cluster-scope release forms cost about a microsecond each, measured)
+              mbar_arrive_expect_tx(kx_ready_bar(ew), kKxWarpBytes);
+              mbar_arrive_cluster_relaxed(mapa_shared(kx_go_bar(ew), kx_peer));
             }
             if (!warp_wait(kx_ready_bar(ew), 0, ctl, kSiteKx)) {
               ok = false;
