@@ -3,12 +3,14 @@ driver for profilers and sweeps.
 
     python -m dense_gemm_blackwell_02_gb300.run M N K [--in f16|bf16|e4m3|e5m2]
                                                 [--out f16|bf16|f32] [--reps R]
-                                                [--config JSON]
+                                                [--config JSON] [--blockwise BM]
     python -m dense_gemm_blackwell_02_gb300.run --moe NAME [--experts E] [--reps R]
 
 Operands are drawn on the device (uniform [-1, 1], fixed seed), then `gemm_run` (or,
 with --moe, `gemm_run_grouped` over the workload's experts, the first E of them with
---experts) is called R times on one stream.  Prints the kernel configuration the
+--experts; with --blockwise BM and FP8 inputs, `gemm_run_blockwise` with scales in
+[2^-3, 2^3] per BM rows of A and 128 of K, and per 128 x 128 of B) is called R times on
+one stream.  Prints the kernel configuration the
 library chose and the device status word; exits non-zero if a launch or the status
 reports an error.
 """
@@ -49,6 +51,8 @@ def main(argv=None) -> int:
     ap.add_argument("--config", default=None, help="JSON gemm_config_t fields")
     ap.add_argument("--moe", default=None, help="a grouped MoE workload of seeded_inputs")
     ap.add_argument("--experts", type=int, default=0, help="with --moe: only the first E experts")
+    ap.add_argument("--blockwise", type=int, default=0,
+                    help="FP8 inputs: block scales, one per BM rows of A and 128 of K")
     a = ap.parse_args(argv)
     if a.moe is None and None in (a.M, a.N, a.K):
         ap.error("M N K are required without --moe")
@@ -67,9 +71,17 @@ def main(argv=None) -> int:
             A = (torch.rand(a.M, a.K, generator=gen, device=dev) * 2 - 1).to(DTYPES[a.din])
             B = (torch.rand(a.N, a.K, generator=gen, device=dev) * 2 - 1).to(DTYPES[a.din])
             C = torch.empty(a.M, a.N, dtype=DTYPES[a.dout], device=dev)
+            if a.blockwise:
+                nkb = -(-a.K // 128)
+                sfa = torch.exp2(torch.rand(nkb, -(-a.M // a.blockwise), generator=gen, device=dev) * 6 - 3)
+                sfb = torch.exp2(torch.rand(nkb, -(-a.N // 128), generator=gen, device=dev) * 6 - 3)
             for _ in range(a.reps):
-                g.run(A, B, C)
-            shape = {"M": a.M, "N": a.N, "K": a.K, "in": a.din, "out": a.dout}
+                if a.blockwise:
+                    g.run_blockwise(A, B, C, sfa, sfb, a.blockwise)
+                else:
+                    g.run(A, B, C)
+            shape = {"M": a.M, "N": a.N, "K": a.K, "in": a.din, "out": a.dout,
+                     "blockwise": a.blockwise}
         torch.cuda.synchronize()
         code, word = g.device_status()
         print(json.dumps({**shape, "kernel": g.last_config(), "status": code, "status_word": word}))
