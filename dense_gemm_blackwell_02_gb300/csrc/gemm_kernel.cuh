@@ -969,46 +969,70 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
       Unit w;
       while (ok && walker_next<GROUPED, CLC, CTA_GROUP>(walk, first_unit, unit_stride, p, w, &clc, &ctl)) {
         const uint32_t idesc = w.half >= 0 ? p.idesc_half : p.idesc;
-        for (int32_t c0 = w.kb0; c0 < w.kb1 && ok; c0 += p.chain_kb) {
-          const int32_t c1 = min(c0 + p.chain_kb, w.kb1);
-          const uint32_t slot = iter & (kSlots - 1u), acc_phase = (iter >> kSlotShift) & 1u;
-          if (!warp_wait_inl(acc_empty_bar(slot), acc_phase ^ 1u, ctl, kSiteAccEmpty)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + slot * BN;
-          for (int32_t kb = c0; kb < c1; ++kb) {
-            if (!warp_wait_inl(full_bar(stage), phase, ctl, kSiteFull)) {
+        if constexpr (KIND == 2) {
+          // Blockwise scales: every K block is a chain of its own, on one operand stage and
+          // one accumulator slot, whose stage commit also tells the epilogue.  A flat loop
+          // with its bound in a register: re-reading the unit's fields (which the asm
+          // statements' memory clobbers force) cost ~140 of the ~830 cycles the loop took
+          // per K block (clock64 trace, 8192^3).
+          const int32_t kb_end = w.kb1;
+          for (int32_t kb = w.kb0; kb < kb_end; ++kb) {
+            const uint32_t slot = iter & (kSlots - 1u), acc_phase = (iter >> kSlotShift) & 1u;
+            if (!warp_wait_inl(acc_empty_bar(slot), acc_phase ^ 1u, ctl, kSiteAccEmpty) ||
+                !warp_wait_inl(full_bar(stage), phase, ctl, kSiteFull)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t da = desc_a0 + ((stage * L::kABytes) >> 4);
-            const uint64_t db = desc_b0 + ((stage * L::kBBytes) >> 4);
-            // four MMAs of 32 bytes of K, then the commit that frees the stage (in both
-            // CTAs) once they are done
-            static_assert(kBlockK * 2 == 128, "umma_stage_elect covers 128 bytes of K");
-            if constexpr (BN == 320) {
-              // columns 0-255 from each CTA's first 128 B rows, 256-319 from the next 32
-              umma_stage320_elect(d_tmem, da, db, p.idesc, p.idesc_half, kb > c0 ? 1u : 0u,
-                                  empty_bar(stage), stage_mask);
-            } else {
-              umma_stage_elect<CTA_GROUP, KIND>(d_tmem, da, db, idesc, kb > c0 ? 1u : 0u,
-                                                empty_bar(stage), stage_mask);
-            }
+            umma_stage_elect<CTA_GROUP, KIND>(tmem_base + slot * BN,
+                                              desc_a0 + ((stage * L::kABytes) >> 4),
+                                              desc_b0 + ((stage * L::kBBytes) >> 4), idesc, 0u,
+                                              empty_bar(stage), stage_mask);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
             }
+            ++iter;
           }
-          if (!ok) break;
-          // (blockwise: a chain is one stage, whose own commit tells the epilogue too)
-          if constexpr (KIND != 2) {
+        } else {
+          for (int32_t c0 = w.kb0; c0 < w.kb1 && ok; c0 += p.chain_kb) {
+            const int32_t c1 = min(c0 + p.chain_kb, w.kb1);
+            const uint32_t slot = iter & (kSlots - 1u), acc_phase = (iter >> kSlotShift) & 1u;
+            if (!warp_wait_inl(acc_empty_bar(slot), acc_phase ^ 1u, ctl, kSiteAccEmpty)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + slot * BN;
+            for (int32_t kb = c0; kb < c1; ++kb) {
+              if (!warp_wait_inl(full_bar(stage), phase, ctl, kSiteFull)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t da = desc_a0 + ((stage * L::kABytes) >> 4);
+              const uint64_t db = desc_b0 + ((stage * L::kBBytes) >> 4);
+              // four MMAs of 32 bytes of K, then the commit that frees the stage (in both
+              // CTAs) once they are done
+              static_assert(kBlockK * 2 == 128, "umma_stage_elect covers 128 bytes of K");
+              if constexpr (BN == 320) {
+                // columns 0-255 from each CTA's first 128 B rows, 256-319 from the next 32
+                umma_stage320_elect(d_tmem, da, db, p.idesc, p.idesc_half, kb > c0 ? 1u : 0u,
+                                    empty_bar(stage), stage_mask);
+              } else {
+                umma_stage_elect<CTA_GROUP, KIND>(d_tmem, da, db, idesc, kb > c0 ? 1u : 0u,
+                                                  empty_bar(stage), stage_mask);
+              }
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+            if (!ok) break;
             if constexpr (CTA_GROUP == 1) umma_commit_elect<1>(acc_full_bar(slot));
             else umma_commit_pair_elect(acc_full_bar(slot), pair_mask);
+            ++iter;
           }
-          ++iter;
         }
       }
       // Every issued MMA must finish before TMEM is released.
@@ -1213,17 +1237,15 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
         // iter + STAGES need the slot of chain iter + STAGES - kSlots >= iter released.
         static_assert(STAGES >= (int)kSlots, "a stage must not come round before its slot");
         const uint32_t st_idx = iter % (uint32_t)STAGES, st_phase = (iter / (uint32_t)STAGES) & 1u;
-        // One lane polls; the warp follows its verdict, so tcgen05.ld below is always
-        // executed by the whole, converged warp.
-        uint32_t good = 1;
-        if (lane == 0)
-          good = wait_parity_inl(empty_bar(st_idx), st_phase, ctl, kSiteAccFull) ? 1u : 0u;
-        good = __shfl_sync(0xFFFFFFFFu, good, 0);
-        if (!good) return false;
+        // Every lane polls and the warp leaves on one verdict (no broadcast of one lane's),
+        // so tcgen05.ld below is executed by the whole, converged warp.
+        if (!warp_wait_inl(empty_bar(st_idx), st_phase, ctl, kSiteAccFull)) return false;
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * BN + h * kHalf;
+        // (the sums start at +0: fma(x, sc, +0) is x * sc rounded once, as the first
+        // product was before, and needs no select per chain)
         if (active) {
-          if constexpr (KIND == 2 && kPieces == 2) {
+          if constexpr (kPieces == 2) {
             // both pieces in flight behind one wait (64 columns: the registers allow it)
             uint32_t r0[32], r1[32];
             tmem_ld_32x32b_x32(taddr, r0);
@@ -1232,9 +1254,8 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
             tie_regs(r1);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              acc[j] = ch == 0 ? __uint_as_float(r0[j]) * sc : fmaf(__uint_as_float(r0[j]), sc, acc[j]);
-              acc[32 + j] =
-                  ch == 0 ? __uint_as_float(r1[j]) * sc : fmaf(__uint_as_float(r1[j]), sc, acc[32 + j]);
+              acc[j] = fmaf(__uint_as_float(r0[j]), sc, acc[j]);
+              acc[32 + j] = fmaf(__uint_as_float(r1[j]), sc, acc[32 + j]);
             }
           } else {
 #pragma unroll
@@ -1242,24 +1263,9 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
               uint32_t r[32];
               tmem_ld_32x32b_x32(taddr + 32u * pc, r);
               tmem_ld_wait(r);
-              if constexpr (KIND == 2) {
-                if (ch == 0) {
 #pragma unroll
-                  for (int j = 0; j < 32; ++j) acc[32 * pc + j] = __uint_as_float(r[j]) * sc;
-                } else {
-#pragma unroll
-                  for (int j = 0; j < 32; ++j)
-                    acc[32 * pc + j] = fmaf(__uint_as_float(r[j]), sc, acc[32 * pc + j]);
-                }
-              } else {
-                if (ch == 0) {
-#pragma unroll
-                  for (int j = 0; j < 32; ++j) acc[32 * pc + j] = __uint_as_float(r[j]);
-                } else {
-#pragma unroll
-                  for (int j = 0; j < 32; ++j) acc[32 * pc + j] += __uint_as_float(r[j]);
-                }
-              }
+              for (int j = 0; j < 32; ++j)
+                acc[32 * pc + j] = fmaf(__uint_as_float(r[j]), sc, acc[32 * pc + j]);
             }
           }
         }
@@ -1287,28 +1293,40 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
         const int32_t m = min(w.m_blk * kRowsTile + (int32_t)(rank * kBlockM + q * 32u + lane),
                               p.M - 1);
         const int32_t n = min(w.n_blk * BN + (w.half >= 0 ? w.half : (int32_t)h) * kHalf, p.N - 1);
-        const float* sfa_col = p.sfa + m / p.sf_bm;
-        const float* sfb_col = p.sfb + (n >> 7);
-        float sa[4], sb[4];
+        // (the scale pointers advance by one K block per chain, in registers: indexing
+        // from the unit's fields re-read them after every asm statement, ~120 cycles per
+        // chain in the epilogue warps, measured).  B's scale is the same for the whole
+        // warp, so lane i holds chain c + i's for 32 chains at once and hands it out with
+        // a shuffle, the next 32 in flight: a warp then has five scale loads in flight,
+        // not eight.
+        const size_t lda = (size_t)p.sf_lda, ldb = (size_t)p.sf_ldb;
+        const float* pa = p.sfa + m / p.sf_bm + (size_t)w.kb0 * lda;
+        const float* pb = p.sfb + (n >> 7) + (size_t)w.kb0 * ldb;
+        float sa[4], sbv = 0.0f, sbv_next = 0.0f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           sa[j] = 0.0f;
-          sb[j] = 0.0f;
-          if (active && j < nchains) {
-            sa[j] = sfa_col[(size_t)(w.kb0 + j) * p.sf_lda];
-            sb[j] = sfb_col[(size_t)(w.kb0 + j) * p.sf_ldb];
-          }
+          if (active && j < nchains) sa[j] = pa[j * lda];
         }
+        pa += 4 * lda;  // chain 4's (read only while chains remain)
+        if (active && (int32_t)lane < nchains) sbv = pb[lane * ldb];
+        if (active && 32 + (int32_t)lane < nchains) sbv_next = pb[(32 + lane) * ldb];
+#pragma unroll
+        for (int j = 0; j < kHalf; ++j) acc[j] = 0.0f;
         for (int32_t c0 = 0; c0 < nchains && ok; c0 += 4) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int32_t ch = c0 + j;
             if (ch < nchains && ok) {
-              const float sc = sa[j] * sb[j];
+              const float sc = sa[j] * __shfl_sync(0xFFFFFFFFu, sbv, ch & 31);
               if (!consume_chain(ch, sc)) ok = false;
-              if (active && ch + 4 < nchains) {
-                sa[j] = sfa_col[(size_t)(w.kb0 + ch + 4) * p.sf_lda];
-                sb[j] = sfb_col[(size_t)(w.kb0 + ch + 4) * p.sf_ldb];
+              if (active && ch + 4 < nchains) sa[j] = *pa;
+              pa += lda;
+              if ((ch & 31) == 31) {
+                // chains ch + 1.. are in sbv_next; fetch ch + 33..
+                const int32_t nc = ch + 33 + (int32_t)lane;
+                sbv = sbv_next;
+                sbv_next = active && nc < nchains ? pb[(size_t)nc * ldb] : 0.0f;
               }
             }
           }
