@@ -1,6 +1,6 @@
 // Inline-PTX wrappers for the sm_103a GEMM: mbarriers, TMA (cp.async.bulk.tensor),
 // Tensor Memory (tcgen05.alloc/ld/dealloc), the tcgen05 MMA and its commit, fences
-// and cluster helpers.  Every wait here is bounded (see wait_parity).
+// and cluster helpers.  Every wait here is bounded (see warp_wait).
 //
 // The operations are the four primitives described in "A Blackwell GEMM by Hand in
 // CuTe DSL", section 2 (TMA, mbarrier, TMEM, tcgen05.mma), and the wrapper list in
