@@ -272,7 +272,7 @@ def measure_decode(g, dev, stream, peaks, iters=20, name="decode_m256"):
     """Secondary figures: the decode shapes (fp16 -> fp16, M = 256 or M = 1..128),
     HBM-bound.  Each is timed over `iters` launches back to back, cycling through
     operand copies at least four times the L2 (cold operands in every launch, as when a
-    model's layers stream their weights).  Their parity is covered by the full-size
+    model's layers stream their weights); the figure is the median of five such batches.  Their parity is covered by the full-size
     tests; here only time is taken."""
     flush = None
     wl = si.WORKLOADS[name]
@@ -294,9 +294,14 @@ def measure_decode(g, dev, stream, peaks, iters=20, name="decode_m256"):
                 flush.fill_(0.5)
             run(*sets[i % len(sets)])
         torch.cuda.synchronize()
-        ms = time_steps(run, sets, stream, iters, flush) / iters
+        # the median of five batches of `iters` launches (one batch alone varied by
+        # about 1% from run to run); every batch's mean is kept in the line
+        batches = sorted(time_steps(run, sets, stream, iters, flush) / iters for _ in range(5))
+        ms = batches[len(batches) // 2]
         gbs = rl.gemm_bytes(s.M, s.N, s.K, 2, 2) / (ms * 1e-3) / 1e9
-        out[f"{s.M}x{s.N}x{s.K}"] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+        out[f"{s.M}x{s.N}x{s.K}"] = {"us": round(ms * 1e3, 2),
+                                     "us_batches": [round(b * 1e3, 2) for b in batches],
+                                     "GB/s": round(gbs, 1),
                                      "frac_of_hbm": round(gbs / hbm, 4),
                                      "frac_of_nominal_hbm": round(gbs / NOMINAL_HBM_GBS, 4),
                                      "TFLOP/s": round(rl.gemm_flops(s.M, s.N, s.K) / (ms * 1e-3) / 1e12, 1),
