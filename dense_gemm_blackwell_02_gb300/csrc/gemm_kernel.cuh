@@ -834,7 +834,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
         const int32_t b_row = w.n_blk * BN +
                               (half ? w.half * (BN / 2) + (int32_t)rank * (L::kRowsB / 2)
                                     : (int32_t)rank * (BN == 320 ? 128 : L::kRowsB));
-        const int32_t b_row320 = w.n_blk * BN + 256 + (int32_t)rank * 32;
+        [[maybe_unused]] const int32_t b_row320 = w.n_blk * BN + 256 + (int32_t)rank * 32;
         const CUtensorMap* mapB = half ? &tmB2 : &tmB;
         const CUtensorMap* mapA = &tmA;
         uint32_t tx = (half ? L::kTxBytesHalf : L::kTxBytes) - p.a_tx_short;

@@ -36,8 +36,8 @@ enum WaitSite : uint32_t {
 
 // One problem of a grouped launch ("CUTLASS Deep Dive: From CuTe Layouts to Blackwell
 // tcgen05", Part 6, Grouped GEMM: each tile fetches its problem's pointers and tensor
-// maps).  Written by the host into device memory; 64-byte aligned for the maps.
-struct alignas(64) GroupDesc {
+// maps).  Written by the host into device memory; aligned as its tensor maps require.
+struct GroupDesc {
   CUtensorMap tmA;        // A_g: box {128 bytes of K, 128 (or M_g < 128) rows}
   CUtensorMap tmB;        // B_g: box {128 bytes of K, BN / CTA_GROUP rows}
   CUtensorMap tmC;        // C_g: box {128 bytes of columns, 32 rows} (when tma_store)
