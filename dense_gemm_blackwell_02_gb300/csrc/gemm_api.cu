@@ -400,7 +400,16 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
     longest = c->kb_per_split;
   const bool one_ok = longest <= c->chain_kb;
   if (f.epilogue == 2 && !one_ok) return GEMM_ERR_UNSUPPORTED;
-  c->one_chain = (f.epilogue == 1 || blockwise) ? false : one_ok;  // epilogue 3: either form
+  // FP8 operands: the general epilogue unless the single-chain one is asked for.  An FP8
+  // tile is half the stages of an fp16 tile of the same K, and the single-chain form
+  // holds its accumulator slot through the stores, which then delays the MMAs of the
+  // tile after next (E4M3 -> bf16, A/B on one GPU, flushed: 4096^3 53.2 -> 50.7 us,
+  // 2048x8192x4096 55.3 -> 51.2, 4096x4096x1024 41.0 -> 34.1, 1024x1024x4096 37.2 ->
+  // 30.7; within 1% at 8192x8192x2048 and 256x8192x4096).  fp16/bf16 keep it
+  // (4096^3 79.4 against 82.0 us).
+  const bool fp8 = kb_elems == 2 * kBlockK;
+  c->one_chain = (f.epilogue == 1 || blockwise || (fp8 && f.epilogue == 0)) ? false : one_ok;
+  // (epilogue 3: either form)
   // The cluster K split: every tile's two K slices run on the two CTA groups of one
   // cluster of 2 * cg CTAs, each group one unit, and meet in distributed shared memory.
   c->kx2 = false;

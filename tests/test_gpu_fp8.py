@@ -80,12 +80,31 @@ def test_fp8_small_integers_exact(g, dt):
     ({"variant": 1, "block_n": 256, "max_ctas": 5}, 5, 3000, 640),        # M-row A box, halves
     ({"variant": 2, "block_n": 256, "chain_kblocks": 3}, 256, 512, 2048), # short chains
     ({"variant": 1, "block_n": 128, "epilogue": 1}, 200, 384, 512),       # general epilogue
+    ({"variant": 2, "block_n": 256, "splits": 2, "epilogue": 2}, 256, 1024, 4096),  # single chain
+    ({"variant": 2, "block_n": 256, "max_ctas": 10, "epilogue": 2}, 640, 1024, 1408),  # its tail
     ({"variant": 2, "block_n": 128, "max_ctas": 4, "group_m": 3}, 640, 1280, 768),  # persistent
 ])
 @pytest.mark.parametrize("dt", [E4M3, E5M2])
 def test_fp8_schedules(g, cfg, M, N, K, dt):
     _case(g, M, N, K, dt, BF16, seed=302, cfg=cfg)
     _case(g, M, N, K, dt, F32, seed=303, cfg=cfg, ints=True)
+
+
+def test_fp8_auto_takes_the_general_epilogue(g):
+    # one-chain FP8 units take the general epilogue unless the single-chain one is
+    # forced; both give the same bits (the same additions in the same order)
+    A, B = _operands(640, 1024, 1408, E4M3, seed=305)
+    out = {}
+    try:
+        for epi in (0, 2):
+            g.set_config(epilogue=epi, variant=2, block_n=256, max_ctas=10)
+            out[epi] = parity.run_gpu(g, A, B, BF16)
+            assert g.device_status()[0] == 0
+            assert g.last_config()["epilogue"] == (1 if epi == 0 else 2), g.last_config()
+    finally:
+        g.reset_config()
+    assert np.array_equal(parity.bits_of(out[0]), parity.bits_of(out[2]))
+    parity.oracle_check(parity.bits_of(out[0]), A, B, E4M3, BF16, what="fp8 general epilogue")
 
 
 def test_fp8_auto_chain_is_4096_elements(g):
