@@ -108,7 +108,10 @@ typedef enum {
  *   epilogue  1 = general (the accumulator is copied to registers, chains summed
  *             there); 2 = single-chain (streamed out of Tensor Memory in 32-column
  *             pieces), valid only when every work unit spans at most chain_kblocks K
- *             blocks (else gemm_run returns GEMM_ERR_UNSUPPORTED); 0 = 2 when valid;
+ *             blocks (else gemm_run returns GEMM_ERR_UNSUPPORTED); 0 = 2 when valid
+ *             for fp16/bf16 inputs, 1 for FP8 inputs (faster there: an FP8 tile is
+ *             half the stages, and the single-chain form holds its accumulator slot
+ *             through the stores);
  *             3 = single-chain with a tile's two K slices run by the two CTA groups of
  *             one cluster (2 CTAs, or 4 for pairs) and summed through distributed
  *             shared memory instead of the global workspace (each slice summed in
