@@ -283,6 +283,28 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
       slots = slots128;
     }
   }
+  // CTA pairs whose 256-column tiles fall short of one wave while 128-column tiles fill
+  // one wave and at most 30% of a second, with tiles of several accumulation chains:
+  // 128-column tiles, for the stream-K rule below to spread over every pair (measured
+  // back to back: 256 x 10240 x 8192 37.7 us against 39.7 for 320-column cluster-split
+  // tiles; 256 x 12288 x 8192 43.6 against 45.7 for a partial wave of whole 256-column
+  // tiles; 256 x 10240 x 16384 66.5 against 78.8; equal at 256 x 11264 x 8192; at 1.47
+  // waves, 256 x 14336 x 8192, whole 256-column tiles stay ahead: 48.7 against 49.6).
+  bool sk_narrow = false;
+  if (cg == 2 && allow_kx && !f.block_n && !f.splits && !f.stages && !f.epilogue &&
+      !f.chain_kblocks && !f.max_ctas && c->bn == 256 && c->tiles < slots &&
+      c->k_blocks > chain_kb_of(kb_elems)) {
+    const int64_t tiles128 = c->num_m * ceil_div(N, (int64_t)128);
+    const int64_t slots128 = resident_units(h, cg, 128, default_stages(cg, 128, small_a), out);
+    if (tiles128 > slots128 && 10 * tiles128 <= 13 * slots128) {
+      c->bn = 128;
+      c->stages = default_stages(cg, 128, small_a);
+      c->num_n = ceil_div(N, (int64_t)128);
+      c->tiles = tiles128;
+      slots = slots128;
+      sk_narrow = true;
+    }
+  }
   // The cluster K split: when one of the two tile widths gives exactly two K slices of
   // single chains for a wave, those slices meet in distributed shared memory rather than
   // in the global workspace (measured, back to back: 256 x 4096 x 4096 16.7 us against
@@ -293,7 +315,7 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   // 128-column tiles stay when K is short (256 x 8192 x 4096: 21.9 us against 23.2).
   bool auto_kx = false;
   if (allow_kx && !f.block_n && !f.splits && !f.stages && !f.epilogue &&
-      !f.chain_kblocks &&
+      !f.chain_kblocks && !sk_narrow &&
       c->k_blocks >= 8) {
     // 320-column pair tiles (two MMAs per K step) have a cluster-K-split kernel for
     // single-chain slices only

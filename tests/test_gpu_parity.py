@@ -573,6 +573,26 @@ def test_320_column_tiles_taken_when_256_do_not_fit_the_split(g):
                         what=f"auto 320-column tiles {cfg}")
 
 
+def test_short_wave_of_wide_tiles_takes_narrow_stream_k(g):
+    # 40 tiles of 256 columns leave 36 of 76 pairs idle; 80 tiles of 128 columns fill one
+    # wave and 5% of a second: with tiles of two accumulation chains, stream-K over every
+    # pair with 128-column tiles (sampled rows and columns against the oracle)
+    M, N, K = 256, 10240, 4608
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=53)
+    C = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    g.reset_config()
+    g.run(A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    assert g.device_status()[0] == 0
+    cfg = g.last_config()
+    if g.sm_count >= 152:
+        assert cfg["block_n"] == 128 and cfg["splits"] < 0, cfg
+    rows = si.sample_indices(M, 24, seed=7, must=(0, 127, 128, 255))
+    cols = si.sample_indices(N, 48, seed=8, must=(0, 127, 128, N - 1))
+    parity.oracle_check(parity.bits_of(C)[np.ix_(rows, cols)], A, B, F16, F16, rows=rows,
+                        cols=cols, what=f"narrow stream-K {cfg}")
+
+
 def test_320_column_rejections(g):
     from dense_gemm_blackwell_02_gb300.binding import GemmError
     A = torch.zeros(256, 16384, dtype=torch.float16, device="cuda")
