@@ -1231,7 +1231,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * BN + h * kHalf;
         // (the sums start at +0: fma(x, sc, +0) is x * sc rounded once, as the first
-        // product was before, and needs no select per chain)
+        // product was before, and needs no select per chain; two per instruction)
         if (active) {
           if constexpr (kPieces == 2) {
             // both pieces in flight behind one wait (64 columns: the registers allow it)
@@ -1241,9 +1241,9 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
             tmem_ld_wait(r0);
             tie_regs(r1);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              acc[j] = fmaf(__uint_as_float(r0[j]), sc, acc[j]);
-              acc[32 + j] = fmaf(__uint_as_float(r1[j]), sc, acc[32 + j]);
+            for (int j = 0; j < 32; j += 2) {
+              fma2_rn(acc[j], acc[j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), sc);
+              fma2_rn(acc[32 + j], acc[33 + j], __uint_as_float(r1[j]), __uint_as_float(r1[j + 1]), sc);
             }
           } else {
 #pragma unroll
@@ -1251,6 +1251,7 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
               uint32_t r[32];
               tmem_ld_32x32b_x32(taddr + 32u * pc, r);
               tmem_ld_wait(r);
+              // (one fmaf each here: the packed form raised this 256-column kernel's spills)
 #pragma unroll
               for (int j = 0; j < 32; ++j)
                 acc[32 * pc + j] = fmaf(__uint_as_float(r[j]), sc, acc[32 * pc + j]);

@@ -259,6 +259,18 @@ __device__ __forceinline__ void bulk_wait_group() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Two fused multiply-adds in one instruction: (a0, a1) = (x0, x1) * s + (a0, a1), each
+// rounded once as fmaf would (fma.rn.f32x2).  Half the issue slots of two fmaf: the
+// blockwise epilogue's warps share an SM sub-partition with the MMA warp, and their
+// issue rate set the pace (8192^3 497.7 -> 482.3 us, same bits).
+__device__ __forceinline__ void fma2_rn(float& a0, float& a1, float x0, float x1, float s) {
+  asm("{\n\t.reg .b64 a_, x_, s_;\n\t"
+      "mov.b64 a_, {%0, %1};\n\tmov.b64 x_, {%2, %3};\n\tmov.b64 s_, {%4, %4};\n\t"
+      "fma.rn.f32x2 a_, x_, s_, a_;\n\tmov.b64 {%0, %1}, a_;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1), "f"(s));
+}
+
 // --------------------------------------------------------------- Tensor Memory --
 template <int CTA_GROUP>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
