@@ -310,6 +310,21 @@ def measure_decode(g, dev, stream, peaks, iters=20, name="decode_m256"):
     return out
 
 
+def measure_swapped(g, dev, stream, peaks):
+    """The decode shapes on which the library takes the swapped tiling, timed like the
+    other decode shapes, with the plain tiling (forced) timed the same way beside them."""
+    auto = measure_decode(g, dev, stream, peaks, name="decode_swapped")
+    g.set_config(swap_ab=1)
+    try:
+        plain = measure_decode(g, dev, stream, peaks, name="decode_swapped")
+    finally:
+        g.reset_config()
+    for key, v in auto.items():
+        v["plain_us"] = plain[key]["us"]
+        v["plain_kernel"] = plain[key]["kernel"]
+    return auto
+
+
 def fp8_peak(peaks):
     """The FP8 dense peak: the measured bf16 peak times the nominal FP8 / bf16 ratio."""
     bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -605,6 +620,7 @@ def run_ours(args):
     decode = measure_decode(g, dev, stream, peaks) if args.decode else None
     decode_small = (measure_decode(g, dev, stream, peaks, name="decode_small_m")
                     if args.decode > 1 else None)
+    decode_swapped = measure_swapped(g, dev, stream, peaks) if args.decode > 1 else None
     fp8 = measure_fp8(g, dev, stream, peaks) if args.fp8 else None
     grouped = measure_grouped(g, dev, stream, peaks) if args.grouped else None
     flops = rl.gemm_flops(M, N, K)
@@ -705,6 +721,8 @@ def run_ours(args):
             line["decode"] = decode
         if decode_small is not None:
             line["decode_small_m"] = decode_small
+        if decode_swapped:
+            line["decode_swapped"] = decode_swapped
         if fp8 is not None:
             line["fp8"] = fp8
         if grouped is not None:

@@ -186,11 +186,12 @@ gemm_status_t choose_swap(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out,
     return GEMM_ERR_UNSUPPORTED;
   c->variant = 2;
   c->bn = f.block_n ? f.block_n : 128;
-  c->stages = f.stages ? f.stages : default_stages(2, c->bn);
-  if (!kernel_supported(2, c->bn, c->stages) || c->stages != default_stages(2, c->bn))
-    return GEMM_ERR_INVALID_ARG;
+  if (c->bn != 128 && c->bn != 256) return GEMM_ERR_INVALID_ARG;
+  c->stages = f.stages ? f.stages : swap_stages(c->bn);
+  if (c->stages != swap_stages(c->bn)) return GEMM_ERR_INVALID_ARG;
   c->k_blocks = ceil_div(K, (int64_t)kb_elems);
-  int64_t pairs = resident_units(h, 2, c->bn, c->stages, out);
+  // (one CTA per SM in pairs, like the plain pair kernel of this width, whose count stands in)
+  int64_t pairs = resident_units(h, 2, c->bn, default_stages(2, c->bn), out);
   if (f.max_ctas) pairs = std::min<int64_t>(pairs, std::max<int64_t>(f.max_ctas / 2, 1));
   c->num_n = ceil_div(M, (int64_t)c->bn);  // tiles along A's rows
   int64_t w = f.swap_rows;
@@ -214,9 +215,11 @@ gemm_status_t choose_swap(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out,
   c->group_m = f.group_m ? f.group_m : 16;
   c->chain_kb = f.chain_kblocks ? f.chain_kblocks : chain_kb_of(kb_elems);
   c->prefetch_kb = f.prefetch_kblocks > 0 ? f.prefetch_kblocks : 0;
-  // One tile of A rows: every B element is read once and A by every tile, so B's lines
-  // are marked first to be evicted and A's last (as for one row of tiles otherwise).
-  c->l2_hint = f.l2_hint ? f.l2_hint : (c->num_n == 1 ? 2 : 1);
+  // One tile of A rows, or one wave: every B element is read once, or by every tile of A
+  // rows at about the same time, and A by every tile, so B's lines are marked first to be
+  // evicted and A's last (as for one row of tiles otherwise; 256 x 8192 x 8192, one wave
+  // of two tiles of A rows: 31.9 us against 33.3 without the hints).
+  c->l2_hint = f.l2_hint ? f.l2_hint : (c->num_n == 1 || c->tiles <= pairs ? 2 : 1);
   c->one_chain = false;
   c->kx2 = false;
   c->grid = (int)(std::min<int64_t>(c->units, pairs) * 2);
@@ -224,15 +227,11 @@ gemm_status_t choose_swap(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out,
   return GEMM_OK;
 }
 
-gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int kb_elems,
-                     bool blockwise, bool allow_kx, Choice* c) {
+gemm_status_t choose_plain(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int kb_elems,
+                           bool blockwise, bool allow_kx, Choice* c) {
   const gemm_config_t& f = h->forced;
   c->swap = false;
   c->swap_rows = 0;
-  if (f.swap_ab == 2) {
-    if (!allow_kx) return GEMM_ERR_UNSUPPORTED;
-    return choose_swap(h, M, N, K, out, kb_elems, c);
-  }
   // A CTA pair (256-row tiles, each CTA loading half of B) whenever M fills one.
   // Blockwise scales hand every K block's accumulator to the epilogue and back: one CTA
   // per 128 x 128 tile, whose kernel keeps four accumulator slots (so the MMAs run up to
@@ -459,6 +458,45 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
     return GEMM_ERR_UNSUPPORTED;
   if (c->units > INT32_MAX || c->tiles * cg * 8 > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
   return GEMM_OK;
+}
+
+gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int kb_elems,
+                     bool blockwise, bool allow_kx, Choice* c) {
+  const gemm_config_t& f = h->forced;
+  if (f.swap_ab == 2) {
+    if (!allow_kx) return GEMM_ERR_UNSUPPORTED;
+    return choose_swap(h, M, N, K, out, kb_elems, c);
+  }
+  gemm_status_t st = choose_plain(h, M, N, K, out, kb_elems, blockwise, allow_kx, c);
+  if (st != GEMM_OK || f.swap_ab == 1 || !allow_kx || f.variant || f.block_n || f.splits ||
+      f.stages || f.max_ctas || f.chain_kblocks || f.dp_tiles || f.epilogue || f.swap_rows)
+    return st;
+  // The swapped tiling in place of the plain choice where it measured faster (back to back
+  // over cold operands, one GB300), when its tiles form one wave with at least 96 rows of
+  // B per CTA, so that B's rows stay most of each stage next to the 64 rows of A:
+  // - 129..256 rows of A, K of less than two accumulation chains, in place of a plain
+  //   choice that splits K (256 x 8192 x 1024 .. 6144: 13.1 to 26.2 us against 16.7 to
+  //   31.9 for 320-column cluster-split tiles; 256 x 9216 x 2048: 14.4 against 20.7; with
+  //   K 8192 the cluster split of 256-column tiles stays ahead, 31.1 against 32.2; unsplit
+  //   plain tiles stay, 256 x 7680 x 4096 19.3 against 19.5);
+  // - 17..128 rows of A, K of two chains or more, in place of plain one-CTA tiles that
+  //   leave a quarter of the SMs idle (17 to 128 x 14336 x 8192: 42.5 to 43.8 us against
+  //   44.3 to 46.3; 32 and 128 x 14336 x 28672: 130.2 and 130.9 against 138.6).  With 16
+  //   rows the plain kernel's 16-row stages are as fast (16 x 14336 x 8192: 42.6 both),
+  //   and a second wave of swapped tiles costs more than the idle SMs (128 x 20480 x 8192:
+  //   75.5 against 65.0).
+  Choice sw;
+  if (choose_swap(h, M, N, K, out, kb_elems, &sw) != GEMM_OK || sw.swap_rows < 96 ||
+      sw.units * 2 > sw.grid)
+    return st;
+  const int64_t chain = chain_kb_of(kb_elems);
+  bool take = false;
+  if (M > kBlockM && M <= 2 * kBlockM)
+    take = c->k_blocks < 2 * chain && (c->splits > 1 || c->sk_workers);
+  else if (M > 16 && M <= kBlockM)
+    take = c->k_blocks >= 2 * chain && 4 * (int64_t)c->grid <= 3 * (int64_t)h->sms;
+  if (take) *c = sw;
+  return st;
 }
 
 gemm_status_t ensure_workspace(gemm_ctx* h, size_t ws_bytes, size_t ctr_count) {

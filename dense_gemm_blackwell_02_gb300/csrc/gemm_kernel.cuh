@@ -598,7 +598,9 @@ __device__ __forceinline__ void one_chain_piece(uint32_t taddr, const Unit& w, c
 // inside the operand ring, after the blocks the K slices exchange, instead of after it:
 // the ring is idle once the unit's MMAs have completed, and the 32 KiB go to one more
 // stage (a CTA streams at about its bytes in flight over the round trip of a stage).
-template <int CTA_GROUP, int BN, int STAGES, bool RING_STAGING = false>
+// NO_STAGING (the swapped tiling, whose epilogue writes C with direct stores): no staging
+// boxes at all, and the 32 KiB go to one more stage for the same reason.
+template <int CTA_GROUP, int BN, int STAGES, bool RING_STAGING = false, bool NO_STAGING = false>
 struct Layout {
   static constexpr int kEpiWarps = 8;
   static constexpr uint32_t kThreads = 32 * (2 + kEpiWarps);
@@ -619,7 +621,7 @@ struct Layout {
   static constexpr uint32_t kKxBytes = kEpiWarps * 32u * (BN / 2) * 4u;
   static constexpr uint32_t kCOff = RING_STAGING ? kKxBytes : kRingEnd;
   static constexpr uint32_t kBarOff =
-      RING_STAGING ? kRingEnd : kCOff + kEpiWarps * kStagingBytes;
+      (RING_STAGING || NO_STAGING) ? kRingEnd : kCOff + kEpiWarps * kStagingBytes;
   // cluster launch control: a ring of 16-byte answers
   static constexpr uint32_t kClcSlots = 4;
   // full[S], empty[S], acc_full[4], acc_empty[4], drain, kx_ready[8], kx_go[8],
@@ -634,6 +636,7 @@ struct Layout {
                     kCOff % 1024 == 0,
                 "every operand stage and staging box must start on a 1024-byte boundary");
   static_assert(kDynamicBytes <= 227 * 1024, "shared memory over the per-block limit");
+  static_assert(!(RING_STAGING && NO_STAGING), "one staging placement");
   static_assert(!RING_STAGING || kCOff + kEpiWarps * kStagingBytes <= kRingEnd,
                 "the staging boxes must fit in the ring after the exchange blocks");
   // the MMA reads 128 rows of A from every stage's A start: inside the ring
@@ -674,11 +677,11 @@ struct Layout {
 template <int CTA_GROUP, int BN, int STAGES, int OUT, bool ONE_CHAIN, bool FUSED, int KIND = 0,
           bool GROUPED = false, bool KX2 = false, bool STAGED = false, bool SWAP = false,
           bool CLC = false>
-__global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads), 1)
+__global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2, SWAP>::kThreads), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
                 const GemmParams p) {
-  using L = Layout<CTA_GROUP, BN, STAGES, KX2>;
+  using L = Layout<CTA_GROUP, BN, STAGES, KX2, SWAP>;
   static_assert(BN == 128 || BN == 256 || BN == 320, "BN must be 128, 256 or 320");
   // 320 columns: two MMAs per K step (N = 256 and N = 64) into one 320-column
   // accumulator; built for the pair's cluster K split with single-chain slices only (one
@@ -876,22 +879,33 @@ __global__ void __launch_bounds__((Layout<CTA_GROUP, BN, STAGES, KX2>::kThreads)
             // with the bytes of the pair.
             const uint32_t leader_full = mapa_shared(full_bar(stage), group_base);
             if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), tx);
+            if constexpr (SWAP) {
+              // the row operand (B's rows, streamed from DRAM) first, as B otherwise
+              if constexpr (kHint)
+                tma_load_2d_pair_hint_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
+                                            leader_full, pol_a);
+              else
+                tma_load_2d_pair_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
+                                       leader_full);
+            }
             if constexpr (kHint) {
               tma_load_2d_pair_hint_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
                                           leader_full, pol_b);
               if constexpr (BN == 320)  // rows 256 + 32 * rank.. of the tile (32-row map)
                 tma_load_2d_pair_hint_elect(sB + stage * L::kBBytes + 128 * 128, &tmB2,
                                             kb * kKbElems, b_row320, leader_full, pol_b);
-              tma_load_2d_pair_hint_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
-                                          leader_full, pol_a);
+              if constexpr (!SWAP)
+                tma_load_2d_pair_hint_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
+                                            leader_full, pol_a);
             } else {
               tma_load_2d_pair_elect(sB + stage * L::kBBytes, mapB, kb * kKbElems, b_row,
                                      leader_full);
               if constexpr (BN == 320)
                 tma_load_2d_pair_elect(sB + stage * L::kBBytes + 128 * 128, &tmB2, kb * kKbElems,
                                        b_row320, leader_full);
-              tma_load_2d_pair_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
-                                     leader_full);
+              if constexpr (!SWAP)
+                tma_load_2d_pair_elect(sA + stage * L::kABytes, mapA, kb * kKbElems, a_row,
+                                       leader_full);
             }
           }
           armed |= 1u << stage;

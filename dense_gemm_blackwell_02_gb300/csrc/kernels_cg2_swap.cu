@@ -6,8 +6,8 @@
 namespace gb300 {
 
 cudaError_t launch_cg2_swap(const LaunchSpec& s) {
-  if (s.bn == 128 && s.stages == 8) return by_out<2, 128, 8, false, false, 0, false, false, false, true>(s);
-  if (s.bn == 256 && s.stages == 6) return by_out<2, 256, 6, false, false, 0, false, false, false, true>(s);
+  if (s.bn == 128 && s.stages == 9) return by_out<2, 128, 9, false, false, 0, false, false, false, true>(s);
+  if (s.bn == 256 && s.stages == 7) return by_out<2, 256, 7, false, false, 0, false, false, false, true>(s);
   return cudaErrorInvalidValue;
 }
 

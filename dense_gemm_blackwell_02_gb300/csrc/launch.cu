@@ -26,6 +26,10 @@ int kx_stages(int cg, int bn, bool small_a) {
   return bn == 320 ? 6 : bn == 256 ? 7 : 9;
 }
 
+// The swapped tiling writes C with direct stores and keeps no staging boxes, which also
+// leaves room for one more stage.
+int swap_stages(int bn) { return bn == 256 ? 7 : 9; }
+
 // One-CTA kernels deeper than 7 stages of 128 columns or 4 of 256 hold 16 rows of A per
 // stage (the Layout's rule).
 int a_rows(int cg, int bn, int stages) {

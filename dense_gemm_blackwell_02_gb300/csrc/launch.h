@@ -58,6 +58,7 @@ bool kernel_supported(int cta_group, int bn, int stages);
 int default_stages(int cta_group, int bn, bool small_a = false);
 // the ring depth of the cluster-K-split kernels (their staging lies inside the ring)
 int kx_stages(int cta_group, int bn, bool small_a = false);
+int swap_stages(int bn);  // the swapped tiling's ring depth
 int a_rows(int cta_group, int bn, int stages);  // A rows a stage of that kernel holds
 // Clusters (CTAs for cta_group 1) of this configuration that can be resident at once
 // on the current device; 0 if the query fails.

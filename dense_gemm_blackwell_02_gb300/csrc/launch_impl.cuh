@@ -11,7 +11,7 @@ template <int CG, int BN, int STAGES, int OUT, bool ONE, bool FUSED, int KIND = 
 cudaError_t launch_one(const LaunchSpec& s) {
   auto kernel = gemm_kernel<CG, BN, STAGES, OUT, ONE, FUSED, KIND, GROUPED, KX2, STAGED, SWAP, CLC>;
   constexpr unsigned kCluster = CG * (KX2 ? 2 : 1);
-  using L = Layout<CG, BN, STAGES, KX2>;
+  using L = Layout<CG, BN, STAGES, KX2, SWAP>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes);
   if (e != cudaSuccess) return e;

@@ -125,8 +125,8 @@ typedef enum {
  *             evict-first and A's evict-last (for one row of tiles, where every B
  *             element is read once and A is re-read by every tile); 0 = 2 when the
  *             tiles form one row (M <= 256 for CTA pairs, M <= 128 for one CTA per
- *             tile; with swap_ab, M <= block_n), else 1.  gemm_last_config reports the
- *             one used.
+ *             tile; with swap_ab, M <= block_n or the tiles form one wave), else 1.
+ *             gemm_last_config reports the one used.
  *   swap_ab   2 = the swapped tiling for a few rows of A (decode shapes): B is the
  *             MMA's row operand, swap_rows of its rows per CTA of a pair, and block_n
  *             (128 or 256) rows of A are the MMA's columns, so a tile covers block_n
@@ -134,7 +134,13 @@ typedef enum {
  *             by direct stores.  Valid for fp16/bf16 inputs without a fused epilogue,
  *             CTA pairs (variant 0 or 2), no K split (splits 0 or 1), the general
  *             epilogue (epilogue 0 or 1); else GEMM_ERR_UNSUPPORTED.  1 = off;
- *             0 = chosen automatically.  gemm_last_config reports 2 or 1.
+ *             0 = chosen automatically (only when no other field but group_m,
+ *             prefetch_kblocks and l2_hint is forced) when the swapped tiles form one
+ *             wave with at least 96 rows of B per CTA: for 129..256 rows of A with K
+ *             under two accumulation chains (8192 fp16/bf16 elements) in place of a K
+ *             split, and for 17..128 rows of A with K of two chains or more when the
+ *             plain one-CTA tiles would leave a quarter of the SMs idle.
+ *             gemm_last_config reports 2 or 1.
  *   swap_rows with swap_ab: rows of B per CTA, 1..128 (0 = the fewest that make one
  *             wave of tiles, rounded up to a multiple of 8, at most 128).
  *             gemm_last_config reports the one used (0 when not swapped).

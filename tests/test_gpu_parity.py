@@ -593,6 +593,35 @@ def test_short_wave_of_wide_tiles_takes_narrow_stream_k(g):
                         cols=cols, what=f"narrow stream-K {cfg}")
 
 
+@pytest.mark.parametrize("M,N,K,swapped", [(256, 8192, 4096, True),    # one chain, one wave
+                                           (200, 8192, 1024, True),    # ragged rows of A
+                                           (256, 9216, 6144, True),    # 128 rows of B per CTA
+                                           (128, 14336, 8192, True),   # plain tiles: 112 CTAs
+                                           (24, 14336, 8192, True),    # a few rows of A
+                                           (256, 8192, 8192, False),   # the cluster split stays
+                                           (256, 7680, 4096, False),   # unsplit plain tiles stay
+                                           (16, 14336, 8192, False),   # 16-row stages stay
+                                           (128, 20480, 8192, False)])  # two waves of swapped
+def test_decode_takes_the_swapped_tiling_where_it_measured_faster(g, M, N, K, swapped):
+    # the automatic choice weighs the swapped tiling against the plain one (sampled rows
+    # and columns against the oracle whichever is taken)
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=54)
+    C = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    g.reset_config()
+    g.run(A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    assert g.device_status()[0] == 0
+    cfg = g.last_config()
+    if g.sm_count >= 152:
+        assert (cfg["swap_ab"] == 2) == swapped, cfg
+        if swapped:
+            assert cfg["swap_rows"] >= 96 and cfg["l2_hint"] == 2 and cfg["splits"] == 1, cfg
+    rows = si.sample_indices(M, 16, seed=9, must=(0, 63, 64, M - 1))
+    cols = si.sample_indices(N, 48, seed=10, must=(0, 111, 112, N - 1))
+    parity.oracle_check(parity.bits_of(C)[np.ix_(rows, cols)], A, B, F16, F16, rows=rows,
+                        cols=cols, what=f"automatic swapped tiling {cfg}")
+
+
 def test_320_column_rejections(g):
     from dense_gemm_blackwell_02_gb300.binding import GemmError
     A = torch.zeros(256, 16384, dtype=torch.float16, device="cuda")
