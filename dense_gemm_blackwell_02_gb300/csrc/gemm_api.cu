@@ -363,12 +363,20 @@ gemm_status_t choose_plain(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out
     dp = 0;
   } else if (allow_kx && !f.max_ctas && !f.block_n && !f.stages && !f.epilogue &&
              !f.chain_kblocks && c->tiles > slots && c->tiles < 2 * slots && c->k_blocks > chain_kb_of(kb_elems) &&
-             c->tiles * c->k_blocks * slots < (int64_t(1) << 32)) {
+             c->tiles * c->k_blocks * slots < (int64_t(1) << 32) &&
+             !(c->num_m > 1 && c->bn == 256 && 2 * (c->tiles % slots) <= slots &&
+               4 * (c->tiles % slots) >= slots)) {
     // Between one and two waves of tiles of several accumulation chains: stream-K over
     // every resident unit instead of a second, mostly idle wave (measured, back to back:
     // 256 x 28672 x 8192 88.9 us against 97.6 for whole tiles and half tiles; 512 x 10240 x
     // 8192 66.4 against 87.2).  Below one wave the segments' fix-up costs more than the
-    // balance gains (512 x 8192 x 8192: 58.7 against 48.4 us).
+    // balance gains (512 x 8192 x 8192: 58.7 against 48.4 us).  With two rows of tiles or
+    // more, the tiles that share B's columns reach the same K at far-apart times under
+    // stream-K, so B comes from DRAM once per row of tiles: whole tiles then take the first
+    // wave and half tiles the last whenever those fill at least half of it (320 .. 512 x
+    // 14336 x 8192: 75.5 to 79.8 us against 93.3 to 96.2; x 16384 143.5 against 174.4),
+    // and stream-K stays for a nearly empty last wave (384 and 512 x 10240 x 8192: 64.9 and
+    // 63.0 against 81.5 and 72.4).
     dp = 0;
     c->sk_workers = slots;
   } else if (c->tiles > slots && c->tiles % slots != 0) {

@@ -622,6 +622,29 @@ def test_decode_takes_the_swapped_tiling_where_it_measured_faster(g, M, N, K, sw
                         cols=cols, what=f"automatic swapped tiling {cfg}")
 
 
+@pytest.mark.parametrize("M,N,K,stream_k", [(384, 14336, 8192, False),  # half tiles fill the tail
+                                            (384, 10240, 8192, True)])  # a nearly empty tail
+def test_two_rows_of_tiles_take_half_tiles_over_stream_k(g, M, N, K, stream_k):
+    # with two rows of 256-row tiles between one and two waves, stream-K gives way to whole
+    # tiles plus a last wave of half tiles when those fill at least half of it (sampled
+    # rows and columns against the oracle either way)
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=55)
+    C = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    g.reset_config()
+    g.run(A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    assert g.device_status()[0] == 0
+    cfg = g.last_config()
+    if g.sm_count >= 152:
+        assert cfg["block_n"] == 256 and (cfg["splits"] < 0) == stream_k, cfg
+        if not stream_k:
+            assert cfg["splits"] == 1 and 0 < cfg["dp_tiles"] < -(-M // 256) * -(-N // 256), cfg
+    rows = si.sample_indices(M, 16, seed=11, must=(0, 255, 256, M - 1))
+    cols = si.sample_indices(N, 48, seed=12, must=(0, 127, 128, N - 1))
+    parity.oracle_check(parity.bits_of(C)[np.ix_(rows, cols)], A, B, F16, F16, rows=rows,
+                        cols=cols, what=f"two rows of tiles {cfg}")
+
+
 def test_320_column_rejections(g):
     from dense_gemm_blackwell_02_gb300.binding import GemmError
     A = torch.zeros(256, 16384, dtype=torch.float16, device="cuda")
