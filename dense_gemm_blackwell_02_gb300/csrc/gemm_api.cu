@@ -327,7 +327,9 @@ gemm_status_t choose_plain(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out
       if (f.max_ctas) sl = std::min<int64_t>(sl, std::max<int64_t>(f.max_ctas / cg, 1));
       const int64_t tl = c->num_m * ceil_div(N, (int64_t)bn);
       if (tl * 2 > sl || std::min<int64_t>({sl / tl, c->k_blocks / 4, 32}) != 2) continue;
-      if (bn == 256 && c->bn == 128 && c->k_blocks < 128) continue;  // keep unsplit narrow tiles
+      // keep unsplit narrow tiles (256 x 8192 x 4096: 19.5 us against 26.0 for 320-column
+      // split tiles; 384 x 4096 x 4096: 18.4 against 25.3)
+      if (bn != 128 && c->bn == 128 && c->k_blocks < 128) continue;
       const int clusters = max_resident_kx_clusters(cg, bn, st, out);
       if (clusters <= 0 || tl > clusters) continue;
       c->bn = bn;
@@ -364,19 +366,19 @@ gemm_status_t choose_plain(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out
   } else if (allow_kx && !f.max_ctas && !f.block_n && !f.stages && !f.epilogue &&
              !f.chain_kblocks && c->tiles > slots && c->tiles < 2 * slots && c->k_blocks > chain_kb_of(kb_elems) &&
              c->tiles * c->k_blocks * slots < (int64_t(1) << 32) &&
-             !(c->num_m > 1 && c->bn == 256 && 2 * (c->tiles % slots) <= slots &&
-               4 * (c->tiles % slots) >= slots)) {
+             !(c->num_m > 1 && 4 * (c->tiles % slots) > slots)) {
     // Between one and two waves of tiles of several accumulation chains: stream-K over
     // every resident unit instead of a second, mostly idle wave (measured, back to back:
     // 256 x 28672 x 8192 88.9 us against 97.6 for whole tiles and half tiles; 512 x 10240 x
     // 8192 66.4 against 87.2).  Below one wave the segments' fix-up costs more than the
     // balance gains (512 x 8192 x 8192: 58.7 against 48.4 us).  With two rows of tiles or
     // more, the tiles that share B's columns reach the same K at far-apart times under
-    // stream-K, so B comes from DRAM once per row of tiles: whole tiles then take the first
-    // wave and half tiles the last whenever those fill at least half of it (320 .. 512 x
-    // 14336 x 8192: 75.5 to 79.8 us against 93.3 to 96.2; x 16384 143.5 against 174.4),
-    // and stream-K stays for a nearly empty last wave (384 and 512 x 10240 x 8192: 64.9 and
-    // 63.0 against 81.5 and 72.4).
+    // stream-K, so B comes from DRAM once per row of tiles: whole tiles (and half tiles in
+    // the last wave where they fit) then win unless the last wave holds at most a quarter
+    // of the units (320 .. 512 x 14336 x 8192: 75.3 to 77.8 us against 94.8 to 96.7;
+    // 768 x 10240 x 8192 84 against 103; 1024 x 8192 x 8192 84 against 110; 2048 x 4096 x
+    // 8192 83 against 99), and stream-K stays for a nearly empty one (384 and 512 x 10240
+    // x 8192: 60.8 and 62.1 against 81.5 and 72.4).
     dp = 0;
     c->sk_workers = slots;
   } else if (c->tiles > slots && c->tiles % slots != 0) {
@@ -479,31 +481,24 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
   if (st != GEMM_OK || f.swap_ab == 1 || !allow_kx || f.variant || f.block_n || f.splits ||
       f.stages || f.max_ctas || f.chain_kblocks || f.dp_tiles || f.epilogue || f.swap_rows)
     return st;
-  // The swapped tiling in place of the plain choice where it measured faster (back to back
-  // over cold operands, one GB300), when its tiles form one wave with at least 96 rows of
-  // B per CTA, so that B's rows stay most of each stage next to the 64 rows of A:
-  // - 129..256 rows of A, K of less than two accumulation chains, in place of a plain
-  //   choice that splits K (256 x 8192 x 1024 .. 6144: 13.1 to 26.2 us against 16.7 to
-  //   31.9 for 320-column cluster-split tiles; 256 x 9216 x 2048: 14.4 against 20.7; with
-  //   K 8192 the cluster split of 256-column tiles stays ahead, 31.1 against 32.2; unsplit
-  //   plain tiles stay, 256 x 7680 x 4096 19.3 against 19.5);
-  // - 17..128 rows of A, K of two chains or more, in place of plain one-CTA tiles that
-  //   leave a quarter of the SMs idle (17 to 128 x 14336 x 8192: 42.5 to 43.8 us against
-  //   44.3 to 46.3; 32 and 128 x 14336 x 28672: 130.2 and 130.9 against 138.6).  With 16
-  //   rows the plain kernel's 16-row stages are as fast (16 x 14336 x 8192: 42.6 both),
-  //   and a second wave of swapped tiles costs more than the idle SMs (128 x 20480 x 8192:
-  //   75.5 against 65.0).
+  // The swapped tiling in place of plain one-CTA tiles (17..128 rows of A, K of two
+  // accumulation chains or more) that leave a quarter of the SMs idle, when the swapped
+  // tiles form one wave with at least 96 rows of B per CTA, so that B's rows stay most of
+  // each stage next to the 64 rows of A (measured back to back over cold operands, one
+  // GB300: 17 to 128 x 14336 x 8192: 42.5 to 43.8 us against 44.3 to 46.3; 32 and 128 x
+  // 14336 x 28672: 130.2 and 130.9 against 138.6).  With 16 rows the plain kernel's
+  // 16-row stages are as fast (16 x 14336 x 8192: 42.6 both), and a second wave of swapped
+  // tiles costs more than the idle SMs (128 x 20480 x 8192: 75.5 against 65.0).  For 129..256
+  // rows the plain pair tiles keep up with it (256 x 8192 x 4096, unsplit 128-column
+  // tiles: 19.5 against 19.8; 256 x 8192 x 8192, the cluster K split: 31.1 against 32.2).
   Choice sw;
+  if (M <= 16 || M > kBlockM || c->k_blocks < 2 * chain_kb_of(kb_elems) ||
+      4 * (int64_t)c->grid > 3 * (int64_t)h->sms)
+    return st;
   if (choose_swap(h, M, N, K, out, kb_elems, &sw) != GEMM_OK || sw.swap_rows < 96 ||
       sw.units * 2 > sw.grid)
     return st;
-  const int64_t chain = chain_kb_of(kb_elems);
-  bool take = false;
-  if (M > kBlockM && M <= 2 * kBlockM)
-    take = c->k_blocks < 2 * chain && (c->splits > 1 || c->sk_workers);
-  else if (M > 16 && M <= kBlockM)
-    take = c->k_blocks >= 2 * chain && 4 * (int64_t)c->grid <= 3 * (int64_t)h->sms;
-  if (take) *c = sw;
+  *c = sw;
   return st;
 }
 

@@ -135,11 +135,10 @@ typedef enum {
  *             CTA pairs (variant 0 or 2), no K split (splits 0 or 1), the general
  *             epilogue (epilogue 0 or 1); else GEMM_ERR_UNSUPPORTED.  1 = off;
  *             0 = chosen automatically (only when no other field but group_m,
- *             prefetch_kblocks and l2_hint is forced) when the swapped tiles form one
- *             wave with at least 96 rows of B per CTA: for 129..256 rows of A with K
- *             under two accumulation chains (8192 fp16/bf16 elements) in place of a K
- *             split, and for 17..128 rows of A with K of two chains or more when the
- *             plain one-CTA tiles would leave a quarter of the SMs idle.
+ *             prefetch_kblocks and l2_hint is forced) for 17..128 rows of A with K of
+ *             two accumulation chains or more (8192 fp16/bf16 elements) when the plain
+ *             one-CTA tiles would leave a quarter of the SMs idle and the swapped tiles
+ *             form one wave with at least 96 rows of B per CTA.
  *             gemm_last_config reports 2 or 1.
  *   swap_rows with swap_ab: rows of B per CTA, 1..128 (0 = the fewest that make one
  *             wave of tiles, rounded up to a multiple of 8, at most 128).

@@ -55,10 +55,10 @@ WORKLOADS = {
     "decode_small_m": Workload("decode_small_m", tuple(
         Shape(m, n, k) for m in (1, 8, 32, 64, 128)
         for n, k in ((8192, 8192), (28672, 8192), (8192, 28672))), F16, F16, "uniform", 5),
-    # decode shapes on which the library takes the swapped tiling (short K for 256 rows;
-    # 17..128 rows with a one-wave row of swapped tiles)
-    "decode_swapped": Workload("decode_swapped", (Shape(256, 8192, 4096), Shape(256, 9216, 2048),
-                                                  Shape(128, 14336, 8192), Shape(32, 14336, 28672)),
+    # decode shapes on which the library takes the swapped tiling (17..128 rows of A where
+    # the plain one-CTA tiles leave SMs idle)
+    "decode_swapped": Workload("decode_swapped", (Shape(128, 14336, 8192), Shape(48, 14336, 8192),
+                                                  Shape(128, 14336, 16384), Shape(32, 14336, 28672)),
                                F16, F16, "uniform", 7),
     "fp8": Workload("fp8", (Shape(4096, 4096, 4096), Shape(8192, 8192, 8192)),
                     E4M3, BF16, "uniform", 6),

@@ -593,15 +593,14 @@ def test_short_wave_of_wide_tiles_takes_narrow_stream_k(g):
                         cols=cols, what=f"narrow stream-K {cfg}")
 
 
-@pytest.mark.parametrize("M,N,K,swapped", [(256, 8192, 4096, True),    # one chain, one wave
-                                           (200, 8192, 1024, True),    # ragged rows of A
-                                           (256, 9216, 6144, True),    # 128 rows of B per CTA
-                                           (128, 14336, 8192, True),   # plain tiles: 112 CTAs
+@pytest.mark.parametrize("M,N,K,swapped", [(128, 14336, 8192, True),   # plain tiles: 112 CTAs
                                            (24, 14336, 8192, True),    # a few rows of A
-                                           (256, 8192, 8192, False),   # the cluster split stays
-                                           (256, 7680, 4096, False),   # unsplit plain tiles stay
+                                           (100, 14336, 16384, True),  # ragged rows of A
                                            (16, 14336, 8192, False),   # 16-row stages stay
-                                           (128, 20480, 8192, False)])  # two waves of swapped
+                                           (128, 20480, 8192, False),  # two waves of swapped
+                                           (128, 14336, 4096, False),  # one chain of K
+                                           (256, 8192, 4096, False),   # pair tiles stay
+                                           (256, 8192, 8192, False)])  # the cluster split stays
 def test_decode_takes_the_swapped_tiling_where_it_measured_faster(g, M, N, K, swapped):
     # the automatic choice weighs the swapped tiling against the plain one (sampled rows
     # and columns against the oracle whichever is taken)
@@ -616,18 +615,19 @@ def test_decode_takes_the_swapped_tiling_where_it_measured_faster(g, M, N, K, sw
         assert (cfg["swap_ab"] == 2) == swapped, cfg
         if swapped:
             assert cfg["swap_rows"] >= 96 and cfg["l2_hint"] == 2 and cfg["splits"] == 1, cfg
-    rows = si.sample_indices(M, 16, seed=9, must=(0, 63, 64, M - 1))
+    rows = si.sample_indices(M, 16, seed=9, must=(0, M // 2, M - 1))
     cols = si.sample_indices(N, 48, seed=10, must=(0, 111, 112, N - 1))
     parity.oracle_check(parity.bits_of(C)[np.ix_(rows, cols)], A, B, F16, F16, rows=rows,
                         cols=cols, what=f"automatic swapped tiling {cfg}")
 
 
 @pytest.mark.parametrize("M,N,K,stream_k", [(384, 14336, 8192, False),  # half tiles fill the tail
+                                            (1024, 8192, 8192, False),  # a second wave of whole tiles
                                             (384, 10240, 8192, True)])  # a nearly empty tail
 def test_two_rows_of_tiles_take_half_tiles_over_stream_k(g, M, N, K, stream_k):
-    # with two rows of 256-row tiles between one and two waves, stream-K gives way to whole
-    # tiles plus a last wave of half tiles when those fill at least half of it (sampled
-    # rows and columns against the oracle either way)
+    # with two rows of 256-row tiles or more between one and two waves, stream-K gives way
+    # to whole tiles (half tiles in the last wave where they fit) unless the last wave holds
+    # at most a quarter of the units (sampled rows and columns against the oracle)
     A, B = si.make_operands(M, N, K, F16, "uniform", seed=55)
     C = torch.empty(M, N, dtype=torch.float16, device="cuda")
     g.reset_config()
@@ -638,11 +638,30 @@ def test_two_rows_of_tiles_take_half_tiles_over_stream_k(g, M, N, K, stream_k):
     if g.sm_count >= 152:
         assert cfg["block_n"] == 256 and (cfg["splits"] < 0) == stream_k, cfg
         if not stream_k:
-            assert cfg["splits"] == 1 and 0 < cfg["dp_tiles"] < -(-M // 256) * -(-N // 256), cfg
+            assert cfg["splits"] == 1, cfg
     rows = si.sample_indices(M, 16, seed=11, must=(0, 255, 256, M - 1))
     cols = si.sample_indices(N, 48, seed=12, must=(0, 127, 128, N - 1))
     parity.oracle_check(parity.bits_of(C)[np.ix_(rows, cols)], A, B, F16, F16, rows=rows,
                         cols=cols, what=f"two rows of tiles {cfg}")
+
+
+@pytest.mark.parametrize("M,N,K", [(384, 4096, 4096), (256, 8192, 2048)])
+def test_unsplit_narrow_tiles_are_not_replaced_by_320_column_split_tiles(g, M, N, K):
+    # 128-column pair tiles that fill one wave without a K split stay (the 320-column
+    # cluster split is for 256-column tiles that do not fit a two-way split)
+    A, B = si.make_operands(M, N, K, F16, "uniform", seed=56)
+    C = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    g.reset_config()
+    g.run(A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    assert g.device_status()[0] == 0
+    cfg = g.last_config()
+    if g.sm_count >= 152:
+        assert cfg["block_n"] == 128 and cfg["splits"] == 1 and cfg["swap_ab"] == 1, cfg
+    rows = si.sample_indices(M, 16, seed=13, must=(0, 255, M - 1))
+    cols = si.sample_indices(N, 48, seed=14, must=(0, 127, 128, N - 1))
+    parity.oracle_check(parity.bits_of(C)[np.ix_(rows, cols)], A, B, F16, F16, rows=rows,
+                        cols=cols, what=f"narrow tiles {cfg}")
 
 
 def test_320_column_rejections(g):
