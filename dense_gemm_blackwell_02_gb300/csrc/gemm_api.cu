@@ -482,21 +482,27 @@ gemm_status_t choose(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out, int 
       f.stages || f.max_ctas || f.chain_kblocks || f.dp_tiles || f.epilogue || f.swap_rows)
     return st;
   // The swapped tiling in place of plain one-CTA tiles (17..128 rows of A, K of two
-  // accumulation chains or more) that leave a quarter of the SMs idle, when the swapped
-  // tiles form one wave with at least 96 rows of B per CTA, so that B's rows stay most of
-  // each stage next to the 64 rows of A (measured back to back over cold operands, one
-  // GB300: 17 to 128 x 14336 x 8192: 42.5 to 43.8 us against 44.3 to 46.3; 32 and 128 x
-  // 14336 x 28672: 130.2 and 130.9 against 138.6).  With 16 rows the plain kernel's
-  // 16-row stages are as fast (16 x 14336 x 8192: 42.6 both), and a second wave of swapped
-  // tiles costs more than the idle SMs (128 x 20480 x 8192: 75.5 against 65.0).  For 129..256
+  // accumulation chains or more) that leave a quarter of the SMs idle, with at least 96
+  // rows of B per CTA, so that B's rows stay most of each stage next to the 64 rows of A,
+  // when the swapped tiles form one wave, or with K of at most two chains a second wave
+  // at least 40% full (measured back to back over cold operands, one GB300: 17 to 128 x
+  // 14336 x 8192, one wave: 42.5 to 43.8 us against 44.3 to 46.3; 32 and 128 x 14336 x
+  // 28672: 130.2 and 130.9 against 138.6; 32 to 128 x 28672 x 8192, a second wave 47%
+  // full: 76.4 to 78.2 against 77.9 to 79.2; with K 16384 from 2% slower to 1.5% faster).
+  // With 16 rows the plain kernel's 16-row stages are as fast (16 x 14336 x 8192: 42.6
+  // both), and a nearly empty second wave costs more than the idle SMs (128 x 20480 x
+  // 8192, 5% full: 75.5 against 65.0).  For 129..256
   // rows the plain pair tiles keep up with it (256 x 8192 x 4096, unsplit 128-column
   // tiles: 19.5 against 19.8; 256 x 8192 x 8192, the cluster K split: 31.1 against 32.2).
   Choice sw;
   if (M <= 16 || M > kBlockM || c->k_blocks < 2 * chain_kb_of(kb_elems) ||
       4 * (int64_t)c->grid > 3 * (int64_t)h->sms)
     return st;
-  if (choose_swap(h, M, N, K, out, kb_elems, &sw) != GEMM_OK || sw.swap_rows < 96 ||
-      sw.units * 2 > sw.grid)
+  if (choose_swap(h, M, N, K, out, kb_elems, &sw) != GEMM_OK || sw.swap_rows < 96)
+    return st;
+  const int64_t pairs = sw.grid / 2, rest = sw.units % pairs;
+  if (sw.units > pairs && (sw.units > 2 * pairs || c->k_blocks > 2 * chain_kb_of(kb_elems) ||
+                           (rest != 0 && 5 * rest < 2 * pairs)))
     return st;
   *c = sw;
   return st;

@@ -137,8 +137,9 @@ typedef enum {
  *             0 = chosen automatically (only when no other field but group_m,
  *             prefetch_kblocks and l2_hint is forced) for 17..128 rows of A with K of
  *             two accumulation chains or more (8192 fp16/bf16 elements) when the plain
- *             one-CTA tiles would leave a quarter of the SMs idle and the swapped tiles
- *             form one wave with at least 96 rows of B per CTA.
+ *             one-CTA tiles would leave a quarter of the SMs idle and the swapped tiles,
+ *             with at least 96 rows of B per CTA, form one wave (or, with K of at most
+ *             two chains, a second wave at least 40% full).
  *             gemm_last_config reports 2 or 1.
  *   swap_rows with swap_ab: rows of B per CTA, 1..128 (0 = the fewest that make one
  *             wave of tiles, rounded up to a multiple of 8, at most 128).

@@ -597,7 +597,8 @@ def test_short_wave_of_wide_tiles_takes_narrow_stream_k(g):
                                            (24, 14336, 8192, True),    # a few rows of A
                                            (100, 14336, 16384, True),  # ragged rows of A
                                            (16, 14336, 8192, False),   # 16-row stages stay
-                                           (128, 20480, 8192, False),  # two waves of swapped
+                                           (128, 20480, 8192, False),  # a nearly empty 2nd wave
+                                           (64, 28672, 8192, True),    # a 2nd wave 47% full
                                            (128, 14336, 4096, False),  # one chain of K
                                            (256, 8192, 4096, False),   # pair tiles stay
                                            (256, 8192, 8192, False)])  # the cluster split stays
