@@ -20,7 +20,7 @@ EXPORTS = ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_epilogue", "gemm
            "gemm_set_config",
            "gemm_last_config", "gemm_device_status", "gemm_set_wait_limit",
            "gemm_set_test_stall", "gemm_sm_count", "gemm_status_string", "gemm_run_noalloc",
-           "gemm_last_cuda_error")
+           "gemm_last_cuda_error", "gemm_plan")
 
 
 class GemmConfig(ctypes.Structure):
@@ -61,6 +61,31 @@ class GemmError(RuntimeError):
         super().__init__(f"{STATUS_NAMES.get(code, code)}{': ' + what if what else ''}")
 
 
+class GemmDeviceModel(ctypes.Structure):
+    """gemm_device_model_t: a GPU described for gemm_plan (SMs, resident CTA pairs,
+    resident clusters of four CTAs)."""
+    _fields_ = [("sms", ctypes.c_int32), ("pairs", ctypes.c_int32), ("clusters4", ctypes.c_int32)]
+
+
+GB300_MODEL = (152, 76, 36)  # a full GB300: 152 SMs, 76 pairs, 36 clusters of four
+
+
+def plan(M, N, K, dtype_in=F16, dtype_out=F16, fused=False, blockwise=False, config=None,
+         device=GB300_MODEL) -> dict:
+    """The configuration the library would launch for this product on the described
+    device (gemm_plan): the host's decisions only, no GPU needed.  Raises GemmError with
+    the call's status when it refuses."""
+    cfg = None
+    if config:
+        cfg = GemmConfig(**{**{n: 0 for n, _ in GemmConfig._fields_}, **config})
+    dev = GemmDeviceModel(*device)
+    out = GemmConfig()
+    _check(lib().gemm_plan(ctypes.byref(dev), ctypes.byref(cfg) if cfg is not None else None,
+                           M, N, K, dtype_in, dtype_out, 1 if fused else 0,
+                           1 if blockwise else 0, ctypes.byref(out)), "gemm_plan")
+    return out.as_dict()
+
+
 _lib = None
 
 
@@ -94,6 +119,8 @@ def lib():
     L.gemm_run_grouped.argtypes = [vp, ctypes.POINTER(GemmProblem), i32, i32, i32, vp]
     L.gemm_status_string.argtypes = [i32]
     L.gemm_status_string.restype = ctypes.c_char_p
+    L.gemm_plan.argtypes = [ctypes.POINTER(GemmDeviceModel), ctypes.POINTER(GemmConfig), i64, i64,
+                            i64, i32, i32, i32, i32, ctypes.POINTER(GemmConfig)]
     L.gemm_last_cuda_error.argtypes = [vp]
     L.gemm_last_cuda_error.restype = ctypes.c_char_p
     for name in EXPORTS:

@@ -64,6 +64,10 @@ struct gemm_ctx {
   TmapEntry cache[kTmapCacheSize] = {};
   int cache_next = 0;
   int resident[2][2][2][3] = {};  // [cta_group-1][bn==256][small A][out]: co-resident units (0: unknown)
+  // gemm_plan: a device described instead of queried (resident CTA pairs, and clusters of
+  // four CTAs for the pair's cluster K split); the GPU is never touched
+  bool model = false;
+  int model_pairs = 0, model_clusters4 = 0;
   // grouped launches: a ring of problem tables (pinned host copy, device copy and the
   // event that marks the host copy reusable)
   static constexpr int kGroupRing = 4;
@@ -157,6 +161,7 @@ int out_kind(gemm_dtype_t d) { return d == GEMM_F16 ? kOutF16 : d == GEMM_BF16 ?
 // Units of this configuration that can run at once: CTAs (variant 1) or CTA pairs
 // (variant 2), from the occupancy query, at most one CTA per SM.
 int resident_units(gemm_ctx* h, int cg, int bn, int stages, int out) {
+  if (h->model) return cg == 1 ? h->sms : std::min(h->model_pairs, h->sms / 2);
   int& slot = h->resident[cg - 1][bn == 256 ? 1 : 0][a_rows(cg, bn, stages) < kBlockM ? 1 : 0][out];
   if (slot == 0) {
     int n = max_resident_units(cg, bn, stages, out);
@@ -164,6 +169,13 @@ int resident_units(gemm_ctx* h, int cg, int bn, int stages, int out) {
     slot = (n <= 0 || n > cap) ? cap : n;
   }
   return slot;
+}
+
+// Clusters of the cluster K split that can be resident at once (pairs: clusters of four
+// CTAs; one CTA: clusters of two).
+int kx_clusters(gemm_ctx* h, int cg, int bn, int stages, int out) {
+  if (h->model) return cg == 1 ? h->sms / 2 : h->model_clusters4;
+  return max_resident_kx_clusters(cg, bn, stages, out);
 }
 
 // The default accumulation chain: K 4096 elements, 64 blocks of fp16/bf16, 32 of FP8.
@@ -330,7 +342,7 @@ gemm_status_t choose_plain(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out
       // keep unsplit narrow tiles (256 x 8192 x 4096: 19.5 us against 26.0 for 320-column
       // split tiles; 384 x 4096 x 4096: 18.4 against 25.3)
       if (bn != 128 && c->bn == 128 && c->k_blocks < 128) continue;
-      const int clusters = max_resident_kx_clusters(cg, bn, st, out);
+      const int clusters = kx_clusters(h, cg, bn, st, out);
       if (clusters <= 0 || tl > clusters) continue;
       c->bn = bn;
       c->stages = st;
@@ -451,7 +463,7 @@ gemm_status_t choose_plain(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out
     const int kst = kx_stages(cg, c->bn, a_rows(cg, c->bn, c->stages) < kBlockM);
     if (f.stages && f.stages != kst) valid = false;
     if (valid) {
-      const int clusters = max_resident_kx_clusters(cg, c->bn, kst, out);
+      const int clusters = kx_clusters(h, cg, c->bn, kst, out);
       valid = clusters > 0 && c->tiles <= clusters;
     }
     if (valid) {
@@ -830,6 +842,53 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
                        int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
                        gemm_stream_t stream) {
   return run_impl(h, A, B, C, M, N, K, dtype_in, dtype_out, nullptr, nullptr, stream);
+}
+
+gemm_status_t gemm_plan(const gemm_device_model_t* dev, const gemm_config_t* forced,
+                        int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in,
+                        gemm_dtype_t dtype_out, int32_t fused, int32_t blockwise,
+                        gemm_config_t* out) {
+  if (!dev || !out || dev->sms < 2 || dev->pairs < 1 || dev->clusters4 < 0)
+    return GEMM_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1) return GEMM_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype_in) || !valid_dtype(dtype_out)) return GEMM_ERR_INVALID_ARG;
+  if (dtype_in == GEMM_F32 || is_fp8(dtype_out)) return GEMM_ERR_UNSUPPORTED;
+  if (blockwise && !is_fp8(dtype_in)) return GEMM_ERR_UNSUPPORTED;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+  if ((K * (int64_t)in_size(dtype_in)) % 16) return GEMM_ERR_UNSUPPORTED;
+  // a context that describes the device instead of querying it (no CUDA call below)
+  gemm_ctx ctx;
+  ctx.model = true;
+  ctx.sms = dev->sms;
+  ctx.model_pairs = dev->pairs;
+  ctx.model_clusters4 = dev->clusters4;
+  if (forced) {
+    const gemm_status_t st = gemm_set_config(&ctx, forced);
+    if (st != GEMM_OK) return st;
+  }
+  const gemm_config_t& fc = ctx.forced;
+  const bool fp8 = is_fp8(dtype_in);
+  // the same decisions as gemm_run: the matrix-vector path for a row of A, else choose()
+  if (fc.variant == 3 || (!fc.variant && !fc.block_n && !fc.splits && !fc.stages && !fc.epilogue &&
+                          !fc.chain_kblocks && fc.swap_ab != 2 && M == 1 && K <= kGemvAutoMaxK &&
+                          !fused && !fp8 && !blockwise)) {
+    if (M > kGemvMaxRows || fused || fp8 || blockwise) return GEMM_ERR_UNSUPPORTED;
+    const int64_t cap = fc.max_ctas ? fc.max_ctas : (int64_t)ctx.sms * 4;
+    const int grid = (int)std::min<int64_t>(ceil_div(N, (int64_t)8), cap);
+    *out = gemm_config_t{3, 0, 1, 0, 0, grid, 0, (int32_t)N, -1, 1, 1, 1, 0, 1};
+    return GEMM_OK;
+  }
+  if (fc.scheduler == 2) return GEMM_ERR_UNSUPPORTED;
+  Choice ch;
+  const gemm_status_t st = choose(&ctx, M, N, K, out_kind(dtype_out), fp8 ? 2 * kBlockK : kBlockK,
+                                  blockwise != 0, !fp8 && !fused && !blockwise, &ch);
+  if (st != GEMM_OK) return st;
+  *out = gemm_config_t{ch.variant,  ch.bn,   ch.sk_workers ? -(int32_t)ch.sk_workers : ch.splits,
+                       ch.stages,
+                       ch.group_m,  ch.grid, ch.chain_kb, (int32_t)ch.dp_tiles,
+                       ch.prefetch_kb ? ch.prefetch_kb : -1, ch.kx2 ? 3 : ch.one_chain ? 2 : 1,
+                       ch.l2_hint, ch.swap ? 2 : 1, ch.swap_rows, 1};
+  return GEMM_OK;
 }
 
 gemm_status_t gemm_run_blockwise(gemm_handle_t h, const void* A, const void* B, void* C,

@@ -323,6 +323,32 @@ gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg);
 /* The configuration the last successful gemm_run on this handle launched. */
 gemm_status_t gemm_last_config(gemm_handle_t h, gemm_config_t* out);
 
+/* A GPU described rather than queried, for gemm_plan: its SM count, the CTA pairs that
+ * can be resident at once (one CTA per SM), and the clusters of four CTAs (two pairs)
+ * that can be resident at once for the pair's cluster K split.  A full GB300:
+ * {152, 76, 36}. */
+typedef struct {
+  int32_t sms;
+  int32_t pairs;
+  int32_t clusters4;
+} gemm_device_model_t;
+
+/* The configuration gemm_run (fused = 0, blockwise = 0), gemm_run_epilogue with a
+ * non-trivial epilogue (fused = 1) or gemm_run_blockwise (blockwise = 1) would launch
+ * for an M x N x K product on the described device, under `forced` (NULL: automatic
+ * choice), without touching a GPU: the same host decisions, with every residency query
+ * answered from *dev instead of the driver.  *out is filled as gemm_last_config would
+ * be.  Errors: NULL dev or out, dev->sms < 2, dev->pairs < 1, dev->clusters4 < 0,
+ * M, N or K < 1, or an invalid dtype -> GEMM_ERR_INVALID_ARG; the combinations gemm_run
+ * refuses (K * element size not a multiple of 16, FP8 output, blockwise scales
+ * without FP8 inputs, a forced configuration that cannot serve the shape) ->
+ * GEMM_ERR_UNSUPPORTED or GEMM_ERR_INVALID_ARG as there.  Pointer alignment, which
+ * gemm_run also checks, is not part of the plan. */
+gemm_status_t gemm_plan(const gemm_device_model_t* dev, const gemm_config_t* forced,
+                        int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in,
+                        gemm_dtype_t dtype_out, int32_t fused, int32_t blockwise,
+                        gemm_config_t* out);
+
 /* Synchronise `stream`, read and clear the handle's device status word.
  * Returns GEMM_ERR_TIMEOUT if a kernel gave up waiting since the last call
  * (the output of that run is undefined), else GEMM_OK.  *detail, if non-NULL,

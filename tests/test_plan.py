@@ -1,0 +1,155 @@
+"""The host's launch choices, without a GPU: gemm_plan runs the same decisions as
+gemm_run with every residency query answered from a described device (a full GB300:
+152 SMs, 76 CTA pairs, 36 clusters of four CTAs).  The GPU tests check the same choices
+on the hardware; these pin each rule on the CPU."""
+import pytest
+
+from dense_gemm_blackwell_02_gb300 import binding as b
+from dense_gemm_blackwell_02_gb300.binding import GemmError
+
+F16, BF16, F32, E4M3 = b.F16, b.BF16, b.F32, b.E4M3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from dense_gemm_blackwell_02_gb300 import build
+    build.build()
+
+
+def plan(M, N, K, **kw):
+    return b.plan(M, N, K, **kw)
+
+
+def test_square_shapes_take_pair_tiles_and_a_half_tile_tail():
+    # 4096^3: 256 tiles of 256 x 256 on 76 pairs, three whole waves (228 tiles) and the
+    # last 28 tiles as half tiles; K = 4096 is one chain, so the single-chain epilogue
+    c = plan(4096, 4096, 4096)
+    assert (c["variant"], c["block_n"], c["splits"], c["dp_tiles"], c["epilogue"]) == (2, 256, 1, 228, 2)
+    assert c["max_ctas"] == 152 and c["chain_kblocks"] == 64
+    # 8192^3: 1024 tiles, 988 whole (13 waves) and 36 as half tiles; two chains per tile
+    c = plan(8192, 8192, 8192, dtype_in=BF16, dtype_out=BF16)
+    assert (c["variant"], c["block_n"], c["dp_tiles"], c["epilogue"]) == (2, 256, 988, 1)
+
+
+def test_the_four_decode_shapes():
+    # 256 x 28672 x 8192: 112 tiles, between one and two waves: stream-K over 76 pairs
+    c = plan(256, 28672, 8192)
+    assert (c["block_n"], c["splits"], c["l2_hint"]) == (256, -76, 2)
+    # 256 x 8192 x 28672 and 256 x 8192 x 8192: 32 tiles in two K slices, each tile's slices
+    # on the two pairs of a cluster of four (epilogue 3), 7-stage ring
+    for K in (28672, 8192):
+        c = plan(256, 8192, K)
+        assert (c["block_n"], c["splits"], c["epilogue"], c["stages"], c["max_ctas"]) == (256, 2, 3, 7, 128)
+    # 256 x 10240 x 8192: 128-column tiles and stream-K over every pair
+    c = plan(256, 10240, 8192)
+    assert (c["block_n"], c["splits"]) == (128, -76)
+
+
+def test_rows_of_tiles_take_whole_tiles_over_stream_k_unless_the_tail_is_nearly_empty():
+    for M, N, K in ((384, 14336, 8192), (1024, 8192, 8192), (2048, 4096, 8192), (768, 10240, 8192)):
+        assert plan(M, N, K)["splits"] == 1, (M, N, K)
+    # 80 tiles on 76 pairs: a last wave of 4 tiles, stream-K
+    assert plan(384, 10240, 8192)["splits"] == -76
+    # one row of tiles keeps stream-K
+    assert plan(256, 28672, 8192)["splits"] == -76
+
+
+def test_unsplit_narrow_tiles_are_not_replaced_by_320_column_tiles():
+    for M, N, K in ((384, 4096, 4096), (256, 8192, 4096), (256, 8192, 2048), (512, 4096, 4096)):
+        c = plan(M, N, K)
+        assert (c["block_n"], c["splits"], c["swap_ab"]) == (128, 1, 1), (M, N, K, c)
+    # 40 tiles of 256 columns need 80 pairs for two K slices: 32 tiles of 320 need 64
+    c = plan(256, 10240, 2048)
+    assert (c["block_n"], c["splits"], c["epilogue"]) == (320, 2, 3)
+
+
+@pytest.mark.parametrize("M,N,K,swapped", [
+    (128, 14336, 8192, True),    # plain one-CTA tiles on 112 SMs; one wave of swapped tiles
+    (24, 14336, 8192, True),
+    (100, 14336, 16384, True),
+    (64, 28672, 8192, True),     # a second wave 47% full, K of two chains
+    (16, 14336, 8192, False),    # 16-row stages
+    (128, 20480, 8192, False),   # a second wave 5% full
+    (128, 28672, 16384, False),  # a second wave with K of four chains
+    (128, 14336, 4096, False),   # K of one chain
+    (128, 8192, 8192, False),    # plain tiles on 128 SMs
+    (256, 8192, 8192, False),    # pair tiles
+])
+def test_swapped_tiling_rules(M, N, K, swapped):
+    c = plan(M, N, K)
+    assert (c["swap_ab"] == 2) == swapped, c
+    if swapped:
+        assert c["variant"] == 2 and c["splits"] == 1 and c["swap_rows"] >= 96 and c["l2_hint"] == 2, c
+
+
+def test_one_row_of_a_takes_the_matrix_vector_path():
+    c = plan(1, 8192, 8192)
+    assert c["variant"] == 3 and c["max_ctas"] == 608 and c["dp_tiles"] == 8192
+    assert plan(1, 8192, 28672)["variant"] != 3      # long rows stay on the tensor cores
+    assert plan(2, 8192, 8192)["variant"] == 1       # two rows: tensor cores
+    assert plan(3, 4096, 1024, config={"variant": 3})["variant"] == 3
+    with pytest.raises(GemmError) as e:              # forced beyond four rows
+        plan(5, 4096, 1024, config={"variant": 3})
+    assert e.value.code == 2
+
+
+def test_rows_of_at_most_16_take_the_deeper_ring():
+    c = plan(8, 8192, 8192)
+    assert (c["variant"], c["block_n"], c["splits"], c["stages"], c["epilogue"]) == (1, 128, 2, 12, 3)
+    assert plan(17, 8192, 8192)["stages"] == 7
+
+
+def test_fp8_takes_the_general_epilogue_and_blockwise_one_chain_per_k_block():
+    c = plan(4096, 4096, 4096, dtype_in=E4M3, dtype_out=BF16)
+    assert (c["variant"], c["block_n"], c["epilogue"], c["chain_kblocks"]) == (2, 256, 1, 32)
+    c = plan(8192, 8192, 8192, dtype_in=E4M3, dtype_out=BF16, blockwise=True)
+    assert (c["variant"], c["block_n"], c["chain_kblocks"], c["epilogue"]) == (1, 128, 1, 1)
+    # the cluster K split and the swapped tiling are fp16/bf16 only
+    c = plan(256, 8192, 8192, dtype_in=E4M3, dtype_out=BF16)
+    assert c["epilogue"] != 3 and c["swap_ab"] == 1
+    c = plan(128, 14336, 16384, dtype_in=E4M3, dtype_out=BF16)
+    assert c["swap_ab"] == 1
+    # a fused epilogue keeps the plain kernels too
+    c = plan(128, 14336, 8192, fused=True)
+    assert c["swap_ab"] == 1 and c["epilogue"] != 3
+
+
+def test_forced_configurations_are_honoured_or_refused_as_by_gemm_run():
+    c = plan(4096, 4096, 4096, config={"variant": 1, "block_n": 128})
+    assert (c["variant"], c["block_n"]) == (1, 128)
+    c = plan(256, 8192, 8192, config={"swap_ab": 2})
+    assert c["swap_ab"] == 2 and c["swap_rows"] == 112
+    assert plan(128, 14336, 8192, config={"swap_ab": 1})["swap_ab"] == 1
+    with pytest.raises(GemmError) as e:              # not a configuration
+        plan(256, 256, 256, config={"block_n": 100})
+    assert e.value.code == 1
+    with pytest.raises(GemmError) as e:              # the swapped tiling takes no FP8
+        plan(256, 8192, 8192, dtype_in=E4M3, dtype_out=BF16, config={"swap_ab": 2})
+    assert e.value.code == 2
+
+
+def test_the_device_model_decides_residency():
+    # half the SMs: the cluster K split of 32 tiles no longer fits one wave of clusters
+    small = plan(256, 8192, 8192, device=(76, 38, 18))
+    assert small["max_ctas"] <= 76 and small["epilogue"] != 3
+    full = plan(256, 8192, 8192)
+    assert full["epilogue"] == 3
+
+
+def test_plan_rejections():
+    for args in ((0, 8, 8), (8, 0, 8), (8, 8, 0)):
+        with pytest.raises(GemmError) as e:
+            plan(*args)
+        assert e.value.code == 1
+    with pytest.raises(GemmError) as e:              # K * 2 bytes not a multiple of 16
+        plan(256, 256, 12)
+    assert e.value.code == 2
+    with pytest.raises(GemmError) as e:              # FP8 output
+        plan(256, 256, 256, dtype_out=E4M3)
+    assert e.value.code == 2
+    with pytest.raises(GemmError) as e:              # block scales without FP8 inputs
+        plan(256, 256, 256, blockwise=True)
+    assert e.value.code == 2
+    with pytest.raises(GemmError) as e:              # not a device
+        plan(256, 256, 256, device=(1, 1, 0))
+    assert e.value.code == 1
