@@ -153,3 +153,52 @@ def test_plan_rejections():
     with pytest.raises(GemmError) as e:              # not a device
         plan(256, 256, 256, device=(1, 1, 0))
     assert e.value.code == 1
+
+
+def _rand_shapes(seed, count):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    for _ in range(count):
+        M = int(rng.choice([rng.integers(1, 300), rng.integers(1, 20000)]))
+        N = int(rng.choice([rng.integers(1, 300), rng.integers(1, 40000)]))
+        K = int(rng.integers(1, 5000)) * 8
+        yield M, N, K, int(rng.integers(0, 6))
+
+
+def test_every_valid_shape_gets_a_consistent_configuration():
+    # the library computes any M, N >= 1 with K % 8 == 0 (K % 16 for FP8): the planner
+    # must never refuse such a product, and what it returns must hold together
+    for M, N, K, kind in _rand_shapes(2024, 1000):
+        din, dout, fused, bw = [(F16, F16, False, False), (BF16, BF16, False, False),
+                                (F16, F32, False, False), (F16, F16, True, False),
+                                (E4M3, BF16, False, False), (E4M3, BF16, False, True)][kind]
+        if din == E4M3 and K % 16:
+            K += 8
+        c = plan(M, N, K, dtype_in=din, dtype_out=dout, fused=fused, blockwise=bw)
+        what = (M, N, K, kind, c)
+        if c["variant"] == 3:                        # the matrix-vector path
+            assert M == 1 and din != E4M3 and not fused and c["max_ctas"] <= 4 * 152, what
+            continue
+        cg = c["variant"]
+        assert cg in (1, 2) and c["block_n"] in (128, 256, 320), what
+        assert 1 <= c["max_ctas"] <= 152 and c["max_ctas"] % cg == 0, what
+        assert c["epilogue"] in (1, 2, 3), what
+        if c["epilogue"] == 3:                       # the cluster K split: two slices
+            assert c["splits"] == 2 and din != E4M3 and not fused, what
+        if c["block_n"] == 320:
+            assert cg == 2 and c["epilogue"] == 3, what
+        if c["splits"] < 0:                          # stream-K over that many units
+            assert -c["splits"] <= 152 // cg and c["dp_tiles"] == 0, what
+        if bw:
+            assert c["chain_kblocks"] == 1 and c["epilogue"] == 1, what
+        if c["swap_ab"] == 2:
+            w = c["swap_rows"]
+            assert din != E4M3 and not fused and cg == 2 and c["splits"] == 1, what
+            assert 1 <= w <= 128 and c["dp_tiles"] == -(-N // (2 * w)) * -(-M // c["block_n"]), what
+            continue
+        rows = 128 * cg
+        tiles = -(-M // rows) * -(-N // c["block_n"])
+        assert 0 <= c["dp_tiles"] <= tiles, what
+        if c["splits"] > 1:                          # every slice at least one K block
+            kb = -(-K // (128 if din == E4M3 else 64))
+            assert c["splits"] <= kb, what
