@@ -359,9 +359,9 @@ gemm_status_t choose_plain(gemm_ctx* h, int64_t M, int64_t N, int64_t K, int out
   if (f.splits < 0) {
     // forced stream-K: every resident unit takes an equal share of the (tile, k-block)
     // iterations ("A Blackwell GEMM by Hand in CuTe DSL", section 9; "CUTLASS Deep
-    // Dive", StreamK).  Measured on the M = 256 decode shapes it lost to split-K (the
-    // three-segment tiles cost more to reduce than the balance saves), so it is not
-    // chosen automatically.
+    // Dive", StreamK).  Below one wave of tiles it lost to split-K on the M = 256 decode
+    // shapes (the three-segment tiles cost more to reduce than the balance saves), so it
+    // is chosen automatically only as below: between one and two waves of tiles.
     dp = 0;
     c->sk_workers = std::min<int64_t>(slots, c->tiles * c->k_blocks);
     // the kernel splits the iteration range in 32-bit arithmetic
