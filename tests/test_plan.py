@@ -202,3 +202,15 @@ def test_every_valid_shape_gets_a_consistent_configuration():
         if c["splits"] > 1:                          # every slice at least one K block
             kb = -(-K // (128 if din == E4M3 else 64))
             assert c["splits"] <= kb, what
+
+
+def test_the_planned_4096_configuration_is_the_captured_one():
+    # profiles/traffic.json holds the DRAM traffic of an ncu capture together with the
+    # configuration the GPU reported for it; the bench uses the traffic only while the
+    # launch configuration still matches, so a host change that moves the 4096^3 choice
+    # shows here first
+    import json
+    import os
+    rec = json.load(open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                                      "profiles", "traffic.json")))
+    assert plan(4096, 4096, 4096) == rec["square_4096"]["config"]
