@@ -13,6 +13,10 @@ CUDA events on the launching stream; a step's time is the sum of its GEMMs'.
 four times the L2 with the step's R launches back to back between two events
 (cold operands in every launch, no launch gap; the GPU then runs at its power
 cap throughout).  The decode shapes are always timed the second way.
+Secondary sections of the line: `decode` (the four M = 256 shapes), `decode_small_m`
+(M = 1..128), `decode_swapped` (shapes the host gives the swapped tiling, with the
+plain tiling forced and timed beside them), `fp8` (per-tensor and blockwise scales)
+and `grouped` (MoE groups and a group of mixed K).
 `value` is TFLOP/s (2MNK per GEMM) over all ranks; `e2e` is the same metric through gemm_run_host with
 pinned host buffers (host->device copies of A and B and the device->host copy
 of C inside the timed region).  `cpu_baseline` times the CPU oracle on a
